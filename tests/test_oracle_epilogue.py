@@ -1,0 +1,101 @@
+"""Pins for the oracle's int8 epilogue (BiasActivationOutputKernel of
+"conv_ops_fused_int8.cc"): hand-worked ties, saturation and ReLU cases, and
+agreement with an exact-rational evaluation of the three rounded steps.
+Also builds the set of inputs on which other orderings of the steps give a
+different int8 result, which the GPU parity tests reuse.  No GPU needed."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import exact
+
+from epilogue_cases import discriminating_cases, random_tuples
+
+
+def _run(acc, cs, side, ss, bias, relu):
+    acc = np.array([[acc]], np.int32)
+    side_a = None if side is None else np.array([[side]], np.int8)
+    return int(oracle.epilogue_i8(acc, np.array([bias], np.float32), side_a, cs, ss, relu)[0, 0])
+
+
+@pytest.mark.parametrize("acc,cs,side,ss,bias,relu,expect", [
+    # ties go to the even integer: 5*0.5 = 2.5 -> 2, 7*0.5 = 3.5 -> 4, -2.5 -> -2
+    (5, 0.5, None, 0.0, 0.0, False, 2),
+    (7, 0.5, None, 0.0, 0.0, False, 4),
+    (-5, 0.5, None, 0.0, 0.0, False, -2),
+    (-7, 0.5, None, 0.0, 0.0, False, -4),
+    (1, 0.5, None, 0.0, 0.0, False, 0),
+    # ReLU floors at 0, BiasAdd at -128
+    (-5, 0.5, None, 0.0, 0.0, True, 0),
+    (-1000, 1.0, None, 0.0, 0.0, False, -128),
+    (-1000, 1.0, None, 0.0, 0.0, True, 0),
+    # saturation at 127
+    (1000, 1.0, None, 0.0, 0.0, False, 127),
+    (127, 1.0, None, 0.0, 0.4, False, 127),
+    (126, 1.0, None, 0.0, 0.6, False, 127),
+    # side input: 0 + 3*0.5 = 1.5 -> 2; 0 + 5*0.5 = 2.5 -> 2
+    (0, 1.0, 3, 0.5, 0.0, False, 2),
+    (0, 1.0, 5, 0.5, 0.0, False, 2),
+    # side scale 0 means no side term at all
+    (4, 1.0, 100, 0.0, 0.0, False, 4),
+    # bias: -0.5 -> -0 -> 0; 1.5 -> 2; 0.5 -> 0
+    (0, 1.0, None, 0.0, -0.5, False, 0),
+    (0, 1.0, None, 0.0, 1.5, False, 2),
+    (0, 1.0, None, 0.0, 0.5, False, 0),
+    # int32 -> fp32 rounds to nearest even: 2^24+1 -> 2^24, scaled by 2^-20 -> 16
+    (2 ** 24 + 1, 2.0 ** -20, None, 0.0, 0.0, False, 16),
+    # 2^24 + 3 -> 2^24 + 4 (tie to even), times 2^-2 -> 4194305 -> saturates
+    (2 ** 24 + 3, 0.25, None, 0.0, 0.0, False, 127),
+])
+def test_epilogue_hand_cases(acc, cs, side, ss, bias, relu, expect):
+    assert _run(acc, cs, side, ss, bias, relu) == expect
+    assert exact.epilogue_i8(acc, cs, side, ss, bias, relu) == expect
+
+
+def test_epilogue_matches_exact_rational_random():
+    tuples = random_tuples(4000, seed=11)
+    acc = np.array([t[0] for t in tuples], np.int32)
+    for relu in (False, True):
+        for (cs, ss) in {(t[1], t[3]) for t in tuples}:
+            sel = [i for i, t in enumerate(tuples) if (t[1], t[3]) == (cs, ss)]
+            a = acc[sel].reshape(-1, 1)
+            side = np.array([tuples[i][2] for i in sel], np.int8).reshape(-1, 1)
+            for i_row, i in enumerate(sel):
+                bias = np.array([tuples[i][4]], np.float32)
+                got = int(oracle.epilogue_i8(a[i_row:i_row + 1], bias, side[i_row:i_row + 1],
+                                             cs, ss, relu)[0, 0])
+                want = exact.epilogue_i8(int(a[i_row, 0]), cs, int(side[i_row, 0]), ss,
+                                         float(bias[0]), relu)
+                assert got == want, (tuples[i], relu)
+
+
+def test_discriminating_set_tells_orders_apart():
+    cases = discriminating_cases()
+    assert len(cases) >= 3
+    seen = set()
+    for (cs, ss, relu), rows in cases.items():
+        for acc, side, bias, variants in rows:
+            got = _run(acc, cs, side, ss, bias, relu)
+            assert got == exact.epilogue_i8(acc, cs, side, ss, bias, relu)
+            for v in variants:
+                assert exact.epilogue_i8_other_order(acc, cs, side, ss, bias, relu, v) != got
+                seen.add(v)
+    # every alternative ordering is caught by at least one case
+    assert seen == {"fma_scale_bias", "no_side_fma", "contract_13"}
+
+
+def test_exact_rounding_helper_pins():
+    from fractions import Fraction
+    # values every reader can check: 1/3 in binary32 is 11184811 * 2^-25
+    assert exact.to_f32(Fraction(1, 3)) == Fraction(11184811, 2 ** 25)
+    # 2^24 + 1 is a tie between 2^24 and 2^24 + 2: even mantissa wins
+    assert exact.to_f32(Fraction(2 ** 24 + 1)) == 2 ** 24
+    assert exact.to_f32(Fraction(2 ** 24 + 3)) == 2 ** 24 + 4
+    assert exact.to_f32(Fraction(-(2 ** 24 + 3))) == -(2 ** 24 + 4)
+    # numpy's float32 conversion is a library RNE rounding of a double
+    rng = np.random.default_rng(12)
+    for v in rng.standard_normal(200) * 1e3:
+        assert exact.to_f32(Fraction(float(v))) == Fraction(float(np.float32(v)))
+    assert exact.round_half_even_int(Fraction(5, 2)) == 2
+    assert exact.round_half_even_int(Fraction(-5, 2)) == -2
+    assert exact.round_half_even_int(Fraction(7, 2)) == 4
