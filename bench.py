@@ -1,0 +1,385 @@
+#!/usr/bin/env python
+"""Benchmark of the fused int8 Conv2D forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fconv|reference]
+
+Prints ONE JSON line (rank 0).  A step is one fconv_run of the whole fused
+path (filter pack, int8 -> fp16 input widening, implicit-GEMM convolution
+with the fused epilogue) over one batch of the workload: N=256 28x28x512
+int8, 3x3 stride 1 SAME, side input, ReLU (implicit GEMM 200704 x 512 x
+4608).  ``value`` is TOPS counted the usual way (2*M*N*K, padded taps
+included) over all ranks; the roofline block reports the convolution
+kernel alone against its own tensor-core peak.
+
+``--impl reference`` times the CPU oracle (the reference this build is
+checked against) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import fconv_inputs as FI  # noqa: E402
+
+METRIC = "fused int8 Conv2D TOPS (1 GB300) and % of dense int8 tensor peak"
+UNIT = "TOPS"
+DEFAULT_WORKLOAD = "large_i8_28x28x512"
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "quantized_conv2d_gb300", "csrc", f)
+                  for f in ("fconv_kernels.cu", "fconv_device.cuh", "fconv_internal.h")]
+
+
+# ---------------------------------------------------------------- geometry
+def axis(in_, filt, stride, padding):
+    if padding == "VALID":
+        out = (in_ - filt) // stride + 1
+        return out, 0
+    out = -(-in_ // stride)
+    total = max(0, (out - 1) * stride + filt - in_)
+    return out, total // 2
+
+
+def ops_counts(wl):
+    """(nominal ops 2*M*N*K with padded taps, ops over in-bounds taps only)."""
+    P, pt = axis(wl.H, wl.R, wl.stride, wl.padding)
+    Q, pl = axis(wl.W, wl.S, wl.stride, wl.padding)
+    nominal = 2 * wl.N * P * Q * wl.K * wl.R * wl.S * wl.C
+    rows = sum(sum(1 for r in range(wl.R) if 0 <= p * wl.stride + r - pt < wl.H) for p in range(P))
+    cols = sum(sum(1 for s in range(wl.S) if 0 <= q * wl.stride + s - pl < wl.W) for q in range(Q))
+    inbounds = 2 * wl.N * wl.K * wl.C * rows * cols
+    return nominal, inbounds, P, Q
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), d.get("hbm_gbs"), "measured"
+    except (OSError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [v.strip() for v in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax = float(f[2])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def time_oracle(wl, P, Q, target_s: float, max_images: int):
+    """Time the CPU oracle on a bounded sample (whole images of the workload,
+    all channels, full epilogue).  Returns (TOPS nominal, images, seconds, threads)."""
+    import oracle
+    oracle.build()
+    pad = oracle.SAME if wl.padding == "SAME" else oracle.VALID
+
+    def run(n):
+        inp = FI.generate(wl, (P, Q), batch=n)
+        t0 = time.perf_counter()
+        acc = oracle.conv_acc_i8(inp["x"], inp["w"], wl.stride, pad)
+        oracle.epilogue_i8(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale, wl.relu)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    n = int(max(1, min(max_images, target_s / max(t1, 1e-6))))
+    t = run(n) if n > 1 else t1
+    per_image = 2 * P * Q * wl.K * wl.R * wl.S * wl.C
+    return per_image * n / t / 1e12, n, t, oracle.num_threads()
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = FI.WORKLOADS[args.workload]
+    _, _, P, Q = ops_counts(wl)
+    step_target = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    values, n_img, threads = [], 1, 1
+    for i in range(args.warmup + args.steps):
+        v, n_img, _, threads = time_oracle(wl, P, Q, step_target, wl.N)
+        if i >= args.warmup:
+            values.append(v)
+    value = statistics.median(values)
+    sample = f"{n_img} of {wl.N} images per step (all {wl.K} channels, full epilogue)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8", "data": "synthetic (seeded)", "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": f"{wl.name}: {wl.note}", "N": wl.N, "H": wl.H, "W": wl.W, "C": wl.C,
+            "K": wl.K, "R": wl.R, "S": wl.S, "stride": wl.stride, "padding": wl.padding,
+            "dtype": wl.dtype, "side_input": wl.has_side, "relu": wl.relu}
+
+
+def run_fconv(args, rank, world, local_rank):
+    import torch
+    import quantized_conv2d_gb300 as fc
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = FI.WORKLOADS[args.workload]
+    nominal, inbounds, P, Q = ops_counts(wl)
+    plan = fc.Conv2dPlan(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.padding,
+                         wl.dtype, wl.relu, device=dev)
+    if args.tile:
+        plan.set_tile(args.tile)
+    assert plan.out_shape == (wl.N, P, Q, wl.K)
+    inp = FI.generate(wl, (P, Q))
+
+    def to_dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    x, w, bias, side = to_dev(inp["x"]), to_dev(inp["w"]), to_dev(inp["bias"]), to_dev(inp["side"])
+    y = plan.new_output()
+    stream = torch.cuda.current_stream(dev)
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def step():
+        plan.run(x, w, bias, side, wl.conv_scale, wl.side_scale, y=y, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    plan.check()
+
+    # stage events: [before pack, after pack, after widen, after conv] per step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank)
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.25)   # let the sampler start before the timed region
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        fc.fconv_plan_set_stage_events(plan.handle, [e.cuda_event for e in evs[i]])
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        tdist.barrier()
+    clk = clocks.stop()
+    fc.fconv_plan_set_stage_events(plan.handle, None)
+    plan.check()
+    total_ms = t_start.elapsed_time(t_end)
+    conv_ms = [evs[i][2].elapsed_time(evs[i][3]) for i in range(args.steps)]
+    pack_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
+    widen_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps * nominal / (total_ms / 1e3) / 1e12
+
+    # ------------------------------------------------ end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        nbytes = fc.fconv_host_workspace_size(plan.handle, side is not None)
+        dws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        hx = torch.from_numpy(inp["x"]).pin_memory()
+        hw = torch.from_numpy(inp["w"]).pin_memory()
+        hb = torch.from_numpy(inp["bias"]).pin_memory()
+        hs = torch.from_numpy(inp["side"]).pin_memory() if inp["side"] is not None else None
+        hy = torch.empty(plan.out_shape, dtype=plan.torch_dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hx, hw, hb, hs) if t is not None)
+        d2h = hy.numel() * hy.element_size()
+
+        def host_step():
+            fc.fconv_run_host(plan.handle, hx.data_ptr(), hw.data_ptr(), hb.data_ptr(),
+                              hs.data_ptr() if hs is not None else None, wl.conv_scale,
+                              wl.side_scale, hy.data_ptr(), dws.data_ptr(), nbytes,
+                              stream.cuda_stream)
+            stream.synchronize()
+
+        for _ in range(3):
+            host_step()
+        n_e2e = max(3, min(args.steps, 50))
+        if dist:
+            tdist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_step()
+        el = time.perf_counter() - t0
+        if dist:
+            t = torch.tensor([el], device=dev)
+            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+            el = float(t.item())
+        plan.check()
+        e2e = {"value": world * n_e2e * nominal / el / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": n_e2e}
+        del dws
+
+    # ------------------------------------------------ roofline of the conv kernel
+    burst, sustained, hbm, src = measured_peaks()
+    long_run = total_ms > 1000.0
+    peak = sustained if long_run else burst
+    conv_avg_s = statistics.mean(conv_ms) / 1e3
+    achieved = inbounds / conv_avg_s / 1e12
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as fh:
+            tr = json.load(fh)
+        rec = tr.get(args.workload)
+        if rec and rec.get("kernel_hash") == kernel_hash() and rec.get("block_n") == plan.config()[0]:
+            traffic = rec["dram_bytes_per_launch"]
+    except (OSError, ValueError):
+        pass
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": f"conv_fprop_kernel<{plan.config()[0]}, int8> (tcgen05.mma kind::f16)",
+                "peak_source": f"{'sustained' if long_run else 'burst'} bf16 dense of {src} "
+                               f"(fp16 rate = bf16 rate; no int8 tensor-core MMA on sm_103a)",
+                "ops_per_launch": inbounds, "ops_definition": "2*MAC over in-bounds taps"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded)",
+        "config": dict(config_of(wl), block_n=plan.config()[0],
+                       l2="inputs larger than L2: x+side+y+workspace = "
+                          f"{(x.numel() + (side.numel() if side is not None else 0) + y.numel() + plan.ws_bytes) / 1e6:.0f} MB > 129 MB"),
+        "stage_ms": {"pack_filter": statistics.mean(pack_ms), "widen_input": statistics.mean(widen_ms),
+                     "conv": statistics.mean(conv_ms)},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (3 if wl.dtype == "int8" else 2),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n_img, t, threads = time_oracle(wl, P, Q, args.cpu_seconds, wl.N)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{n_img} of {wl.N} images, all channels, full epilogue "
+                                          f"({t:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fconv", "reference"], default="fconv")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(FI.WORKLOADS))
+    ap.add_argument("--tile", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+    run_fconv(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -109,7 +109,7 @@ def generate(wl: Workload, out_hw: tuple[int, int], batch: int | None = None):
 
 
 def random_case(seed: int, N, H, W, C, K, R, S, dtype: str, out_hw, with_side: bool,
-                x_range=(-128, 127), w_range=(-128, 127), w_std=None):
+                x_range=(-128, 127), w_range=(-128, 127), w_std=None, bias_std=1.0):
     """Inputs for a parity sweep case of any shape, same recipe as above."""
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
@@ -120,7 +120,7 @@ def random_case(seed: int, N, H, W, C, K, R, S, dtype: str, out_hw, with_side: b
         wd = ("normal", w_std if w_std is not None else 1.0 / np.sqrt(R * S * C))
     x = _draw(gen, (N, H, W, C), xd, dtype)
     w = _draw(gen, (R, S, C, K), wd, dtype)
-    bias = torch.randn((K,), dtype=torch.float32, generator=gen).numpy()
+    bias = (torch.randn((K,), dtype=torch.float32, generator=gen) * bias_std).numpy()
     side = None
     if with_side:
         P, Q = out_hw

@@ -1,0 +1,188 @@
+/*
+ * fconv -- fused quantized Conv2D forward pass for GB300 (sm_103a).
+ *
+ * One operation, the vertically fused 2-D convolution forward pass of
+ * TensorFlow's fused int8 kernel ("conv_ops_fused_int8.cc", the
+ * LaunchFusedConv2DOp helpers and BiasActivationOutputKernel):
+ *
+ *   acc[n,p,q,k] = sum_{r,s,c} x[n, p*sh + r - pt, q*sw + s - pl, c] * w[r,s,c,k]
+ *                  (cross-correlation; taps outside the image contribute 0)
+ *   y = float(acc) * conv_scale                  (1) one fp32 rounding
+ *   y = fmaf(float(side), side_scale, y)         (2) only if side != NULL and
+ *                                                    side_scale != 0
+ *   y = y + bias[k]                              (3) one fp32 rounding
+ *   int8 out: clip(round_half_even(y), lower, 127), lower = -128 (BiasAdd)
+ *             or 0 (BiasAdd + Relu)
+ *   bf16 out: bf16_round_nearest_even(relu ? max(y, 0) : y)
+ *
+ * The order (1)(2)(3), each rounded once, is the one that page's epilogue
+ * implements and its comment attributes to cuDNN 8 on sm75+.  int8 sums are
+ * exact (int32 semantics); bf16 sums are fp32.
+ *
+ * Layouts (all row-major, densely packed):
+ *   x    NHWC  [N][H][W][C]         int8 or bf16
+ *   w    HWIO  [R][S][C][K]         same dtype as x
+ *   bias [K]                        fp32
+ *   side NHWC  [N][P][Q][K]         same dtype as the output (nullable)
+ *   y    NHWC  [N][P][Q][K]         int8 or bf16
+ * Output geometry follows the TensorFlow rule on the same page (the comment
+ * on the total padding) and the Im2col output size of
+ * "conv_grad_filter_ops.cc": SAME gives P = ceil(H / sh) with total padding
+ * max(0, (P-1)*sh + R - H), of which the smaller half goes on top and the
+ * odd pixel at the bottom (likewise left/right); VALID gives
+ * P = (H - R) / sh + 1 and no padding.
+ *
+ * The plan lifecycle (create once, run many times with new pointers,
+ * destroy) follows the fusion-plan workflow of MIOpen's "use-fusion-api"
+ * page: plan creation validates and fixes the kernel configuration, runs
+ * only bind buffers.
+ *
+ * Ownership and errors: the caller owns every buffer and the stream; a plan
+ * owns only host memory.  Every call returns a status and never aborts.
+ * Device pointers must be device-accessible memory of the current device.
+ * Runs are asynchronous on the given stream; a kernel that gives up waiting
+ * (a stalled pipeline) records FCONV_ERR_TIMEOUT in a per-device word that
+ * fconv_plan_check() reads.
+ */
+#ifndef FCONV_H_
+#define FCONV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fconv_plan fconv_plan;
+/* A cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *fconv_stream_t;
+
+typedef enum {
+  FCONV_OK = 0,
+  FCONV_ERR_INVALID_VALUE = 1, /* bad dimension, NULL required pointer, ... */
+  FCONV_ERR_NOT_SUPPORTED = 2, /* valid convolution this library does not run */
+  FCONV_ERR_MISALIGNED = 3,    /* pointer or channel count breaks 16-byte rule */
+  FCONV_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  FCONV_ERR_TIMEOUT = 5,       /* a kernel gave up on a pipeline wait */
+  FCONV_ERR_INTERNAL = 6,
+  FCONV_ERR_WORKSPACE = 7      /* workspace missing or smaller than required */
+} fconv_status;
+
+typedef enum { FCONV_SAME = 0, FCONV_VALID = 1 } fconv_padding;
+typedef enum { FCONV_INT8 = 0, FCONV_BF16 = 1 } fconv_dtype;
+/* BiasAdd and BiasAdd+Relu, the two fusions the TensorFlow kernel accepts. */
+typedef enum { FCONV_ACT_NONE = 0, FCONV_ACT_RELU = 1 } fconv_act;
+
+/* Create a plan for one convolution shape.
+ * N,H,W,C: input NHWC extents; K: output channels; R,S: filter height and
+ * width; stride_h/stride_w >= 1; dilation is 1 and groups are 1 by
+ * construction (the filter's input depth is C).
+ * Constraints (else FCONV_ERR_NOT_SUPPORTED): C and K multiples of 16 for
+ * int8 and of 8 for bf16 (16-byte vectors), and every tensor below 2^31
+ * elements.  Non-positive extents, a VALID filter larger than
+ * the input, or an unknown enum give FCONV_ERR_INVALID_VALUE.
+ * Pure host work: needs no GPU.  *plan is set to NULL on failure. */
+fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C,
+                               int K, int R, int S, int stride_h, int stride_w,
+                               fconv_padding padding, fconv_dtype dtype,
+                               fconv_act act);
+
+/* Free a plan (NULL is accepted).  Does not synchronize any stream. */
+fconv_status fconv_plan_destroy(fconv_plan *plan);
+
+/* Output extents [N][P][Q][K]. */
+fconv_status fconv_plan_output_shape(const fconv_plan *plan, int *N, int *P,
+                                     int *Q, int *K);
+
+/* Padding the plan applies: top, bottom, left, right. */
+fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top,
+                                int *pad_bottom, int *pad_left,
+                                int *pad_right);
+
+/* Device scratch bytes fconv_run needs (the filter repacked K-major in
+ * 16-bit form, and for int8 plans the input widened to fp16). */
+fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes);
+
+/* Run the fused convolution on `stream`.
+ * x, w, y: device pointers, 16-byte aligned.  bias: device fp32 [K].
+ * side: device, output shape and dtype, 16-byte aligned, or NULL.
+ * conv_scale, side_scale: host scalars (the TensorFlow GPU helper reads
+ * them as host scalars too).  workspace: device, 256-byte aligned,
+ * workspace_bytes >= fconv_workspace_size().  x/w must not alias y or
+ * the workspace.  Asynchronous; returns after enqueueing. */
+fconv_status fconv_run(fconv_plan *plan, const void *x, const void *w,
+                       const float *bias, const void *side, float conv_scale,
+                       float side_scale, void *y, void *workspace,
+                       size_t workspace_bytes, fconv_stream_t stream);
+
+/* The convolution sums alone, before the epilogue: int32 [N][P][Q][K] for
+ * int8 plans (exact), fp32 for bf16 plans.  Same rules as fconv_run. */
+fconv_status fconv_run_accumulators(fconv_plan *plan, const void *x,
+                                    const void *w, void *acc, void *workspace,
+                                    size_t workspace_bytes,
+                                    fconv_stream_t stream);
+
+/* Bytes of device memory fconv_run_host needs: the workspace plus device
+ * copies of x, w, bias, side (if with_side) and y. */
+fconv_status fconv_host_workspace_size(const fconv_plan *plan, int with_side,
+                                       size_t *bytes);
+
+/* fconv_run on HOST buffers: copies x, w, bias and side (if not NULL) to
+ * `device_workspace`, runs, and copies y back to `y_host`, all enqueued on
+ * `stream`.  Pinned host buffers keep this asynchronous; the caller
+ * synchronizes the stream before reading y_host.  Pageable buffers work
+ * but make the copies synchronous with the host. */
+fconv_status fconv_run_host(fconv_plan *plan, const void *x_host,
+                            const void *w_host, const float *bias_host,
+                            const void *side_host, float conv_scale,
+                            float side_scale, void *y_host,
+                            void *device_workspace, size_t workspace_bytes,
+                            fconv_stream_t stream);
+
+/* Synchronize `stream`, then read and clear the current device's kernel
+ * status word: FCONV_ERR_TIMEOUT if any kernel since the last check gave up
+ * waiting, FCONV_ERR_CUDA if the stream reports an error, else FCONV_OK. */
+fconv_status fconv_plan_check(fconv_plan *plan, fconv_stream_t stream);
+
+/* Override the output-channel tile: 32, 64, 128 or 256 (0 restores the
+ * plan's own choice).  int8 plans whose sums are chunked (more than 960
+ * k-values) accept at most 128.  For benchmarking and tests. */
+fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n);
+
+/* The plan's kernel configuration: output-channel tile, k-blocks summed in
+ * one fp32 accumulator before they are folded into int32 (int8 plans), and
+ * the number of output tiles. */
+fconv_status fconv_plan_get_config(const fconv_plan *plan, int *block_n,
+                                   int *kblocks_per_chunk, int *num_tiles);
+
+/* Limit, in milliseconds, on any single pipeline wait inside the kernel
+ * (default 2000).  After it the kernel stops, records FCONV_ERR_TIMEOUT and
+ * returns. */
+fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms);
+
+/* Test hook: FCONV_DEBUG_DROP_ARRIVE makes the input loaders skip their
+ * "stage full" signal, so the MMA issuer's wait runs out and the kernel
+ * exercises its timeout exit.  0 restores normal runs. */
+#define FCONV_DEBUG_DROP_ARRIVE 1
+fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
+
+/* Record caller-created CUDA events (cudaEvent_t) at the stage boundaries
+ * of every later fconv_run / fconv_run_accumulators on this plan, on the
+ * run's stream: events[0] before the filter pack, events[1] after it,
+ * events[2] after the int8 -> fp16 input widening (same point as events[1]
+ * for bf16 plans), events[3] after the convolution kernel.  NULL disables.
+ * The events must outlive the runs that record them. */
+fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]);
+
+/* Static text for a status code. */
+const char *fconv_status_string(fconv_status status);
+
+/* Detail of the last failing call on this host thread ("" if none). */
+const char *fconv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FCONV_H_ */

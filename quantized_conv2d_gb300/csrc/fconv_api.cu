@@ -1,0 +1,483 @@
+// Host side of the fconv C ABI: plan creation (validation, output
+// geometry, tile choice), workspace layout, tensor-map encoding and the
+// launch sequence of one fused convolution.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "../../include/fconv.h"
+#include "fconv_internal.h"
+
+struct fconv_plan {
+  int N, H, W, C, K, R, S, sh, sw;
+  fconv_padding padding;
+  fconv_dtype dtype;
+  fconv_act act;
+  int P, Q, pt, pb, pl, pr;
+  long long M;
+  int Ktot, num_kb, Kpad;
+  int block_n, kb_chunk, num_n_tiles, num_tiles;
+  int auto_block_n;
+  uint32_t timeout_ms;
+  int debug;
+  size_t wt_bytes, xh_bytes;
+  cudaEvent_t events[4];
+  bool use_events;
+};
+
+namespace {
+
+thread_local std::string t_last_error;
+
+fconv_status fail(fconv_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+fconv_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(FCONV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+constexpr long long kLimit = 0x7FFFFFFFLL;
+
+// Output extent and padding split of one axis under TensorFlow's rule:
+// SAME keeps ceil(in / stride) outputs and pads max(0, (out-1)*stride +
+// filt - in) in total, the smaller half before; VALID pads nothing.
+bool axis_geometry(int in, int filt, int stride, fconv_padding pad, int *out, int *before,
+                   int *after) {
+  if (pad == FCONV_VALID) {
+    if (filt > in) return false;
+    *out = (in - filt) / stride + 1;
+    *before = *after = 0;
+    return true;
+  }
+  const int o = (in + stride - 1) / stride;
+  long long total = static_cast<long long>(o - 1) * stride + filt - in;
+  if (total < 0) total = 0;
+  *out = o;
+  *before = static_cast<int>(total / 2);
+  *after = static_cast<int>(total - total / 2);
+  return true;
+}
+
+int sm_count_of_current_device(int fallback) {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    cudaGetLastError();  // clear the non-sticky error of a GPU-less host
+    return fallback;
+  }
+  return v;
+}
+
+// Output-channel tile: the candidate with the least estimated time, where
+// a tile of BN channels costs about (BN + 64) per k-block (the A gather is
+// paid per tile whatever BN is) and tiles run in waves over the SMs.
+int choose_block_n(const fconv_plan &p, int sms) {
+  const long long m_tiles = (p.M + 127) / 128;
+  const bool chunked = p.kb_chunk < p.num_kb;
+  const int kp = (p.K + 31) / 32 * 32;
+  int best = 32;
+  long long best_cost = -1;
+  for (int bn : {256, 128, 64, 32}) {
+    if (bn > kp) continue;
+    if (chunked && !fconv::block_n_can_chunk(bn)) continue;
+    const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
+    const long long waves = (tiles + sms - 1) / sms;
+    const long long cost = waves * (bn + 64);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+void set_tiling(fconv_plan &p, int bn) {
+  p.block_n = bn;
+  p.num_n_tiles = (p.K + bn - 1) / bn;
+  p.num_tiles = static_cast<int>((p.M + 127) / 128) * p.num_n_tiles;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  std::atomic<int> sm_count{0};
+};
+DeviceInfo g_devices[64];
+
+int device_sm_count(int *dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev_out) *dev_out = dev;
+  if (dev < 0 || dev >= 64) return sm_count_of_current_device(-1);
+  int v = g_devices[dev].sm_count.load();
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    g_devices[dev].sm_count.store(v);
+  }
+  return v;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *bias,
+                     const void *side, float conv_scale, float side_scale, void *y,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream, int mode) {
+  if (!p) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (!x || !w || !y) return fail(FCONV_ERR_INVALID_VALUE, "x, w and y must not be NULL");
+  if (mode == fconv::kModeFused && !bias)
+    return fail(FCONV_ERR_INVALID_VALUE, "bias must not be NULL");
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || (side && !aligned(side, 16)) ||
+      (bias && !aligned(bias, 16)))
+    return fail(FCONV_ERR_MISALIGNED, "x, w, y, side and bias must be 16-byte aligned");
+  const size_t need = p->wt_bytes + p->xh_bytes;
+  if (!workspace || workspace_bytes < need)
+    return fail(FCONV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : static_cast<size_t>(0));
+  if (!aligned(workspace, 256))
+    return fail(FCONV_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+
+  int dev = 0;
+  const int sms = device_sm_count(&dev);
+  if (sms <= 0) return fail(FCONV_ERR_CUDA, "no usable CUDA device");
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (!encode) return fail(FCONV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+
+  const bool is_int8 = p->dtype == FCONV_INT8;
+  auto mark = [&](int i) -> cudaError_t {
+    return p->use_events ? cudaEventRecord(p->events[i], stream) : cudaSuccess;
+  };
+  uint16_t *wt = static_cast<uint16_t *>(workspace);
+  __half *xh = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + p->wt_bytes);
+
+  cudaError_t e = mark(0);
+  if (e != cudaSuccess) return cuda_fail(e, "event record");
+  e = fconv::launch_pack_filter(is_int8, w, wt, p->Ktot, p->K, p->Kpad, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "filter pack launch");
+  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
+  const void *act = x;
+  if (is_int8) {
+    const long long n = static_cast<long long>(p->N) * p->H * p->W * p->C;
+    e = fconv::launch_widen_i8(static_cast<const int8_t *>(x), xh, n, sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "input widen launch");
+    act = xh;
+  }
+  if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
+
+  CUtensorMap tmap;
+  memset(&tmap, 0, sizeof tmap);
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->Kpad), static_cast<cuuint64_t>(p->K)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->Kpad) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(p->block_n)};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(&tmap, is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                       2, wt, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
+
+  fconv::ConvArgs a;
+  memset(&a, 0, sizeof a);
+  a.a = act;
+  a.use_side = (mode == fconv::kModeFused && side != nullptr && side_scale != 0.0f) ? 1 : 0;
+  a.side = a.use_side ? side : nullptr;
+  a.bias = bias;
+  a.y = y;
+  a.N = p->N; a.H = p->H; a.W = p->W; a.C = p->C; a.K = p->K; a.R = p->R; a.S = p->S;
+  a.sh = p->sh; a.sw = p->sw; a.pt = p->pt; a.pl = p->pl; a.P = p->P; a.Q = p->Q;
+  a.M = p->M;
+  a.Ktot = p->Ktot;
+  a.num_kb = p->num_kb;
+  a.kb_chunk = p->kb_chunk;
+  a.num_n_tiles = p->num_n_tiles;
+  a.num_tiles = p->num_tiles;
+  a.conv_scale = conv_scale;
+  a.side_scale = side_scale;
+  a.relu = p->act == FCONV_ACT_RELU ? 1 : 0;
+  a.mode = mode;
+  a.debug = p->debug;
+  a.timeout_ns = static_cast<unsigned long long>(p->timeout_ms) * 1000000ull;
+  const int grid = p->num_tiles < sms ? p->num_tiles : sms;
+  e = fconv::launch_conv(p->block_n, is_int8, tmap, a, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "convolution launch");
+  if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event record");
+  return FCONV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, int K, int R, int S,
+                               int stride_h, int stride_w, fconv_padding padding,
+                               fconv_dtype dtype, fconv_act act) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan output pointer is NULL");
+  *plan = nullptr;
+  if (N <= 0 || H <= 0 || W <= 0 || C <= 0 || K <= 0 || R <= 0 || S <= 0)
+    return fail(FCONV_ERR_INVALID_VALUE, "every extent must be positive");
+  if (stride_h <= 0 || stride_w <= 0) return fail(FCONV_ERR_INVALID_VALUE, "strides must be >= 1");
+  if (padding != FCONV_SAME && padding != FCONV_VALID)
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown padding %d", (int)padding);
+  if (dtype != FCONV_INT8 && dtype != FCONV_BF16)
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown dtype %d", (int)dtype);
+  if (act != FCONV_ACT_NONE && act != FCONV_ACT_RELU)
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown activation %d", (int)act);
+
+  fconv_plan p;
+  memset(&p, 0, sizeof p);
+  p.N = N; p.H = H; p.W = W; p.C = C; p.K = K; p.R = R; p.S = S;
+  p.sh = stride_h; p.sw = stride_w;
+  p.padding = padding; p.dtype = dtype; p.act = act;
+  if (!axis_geometry(H, R, stride_h, padding, &p.P, &p.pt, &p.pb) ||
+      !axis_geometry(W, S, stride_w, padding, &p.Q, &p.pl, &p.pr))
+    return fail(FCONV_ERR_INVALID_VALUE, "VALID padding with a filter larger than the input");
+
+  const int vec = dtype == FCONV_INT8 ? 16 : 8;
+  if (C % vec != 0 || K % vec != 0)
+    return fail(FCONV_ERR_NOT_SUPPORTED,
+                "C and K must be multiples of %d for this dtype (16-byte vectors); got C=%d K=%d",
+                vec, C, K);
+  const long long in_elems = static_cast<long long>(N) * H * W * C;
+  const long long out_elems = static_cast<long long>(N) * p.P * p.Q * K;
+  const long long ktot = static_cast<long long>(R) * S * C;
+  if (in_elems > kLimit || out_elems > kLimit || ktot * K > kLimit)
+    return fail(FCONV_ERR_NOT_SUPPORTED, "a tensor has 2^31 or more elements");
+
+  p.M = static_cast<long long>(N) * p.P * p.Q;
+  p.Ktot = static_cast<int>(ktot);
+  p.num_kb = (p.Ktot + 63) / 64;
+  p.Kpad = p.num_kb * 64;
+  if (dtype == FCONV_INT8 && p.num_kb > fconv::kMaxExactKBlocks) {
+    const int chunks = (p.num_kb + fconv::kMaxExactKBlocks - 1) / fconv::kMaxExactKBlocks;
+    p.kb_chunk = (p.num_kb + chunks - 1) / chunks;
+  } else {
+    p.kb_chunk = p.num_kb;
+  }
+  const long long m_tiles = (p.M + 127) / 128;
+  if (m_tiles * ((K + 31) / 32) > kLimit)
+    return fail(FCONV_ERR_NOT_SUPPORTED, "too many output tiles");
+  p.auto_block_n = choose_block_n(p, sm_count_of_current_device(148));
+  set_tiling(p, p.auto_block_n);
+  p.timeout_ms = 2000;
+  p.wt_bytes = align_up(static_cast<size_t>(K) * p.Kpad * 2, 256);
+  p.xh_bytes = dtype == FCONV_INT8 ? align_up(static_cast<size_t>(in_elems) * 2, 256) : 0;
+
+  fconv_plan *out = new (std::nothrow) fconv_plan(p);
+  if (!out) return fail(FCONV_ERR_INTERNAL, "out of host memory");
+  *plan = out;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_destroy(fconv_plan *plan) {
+  delete plan;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_output_shape(const fconv_plan *plan, int *N, int *P, int *Q, int *K) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (N) *N = plan->N;
+  if (P) *P = plan->P;
+  if (Q) *Q = plan->Q;
+  if (K) *K = plan->K;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top, int *pad_bottom,
+                                int *pad_left, int *pad_right) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (pad_top) *pad_top = plan->pt;
+  if (pad_bottom) *pad_bottom = plan->pb;
+  if (pad_left) *pad_left = plan->pl;
+  if (pad_right) *pad_right = plan->pr;
+  return FCONV_OK;
+}
+
+fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes) {
+  if (!plan || !bytes) return fail(FCONV_ERR_INVALID_VALUE, "plan and bytes must not be NULL");
+  *bytes = plan->wt_bytes + plan->xh_bytes;
+  return FCONV_OK;
+}
+
+fconv_status fconv_run(fconv_plan *plan, const void *x, const void *w, const float *bias,
+                       const void *side, float conv_scale, float side_scale, void *y,
+                       void *workspace, size_t workspace_bytes, fconv_stream_t stream) {
+  return enqueue(plan, x, w, bias, side, conv_scale, side_scale, y, workspace, workspace_bytes,
+                 reinterpret_cast<cudaStream_t>(stream), fconv::kModeFused);
+}
+
+fconv_status fconv_run_accumulators(fconv_plan *plan, const void *x, const void *w, void *acc,
+                                    void *workspace, size_t workspace_bytes,
+                                    fconv_stream_t stream) {
+  return enqueue(plan, x, w, nullptr, nullptr, 1.0f, 0.0f, acc, workspace, workspace_bytes,
+                 reinterpret_cast<cudaStream_t>(stream), fconv::kModeAccumulators);
+}
+
+static void host_layout(const fconv_plan *p, int with_side, size_t off[6]) {
+  const size_t elt = p->dtype == FCONV_INT8 ? 1 : 2;
+  const size_t x_b = static_cast<size_t>(p->N) * p->H * p->W * p->C * elt;
+  const size_t w_b = static_cast<size_t>(p->R) * p->S * p->C * p->K * elt;
+  const size_t b_b = static_cast<size_t>(p->K) * 4;
+  const size_t y_b = static_cast<size_t>(p->M) * p->K * elt;
+  off[0] = 0;                                                 // workspace
+  off[1] = align_up(off[0] + p->wt_bytes + p->xh_bytes, 256);  // x
+  off[2] = align_up(off[1] + x_b, 256);                        // w
+  off[3] = align_up(off[2] + w_b, 256);                        // bias
+  off[4] = align_up(off[3] + b_b, 256);                        // side
+  off[5] = align_up(off[4] + (with_side ? y_b : 0), 256);      // y
+  (void)y_b;
+}
+
+fconv_status fconv_host_workspace_size(const fconv_plan *plan, int with_side, size_t *bytes) {
+  if (!plan || !bytes) return fail(FCONV_ERR_INVALID_VALUE, "plan and bytes must not be NULL");
+  size_t off[6];
+  host_layout(plan, with_side, off);
+  const size_t elt = plan->dtype == FCONV_INT8 ? 1 : 2;
+  *bytes = align_up(off[5] + static_cast<size_t>(plan->M) * plan->K * elt, 256);
+  return FCONV_OK;
+}
+
+fconv_status fconv_run_host(fconv_plan *plan, const void *x_host, const void *w_host,
+                            const float *bias_host, const void *side_host, float conv_scale,
+                            float side_scale, void *y_host, void *device_workspace,
+                            size_t workspace_bytes, fconv_stream_t stream) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (!x_host || !w_host || !bias_host || !y_host)
+    return fail(FCONV_ERR_INVALID_VALUE, "x, w, bias and y must not be NULL");
+  size_t need = 0;
+  fconv_host_workspace_size(plan, side_host != nullptr, &need);
+  if (!device_workspace || workspace_bytes < need)
+    return fail(FCONV_ERR_WORKSPACE, "device workspace of %zu bytes needed", need);
+  if (!aligned(device_workspace, 256))
+    return fail(FCONV_ERR_MISALIGNED, "device workspace must be 256-byte aligned");
+  size_t off[6];
+  host_layout(plan, side_host != nullptr, off);
+  uint8_t *base = static_cast<uint8_t *>(device_workspace);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t elt = plan->dtype == FCONV_INT8 ? 1 : 2;
+  const size_t x_b = static_cast<size_t>(plan->N) * plan->H * plan->W * plan->C * elt;
+  const size_t w_b = static_cast<size_t>(plan->R) * plan->S * plan->C * plan->K * elt;
+  const size_t y_b = static_cast<size_t>(plan->M) * plan->K * elt;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(base + off[1], x_host, x_b, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(base + off[2], w_host, w_b, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(base + off[3], bias_host, static_cast<size_t>(plan->K) * 4,
+                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cuda_fail(e, "host-to-device copy");
+  if (side_host && (e = cudaMemcpyAsync(base + off[4], side_host, y_b, cudaMemcpyHostToDevice,
+                                        st)) != cudaSuccess)
+    return cuda_fail(e, "host-to-device copy of the side input");
+  fconv_status s = enqueue(plan, base + off[1], base + off[2],
+                           reinterpret_cast<const float *>(base + off[3]),
+                           side_host ? base + off[4] : nullptr, conv_scale, side_scale,
+                           base + off[5], base, off[1], st, fconv::kModeFused);
+  if (s != FCONV_OK) return s;
+  if ((e = cudaMemcpyAsync(y_host, base + off[5], y_b, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "device-to-host copy");
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_check(fconv_plan *plan, fconv_stream_t stream) {
+  (void)plan;
+  unsigned int st = 0;
+  cudaError_t e = fconv::status_read_and_clear(reinterpret_cast<cudaStream_t>(stream), &st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream");
+  if (st != 0)
+    return fail(static_cast<fconv_status>(st), "a kernel reported %s",
+                fconv_status_string(static_cast<fconv_status>(st)));
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (block_n == 0) {
+    set_tiling(*plan, plan->auto_block_n);
+    return FCONV_OK;
+  }
+  if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256)
+    return fail(FCONV_ERR_NOT_SUPPORTED, "tile %d: this build has 32, 64, 128 and 256", block_n);
+  if (plan->kb_chunk < plan->num_kb && !fconv::block_n_can_chunk(block_n))
+    return fail(FCONV_ERR_NOT_SUPPORTED,
+                "tile %d leaves no tensor memory for the int32 sums this plan needs", block_n);
+  set_tiling(*plan, block_n);
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_get_config(const fconv_plan *plan, int *block_n, int *kblocks_per_chunk,
+                                   int *num_tiles) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (block_n) *block_n = plan->block_n;
+  if (kblocks_per_chunk) *kblocks_per_chunk = plan->kb_chunk;
+  if (num_tiles) *num_tiles = plan->num_tiles;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms) {
+  if (!plan || ms == 0) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL or timeout is 0");
+  plan->timeout_ms = ms;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (flags & ~FCONV_DEBUG_DROP_ARRIVE) return fail(FCONV_ERR_INVALID_VALUE, "unknown flags");
+  plan->debug = flags;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (!events) {
+    plan->use_events = false;
+    return FCONV_OK;
+  }
+  for (int i = 0; i < 4; ++i)
+    if (!events[i]) return fail(FCONV_ERR_INVALID_VALUE, "event %d is NULL", i);
+  for (int i = 0; i < 4; ++i) plan->events[i] = static_cast<cudaEvent_t>(events[i]);
+  plan->use_events = true;
+  return FCONV_OK;
+}
+
+const char *fconv_status_string(fconv_status s) {
+  switch (s) {
+    case FCONV_OK: return "FCONV_OK";
+    case FCONV_ERR_INVALID_VALUE: return "FCONV_ERR_INVALID_VALUE";
+    case FCONV_ERR_NOT_SUPPORTED: return "FCONV_ERR_NOT_SUPPORTED";
+    case FCONV_ERR_MISALIGNED: return "FCONV_ERR_MISALIGNED";
+    case FCONV_ERR_CUDA: return "FCONV_ERR_CUDA";
+    case FCONV_ERR_TIMEOUT: return "FCONV_ERR_TIMEOUT";
+    case FCONV_ERR_INTERNAL: return "FCONV_ERR_INTERNAL";
+    case FCONV_ERR_WORKSPACE: return "FCONV_ERR_WORKSPACE";
+  }
+  return "FCONV_ERR_UNKNOWN";
+}
+
+const char *fconv_last_error(void) { return t_last_error.c_str(); }
+
+}  // extern "C"

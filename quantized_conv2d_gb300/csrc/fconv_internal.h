@@ -1,0 +1,50 @@
+// Internal interface between the host API (fconv_api.cu) and the kernels
+// (fconv_kernels.cu).  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fconv {
+
+constexpr int kModeFused = 0;         // full epilogue, int8/bf16 output
+constexpr int kModeAccumulators = 1;  // raw sums: int32 (int8 plans) / fp32 (bf16 plans)
+
+// Largest number of 64-wide k-blocks one fp32 accumulation may cover for
+// int8 operands: 15 * 64 = 960 products of magnitude <= 2^14 stay below
+// 2^24, so every partial sum is an exactly representable integer.
+constexpr int kMaxExactKBlocks = 15;
+
+// Everything the convolution kernel needs besides the B-operand tensor map.
+struct ConvArgs {
+  const void *a;       // activations NHWC, 16-bit (fp16 widened from int8, or bf16)
+  const void *side;    // side input NHWC [M][K] (int8 or bf16), or nullptr
+  const float *bias;   // [K]
+  void *y;             // output [M][K] (int8/bf16, or int32/fp32 sums)
+  int N, H, W, C, K, R, S, sh, sw, pt, pl, P, Q;
+  long long M;         // N * P * Q
+  int Ktot;            // R * S * C
+  int num_kb;          // ceil(Ktot / 64)
+  int kb_chunk;        // k-blocks per fp32 accumulation
+  int num_n_tiles;     // ceil(K / BN)
+  int num_tiles;       // ceil(M / 128) * num_n_tiles
+  float conv_scale, side_scale;
+  int relu;
+  int use_side;
+  int mode;
+  int debug;
+  unsigned long long timeout_ns;
+};
+
+cudaError_t launch_conv(int block_n, bool is_int8, const CUtensorMap &tmap_b,
+                        const ConvArgs &args, int grid, cudaStream_t stream);
+bool block_n_can_chunk(int block_n);
+cudaError_t launch_pack_filter(bool is_int8, const void *w, uint16_t *wt, int RSC, int K,
+                               int Kpad, cudaStream_t stream);
+cudaError_t launch_widen_i8(const int8_t *x, __half *xh, long long n, int sm_count,
+                            cudaStream_t stream);
+cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out);
+
+}  // namespace fconv

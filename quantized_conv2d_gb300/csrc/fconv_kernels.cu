@@ -1,0 +1,594 @@
+// Kernels of the fused Conv2D forward pass for sm_103a.
+//
+// The convolution is an implicit GEMM (the im2col view of
+// "conv_grad_filter_ops.cc", Im2col, without materialising the patch
+// matrix):
+//     D[m][n] = sum_k A[m][k] * B[n][k]
+//     m = (n_img, p, q) output pixel, n = output channel,
+//     k = (r, s, c) in the HWIO flattening order,
+//     A[m][k] = x[n_img, p*sh + r - pt, q*sw + s - pl, c] or 0 off the image,
+//     B[n][k] = w[r, s, c, n].
+// D accumulates in fp32 in tensor memory (TMEM) on the 5th-generation tensor
+// cores (tcgen05.mma kind::f16).  sm_103a has no integer tensor-core MMA, so
+// int8 operands are widened to fp16, where every int8 value is exact; each
+// product is then at most 2^14 and exact in fp32, and the plan limits one
+// fp32 accumulation to 960 k-values (15 k-blocks of 64), so every partial
+// sum stays below 2^24 and is exact.  Longer reductions are split into such
+// chunks and the chunks are summed in int32 by the epilogue, which makes the
+// int8 result the exact int32 sum the TensorFlow kernel describes.
+//
+// CTA layout (288 threads, one CTA per SM, persistent over output tiles):
+//   warps 0-3  loaders: gather the 128 x 64 A tile of each k-block with
+//              16-byte cp.async (zero fill for padding taps) into the
+//              128-byte-swizzled K-major layout; thread 0 also issues the
+//              TMA load of the BN x 64 B tile.
+//   warp 4     allocates TMEM; lane 0 issues the MMAs (4 per k-block).
+//   warps 5-8  epilogue (warp w reads TMEM lanes 32*(w%4) .. +31): TMEM -> registers, BiasActivationOutputKernel's
+//              three fp32 steps, rounding, saturation, 16-byte stores.
+// The accumulator is double-buffered in TMEM so the epilogue of one tile
+// overlaps the mainloop of the next.
+#include "fconv_device.cuh"
+#include "fconv_internal.h"
+
+namespace fconv {
+
+constexpr int kBM = 128;                // output pixels per tile (MMA M)
+constexpr int kBK = 64;                 // k-values per k-block (128 bytes of 16-bit)
+constexpr int kThreads = 288;
+constexpr int kLoaderThreads = 128;
+constexpr int kMmaWarp = 4;
+constexpr int kLag = 2;                 // k-blocks of cp.async kept in flight per loader
+
+template <int BN>
+struct Cfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  static constexpr bool kCanChunk = 3 * BN <= 512;
+  static constexpr int kColsNeeded = kCanChunk ? 3 * BN : 2 * BN;
+  static constexpr int kTmemCols = kColsNeeded <= 32    ? 32
+                                   : kColsNeeded <= 64  ? 64
+                                   : kColsNeeded <= 128 ? 128
+                                   : kColsNeeded <= 256 ? 256
+                                                        : 512;
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
+  static_assert(kStages >= kLag + 2, "pipeline too shallow");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+};
+
+struct Smem {
+  uint64_t full_a[8];
+  uint64_t full_b[8];
+  uint64_t empty[8];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
+  return __uint_as_float(b16 << 16);
+}
+
+// Raw int32 sums of one 32-column slice (chunked int8 accumulation).
+__device__ __forceinline__ void store_i32_slice(const ConvArgs &a, long long m, int col0,
+                                                const uint32_t (&u)[32]) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int col = col0 + 4 * g;
+    if (col < a.K)
+      stg_v4(static_cast<uint32_t *>(a.y) + m * a.K + col,
+             make_uint4(u[4 * g], u[4 * g + 1], u[4 * g + 2], u[4 * g + 3]));
+  }
+}
+
+// One 32-column slice of the epilogue for one output row.
+// vals: the 32 pre-epilogue sums as fp32 (exact integers for int8 plans).
+template <bool IS_INT8>
+__device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
+                                               const float (&vals)[32]) {
+  const int K = a.K;
+  if (a.mode == kModeAccumulators) {
+    // raw sums: int32 for int8 plans, fp32 for bf16 plans; 4 columns per store
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int col = col0 + 4 * g;
+      if (col < K) {
+        uint4 o;
+        if (IS_INT8) {
+          o.x = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 0]));
+          o.y = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 1]));
+          o.z = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 2]));
+          o.w = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 3]));
+        } else {
+          o.x = __float_as_uint(vals[4 * g + 0]);
+          o.y = __float_as_uint(vals[4 * g + 1]);
+          o.z = __float_as_uint(vals[4 * g + 2]);
+          o.w = __float_as_uint(vals[4 * g + 3]);
+        }
+        stg_v4(static_cast<uint32_t *>(a.y) + m * K + col, o);
+      }
+    }
+    return;
+  }
+
+  // bias: all lanes read the same addresses (broadcast)
+  float b[32];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int col = col0 + 4 * g;
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col < K) t = __ldg(reinterpret_cast<const float4 *>(a.bias + col));
+    b[4 * g + 0] = t.x;
+    b[4 * g + 1] = t.y;
+    b[4 * g + 2] = t.z;
+    b[4 * g + 3] = t.w;
+  }
+
+  float sd[32];
+  if (a.use_side) {
+    if (IS_INT8) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int col = col0 + 16 * h;
+        uint4 t = make_uint4(0, 0, 0, 0);
+        if (col < K) t = ldg_nc_v4(static_cast<const int8_t *>(a.side) + m * K + col);
+        const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int v = static_cast<int>(static_cast<int8_t>((w4[e >> 2] >> (8 * (e & 3))) & 0xFFu));
+          sd[16 * h + e] = static_cast<float>(v);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int qd = 0; qd < 4; ++qd) {
+        const int col = col0 + 8 * qd;
+        uint4 t = make_uint4(0, 0, 0, 0);
+        if (col < K) t = ldg_nc_v4(static_cast<const __nv_bfloat16 *>(a.side) + m * K + col);
+        const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          sd[8 * qd + e] = bf16_bits_to_float((w4[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+      }
+    }
+  }
+
+  float y[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    // (1) scale; (2) side input, one fused rounding; (3) bias.  Explicit
+    // round-to-nearest intrinsics keep nvcc from contracting (1) and (3).
+    float v = __fmul_rn(vals[i], a.conv_scale);
+    if (a.use_side) v = __fmaf_rn(sd[i], a.side_scale, v);
+    y[i] = __fadd_rn(v, b[i]);
+  }
+
+  if (IS_INT8) {
+    const int lo = a.relu ? 0 : -128;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = col0 + 16 * h;
+      uint32_t w4[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          int r = __float2int_rn(y[16 * h + 4 * g + e]);  // round half to even
+          r = min(max(r, lo), 127);
+          word |= (static_cast<uint32_t>(r) & 0xFFu) << (8 * e);
+        }
+        w4[g] = word;
+      }
+      if (col < K)
+        stg_v4(static_cast<int8_t *>(a.y) + m * K + col, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+    }
+  } else {
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      const int col = col0 + 8 * qd;
+      uint32_t w4[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float v0 = y[8 * qd + 2 * g], v1 = y[8 * qd + 2 * g + 1];
+        if (a.relu) {
+          v0 = fmaxf(v0, 0.0f);
+          v1 = fmaxf(v1, 0.0f);
+        }
+        const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(v0));
+        const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(v1));
+        w4[g] = b0 | (b1 << 16);
+      }
+      if (col < K)
+        stg_v4(static_cast<__nv_bfloat16 *>(a.y) + m * K + col,
+               make_uint4(w4[0], w4[1], w4[2], w4[3]));
+    }
+  }
+}
+
+template <int BN, bool IS_INT8>
+__global__ void __launch_bounds__(kThreads, 1)
+    conv_fprop_kernel(const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
+  using C = Cfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + kStages * C::kABytes;
+  Smem *bars = reinterpret_cast<Smem *>(smem + C::kBarOffset);
+  volatile int *abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t tmo = args.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->full_a[s]), kLoaderThreads);
+      mbar_init(smem_u32(&bars->full_b[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->acc_full[s]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[s]), 4);
+    }
+    mbar_init(smem_u32(&bars->mma_done), 1);
+    bars->abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+
+  const int num_kb = args.num_kb;
+  const int kb_chunk = args.kb_chunk;
+  const int n_chunks = (num_kb + kb_chunk - 1) / kb_chunk;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ loaders
+    const int t = threadIdx.x;
+    const int j = t & 7;            // 16-byte chunk (8 channels) of the 128-byte row
+    const int rsub = t >> 3;        // rows rsub + 16*i, i = 0..7
+    const int Cc = args.C, Hh = args.H, Ww = args.W, Rr = args.R, Ss = args.S;
+    const long long PQ = static_cast<long long>(args.P) * args.Q;
+    const uint16_t *act = static_cast<const uint16_t *>(args.a);
+    uint32_t stage = 0, phase = 0, arr_stage = 0;
+    uint32_t issued = 0;            // TMA issues by thread 0
+    int pending = 0;
+    bool ok = true;
+    const bool drop = (args.debug & 1) != 0;
+
+    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+      const int m_tile = tile / args.num_n_tiles;
+      const int n_tile = tile - m_tile * args.num_n_tiles;
+      int ih0[8], iw0[8];
+      long long off[8];
+      uint32_t rowmask = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const long long m = static_cast<long long>(m_tile) * kBM + rsub + 16 * i;
+        ih0[i] = 0;
+        iw0[i] = 0;
+        off[i] = 0;
+        if (m < args.M) {
+          const long long nimg = m / PQ;
+          const int rem = static_cast<int>(m - nimg * PQ);
+          const int p = rem / args.Q, q = rem - (rem / args.Q) * args.Q;
+          ih0[i] = p * args.sh - args.pt;
+          iw0[i] = q * args.sw - args.pl;
+          off[i] = ((nimg * Hh + ih0[i]) * static_cast<long long>(Ww) + iw0[i]) * Cc;
+          rowmask |= 1u << i;
+        }
+      }
+      // (r, s, c) of this thread's chunk in k-block 0
+      int c = j * 8, r = 0, s = 0;
+      while (c >= Cc) {
+        c -= Cc;
+        if (++s == Ss) { s = 0; ++r; }
+      }
+
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        if (t == 0) {
+          const uint32_t fb = smem_u32(&bars->full_b[stage]);
+          mbar_arrive_expect_tx(fb, C::kBBytes);
+          tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb * kBK, n_tile * BN, fb);
+          ++issued;
+        }
+        const uint32_t a_base = smem_u32(sA + stage * C::kABytes);
+        const bool kvalid = r < Rr;
+        const long long koff = (static_cast<long long>(r) * Ww + s) * Cc + c;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int ih = ih0[i] + r, iw = iw0[i] + s;
+          const bool v = ((rowmask >> i) & 1u) && kvalid && static_cast<unsigned>(ih) < static_cast<unsigned>(Hh) &&
+                         static_cast<unsigned>(iw) < static_cast<unsigned>(Ww);
+          const uint16_t *src = v ? act + off[i] + koff : act;
+          const int row = rsub + 16 * i;
+          cp_async_16(a_base + row * 128 + ((j ^ (row & 7)) << 4), src, v ? 16u : 0u);
+        }
+        cp_async_commit();
+        ++pending;
+        if (pending > kLag) {
+          cp_async_wait<kLag>();
+          fence_proxy_async_smem();
+          if (!drop) mbar_arrive(smem_u32(&bars->full_a[arr_stage]));
+          if (++arr_stage == kStages) arr_stage = 0;
+          --pending;
+        }
+        // advance this thread's chunk by 64 k-values
+        c += kBK;
+        while (c >= Cc) {
+          c -= Cc;
+          if (++s == Ss) { s = 0; ++r; }
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    while (pending > 0) {
+      if (ok && !drop) mbar_arrive(smem_u32(&bars->full_a[arr_stage]));
+      if (++arr_stage == kStages) arr_stage = 0;
+      --pending;
+    }
+    if (t == 0) {
+      // let any B-tile copy still in flight land before the CTA exits (after
+      // an abort); on the normal path every one of them has completed
+      const uint32_t first = issued > static_cast<uint32_t>(kStages) ? issued - kStages : 0;
+      for (uint32_t i = first; i < issued; ++i)
+        mbar_wait_drain(smem_u32(&bars->full_b[i % kStages]), (i / kStages) & 1u, 100000000ull);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+        for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kb_chunk) {
+          const int kb1 = min(kb0 + kb_chunk, num_kb);
+          if (!mbar_wait(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + astage * BN;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(smem_u32(&bars->full_a[stage]), phase, abort_flag, tmo) ||
+                !mbar_wait(smem_u32(&bars->full_b[stage]), phase, abort_flag, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_f16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_commit(smem_u32(&bars->empty[stage]));
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&bars->acc_full[astage]));
+          if (++astage == 2) { astage = 0; aphase ^= 1; }
+        }
+      }
+      // every MMA issued above has completed once this arrives
+      umma_commit(smem_u32(&bars->mma_done));
+      mbar_wait_drain(smem_u32(&bars->mma_done), 0, 1000000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t astage = 0, aphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+      const int m_tile = tile / args.num_n_tiles;
+      const int n_tile = tile - m_tile * args.num_n_tiles;
+      const long long m = static_cast<long long>(m_tile) * kBM + row;
+      const bool mvalid = m < args.M;
+      const int n0 = n_tile * BN;
+      for (int ch = 0; ch < n_chunks; ++ch) {
+        if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_acc = tmem_base + lane_off + astage * BN;
+        const bool last = ch == n_chunks - 1;
+#pragma unroll 1
+        for (int jj = 0; jj < BN / 32; ++jj) {
+          uint32_t v[32];
+          tmem_ld32(t_acc + jj * 32, v);
+          tmem_wait_ld(v);
+          float vals[32];
+          if (IS_INT8 && C::kCanChunk && n_chunks > 1) {
+            // fold this chunk's exact fp32 sums into the int32 running sums
+            const uint32_t t_sum = tmem_base + lane_off + 2 * BN + jj * 32;
+            uint32_t sacc[32];
+            if (ch > 0) {
+              tmem_ld32(t_sum, sacc);
+              tmem_wait_ld(sacc);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sacc[i] = 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              sacc[i] = static_cast<uint32_t>(static_cast<int>(sacc[i]) +
+                                              __float2int_rn(__uint_as_float(v[i])));
+            if (!last) {
+              tmem_st32(t_sum, sacc);
+              continue;
+            }
+            if (args.mode == kModeAccumulators) {
+              if (mvalid) store_i32_slice(args, m, n0 + jj * 32, sacc);
+              continue;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(static_cast<int>(sacc[i]));
+          } else {
+            // + 0.0f turns a -0 sum into the +0 that float(int32 0) gives
+#pragma unroll
+            for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
+          }
+          if (mvalid) epilogue_slice<IS_INT8>(args, m, n0 + jj * 32, vals);
+        }
+        if (!last) tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[astage]));
+        if (++astage == 2) { astage = 0; aphase ^= 1; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------- pre-pass
+// HWIO filter [RSC][K] -> K-major 16-bit [K][Kpad] (zero for k >= RSC);
+// int8 values widen exactly to fp16, bf16 values are copied.
+template <bool IS_INT8>
+__global__ void pack_filter_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt,
+                                   int RSC, int K, int Kpad) {
+  __shared__ uint16_t tile[32][33];
+  const int k0 = blockIdx.y * 32, rsc0 = blockIdx.x * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int rsc = rsc0 + i, k = k0 + threadIdx.x;
+    uint16_t v = 0;
+    if (rsc < RSC && k < K) {
+      const long long e = static_cast<long long>(rsc) * K + k;
+      if (IS_INT8)
+        v = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<const int8_t *>(w)[e])));
+      else
+        v = static_cast<const uint16_t *>(w)[e];
+    }
+    tile[i][threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int k = k0 + i, rsc = rsc0 + threadIdx.x;
+    if (k < K && rsc < Kpad) wt[static_cast<long long>(k) * Kpad + rsc] = tile[threadIdx.x][i];
+  }
+}
+
+// int8 -> fp16 (exact), 16 elements per thread per step; n16 = elements / 16.
+__global__ void widen_i8_kernel(const int8_t *__restrict__ x, __half *__restrict__ xh,
+                                long long n16) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 in = ldg_nc_v4(x + 16 * i);
+    const uint32_t w4[4] = {in.x, in.y, in.z, in.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t word = w4[e >> 1];
+      const int lo = static_cast<int8_t>((word >> (16 * (e & 1))) & 0xFFu);
+      const int hi = static_cast<int8_t>((word >> (16 * (e & 1) + 8)) & 0xFFu);
+      out[e] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
+               (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
+    }
+    stg_v4(xh + 16 * i, make_uint4(out[0], out[1], out[2], out[3]));
+    stg_v4(xh + 16 * i + 8, make_uint4(out[4], out[5], out[6], out[7]));
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+template <int BN, bool IS_INT8>
+static cudaError_t launch_conv_t(const CUtensorMap &tmap, const ConvArgs &args, int grid,
+                                 cudaStream_t stream) {
+  using C = Cfg<BN>;
+  auto kern = conv_fprop_kernel<BN, IS_INT8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmap, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv(int block_n, bool is_int8, const CUtensorMap &tmap, const ConvArgs &args,
+                        int grid, cudaStream_t stream) {
+  // chunked accumulation needs a third TMEM region, and only int8 plans use it
+  if (args.kb_chunk < args.num_kb && (!is_int8 || !block_n_can_chunk(block_n)))
+    return cudaErrorInvalidValue;
+  if (args.kb_chunk <= 0 || grid <= 0) return cudaErrorInvalidValue;
+#define FCONV_CASE(BN)                                                              \
+  case BN:                                                                          \
+    return is_int8 ? launch_conv_t<BN, true>(tmap, args, grid, stream)              \
+                   : launch_conv_t<BN, false>(tmap, args, grid, stream);
+  switch (block_n) {
+    FCONV_CASE(32)
+    FCONV_CASE(64)
+    FCONV_CASE(128)
+    FCONV_CASE(256)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef FCONV_CASE
+}
+
+bool block_n_can_chunk(int block_n) { return 3 * block_n <= 512; }
+
+cudaError_t launch_pack_filter(bool is_int8, const void *w, uint16_t *wt, int RSC, int K,
+                               int Kpad, cudaStream_t stream) {
+  dim3 block(32, 8);
+  dim3 grid((Kpad + 31) / 32, (K + 31) / 32);
+  if (is_int8)
+    pack_filter_kernel<true><<<grid, block, 0, stream>>>(w, wt, RSC, K, Kpad);
+  else
+    pack_filter_kernel<false><<<grid, block, 0, stream>>>(w, wt, RSC, K, Kpad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_widen_i8(const int8_t *x, __half *xh, long long n, int sm_count,
+                            cudaStream_t stream) {
+  const long long n16 = n / 16;
+  if (n16 == 0) return cudaSuccess;
+  long long blocks = (n16 + 255) / 256;
+  const long long cap = static_cast<long long>(sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  widen_i8_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xh, n16);
+  return cudaGetLastError();
+}
+
+cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(unsigned int), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  if (*out != 0) {
+    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice,
+                                stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+  }
+  return e;
+}
+
+}  // namespace fconv

@@ -1,0 +1,182 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+the public header declares, validates arguments and computes the output
+geometry -- all without a GPU (no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import quantized_conv2d_gb300 as fc
+from quantized_conv2d_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fconv.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    fbuild.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fconv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fconv_plan_create", "fconv_run", "fconv_plan_destroy",
+                     "fconv_workspace_size", "fconv_plan_output_shape", "fconv_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(fc.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    for code in range(8):
+        assert fc.fconv_status_string(code).startswith("FCONV_")
+
+
+def _err(fn, *args):
+    with pytest.raises(fc.FconvError) as ei:
+        fn(*args)
+    return ei.value.status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 8, 8, 16, 16, 3, 3, 1, 1, 0, 0, 1), fc.FCONV_ERR_INVALID_VALUE),
+    ((1, 8, 8, 16, 16, 3, 3, 0, 1, 0, 0, 1), fc.FCONV_ERR_INVALID_VALUE),
+    ((1, 8, 8, 16, 16, 3, 3, 1, 1, 7, 0, 1), fc.FCONV_ERR_INVALID_VALUE),
+    ((1, 8, 8, 16, 16, 3, 3, 1, 1, 0, 5, 1), fc.FCONV_ERR_INVALID_VALUE),
+    ((1, 8, 8, 16, 16, 3, 3, 1, 1, 0, 0, 3), fc.FCONV_ERR_INVALID_VALUE),
+    ((1, 2, 8, 16, 16, 3, 3, 1, 1, 1, 0, 1), fc.FCONV_ERR_INVALID_VALUE),   # VALID, R > H
+    ((1, 8, 8, 24, 16, 3, 3, 1, 1, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),   # int8 C % 16
+    ((1, 8, 8, 16, 40, 3, 3, 1, 1, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),   # int8 K % 16
+    ((1, 8, 8, 12, 16, 3, 3, 1, 1, 0, 1, 1), fc.FCONV_ERR_NOT_SUPPORTED),   # bf16 C % 8
+    ((4096, 1024, 1024, 64, 16, 1, 1, 1, 1, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),  # 2^31 elems
+])
+def test_plan_create_rejects(args, status):
+    assert _err(fc.fconv_plan_create, *args) == status
+    assert fc.fconv_last_error() != ""
+
+
+def test_plan_create_accepts_bf16_multiples_of_8():
+    h = fc.fconv_plan_create(1, 8, 8, 24, 40, 3, 3, 1, 1, 0, 1, 1)
+    assert fc.fconv_plan_output_shape(h) == (1, 8, 8, 40)
+    fc.fconv_plan_destroy(h)
+
+
+def _geometry_rows():
+    rows = []
+    for line in open(os.path.join(ROOT, "tests", "golden", "geometry_cases.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            a = line.split()
+            rows.append((int(a[0]), int(a[1]), int(a[2]), a[3], int(a[4])))
+    return rows
+
+
+@pytest.mark.parametrize("row", _geometry_rows())
+def test_plan_geometry_matches_oracle(row):
+    size, filt, stride, pad, out = row
+    pad_code = 0 if pad == "SAME" else 1
+    args = (1, size, 3, 16, 16, filt, 1, stride, 1, pad_code, 0, 1)
+    if out < 0:
+        assert _err(fc.fconv_plan_create, *args) == fc.FCONV_ERR_INVALID_VALUE
+        return
+    h = fc.fconv_plan_create(*args)
+    try:
+        _, P, _, _ = fc.fconv_plan_output_shape(h)
+        top, bottom, _, _ = fc.fconv_plan_padding(h)
+        assert (P, top, bottom) == oracle.out_geometry(size, filt, stride, pad_code)
+    finally:
+        fc.fconv_plan_destroy(h)
+
+
+def test_tile_override_rules():
+    # 3x3x512 int8: 72 k-blocks, so the sums are chunked and need a 3rd TMEM region
+    h = fc.fconv_plan_create(2, 8, 8, 512, 512, 3, 3, 1, 1, 0, 0, 1)
+    try:
+        bn, chunk, _ = fc.fconv_plan_get_config(h)
+        assert chunk == 15 and bn <= 128
+        assert _err(fc.fconv_plan_set_tile, h, 256) == fc.FCONV_ERR_NOT_SUPPORTED
+        assert _err(fc.fconv_plan_set_tile, h, 48) == fc.FCONV_ERR_NOT_SUPPORTED
+        fc.fconv_plan_set_tile(h, 64)
+        assert fc.fconv_plan_get_config(h)[0] == 64
+        fc.fconv_plan_set_tile(h, 0)
+        assert fc.fconv_plan_get_config(h)[0] == bn
+    finally:
+        fc.fconv_plan_destroy(h)
+    # bf16 sums are never chunked: 256 is allowed
+    h = fc.fconv_plan_create(2, 8, 8, 512, 512, 3, 3, 1, 1, 0, 1, 1)
+    try:
+        assert fc.fconv_plan_get_config(h)[1] == 72
+        fc.fconv_plan_set_tile(h, 256)
+    finally:
+        fc.fconv_plan_destroy(h)
+
+
+def test_exact_chunk_bound():
+    # every chunk holds at most 960 k-values: 960 * 128 * 128 < 2^24
+    for C, R in [(16, 1), (64, 3), (256, 3), (512, 3), (512, 5), (1024, 3)]:
+        h = fc.fconv_plan_create(1, 8, 8, C, 16, R, R, 1, 1, 0, 0, 1)
+        try:
+            chunk = fc.fconv_plan_get_config(h)[1]
+            assert chunk * 64 * 128 * 128 < 2 ** 24
+        finally:
+            fc.fconv_plan_destroy(h)
+
+
+def test_run_argument_errors_before_any_launch():
+    h = fc.fconv_plan_create(1, 8, 8, 16, 16, 3, 3, 1, 1, 0, 0, 1)
+    ws = fc.fconv_workspace_size(h)
+    try:
+        A = 1 << 20  # an aligned fake address: never dereferenced, every call fails first
+        assert _err(fc.fconv_run, None, A, A, A, None, 1.0, 0.0, A, A, ws, None) == fc.FCONV_ERR_INVALID_VALUE
+        assert _err(fc.fconv_run, h, None, A, A, None, 1.0, 0.0, A, A, ws, None) == fc.FCONV_ERR_INVALID_VALUE
+        assert _err(fc.fconv_run, h, A, A, None, None, 1.0, 0.0, A, A, ws, None) == fc.FCONV_ERR_INVALID_VALUE
+        assert _err(fc.fconv_run, h, A + 8, A, A, None, 1.0, 0.0, A, A, ws, None) == fc.FCONV_ERR_MISALIGNED
+        assert _err(fc.fconv_run, h, A, A, A, A + 4, 1.0, 0.5, A, A, ws, None) == fc.FCONV_ERR_MISALIGNED
+        assert _err(fc.fconv_run, h, A, A, A, None, 1.0, 0.0, A, A, ws - 1, None) == fc.FCONV_ERR_WORKSPACE
+        assert _err(fc.fconv_run, h, A, A, A, None, 1.0, 0.0, A, None, ws, None) == fc.FCONV_ERR_WORKSPACE
+        assert _err(fc.fconv_run, h, A, A, A, None, 1.0, 0.0, A, A + 16, ws, None) == fc.FCONV_ERR_MISALIGNED
+        assert _err(fc.fconv_plan_set_timeout_ms, h, 0) == fc.FCONV_ERR_INVALID_VALUE
+        assert _err(fc.fconv_plan_set_debug, h, 8) == fc.FCONV_ERR_INVALID_VALUE
+    finally:
+        fc.fconv_plan_destroy(h)
+
+
+def test_workspace_sizes():
+    h = fc.fconv_plan_create(256, 28, 28, 512, 512, 3, 3, 1, 1, 0, 0, 1)
+    try:
+        ws = fc.fconv_workspace_size(h)
+        # fp16 filter [512][4608] + fp16 copy of the input
+        assert ws == 512 * 4608 * 2 + 256 * 28 * 28 * 512 * 2
+        hw = fc.fconv_host_workspace_size(h, True)
+        assert hw >= ws + 3 * 256 * 28 * 28 * 512 + 4608 * 512 + 512 * 4
+    finally:
+        fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create(32, 14, 14, 256, 256, 3, 3, 1, 1, 0, 1, 1)
+    try:
+        assert fc.fconv_workspace_size(h) == 256 * 2304 * 2
+    finally:
+        fc.fconv_plan_destroy(h)
+
+
+def test_binding_and_oracle_are_separate():
+    pkg = os.path.join(ROOT, "quantized_conv2d_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in re.sub(r"#.*|//.*", "", text).lower().replace("oracle-free", ""), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            assert "quantized_conv2d_gb300" not in open(os.path.join(ROOT, "oracle", f)).read()

@@ -1,0 +1,263 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU
+oracle on the same seeded inputs.  int8 outputs and int32 sums must match
+bit for bit; bf16 outputs must meet max relative error <= 2e-2 (|ref|
+floored at 1e-2) and mean absolute error <= 1e-3 against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import fconv_inputs as FI
+import oracle
+import quantized_conv2d_gb300 as fc
+from gpu_util import Case, PAD, bf16_metric, to_dev, to_host, BF16_MAX_REL, BF16_MEAN_ABS
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["small_i8_16x16x32", "resnet_i8_56x56x64", "proj1x1s2_i8_28x28x256", "bf16_14x14x256"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_conv2d_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def workload_case(name, batch=None):
+    wl = FI.WORKLOADS[name]
+    g = oracle.Geometry(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.stride,
+                        PAD[wl.padding])
+    inputs = FI.generate(wl, (g.P, g.Q), batch=batch)
+    n = wl.N if batch is None else batch
+    return Case(n, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.padding, wl.dtype,
+                wl.relu, wl.conv_scale, wl.side_scale, inputs)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_parity(name):
+    c = workload_case(name)
+    acc_ref = c.oracle_acc()
+    c.check_acc(c.accumulators_gpu(), acc_ref)
+    c.check_output(c.run_gpu(), c.oracle_out(acc_ref), unit_variance_bar=True)
+
+
+def test_large_workload_sampled_parity():
+    """N=256 28x28x512 3x3: whole images 0 and 255, plus 3000 random pixels
+    (all 512 channels each), in the launch configuration the benchmark uses."""
+    c = workload_case("large_i8_28x28x512")
+    got = c.run_gpu()
+    acc_gpu = c.accumulators_gpu()
+    for n in (0, c.N - 1):
+        sub = Case(1, c.H, c.W, c.C, c.K, c.R, c.S, c.stride, c.padding, c.dtype, c.relu,
+                   c.conv_scale, c.side_scale,
+                   {"x": c.x[n:n + 1], "w": c.w, "bias": c.bias, "side": c.side[n:n + 1]})
+        acc = sub.oracle_acc()
+        c.check_acc(acc_gpu[n:n + 1], acc)
+        c.check_output(got[n:n + 1], sub.oracle_out(acc))
+    rng = np.random.default_rng(0)
+    N, P, Q, K = got.shape
+    pix = rng.choice(N * P * Q, size=3000, replace=False)
+    idx = (pix[:, None] * K + np.arange(K)[None, :]).ravel()
+    acc = oracle.conv_acc_i8_points(c.x, c.w, idx, c.stride, PAD[c.padding]).reshape(-1, K)
+    assert np.array_equal(acc_gpu.reshape(-1, K)[pix], acc)
+    ref = oracle.epilogue_i8(acc, c.bias, c.side.reshape(-1, K)[pix], c.conv_scale,
+                             c.side_scale, c.relu)
+    assert np.array_equal(got.reshape(-1, K)[pix], ref)
+
+
+SWEEP = [
+    # N, H, W, C, K, R, S, stride, padding, side, relu
+    (1, 1, 1, 16, 16, 1, 1, 1, "SAME", False, False),
+    (1, 5, 7, 16, 48, 3, 3, 1, "SAME", True, True),
+    (2, 9, 11, 48, 80, 3, 3, 2, "SAME", True, False),      # odd sizes, stride 2, odd pads
+    (3, 8, 8, 32, 16, 3, 3, 2, "SAME", False, True),       # total pad 1: 0 before, 1 after
+    (1, 13, 6, 80, 144, 5, 5, 1, "SAME", True, True),      # K tail over 128 / 64 / 32 tiles
+    (2, 2, 3, 16, 32, 3, 3, 1, "SAME", False, False),      # image smaller than the filter
+    (2, 10, 10, 64, 64, 3, 3, (1, 2), "SAME", True, True),
+    (4, 7, 7, 16, 32, 2, 4, 1, "VALID", False, False),
+    (1, 7, 7, 128, 32, 7, 7, 1, "VALID", True, True),      # full-window VALID = matmul
+    (5, 6, 6, 256, 256, 1, 1, 1, "SAME", False, False),    # 1x1 stride 1 = matmul
+    (3, 17, 15, 32, 96, 3, 3, 3, "SAME", True, False),
+    (1, 30, 30, 1024, 32, 3, 3, 1, "SAME", True, True),    # 9216 k-values: 10 chunks
+    (2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True),    # 4608 k-values, K tail
+    (7, 9, 9, 16, 16, 1, 1, 2, "VALID", True, False),
+]
+
+
+def sweep_case(i, params, dtype):
+    N, H, W, C, K, R, S, stride, pad, side, relu = params
+    sh, sw = (stride, stride) if isinstance(stride, int) else stride
+    P, _, _ = oracle.out_geometry(H, R, sh, PAD[pad])
+    Q, _, _ = oracle.out_geometry(W, S, sw, PAD[pad])
+    inputs = FI.random_case(1000 + i, N, H, W, C, K, R, S, dtype, (P, Q), side,
+                            bias_std=1.0 if dtype == "int8" else 0.1)
+    cs = 0.001 if dtype == "int8" else 1.0
+    return Case(N, H, W, C, K, R, S, (sh, sw), pad, dtype, relu, cs, 0.25 if side else 0.0,
+                inputs)
+
+
+@pytest.mark.parametrize("i,params", list(enumerate(SWEEP)))
+def test_sweep_int8(i, params):
+    c = sweep_case(i, params, "int8")
+    acc_ref = c.oracle_acc()
+    c.check_acc(c.accumulators_gpu(), acc_ref)
+    c.check_output(c.run_gpu(), c.oracle_out(acc_ref))
+
+
+@pytest.mark.parametrize("i,params", [(i, p) for i, p in enumerate(SWEEP) if p[3] % 8 == 0])
+def test_sweep_bf16(i, params):
+    c = sweep_case(i, params, "bf16")
+    acc_ref = c.oracle_acc()
+    c.check_acc(c.accumulators_gpu(), acc_ref)
+    c.check_output(c.run_gpu(), c.oracle_out(acc_ref))
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+def test_every_tile_gives_the_same_result(dtype):
+    c = sweep_case(50, (2, 9, 9, 64, 256, 3, 3, 1, "SAME", True, True), dtype)
+    ref = c.oracle_out()
+    outs = {}
+    for bn in (32, 64, 128, 256):
+        try:
+            outs[bn] = c.run_gpu(block_n=bn)
+        except fc.FconvError as e:
+            assert e.status == fc.FCONV_ERR_NOT_SUPPORTED
+            continue
+        c.check_output(outs[bn], ref)
+    assert len(outs) >= 3
+    if dtype == "int8":
+        first = next(iter(outs.values()))
+        for v in outs.values():
+            assert np.array_equal(v, first)
+
+
+@pytest.mark.parametrize("xv,wv", [(127, 127), (-128, -128), (-128, 127), (None, None)])
+def test_chunked_sums_are_exact_at_extreme_magnitudes(xv, wv):
+    """Sums far beyond 2^24 (up to 9*1024*16384), where a single fp32
+    accumulation would round: the int32 folding of exact chunks must give
+    the exact sum."""
+    N, H, W, C, K = 2, 6, 6, 1024, 32
+    rng = np.random.default_rng(7)
+    if xv is None:
+        x = rng.choice(np.array([-128, 127, 127, 126], np.int8), size=(N, H, W, C))
+        w = rng.choice(np.array([-128, 127, -127], np.int8), size=(3, 3, C, K))
+    else:
+        x = np.full((N, H, W, C), xv, np.int8)
+        w = np.full((3, 3, C, K), wv, np.int8)
+    inputs = {"x": x, "w": w, "bias": np.zeros(K, np.float32), "side": None}
+    c = Case(N, H, W, C, K, 3, 3, 1, "SAME", "int8", False, 1e-7, 0.0, inputs)
+    acc_ref = c.oracle_acc()
+    assert np.abs(acc_ref).max() > 2 ** 24 or xv is None
+    c.check_acc(c.accumulators_gpu(), acc_ref)
+    c.check_output(c.run_gpu(), c.oracle_out(acc_ref))
+
+
+def test_epilogue_rounding_order_cases():
+    """Inputs on which any other arrangement of the three fp32 steps changes
+    the int8 result (found by exact rational search): each sum is built by a
+    1x1 conv over 32 channels, w = (127, ..., 127, 1)."""
+    from epilogue_cases import discriminating_groups
+    C, K = 32, 16
+    groups = discriminating_groups()
+    assert groups
+    for (cs, ss, bias, relu), rows in groups:
+        M = len(rows)
+        x = np.zeros((M, 1, 1, C), np.int8)
+        for i, (acc, _, _) in enumerate(rows):
+            q, r = divmod(acc, 127)
+            if r > 63:
+                q, r = q + 1, r - 127
+            # spread q over 31 channels of weight 127, r on the weight-1 channel
+            parts = np.full(31, q // 31, np.int64)
+            parts[: q % 31] += 1
+            assert np.abs(parts).max() <= 127 and abs(r) <= 127
+            x[i, 0, 0, :31] = parts
+            x[i, 0, 0, 31] = r
+            assert int(x[i, 0, 0, :31].astype(np.int64).sum()) * 127 + int(x[i, 0, 0, 31]) == acc
+        w = np.zeros((1, 1, C, K), np.int8)
+        w[0, 0, :31, :] = 127
+        w[0, 0, 31, :] = 1
+        side = None
+        if ss != 0.0:
+            side = np.zeros((M, 1, 1, K), np.int8)
+            for i, (_, s, _) in enumerate(rows):
+                side[i] = s
+        inputs = {"x": x, "w": w, "bias": np.full(K, bias, np.float32), "side": side}
+        c = Case(M, 1, 1, C, K, 1, 1, 1, "SAME", "int8", relu, cs, ss, inputs)
+        got = c.run_gpu()
+        expect = np.array([r[2] for r in rows], np.int8)
+        assert np.array_equal(got[:, 0, 0, :], np.repeat(expect[:, None], K, axis=1)), (cs, ss, bias)
+        assert np.array_equal(got, c.oracle_out())
+
+
+def test_side_stream_and_guard_bytes():
+    c = sweep_case(60, (3, 11, 9, 48, 48, 3, 3, 1, "SAME", True, True), "int8")
+    p = c.plan()
+    x, w = to_dev(c.x, "int8"), to_dev(c.w, "int8")
+    bias = torch.from_numpy(c.bias).cuda()
+    side = to_dev(c.side, "int8")
+    n_out = int(np.prod(p.out_shape))
+    guard = torch.full((n_out + 4096,), 0x5A, dtype=torch.int8, device="cuda")
+    y = guard[:n_out].view(p.out_shape)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        p.run(x, w, bias, side, c.conv_scale, c.side_scale, y=y, stream=s)
+    p.check(s)
+    assert torch.all(guard[n_out:] == 0x5A)
+    c.check_output(to_host(y), c.oracle_out())
+    p.close()
+
+
+def test_run_host_buffers():
+    c = workload_case("small_i8_16x16x32")
+    p = c.plan()
+    nbytes = fc.fconv_host_workspace_size(p.handle, False)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    xh = torch.from_numpy(c.x).pin_memory()
+    wh = torch.from_numpy(c.w).pin_memory()
+    bh = torch.from_numpy(c.bias).pin_memory()
+    yh = torch.empty(p.out_shape, dtype=torch.int8).pin_memory()
+    s = torch.cuda.current_stream()
+    fc.fconv_run_host(p.handle, xh.data_ptr(), wh.data_ptr(), bh.data_ptr(), None, c.conv_scale,
+                      c.side_scale, yh.data_ptr(), dev.data_ptr(), nbytes, s.cuda_stream)
+    p.check()
+    c.check_output(yh.numpy(), c.oracle_out())
+    p.close()
+
+
+def test_timeout_exit_keeps_context_usable():
+    """A loader that never signals 'stage full' makes the MMA issuer's wait
+    run out: the kernel must stop, report FCONV_ERR_TIMEOUT, and the next run
+    must work."""
+    c = sweep_case(70, (1, 8, 8, 16, 16, 3, 3, 1, "SAME", False, True), "int8")
+    p = c.plan()
+    fc.fconv_plan_set_timeout_ms(p.handle, 50)
+    fc.fconv_plan_set_debug(p.handle, fc.FCONV_DEBUG_DROP_ARRIVE)
+    x, w = to_dev(c.x, "int8"), to_dev(c.w, "int8")
+    bias = torch.from_numpy(c.bias).cuda()
+    p.run(x, w, bias, None, c.conv_scale, 0.0)
+    with pytest.raises(fc.FconvError) as ei:
+        p.check()
+    assert ei.value.status == fc.FCONV_ERR_TIMEOUT
+    fc.fconv_plan_set_debug(p.handle, 0)
+    y = p.run(x, w, bias, None, c.conv_scale, 0.0)
+    p.check()
+    c.check_output(to_host(y), c.oracle_out())
+    p.close()
+
+
+def test_misaligned_device_pointer_is_rejected():
+    c = sweep_case(80, (1, 8, 8, 16, 16, 3, 3, 1, "SAME", False, True), "int8")
+    p = c.plan()
+    buf = torch.zeros(8 * 8 * 16 + 64, dtype=torch.int8, device="cuda")
+    w = to_dev(c.w, "int8")
+    bias = torch.from_numpy(c.bias).cuda()
+    y = p.new_output()
+    with pytest.raises(fc.FconvError) as ei:
+        fc.fconv_run(p.handle, buf.data_ptr() + 1, w.data_ptr(), bias.data_ptr(), None, 1.0, 0.0,
+                     y.data_ptr(), p.workspace.data_ptr(), p.workspace.numel(),
+                     torch.cuda.current_stream().cuda_stream)
+    assert ei.value.status == fc.FCONV_ERR_MISALIGNED
+    p.close()
