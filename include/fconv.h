@@ -175,6 +175,27 @@ fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
  * The events must outlive the runs that record them. */
 fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]);
 
+/* fconv_run for callers that cannot allocate device memory: a plugin inside
+ * an engine that owns the whole device-memory budget, a latency-bound loop
+ * where cudaMalloc/cudaFree (which can synchronize the device) is not
+ * acceptable, or code limited to memory reserved at start-up.  The pages
+ * have no counterpart of this call; it is a property of this library.
+ * Same arguments and results as fconv_run, minus the workspace: the scratch
+ * comes from a 32 MiB array the library reserves on every device that loads
+ * it (held until the process exits).  Plans whose fconv_workspace_size()
+ * exceeds 32 MiB get FCONV_ERR_WORKSPACE.  The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ * The first call on each device looks up the array's device address (a
+ * one-time set-up with that device current); make that first call before
+ * any stream capture.  All calls on a device share the array and it keeps
+ * the previous call's contents; each call writes every scratch byte it
+ * reads, so nothing needs clearing, but calls whose kernels overlap on the
+ * GPU (other streams, other host threads) race on it: serialize them. */
+fconv_status fconv_run_no_alloc(fconv_plan *plan, const void *x, const void *w,
+                                const float *bias, const void *side,
+                                float conv_scale, float side_scale, void *y,
+                                fconv_stream_t stream);
+
 /* Static text for a status code. */
 const char *fconv_status_string(fconv_status status);
 

@@ -70,6 +70,7 @@ def _load():
         "fconv_plan_set_timeout_ms": [p, u32],
         "fconv_plan_set_debug": [p, i32],
         "fconv_plan_set_stage_events": [p, ctypes.POINTER(ctypes.c_void_p)],
+        "fconv_run_no_alloc": [p, p, p, p, p, f32, f32, p, p],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -130,6 +131,13 @@ def fconv_run(plan, x, w, bias, side, conv_scale, side_scale, y, workspace, work
               stream) -> None:
     _check(_load().fconv_run(plan, x, w, bias, side, conv_scale, side_scale, y, workspace,
                              workspace_bytes, stream), "fconv_run")
+
+
+def fconv_run_no_alloc(plan, x, w, bias, side, conv_scale, side_scale, y, stream) -> None:
+    """fconv_run with scratch from the library's built-in 32 MiB device array,
+    for callers that cannot allocate device memory."""
+    _check(_load().fconv_run_no_alloc(plan, x, w, bias, side, conv_scale, side_scale, y, stream),
+           "fconv_run_no_alloc")
 
 
 def fconv_run_accumulators(plan, x, w, acc, workspace, workspace_bytes, stream) -> None:

@@ -3,7 +3,7 @@
     python -m quantized_conv2d_gb300.build [--force] [--verbose]
 
 Produces quantized_conv2d_gb300/libfconv.so (C ABI declared in
-include/fconv.h).  The two translation units compile in parallel.
+include/fconv.h).  The translation units compile in parallel.
 """
 from __future__ import annotations
 
@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfconv.so")
-SOURCES = ["fconv_kernels.cu", "fconv_api.cu"]
+SOURCES = ["fconv_kernels.cu", "fconv_api.cu", "fconv_no_alloc.cu"]
 HEADERS = ["fconv_device.cuh", "fconv_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -233,6 +233,20 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
 
 }  // namespace
 
+namespace fconv {
+// Record the detail fconv_last_error() returns, for other translation units.
+fconv_status record_error(fconv_status st, const char *msg) { return fail(st, "%s", msg); }
+
+// The fused run with a caller-chosen workspace, for other translation units
+// of this library (the no-allocation entry point).
+fconv_status enqueue_fused(fconv_plan *p, const void *x, const void *w, const float *bias,
+                           const void *side, float conv_scale, float side_scale, void *y,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return enqueue(p, x, w, bias, side, conv_scale, side_scale, y, workspace, workspace_bytes,
+                 stream, kModeFused);
+}
+}  // namespace fconv
+
 extern "C" {
 
 fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, int K, int R, int S,
