@@ -161,10 +161,13 @@ fconv_status fconv_plan_get_config(const fconv_plan *plan, int *block_n,
  * returns. */
 fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms);
 
-/* Test hook: FCONV_DEBUG_DROP_ARRIVE makes the input loaders skip their
+/* Test hooks.  FCONV_DEBUG_DROP_ARRIVE makes the input loaders skip their
  * "stage full" signal, so the MMA issuer's wait runs out and the kernel
- * exercises its timeout exit.  0 restores normal runs. */
+ * exercises its timeout exit.  FCONV_DEBUG_GATHER_CPASYNC makes plans whose
+ * channel count allows the TMA im2col input gather (C % 64 == 0) use the
+ * general cp.async gather instead.  0 restores normal runs. */
 #define FCONV_DEBUG_DROP_ARRIVE 1
+#define FCONV_DEBUG_GATHER_CPASYNC 2
 fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
 
 /* Record caller-created CUDA events (cudaEvent_t) at the stage boundaries

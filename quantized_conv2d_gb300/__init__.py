@@ -29,6 +29,7 @@ FCONV_SAME, FCONV_VALID = 0, 1
 FCONV_INT8, FCONV_BF16 = 0, 1
 FCONV_ACT_NONE, FCONV_ACT_RELU = 0, 1
 FCONV_DEBUG_DROP_ARRIVE = 1
+FCONV_DEBUG_GATHER_CPASYNC = 2
 
 
 class FconvError(RuntimeError):

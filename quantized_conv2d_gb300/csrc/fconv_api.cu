@@ -82,9 +82,31 @@ int sm_count_of_current_device(int fallback) {
   return v;
 }
 
-// Output-channel tile: the candidate with the least estimated time, where
-// a tile of BN channels costs about (BN + 64) per k-block (the A gather is
-// paid per tile whatever BN is) and tiles run in waves over the SMs.
+// The A tile can be loaded by one TMA im2col copy when a k-block never
+// straddles two filter taps (C % 64 == 0) and the convolution fits the
+// tensor map's limits for a 4-D tensor: bounding-box corners in [-128, 127],
+// traversal strides <= 8, filter offsets small.
+bool im2col_ok(const fconv_plan &p) {
+  if (p.C % 64 != 0 || p.sh > 8 || p.sw > 8 || p.R > 16 || p.S > 16) return false;
+  const int corners[4] = {-p.pl, -p.pt, p.pr - (p.S - 1), p.pb - (p.R - 1)};
+  for (int c : corners)
+    if (c < -128 || c > 127) return false;
+  return true;
+}
+
+// The gather a run uses for a given tile: TMA im2col when the shape and
+// tile allow it, else the general cp.async gather.
+fconv::Gather gather_for(const fconv_plan &p, int bn, bool force_cpasync) {
+  const bool chunked = p.kb_chunk < p.num_kb;
+  if (!force_cpasync && im2col_ok(p) && fconv::gather_supports(fconv::Gather::kTmaIm2col, bn, chunked))
+    return fconv::Gather::kTmaIm2col;
+  return fconv::Gather::kCpAsync;
+}
+
+// Output-channel tile: the candidate with the least estimated time.  A
+// k-block costs about max(2*BN, G) cycles: the 128 x BN x 64 MMA takes ~2*BN
+// and loading the 16 KB A tile costs a fixed G (~600 cycles by TMA im2col,
+// ~800 by cp.async) whatever BN is; tiles run in waves over the SMs.
 int choose_block_n(const fconv_plan &p, int sms) {
   const long long m_tiles = (p.M + 127) / 128;
   const bool chunked = p.kb_chunk < p.num_kb;
@@ -93,10 +115,12 @@ int choose_block_n(const fconv_plan &p, int sms) {
   long long best_cost = -1;
   for (int bn : {256, 128, 64, 32}) {
     if (bn > kp) continue;
-    if (chunked && !fconv::block_n_can_chunk(bn)) continue;
+    const fconv::Gather g = gather_for(p, bn, false);
+    if (!fconv::gather_supports(g, bn, chunked)) continue;
+    const long long fixed = g == fconv::Gather::kTmaIm2col ? 600 : 800;
     const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
     const long long waves = (tiles + sms - 1) / sms;
-    const long long cost = waves * (bn + 64);
+    const long long cost = waves * (2 * bn > fixed ? 2 * bn : fixed);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = bn;
@@ -109,6 +133,22 @@ void set_tiling(fconv_plan &p, int bn) {
   p.block_n = bn;
   p.num_n_tiles = (p.K + bn - 1) / bn;
   p.num_tiles = static_cast<int>((p.M + 127) / 128) * p.num_n_tiles;
+}
+
+PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeIm2col_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -203,6 +243,37 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
 
+  const fconv::Gather gather =
+      gather_for(*p, p->block_n, (p->debug & FCONV_DEBUG_GATHER_CPASYNC) != 0);
+  if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb))
+    return fail(FCONV_ERR_NOT_SUPPORTED,
+                "tile %d has no cp.async kernel for a sum of %d k-values (chunked sums need "
+                "BN <= 128 there)", p->block_n, p->Ktot);
+  CUtensorMap tmap_a;
+  memset(&tmap_a, 0, sizeof tmap_a);
+  if (gather == fconv::Gather::kTmaIm2col) {
+    PFN_cuTensorMapEncodeIm2col_v12000 enc_a = encode_im2col_fn();
+    if (!enc_a) return fail(FCONV_ERR_CUDA, "cuTensorMapEncodeIm2col is unavailable");
+    // NHWC, innermost first: C, W, H, N.  The bounding box of filter-window
+    // origins runs from -pad_before to (extent - 1) + pad_after - (filter - 1).
+    const cuuint64_t adim[4] = {static_cast<cuuint64_t>(p->C), static_cast<cuuint64_t>(p->W),
+                                static_cast<cuuint64_t>(p->H), static_cast<cuuint64_t>(p->N)};
+    const cuuint64_t astride[3] = {static_cast<cuuint64_t>(p->C) * 2,
+                                   static_cast<cuuint64_t>(p->W) * p->C * 2,
+                                   static_cast<cuuint64_t>(p->H) * p->W * p->C * 2};
+    const int lower[2] = {-p->pl, -p->pt};
+    const int upper[2] = {p->pr - (p->S - 1), p->pb - (p->R - 1)};
+    const cuuint32_t traverse[4] = {1, static_cast<cuuint32_t>(p->sw),
+                                    static_cast<cuuint32_t>(p->sh), 1};
+    CUresult cra = enc_a(&tmap_a,
+                         is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         4, const_cast<void *>(act), adim, astride, lower, upper, 64, 128, traverse,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cra != CUDA_SUCCESS)
+      return fail(FCONV_ERR_INTERNAL, "im2col tensor map encode failed (%d)", (int)cra);
+  }
+
   fconv::ConvArgs a;
   memset(&a, 0, sizeof a);
   a.a = act;
@@ -225,8 +296,10 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.debug = p->debug;
   a.timeout_ns = static_cast<unsigned long long>(p->timeout_ms) * 1000000ull;
   const int grid = p->num_tiles < sms ? p->num_tiles : sms;
-  e = fconv::launch_conv(p->block_n, is_int8, tmap, a, grid, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "convolution launch");
+  e = fconv::launch_conv(p->block_n, is_int8, gather, tmap_a, tmap, a, grid, stream);
+  if (e != cudaSuccess)
+    return fail(FCONV_ERR_CUDA, "convolution launch: %s (%s)", cudaGetErrorString(e),
+                fconv::last_launch_note());
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event record");
   return FCONV_OK;
 }
@@ -436,7 +509,8 @@ fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
   }
   if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256)
     return fail(FCONV_ERR_NOT_SUPPORTED, "tile %d: this build has 32, 64, 128 and 256", block_n);
-  if (plan->kb_chunk < plan->num_kb && !fconv::block_n_can_chunk(block_n))
+  if (!fconv::gather_supports(gather_for(*plan, block_n, false), block_n,
+                              plan->kb_chunk < plan->num_kb))
     return fail(FCONV_ERR_NOT_SUPPORTED,
                 "tile %d leaves no tensor memory for the int32 sums this plan needs", block_n);
   set_tiling(*plan, block_n);
@@ -460,7 +534,8 @@ fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms) {
 
 fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags) {
   if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
-  if (flags & ~FCONV_DEBUG_DROP_ARRIVE) return fail(FCONV_ERR_INVALID_VALUE, "unknown flags");
+  if (flags & ~(FCONV_DEBUG_DROP_ARRIVE | FCONV_DEBUG_GATHER_CPASYNC))
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown flags");
   plan->debug = flags;
   return FCONV_OK;
 }

@@ -133,6 +133,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// 4-D im2col load (NHWC tensor map): pixelsPerColumn output pixels starting
+// at the filter-window origin (w, h, n) of the first one, walking the
+// tensor map's bounding box with its traversal strides, each pixel shifted by
+// the filter tap (off_w, off_h); channelsPerPixel channels from c.  Pixels
+// outside the tensor read as zero.  c * element size must be a multiple of
+// 16 bytes.
+__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap *map, int c,
+                                                   int w, int h, int n, uint16_t off_w,
+                                                   uint16_t off_h, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar),
+      "h"(off_w), "h"(off_h)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -244,6 +261,18 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
          | ((bf16 ? 1u : 0u) << 10)             // B format
          | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+
+// Warpgroup-wide register re-allocation (all 128 threads of a warpgroup
+// execute it).  dec returns registers to the CTA's pool; inc waits until the
+// pool can supply them.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------- globals

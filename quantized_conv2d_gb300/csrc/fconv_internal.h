@@ -38,13 +38,24 @@ struct ConvArgs {
   unsigned long long timeout_ns;
 };
 
-cudaError_t launch_conv(int block_n, bool is_int8, const CUtensorMap &tmap_b,
-                        const ConvArgs &args, int grid, cudaStream_t stream);
-bool block_n_can_chunk(int block_n);
+// How the kernel gathers the A (activation) tile of each k-block.
+enum class Gather {
+  kCpAsync = 0,  // 16-byte cp.async per (pixel, 8 channels) with zero fill; any C % 8 == 0
+  kTmaIm2col = 1 // one TMA im2col load of 128 pixels x 64 channels; needs C % 64 == 0
+};
+
+cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensorMap &tmap_a,
+                        const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
+                        cudaStream_t stream);
+// Whether a gather mode has a kernel for this output-channel tile; chunked
+// int8 sums on the cp.async path need a third TMEM region (BN <= 128).
+bool gather_supports(Gather gather, int block_n, bool chunked);
 cudaError_t launch_pack_filter(bool is_int8, const void *w, uint16_t *wt, int RSC, int K,
                                int Kpad, cudaStream_t stream);
 cudaError_t launch_widen_i8(const int8_t *x, __half *xh, long long n, int sm_count,
                             cudaStream_t stream);
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out);
+// Resource description of the kernel whose launch failed last on this thread.
+const char *last_launch_note();
 
 }  // namespace fconv

@@ -18,15 +18,20 @@
 // int8 result the exact int32 sum the TensorFlow kernel describes.
 //
 // CTA layout (288 threads, one CTA per SM, persistent over output tiles):
-//   warps 0-3  loaders: gather the 128 x 64 A tile of each k-block with
-//              16-byte cp.async (zero fill for padding taps) into the
-//              128-byte-swizzled K-major layout; thread 0 also issues the
-//              TMA load of the BN x 64 B tile.
+//   warps 0-3  loaders.  When C % 64 == 0, thread 0 alone loads each
+//              k-block with two TMA copies: the 128 x 64 A tile by an im2col
+//              load (the hardware walks the output pixels and zero-fills
+//              padding taps) and the BN x 64 B tile by a tiled load.
+//              Otherwise all 128 threads gather the A tile with 16-byte
+//              cp.async (zero fill for padding taps) into the same
+//              128-byte-swizzled K-major layout and thread 0 loads B by TMA.
 //   warp 4     allocates TMEM; lane 0 issues the MMAs (4 per k-block).
 //   warps 5-8  epilogue (warp w reads TMEM lanes 32*(w%4) .. +31): TMEM -> registers, BiasActivationOutputKernel's
 //              three fp32 steps, rounding, saturation, 16-byte stores.
 // The accumulator is double-buffered in TMEM so the epilogue of one tile
 // overlaps the mainloop of the next.
+#include <cstdio>
+
 #include "fconv_device.cuh"
 #include "fconv_internal.h"
 
@@ -37,7 +42,6 @@ constexpr int kBK = 64;                 // k-values per k-block (128 bytes of 16
 constexpr int kThreads = 288;
 constexpr int kLoaderThreads = 128;
 constexpr int kMmaWarp = 4;
-constexpr int kLag = 2;                 // k-blocks of cp.async kept in flight per loader
 
 template <int BN>
 struct Cfg {
@@ -46,6 +50,9 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages0 = (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  // k-blocks of cp.async each loader keeps in flight beyond the newest one:
+  // all stages but two (one being consumed by the MMA, one being refilled)
+  static constexpr int kLag = kStages - 2;
   static constexpr bool kCanChunk = 3 * BN <= 512;
   static constexpr int kColsNeeded = kCanChunk ? 3 * BN : 2 * BN;
   static constexpr int kTmemCols = kColsNeeded <= 32    ? 32
@@ -55,7 +62,7 @@ struct Cfg {
                                                         : 512;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
-  static_assert(kStages >= kLag + 2, "pipeline too shallow");
+  static_assert(kLag >= 2, "pipeline too shallow");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
 };
 
@@ -86,8 +93,10 @@ __device__ __forceinline__ void store_i32_slice(const ConvArgs &a, long long m, 
   }
 }
 
-// One 32-column slice of the epilogue for one output row.
+// One 32-column slice of the epilogue for one output row, streamed in
+// groups of 16 (int8) or 8 (bf16) columns so few values are live at once.
 // vals: the 32 pre-epilogue sums as fp32 (exact integers for int8 plans).
+// Columns at or beyond K are skipped (K is a multiple of the group width).
 template <bool IS_INT8>
 __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
                                                const float (&vals)[32]) {
@@ -115,105 +124,80 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
     }
     return;
   }
-
-  // bias: all lanes read the same addresses (broadcast)
-  float b[32];
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const int col = col0 + 4 * g;
-    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (col < K) t = __ldg(reinterpret_cast<const float4 *>(a.bias + col));
-    b[4 * g + 0] = t.x;
-    b[4 * g + 1] = t.y;
-    b[4 * g + 2] = t.z;
-    b[4 * g + 3] = t.w;
-  }
-
-  float sd[32];
-  if (a.use_side) {
-    if (IS_INT8) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int col = col0 + 16 * h;
-        uint4 t = make_uint4(0, 0, 0, 0);
-        if (col < K) t = ldg_nc_v4(static_cast<const int8_t *>(a.side) + m * K + col);
-        const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int v = static_cast<int>(static_cast<int8_t>((w4[e >> 2] >> (8 * (e & 3))) & 0xFFu));
-          sd[16 * h + e] = static_cast<float>(v);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        const int col = col0 + 8 * qd;
-        uint4 t = make_uint4(0, 0, 0, 0);
-        if (col < K) t = ldg_nc_v4(static_cast<const __nv_bfloat16 *>(a.side) + m * K + col);
-        const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          sd[8 * qd + e] = bf16_bits_to_float((w4[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
-      }
-    }
-  }
-
-  float y[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    // (1) scale; (2) side input, one fused rounding; (3) bias.  Explicit
-    // round-to-nearest intrinsics keep nvcc from contracting (1) and (3).
-    float v = __fmul_rn(vals[i], a.conv_scale);
-    if (a.use_side) v = __fmaf_rn(sd[i], a.side_scale, v);
-    y[i] = __fadd_rn(v, b[i]);
-  }
-
+  const float cs = a.conv_scale, ss = a.side_scale;
+  const bool use_side = a.use_side != 0;
   if (IS_INT8) {
     const int lo = a.relu ? 0 : -128;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int col = col0 + 16 * h;
-      uint32_t w4[4];
+      if (col >= K) continue;
+      uint4 sv = make_uint4(0, 0, 0, 0);
+      if (use_side) sv = ldg_nc_v4(static_cast<const int8_t *>(a.side) + m * K + col);
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+      uint32_t out[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
+        // bias: every lane reads the same 16 bytes (a broadcast)
+        const float4 bb = __ldg(reinterpret_cast<const float4 *>(a.bias + col + 4 * g));
+        const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
         uint32_t word = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          int r = __float2int_rn(y[16 * h + 4 * g + e]);  // round half to even
+          // (1) scale; (2) side input, one fused rounding; (3) bias.  The
+          // explicit round-to-nearest intrinsics keep nvcc from contracting
+          // (1) and (3) into an fma.
+          float v = __fmul_rn(vals[16 * h + 4 * g + e], cs);
+          if (use_side) {
+            const float sd = static_cast<float>(static_cast<int8_t>((sw[g] >> (8 * e)) & 0xFFu));
+            v = __fmaf_rn(sd, ss, v);
+          }
+          v = __fadd_rn(v, bv[e]);
+          int r = __float2int_rn(v);  // round half to even, saturating
           r = min(max(r, lo), 127);
           word |= (static_cast<uint32_t>(r) & 0xFFu) << (8 * e);
         }
-        w4[g] = word;
+        out[g] = word;
       }
-      if (col < K)
-        stg_v4(static_cast<int8_t *>(a.y) + m * K + col, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+      stg_v4(static_cast<int8_t *>(a.y) + m * K + col, make_uint4(out[0], out[1], out[2], out[3]));
     }
   } else {
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
       const int col = col0 + 8 * qd;
-      uint32_t w4[4];
+      if (col >= K) continue;
+      uint4 sv = make_uint4(0, 0, 0, 0);
+      if (use_side) sv = ldg_nc_v4(static_cast<const __nv_bfloat16 *>(a.side) + m * K + col);
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+      const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + col));
+      const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + col + 4));
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      uint32_t out[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float v0 = y[8 * qd + 2 * g], v1 = y[8 * qd + 2 * g + 1];
-        if (a.relu) {
-          v0 = fmaxf(v0, 0.0f);
-          v1 = fmaxf(v1, 0.0f);
+        uint32_t word = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          float v = __fmul_rn(vals[8 * qd + 2 * g + t], cs);
+          if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
+          v = __fadd_rn(v, bv[2 * g + t]);
+          if (a.relu) v = fmaxf(v, 0.0f);
+          word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << (16 * t);
         }
-        const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(v0));
-        const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(v1));
-        w4[g] = b0 | (b1 << 16);
+        out[g] = word;
       }
-      if (col < K)
-        stg_v4(static_cast<__nv_bfloat16 *>(a.y) + m * K + col,
-               make_uint4(w4[0], w4[1], w4[2], w4[3]));
+      stg_v4(static_cast<__nv_bfloat16 *>(a.y) + m * K + col,
+             make_uint4(out[0], out[1], out[2], out[3]));
     }
   }
 }
 
+// General path: cp.async gather of A by 4 loader warps, 4 epilogue warps.
+// int8 sums longer than one exact chunk are folded into int32 in a third
+// TMEM region, so chunked plans use BN <= 128.
 template <int BN, bool IS_INT8>
 __global__ void __launch_bounds__(kThreads, 1)
-    conv_fprop_kernel(const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
+    conv_fprop_cpasync_kernel(const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
   using C = Cfg<BN>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8);
@@ -326,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_commit();
         ++pending;
-        if (pending > kLag) {
-          cp_async_wait<kLag>();
+        if (pending > C::kLag) {
+          cp_async_wait<C::kLag>();
           fence_proxy_async_smem();
           if (!drop) mbar_arrive(smem_u32(&bars->full_a[arr_stage]));
           if (++arr_stage == kStages) arr_stage = 0;
@@ -469,6 +453,265 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
+
+// ---------------------------------------------------------------- TMA path
+// Used when C % 64 == 0 (a k-block is 64 channels of one filter tap).
+// 384 threads in three warpgroups.  Warpgroup 0: warp 0 lane 0 issues the
+// TMA loads (A by im2col, B tiled) onto one barrier per stage; warp 1
+// allocates TMEM and lane 0 issues the MMAs; warps 2-3 idle.  Warpgroups 1-2
+// (warps 4-11) run the epilogue, two warps per TMEM lane quarter, each owning
+// half of the BN columns.  int8 sums longer than one exact chunk are folded
+// into int32 registers of those threads, so all 512 TMEM columns hold a
+// double-buffered 128 x 256 accumulator.
+//
+// Registers: the register file is split over the SM's four sub-partitions,
+// so 12 warps launch at 168 a thread (384 x 168 = 64512).  Warpgroup 0 then
+// gives back down to 56 and the epilogue warpgroups take 224:
+// 128 x 56 + 256 x 224 = 64512, the launch total; per sub-partition that is
+// one warp of each warpgroup, 56 + 224 + 224 = 504 <= 512 per lane.
+constexpr int kTmaThreads = 384;
+constexpr int kTmaEpiWarp0 = 4;
+constexpr int kTmaEpiWarps = 8;
+constexpr int kTmaCtlRegs = 56;
+constexpr int kTmaEpiRegs = 224;
+static_assert(128 * kTmaCtlRegs + 256 * kTmaEpiRegs <= kTmaThreads * 168,
+              "register split exceeds the launch allocation");
+
+template <int BN>
+struct TmaCfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
+  static constexpr int kHalfCols = BN / 2;   // columns per epilogue thread
+  static constexpr int kSlices = kHalfCols / 32;
+  static_assert(BN == 64 || BN == 128 || BN == 256, "TMA path tile");
+  static_assert(kStages >= 3, "pipeline too shallow");
+};
+
+template <int BN, bool IS_INT8>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    conv_fprop_tma_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                          const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
+  using C = TmaCfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + kStages * C::kABytes;
+  Smem *bars = reinterpret_cast<Smem *>(smem + C::kBarOffset);
+  volatile int *abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t tmo = args.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars->full_b[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars->acc_full[s]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[s]), kTmaEpiWarps);
+    }
+    mbar_init(smem_u32(&bars->mma_done), 1);
+    bars->abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+
+  const int num_kb = args.num_kb;
+  const int kb_chunk = args.kb_chunk;
+  const int n_chunks = (num_kb + kb_chunk - 1) / kb_chunk;
+
+  if (warp < kTmaEpiWarp0) {
+   setmaxnreg_dec<kTmaCtlRegs>();
+   if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const long long PQ = static_cast<long long>(args.P) * args.Q;
+      const int cblocks = args.C / kBK;
+      const bool drop = (args.debug & 1) != 0;
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+        const int m_tile = tile / args.num_n_tiles;
+        const int n_tile = tile - m_tile * args.num_n_tiles;
+        const long long m0 = static_cast<long long>(m_tile) * kBM;
+        const int n0 = static_cast<int>(m0 / PQ);
+        const int rem = static_cast<int>(m0 - static_cast<long long>(n0) * PQ);
+        const int p0 = rem / args.Q, q0 = rem - (rem / args.Q) * args.Q;
+        // filter-window origin of the tile's first output pixel
+        const int w0 = q0 * args.sw - args.pl, h0 = p0 * args.sh - args.pt;
+        int r = 0, s = 0, cb = 0;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          if (!drop) {
+            const uint32_t fb = smem_u32(&bars->full_b[stage]);
+            mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
+            tma_load_im2col_4d(smem_u32(sA + stage * C::kABytes), &tmap_a, cb * kBK, w0, h0, n0,
+                               static_cast<uint16_t>(s), static_cast<uint16_t>(r), fb);
+            tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb * kBK, n_tile * BN, fb);
+            ++issued;
+          }
+          if (++cb == cblocks) {
+            cb = 0;
+            if (++s == args.S) { s = 0; ++r; }
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      // let any copy still in flight land before the CTA exits (after an
+      // abort); on the normal path every one of them has completed
+      const uint32_t first = issued > static_cast<uint32_t>(kStages) ? issued - kStages : 0;
+      for (uint32_t i = first; i < issued; ++i)
+        mbar_wait_drain(smem_u32(&bars->full_b[i % kStages]), (i / kStages) & 1u, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+        for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kb_chunk) {
+          const int kb1 = min(kb0 + kb_chunk, num_kb);
+          if (!mbar_wait(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + astage * BN;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(smem_u32(&bars->full_b[stage]), phase, abort_flag, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_f16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            umma_commit(smem_u32(&bars->empty[stage]));
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&bars->acc_full[astage]));
+          if (++astage == 2) { astage = 0; aphase ^= 1; }
+        }
+      }
+      // every MMA issued above has completed once this arrives
+      umma_commit(smem_u32(&bars->mma_done));
+      mbar_wait_drain(smem_u32(&bars->mma_done), 0, 1000000000ull);
+    }
+    __syncwarp();
+   }
+  } else {
+    setmaxnreg_inc<kTmaEpiRegs>();
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+    const int half = (warp - kTmaEpiWarp0) >> 2;  // which half of the BN columns
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int cbase = half * C::kHalfCols;
+    int32_t sums[IS_INT8 ? C::kHalfCols : 1];  // int32 running sums across chunks
+    uint32_t astage = 0, aphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+      const int m_tile = tile / args.num_n_tiles;
+      const int n_tile = tile - m_tile * args.num_n_tiles;
+      const long long m = static_cast<long long>(m_tile) * kBM + row;
+      const bool mvalid = m < args.M;
+      const int c0 = n_tile * BN + cbase;
+      for (int ch = 0; ch < n_chunks; ++ch) {
+        if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_acc = tmem_base + lane_off + astage * BN + cbase;
+        if (n_chunks == 1) {
+          // the whole sum is in TMEM: epilogue straight from it
+#pragma unroll 1
+          for (int jj = 0; jj < C::kSlices; ++jj) {
+            uint32_t v[32];
+            tmem_ld32(t_acc + jj * 32, v);
+            tmem_wait_ld(v);
+            float vals[32];
+            // + 0.0f turns a -0 sum into the +0 that float(int32 0) gives
+#pragma unroll
+            for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
+            if (mvalid) epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[astage]));
+        } else if constexpr (IS_INT8) {
+          // fold this chunk's exact fp32 sums into the int32 registers, hand
+          // the accumulator back, and finish the tile from the registers
+#pragma unroll
+          for (int jj = 0; jj < C::kSlices; ++jj) {
+            uint32_t v[32];
+            tmem_ld32(t_acc + jj * 32, v);
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int add = __float2int_rn(__uint_as_float(v[i]));
+              sums[jj * 32 + i] = (ch == 0 ? 0 : sums[jj * 32 + i]) + add;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[astage]));
+          if (ch == n_chunks - 1 && mvalid) {
+#pragma unroll
+            for (int jj = 0; jj < C::kSlices; ++jj) {
+              if (args.mode == kModeAccumulators) {
+                uint32_t u[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) u[i] = static_cast<uint32_t>(sums[jj * 32 + i]);
+                store_i32_slice(args, m, c0 + jj * 32, u);
+              } else {
+                float vals[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(sums[jj * 32 + i]);
+                epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals);
+              }
+            }
+          }
+        }
+        if (++astage == 2) { astage = 0; aphase ^= 1; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
 // ---------------------------------------------------------------- pre-pass
 // HWIO filter [RSC][K] -> K-major 16-bit [K][Kpad] (zero for k >= RSC);
 // int8 values widen exactly to fp16, bf16 values are copied.
@@ -519,39 +762,83 @@ __global__ void widen_i8_kernel(const int8_t *__restrict__ x, __half *__restrict
 
 // ---------------------------------------------------------------- launchers
 template <int BN, bool IS_INT8>
-static cudaError_t launch_conv_t(const CUtensorMap &tmap, const ConvArgs &args, int grid,
-                                 cudaStream_t stream) {
-  using C = Cfg<BN>;
-  auto kern = conv_fprop_kernel<BN, IS_INT8>;
+static cudaError_t launch_cpasync_t(const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
+                                    cudaStream_t stream) {
+  auto kern = conv_fprop_cpasync_kernel<BN, IS_INT8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tmap, args);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_conv(int block_n, bool is_int8, const CUtensorMap &tmap, const ConvArgs &args,
-                        int grid, cudaStream_t stream) {
-  // chunked accumulation needs a third TMEM region, and only int8 plans use it
-  if (args.kb_chunk < args.num_kb && (!is_int8 || !block_n_can_chunk(block_n)))
-    return cudaErrorInvalidValue;
-  if (args.kb_chunk <= 0 || grid <= 0) return cudaErrorInvalidValue;
-#define FCONV_CASE(BN)                                                              \
-  case BN:                                                                          \
-    return is_int8 ? launch_conv_t<BN, true>(tmap, args, grid, stream)              \
-                   : launch_conv_t<BN, false>(tmap, args, grid, stream);
-  switch (block_n) {
-    FCONV_CASE(32)
-    FCONV_CASE(64)
-    FCONV_CASE(128)
-    FCONV_CASE(256)
-    default:
-      return cudaErrorInvalidValue;
+                                       Cfg<BN>::kSmemBytes);
+  if (e == cudaSuccess) {
+    kern<<<grid, kThreads, Cfg<BN>::kSmemBytes, stream>>>(tmap_b, args);
+    e = cudaGetLastError();
   }
-#undef FCONV_CASE
+  if (e != cudaSuccess) note_attributes(kern, kThreads, Cfg<BN>::kSmemBytes);
+  return e;
 }
 
-bool block_n_can_chunk(int block_n) { return 3 * block_n <= 512; }
+// Attributes of the kernel a failed launch used, for the error message.
+thread_local char t_kernel_note[256];
+
+template <typename Kern>
+static void note_attributes(Kern kern, int threads, int smem) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess)
+    snprintf(t_kernel_note, sizeof t_kernel_note,
+             "kernel: %d registers, %zu B local, max %d threads/block; launch: %d threads, %d B "
+             "dynamic shared memory",
+             fa.numRegs, fa.localSizeBytes, fa.maxThreadsPerBlock, threads, smem);
+}
+
+const char *last_launch_note() { return t_kernel_note; }
+
+template <int BN, bool IS_INT8>
+static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
+                                const ConvArgs &args, int grid, cudaStream_t stream) {
+  auto kern = conv_fprop_tma_kernel<BN, IS_INT8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TmaCfg<BN>::kSmemBytes);
+  if (e == cudaSuccess) {
+    kern<<<grid, kTmaThreads, TmaCfg<BN>::kSmemBytes, stream>>>(tmap_a, tmap_b, args);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) note_attributes(kern, kTmaThreads, TmaCfg<BN>::kSmemBytes);
+  return e;
+}
+
+bool gather_supports(Gather gather, int block_n, bool chunked) {
+  if (gather == Gather::kTmaIm2col) return block_n == 64 || block_n == 128 || block_n == 256;
+  if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256) return false;
+  return !chunked || 3 * block_n <= 512;
+}
+
+cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensorMap &tmap_a,
+                        const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
+                        cudaStream_t stream) {
+  const bool chunked = args.kb_chunk < args.num_kb;
+  if (chunked && !is_int8) return cudaErrorInvalidValue;
+  if (!gather_supports(gather, block_n, chunked)) return cudaErrorInvalidValue;
+  if (args.kb_chunk <= 0 || grid <= 0) return cudaErrorInvalidValue;
+  if (gather == Gather::kTmaIm2col) {
+    if (args.C % kBK != 0) return cudaErrorInvalidValue;
+    switch (block_n) {
+      case 64: return is_int8 ? launch_tma_t<64, true>(tmap_a, tmap_b, args, grid, stream)
+                              : launch_tma_t<64, false>(tmap_a, tmap_b, args, grid, stream);
+      case 128: return is_int8 ? launch_tma_t<128, true>(tmap_a, tmap_b, args, grid, stream)
+                               : launch_tma_t<128, false>(tmap_a, tmap_b, args, grid, stream);
+      default: return is_int8 ? launch_tma_t<256, true>(tmap_a, tmap_b, args, grid, stream)
+                              : launch_tma_t<256, false>(tmap_a, tmap_b, args, grid, stream);
+    }
+  }
+  switch (block_n) {
+    case 32: return is_int8 ? launch_cpasync_t<32, true>(tmap_b, args, grid, stream)
+                            : launch_cpasync_t<32, false>(tmap_b, args, grid, stream);
+    case 64: return is_int8 ? launch_cpasync_t<64, true>(tmap_b, args, grid, stream)
+                            : launch_cpasync_t<64, false>(tmap_b, args, grid, stream);
+    case 128: return is_int8 ? launch_cpasync_t<128, true>(tmap_b, args, grid, stream)
+                             : launch_cpasync_t<128, false>(tmap_b, args, grid, stream);
+    default: return is_int8 ? launch_cpasync_t<256, true>(tmap_b, args, grid, stream)
+                            : launch_cpasync_t<256, false>(tmap_b, args, grid, stream);
+  }
+}
 
 cudaError_t launch_pack_filter(bool is_int8, const void *w, uint16_t *wt, int RSC, int K,
                                int Kpad, cudaStream_t stream) {

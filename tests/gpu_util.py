@@ -55,16 +55,22 @@ class Case:
         return oracle.Geometry(self.N, self.H, self.W, self.C, self.K, self.R, self.S,
                                self.stride[0], self.stride[1], PAD[self.padding])
 
-    def plan(self, block_n=None):
+    def plan(self, block_n=None, debug=0):
         p = fc.Conv2dPlan(self.N, self.H, self.W, self.C, self.K, self.R, self.S, self.stride,
                           self.padding, self.dtype, self.relu)
         if block_n:
             p.set_tile(block_n)
+        if debug:
+            fc.fconv_plan_set_debug(p.handle, debug)
+            bn, chunk, _ = p.config()
+            chunked = chunk * 64 < self.R * self.S * self.C
+            if debug & fc.FCONV_DEBUG_GATHER_CPASYNC and chunked and bn > 128:
+                p.set_tile(128)   # the cp.async kernel folds chunks in TMEM: BN <= 128
         return p
 
     # ------------------------------------------------------------ GPU side
-    def run_gpu(self, block_n=None, stream=None):
-        p = self.plan(block_n)
+    def run_gpu(self, block_n=None, stream=None, debug=0):
+        p = self.plan(block_n, debug)
         x, w = to_dev(self.x, self.dtype), to_dev(self.w, self.dtype)
         bias = torch.from_numpy(self.bias).cuda()
         side = to_dev(self.side, self.dtype)
@@ -74,8 +80,8 @@ class Case:
         p.close()
         return out
 
-    def accumulators_gpu(self, block_n=None):
-        p = self.plan(block_n)
+    def accumulators_gpu(self, block_n=None, debug=0):
+        p = self.plan(block_n, debug)
         x, w = to_dev(self.x, self.dtype), to_dev(self.w, self.dtype)
         acc = p.accumulators(x, w)
         p.check()

@@ -101,17 +101,28 @@ def test_plan_geometry_matches_oracle(row):
 
 
 def test_tile_override_rules():
-    # 3x3x512 int8: 72 k-blocks, so the sums are chunked and need a 3rd TMEM region
+    # 3x3x512 int8: 72 k-blocks, so the sums are chunked.  C % 64 == 0 lets
+    # the kernel gather by TMA, whose epilogue folds the chunks in registers:
+    # every tile from 64 to 256 is allowed.
     h = fc.fconv_plan_create(2, 8, 8, 512, 512, 3, 3, 1, 1, 0, 0, 1)
     try:
         bn, chunk, _ = fc.fconv_plan_get_config(h)
-        assert chunk == 15 and bn <= 128
-        assert _err(fc.fconv_plan_set_tile, h, 256) == fc.FCONV_ERR_NOT_SUPPORTED
+        assert chunk == 15
+        for t in (64, 128, 256):
+            fc.fconv_plan_set_tile(h, t)
+            assert fc.fconv_plan_get_config(h)[0] == t
         assert _err(fc.fconv_plan_set_tile, h, 48) == fc.FCONV_ERR_NOT_SUPPORTED
-        fc.fconv_plan_set_tile(h, 64)
-        assert fc.fconv_plan_get_config(h)[0] == 64
         fc.fconv_plan_set_tile(h, 0)
         assert fc.fconv_plan_get_config(h)[0] == bn
+    finally:
+        fc.fconv_plan_destroy(h)
+    # C = 176: the cp.async gather folds chunks in TMEM, which caps the tile at 128
+    h = fc.fconv_plan_create(2, 8, 8, 176, 256, 3, 3, 1, 1, 0, 0, 1)
+    try:
+        bn, chunk, _ = fc.fconv_plan_get_config(h)
+        assert chunk < 25 and bn <= 128
+        assert _err(fc.fconv_plan_set_tile, h, 256) == fc.FCONV_ERR_NOT_SUPPORTED
+        fc.fconv_plan_set_tile(h, 32)
     finally:
         fc.fconv_plan_destroy(h)
     # bf16 sums are never chunked: 256 is allowed

@@ -83,7 +83,14 @@ SWEEP = [
     (1, 30, 30, 1024, 32, 3, 3, 1, "SAME", True, True),    # 9216 k-values: 10 chunks
     (2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True),    # 4608 k-values, K tail
     (7, 9, 9, 16, 16, 1, 1, 2, "VALID", True, False),
+    (2, 11, 9, 64, 96, 5, 3, 2, "SAME", True, True),       # R != S, stride 2, odd pads
+    (3, 8, 8, 128, 64, 3, 3, 2, "SAME", False, False),     # total pad 1: 0 before, 1 after
+    (2, 7, 12, 192, 48, 1, 3, (2, 1), "VALID", True, True),
+    (1, 20, 3, 64, 32, 4, 2, 3, "SAME", False, True),      # stride 3, even filters
 ]
+
+# shapes whose channel count lets the kernel gather A with TMA im2col loads
+TMA_SHAPES = [i for i, p in enumerate(SWEEP) if p[3] % 64 == 0]
 
 
 def sweep_case(i, params, dtype):
@@ -112,6 +119,21 @@ def test_sweep_bf16(i, params):
     acc_ref = c.oracle_acc()
     c.check_acc(c.accumulators_gpu(), acc_ref)
     c.check_output(c.run_gpu(), c.oracle_out(acc_ref))
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+@pytest.mark.parametrize("i", TMA_SHAPES)
+def test_both_gathers_agree(i, dtype):
+    """The TMA im2col gather and the cp.async gather give the same sums."""
+    c = sweep_case(i, SWEEP[i], dtype)
+    acc_ref = c.oracle_acc()
+    tma = c.accumulators_gpu()
+    cpa = c.accumulators_gpu(debug=fc.FCONV_DEBUG_GATHER_CPASYNC)
+    c.check_acc(tma, acc_ref)
+    c.check_acc(cpa, acc_ref)
+    if dtype == "int8":
+        assert np.array_equal(tma, cpa)
+    c.check_output(c.run_gpu(debug=fc.FCONV_DEBUG_GATHER_CPASYNC), c.oracle_out(acc_ref))
 
 
 @pytest.mark.parametrize("dtype", ["int8", "bf16"])
@@ -227,11 +249,12 @@ def test_run_host_buffers():
     p.close()
 
 
-def test_timeout_exit_keeps_context_usable():
+@pytest.mark.parametrize("C", [16, 64])
+def test_timeout_exit_keeps_context_usable(C):
     """A loader that never signals 'stage full' makes the MMA issuer's wait
     run out: the kernel must stop, report FCONV_ERR_TIMEOUT, and the next run
-    must work."""
-    c = sweep_case(70, (1, 8, 8, 16, 16, 3, 3, 1, "SAME", False, True), "int8")
+    must work.  C=16 exercises the cp.async loaders, C=64 the TMA producer."""
+    c = sweep_case(70, (1, 8, 8, C, 16, 3, 3, 1, "SAME", False, True), "int8")
     p = c.plan()
     fc.fconv_plan_set_timeout_ms(p.handle, 50)
     fc.fconv_plan_set_debug(p.handle, fc.FCONV_DEBUG_DROP_ARRIVE)
