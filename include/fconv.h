@@ -129,16 +129,26 @@ fconv_status fconv_host_workspace_size(const fconv_plan *plan, int with_side,
                                        size_t *bytes);
 
 /* fconv_run on HOST buffers: copies x, w, bias and side (if not NULL) to
- * `device_workspace`, runs, and copies y back to `y_host`, all enqueued on
- * `stream`.  Pinned host buffers keep this asynchronous; the caller
- * synchronizes the stream before reading y_host.  Pageable buffers work
- * but make the copies synchronous with the host. */
+ * `device_workspace`, runs, and copies y back to `y_host`.  Large batches
+ * are processed in chunks of images on two internal copy streams, so the
+ * copy-in of one chunk and the copy-out of another overlap the compute of a
+ * third (see fconv_plan_set_host_chunks); everything is ordered after the
+ * work already queued on `stream`, and `stream` waits for the last copy-out.
+ * Pinned host buffers keep this asynchronous; the caller synchronizes the
+ * stream before reading y_host.  Pageable buffers work but make the copies
+ * synchronous with the host.  A plan must not run two fconv_run_host calls
+ * at once (they share its internal streams). */
 fconv_status fconv_run_host(fconv_plan *plan, const void *x_host,
                             const void *w_host, const float *bias_host,
                             const void *side_host, float conv_scale,
                             float side_scale, void *y_host,
                             void *device_workspace, size_t workspace_bytes,
                             fconv_stream_t stream);
+
+/* Number of batch chunks fconv_run_host pipelines over (1..16; 0 restores
+ * the automatic choice: one chunk per >= 5 waves of output tiles, at most 8,
+ * so small problems run as one). */
+fconv_status fconv_plan_set_host_chunks(fconv_plan *plan, int chunks);
 
 /* Synchronize `stream`, then read and clear the current device's kernel
  * status word: FCONV_ERR_TIMEOUT if any kernel since the last check gave up

@@ -72,6 +72,7 @@ def _load():
         "fconv_plan_set_debug": [p, i32],
         "fconv_plan_set_stage_events": [p, ctypes.POINTER(ctypes.c_void_p)],
         "fconv_run_no_alloc": [p, p, p, p, p, f32, f32, p, p],
+        "fconv_plan_set_host_chunks": [p, i32],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -160,6 +161,10 @@ def fconv_run_host(plan, x_host, w_host, bias_host, side_host, conv_scale, side_
            "fconv_run_host")
 
 
+def fconv_plan_set_host_chunks(plan, chunks: int) -> None:
+    _check(_load().fconv_plan_set_host_chunks(plan, chunks), "fconv_plan_set_host_chunks")
+
+
 def fconv_plan_check(plan, stream) -> None:
     _check(_load().fconv_plan_check(plan, stream), "fconv_plan_check")
 
@@ -230,8 +235,17 @@ class Conv2dPlan:
         import torch
         return torch.empty(self.out_shape, dtype=self.torch_dtype, device=self.device)
 
+    def _ensure_workspace(self):
+        # the scratch a run needs depends on the tile and gather in force
+        need = fconv_workspace_size(self.handle)
+        if need > self.workspace.numel():
+            import torch
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self.ws_bytes = need
+
     def run(self, x, w, bias, side=None, conv_scale=1.0, side_scale=0.0, y=None, stream=None):
         import torch
+        self._ensure_workspace()
         if y is None:
             y = self.new_output()
         st = stream if stream is not None else torch.cuda.current_stream(self.device)
@@ -242,6 +256,7 @@ class Conv2dPlan:
 
     def accumulators(self, x, w, acc=None, stream=None):
         import torch
+        self._ensure_workspace()
         if acc is None:
             dt = torch.int32 if self.dtype == "int8" else torch.float32
             acc = torch.empty(self.out_shape, dtype=dt, device=self.device)

@@ -3,6 +3,7 @@
 // launch sequence of one fused convolution.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -11,7 +12,7 @@
 #include <new>
 #include <string>
 
-#include "../../include/fconv.h"
+#include "fconv.h"
 #include "fconv_internal.h"
 
 struct fconv_plan {
@@ -29,7 +30,14 @@ struct fconv_plan {
   size_t wt_bytes, xh_bytes;
   cudaEvent_t events[4];
   bool use_events;
+  // fconv_run_host pipeline: batch chunks, two copy streams and their events
+  int host_chunks;  // 0 = automatic
+  int pipe_dev;     // device the streams/events below belong to, -1 = none
+  cudaStream_t s_in, s_out;
+  cudaEvent_t ev_entry, ev_out, ev_in[16], ev_comp[16];
 };
+
+constexpr int kMaxHostChunks = 16;
 
 namespace {
 
@@ -187,9 +195,16 @@ int device_sm_count(int *dev_out) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+bool force_cpasync(const fconv_plan &p) { return (p.debug & FCONV_DEBUG_GATHER_CPASYNC) != 0; }
+
+// Scratch a run needs: the packed filter, and for int8 plans the fp16 copy of
+// the input the gathers read.
+size_t workspace_need(const fconv_plan &p) { return p.wt_bytes + p.xh_bytes; }
+
 fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *bias,
                      const void *side, float conv_scale, float side_scale, void *y,
-                     void *workspace, size_t workspace_bytes, cudaStream_t stream, int mode) {
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream, int mode,
+                     bool skip_pack = false) {
   if (!p) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
   if (!x || !w || !y) return fail(FCONV_ERR_INVALID_VALUE, "x, w and y must not be NULL");
   if (mode == fconv::kModeFused && !bias)
@@ -197,7 +212,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || (side && !aligned(side, 16)) ||
       (bias && !aligned(bias, 16)))
     return fail(FCONV_ERR_MISALIGNED, "x, w, y, side and bias must be 16-byte aligned");
-  const size_t need = p->wt_bytes + p->xh_bytes;
+  const size_t need = workspace_need(*p);
   if (!workspace || workspace_bytes < need)
     return fail(FCONV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? workspace_bytes : static_cast<size_t>(0));
@@ -217,10 +232,18 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   uint16_t *wt = static_cast<uint16_t *>(workspace);
   __half *xh = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + p->wt_bytes);
 
+  const fconv::Gather gather = gather_for(*p, p->block_n, force_cpasync(*p));
+  if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb))
+    return fail(FCONV_ERR_NOT_SUPPORTED,
+                "tile %d has no cp.async kernel for a sum of %d k-values (chunked sums need "
+                "BN <= 128 there)", p->block_n, p->Ktot);
+
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
-  e = fconv::launch_pack_filter(is_int8, w, wt, p->Ktot, p->K, p->Kpad, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "filter pack launch");
+  if (!skip_pack) {
+    e = fconv::launch_pack_filter(is_int8, w, wt, p->Ktot, p->K, p->Kpad, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "filter pack launch");
+  }
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   const void *act = x;
   if (is_int8) {
@@ -243,12 +266,6 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
 
-  const fconv::Gather gather =
-      gather_for(*p, p->block_n, (p->debug & FCONV_DEBUG_GATHER_CPASYNC) != 0);
-  if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb))
-    return fail(FCONV_ERR_NOT_SUPPORTED,
-                "tile %d has no cp.async kernel for a sum of %d k-values (chunked sums need "
-                "BN <= 128 there)", p->block_n, p->Ktot);
   CUtensorMap tmap_a;
   memset(&tmap_a, 0, sizeof tmap_a);
   if (gather == fconv::Gather::kTmaIm2col) {
@@ -301,6 +318,57 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     return fail(FCONV_ERR_CUDA, "convolution launch: %s (%s)", cudaGetErrorString(e),
                 fconv::last_launch_note());
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event record");
+  return FCONV_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// The same convolution on the first n images of the batch (all derived
+// extents recomputed; tile choice and workspace layout kept).
+fconv_plan batch_slice(const fconv_plan &p, int n) {
+  fconv_plan q = p;
+  q.N = n;
+  q.M = static_cast<long long>(n) * p.P * p.Q;
+  q.num_tiles = static_cast<int>((q.M + 127) / 128) * p.num_n_tiles;
+  q.use_events = false;
+  return q;
+}
+
+void destroy_pipeline(fconv_plan *p) {
+  if (p->pipe_dev < 0) return;
+  cudaStreamDestroy(p->s_in);
+  cudaStreamDestroy(p->s_out);
+  cudaEventDestroy(p->ev_entry);
+  cudaEventDestroy(p->ev_out);
+  for (int i = 0; i < kMaxHostChunks; ++i) {
+    cudaEventDestroy(p->ev_in[i]);
+    cudaEventDestroy(p->ev_comp[i]);
+  }
+  p->pipe_dev = -1;
+}
+
+// Streams and events for the host-buffer pipeline, on the current device.
+fconv_status ensure_pipeline(fconv_plan *p) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->pipe_dev == dev) return FCONV_OK;
+  destroy_pipeline(p);
+  const unsigned ef = cudaEventDisableTiming;
+  bool ok = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p->ev_entry, ef) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p->ev_out, ef) == cudaSuccess;
+  for (int i = 0; ok && i < kMaxHostChunks; ++i)
+    ok = cudaEventCreateWithFlags(&p->ev_in[i], ef) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->ev_comp[i], ef) == cudaSuccess;
+  if (!ok) {
+    e = cudaGetLastError();
+    return cuda_fail(e, "creating the copy streams");
+  }
+  p->pipe_dev = dev;
   return FCONV_OK;
 }
 
@@ -373,6 +441,8 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, in
   p.auto_block_n = choose_block_n(p, sm_count_of_current_device(148));
   set_tiling(p, p.auto_block_n);
   p.timeout_ms = 2000;
+  p.host_chunks = 0;
+  p.pipe_dev = -1;
   p.wt_bytes = align_up(static_cast<size_t>(K) * p.Kpad * 2, 256);
   p.xh_bytes = dtype == FCONV_INT8 ? align_up(static_cast<size_t>(in_elems) * 2, 256) : 0;
 
@@ -383,6 +453,7 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, in
 }
 
 fconv_status fconv_plan_destroy(fconv_plan *plan) {
+  if (plan) destroy_pipeline(plan);
   delete plan;
   return FCONV_OK;
 }
@@ -408,7 +479,7 @@ fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top, int *pad_b
 
 fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes) {
   if (!plan || !bytes) return fail(FCONV_ERR_INVALID_VALUE, "plan and bytes must not be NULL");
-  *bytes = plan->wt_bytes + plan->xh_bytes;
+  *bytes = workspace_need(*plan);
   return FCONV_OK;
 }
 
@@ -433,7 +504,7 @@ static void host_layout(const fconv_plan *p, int with_side, size_t off[6]) {
   const size_t b_b = static_cast<size_t>(p->K) * 4;
   const size_t y_b = static_cast<size_t>(p->M) * p->K * elt;
   off[0] = 0;                                                 // workspace
-  off[1] = align_up(off[0] + p->wt_bytes + p->xh_bytes, 256);  // x
+  off[1] = align_up(off[0] + workspace_need(*p), 256);         // x
   off[2] = align_up(off[1] + x_b, 256);                        // w
   off[3] = align_up(off[2] + w_b, 256);                        // bias
   off[4] = align_up(off[3] + b_b, 256);                        // side
@@ -468,25 +539,84 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host, const void *w_
   uint8_t *base = static_cast<uint8_t *>(device_workspace);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t elt = plan->dtype == FCONV_INT8 ? 1 : 2;
-  const size_t x_b = static_cast<size_t>(plan->N) * plan->H * plan->W * plan->C * elt;
+  const size_t img_x = static_cast<size_t>(plan->H) * plan->W * plan->C * elt;
+  const size_t img_y = static_cast<size_t>(plan->P) * plan->Q * plan->K * elt;
   const size_t w_b = static_cast<size_t>(plan->R) * plan->S * plan->C * plan->K * elt;
-  const size_t y_b = static_cast<size_t>(plan->M) * plan->K * elt;
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(base + off[1], x_host, x_b, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(base + off[2], w_host, w_b, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(base + off[3], bias_host, static_cast<size_t>(plan->K) * 4,
-                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
-    return cuda_fail(e, "host-to-device copy");
-  if (side_host && (e = cudaMemcpyAsync(base + off[4], side_host, y_b, cudaMemcpyHostToDevice,
-                                        st)) != cudaSuccess)
-    return cuda_fail(e, "host-to-device copy of the side input");
-  fconv_status s = enqueue(plan, base + off[1], base + off[2],
-                           reinterpret_cast<const float *>(base + off[3]),
-                           side_host ? base + off[4] : nullptr, conv_scale, side_scale,
-                           base + off[5], base, off[1], st, fconv::kModeFused);
+
+  // Batch chunks: copy-in of chunk i+1 and copy-out of chunk i-1 overlap the
+  // compute of chunk i.  Automatic: one chunk per >= 5 waves of output tiles.
+  int chunks = plan->host_chunks;
+  if (chunks <= 0) {
+    const int sms = device_sm_count(nullptr);
+    chunks = sms > 0 ? plan->num_tiles / (5 * sms) : 1;
+    if (chunks > 8) chunks = 8;
+  }
+  if (chunks < 1) chunks = 1;
+  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
+  if (chunks > plan->N) chunks = plan->N;
+  const int per = (plan->N + chunks - 1) / chunks;
+  chunks = (plan->N + per - 1) / per;
+
+  fconv_status s = ensure_pipeline(plan);
   if (s != FCONV_OK) return s;
-  if ((e = cudaMemcpyAsync(y_host, base + off[5], y_b, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-    return cuda_fail(e, "device-to-host copy");
+  cudaError_t e;
+  // the copy streams start after everything already queued on the caller's stream
+  if ((e = cudaEventRecord(plan->ev_entry, st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(plan->s_in, plan->ev_entry, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(plan->s_out, plan->ev_entry, 0)) != cudaSuccess)
+    return cuda_fail(e, "stream ordering");
+  if ((e = cudaMemcpyAsync(base + off[2], w_host, w_b, cudaMemcpyHostToDevice, plan->s_in)) !=
+          cudaSuccess ||
+      (e = cudaMemcpyAsync(base + off[3], bias_host, static_cast<size_t>(plan->K) * 4,
+                           cudaMemcpyHostToDevice, plan->s_in)) != cudaSuccess)
+    return cuda_fail(e, "host-to-device copy");
+  for (int i = 0; i < chunks; ++i) {
+    const size_t n0 = static_cast<size_t>(i) * per;
+    const size_t n = std::min(static_cast<size_t>(per), static_cast<size_t>(plan->N) - n0);
+    if ((e = cudaMemcpyAsync(base + off[1] + n0 * img_x, static_cast<const uint8_t *>(x_host) +
+                                 n0 * img_x, n * img_x, cudaMemcpyHostToDevice, plan->s_in)) !=
+        cudaSuccess)
+      return cuda_fail(e, "host-to-device copy");
+    if (side_host &&
+        (e = cudaMemcpyAsync(base + off[4] + n0 * img_y, static_cast<const uint8_t *>(side_host) +
+                                 n0 * img_y, n * img_y, cudaMemcpyHostToDevice, plan->s_in)) !=
+            cudaSuccess)
+      return cuda_fail(e, "host-to-device copy of the side input");
+    if ((e = cudaEventRecord(plan->ev_in[i], plan->s_in)) != cudaSuccess)
+      return cuda_fail(e, "event record");
+  }
+  for (int i = 0; i < chunks; ++i) {
+    const size_t n0 = static_cast<size_t>(i) * per;
+    const int n = static_cast<int>(std::min(static_cast<size_t>(per), static_cast<size_t>(plan->N) - n0));
+    if ((e = cudaStreamWaitEvent(st, plan->ev_in[i], 0)) != cudaSuccess)
+      return cuda_fail(e, "stream ordering");
+    fconv_plan q = batch_slice(*plan, n);
+    s = enqueue(&q, base + off[1] + n0 * img_x, base + off[2],
+                reinterpret_cast<const float *>(base + off[3]),
+                side_host ? base + off[4] + n0 * img_y : nullptr, conv_scale, side_scale,
+                base + off[5] + n0 * img_y, base, off[1], st, fconv::kModeFused,
+                /*skip_pack=*/i > 0);
+    if (s != FCONV_OK) return s;
+    if ((e = cudaEventRecord(plan->ev_comp[i], st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(plan->s_out, plan->ev_comp[i], 0)) != cudaSuccess)
+      return cuda_fail(e, "stream ordering");
+    if ((e = cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + n0 * img_y,
+                             base + off[5] + n0 * img_y, n * img_y, cudaMemcpyDeviceToHost,
+                             plan->s_out)) != cudaSuccess)
+      return cuda_fail(e, "device-to-host copy");
+  }
+  // the caller's stream continues once the last result byte is on the host
+  if ((e = cudaEventRecord(plan->ev_out, plan->s_out)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(st, plan->ev_out, 0)) != cudaSuccess)
+    return cuda_fail(e, "stream ordering");
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_host_chunks(fconv_plan *plan, int chunks) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (chunks < 0 || chunks > kMaxHostChunks)
+    return fail(FCONV_ERR_INVALID_VALUE, "chunks must be 0 (automatic) .. %d", kMaxHostChunks);
+  plan->host_chunks = chunks;
   return FCONV_OK;
 }
 

@@ -26,7 +26,7 @@
 
 #include <mutex>
 
-#include "../../include/fconv.h"
+#include "fconv.h"
 #include "fconv_internal.h"
 
 namespace fconv {

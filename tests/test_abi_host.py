@@ -167,15 +167,21 @@ def test_run_argument_errors_before_any_launch():
 def test_workspace_sizes():
     h = fc.fconv_plan_create(256, 28, 28, 512, 512, 3, 3, 1, 1, 0, 0, 1)
     try:
-        ws = fc.fconv_workspace_size(h)
         # fp16 filter [512][4608] + fp16 copy of the input
+        ws = fc.fconv_workspace_size(h)
         assert ws == 512 * 4608 * 2 + 256 * 28 * 28 * 512 * 2
         hw = fc.fconv_host_workspace_size(h, True)
         assert hw >= ws + 3 * 256 * 28 * 28 * 512 + 4608 * 512 + 512 * 4
     finally:
         fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create(8, 14, 14, 48, 64, 3, 3, 1, 1, 0, 0, 1)
+    try:
+        assert fc.fconv_workspace_size(h) == 64 * 448 * 2 + 8 * 14 * 14 * 48 * 2
+    finally:
+        fc.fconv_plan_destroy(h)
     h = fc.fconv_plan_create(32, 14, 14, 256, 256, 3, 3, 1, 1, 0, 1, 1)
     try:
+        # bf16 plans read the input as it is: the packed filter alone
         assert fc.fconv_workspace_size(h) == 256 * 2304 * 2
     finally:
         fc.fconv_plan_destroy(h)

@@ -232,20 +232,33 @@ def test_side_stream_and_guard_bytes():
     p.close()
 
 
-def test_run_host_buffers():
-    c = workload_case("small_i8_16x16x32")
+@pytest.mark.parametrize("chunks", [0, 1, 3])
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+def test_run_host_buffers(chunks, dtype):
+    """fconv_run_host: host buffers in, host buffer out, the batch split into
+    pipelined chunks (7 images in 3 chunks leaves a ragged last chunk)."""
+    c = sweep_case(90, (7, 12, 10, 64, 48, 3, 3, 1, "SAME", True, True), dtype)
     p = c.plan()
-    nbytes = fc.fconv_host_workspace_size(p.handle, False)
+    fc.fconv_plan_set_host_chunks(p.handle, chunks)
+    nbytes = fc.fconv_host_workspace_size(p.handle, True)
     dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    xh = torch.from_numpy(c.x).pin_memory()
-    wh = torch.from_numpy(c.w).pin_memory()
-    bh = torch.from_numpy(c.bias).pin_memory()
-    yh = torch.empty(p.out_shape, dtype=torch.int8).pin_memory()
+
+    def pinned(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).pin_memory()
+        return torch.from_numpy(a).pin_memory()
+
+    xh, wh, bh, sh = pinned(c.x), pinned(c.w), pinned(c.bias), pinned(c.side)
+    yh = torch.empty(p.out_shape, dtype=torch.int8 if dtype == "int8" else torch.int16).pin_memory()
     s = torch.cuda.current_stream()
-    fc.fconv_run_host(p.handle, xh.data_ptr(), wh.data_ptr(), bh.data_ptr(), None, c.conv_scale,
-                      c.side_scale, yh.data_ptr(), dev.data_ptr(), nbytes, s.cuda_stream)
-    p.check()
-    c.check_output(yh.numpy(), c.oracle_out())
+    for _ in range(2):   # twice: the internal streams and events are reused
+        yh.zero_()
+        fc.fconv_run_host(p.handle, xh.data_ptr(), wh.data_ptr(), bh.data_ptr(), sh.data_ptr(),
+                          c.conv_scale, c.side_scale, yh.data_ptr(), dev.data_ptr(), nbytes,
+                          s.cuda_stream)
+        p.check()
+        got = yh.numpy() if dtype == "int8" else yh.numpy().view(np.uint16)
+        c.check_output(got, c.oracle_out())
     p.close()
 
 
