@@ -4,8 +4,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fconv|reference]
 
 Prints ONE JSON line (rank 0).  A step is one fconv_run of the whole fused
-path (filter pack, int8 -> fp16 input widening, implicit-GEMM convolution
-with the fused epilogue) over one batch of the workload: N=256 28x28x512
+path (one launch that packs the filter and widens the int8 input to fp16,
+then the implicit-GEMM convolution with the fused epilogue) over one batch
+of the workload: N=256 28x28x512
 int8, 3x3 stride 1 SAME, side input, ReLU (implicit GEMM 200704 x 512 x
 4608).  ``value`` is TOPS counted the usual way (2*M*N*K, padded taps
 included) over all ranks; the roofline block reports the convolution
@@ -256,8 +257,7 @@ def run_fconv(args, rank, world, local_rank):
     plan.check()
     total_ms = t_start.elapsed_time(t_end)
     conv_ms = [evs[i][2].elapsed_time(evs[i][3]) for i in range(args.steps)]
-    pack_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
-    widen_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+    prep_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
     if dist:
         t = torch.tensor([total_ms], device=dev)
         tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
@@ -333,11 +333,11 @@ def run_fconv(args, rank, world, local_rank):
         "config": dict(config_of(wl), block_n=plan.config()[0],
                        l2="inputs larger than L2: x+side+y+workspace = "
                           f"{(x.numel() + (side.numel() if side is not None else 0) + y.numel() + plan.ws_bytes) / 1e6:.0f} MB > 129 MB"),
-        "stage_ms": {"pack_filter": statistics.mean(pack_ms), "widen_input": statistics.mean(widen_ms),
+        "stage_ms": {"prep (filter pack + int8->fp16 widening)": statistics.mean(prep_ms),
                      "conv": statistics.mean(conv_ms)},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * (3 if wl.dtype == "int8" else 2),
+        "gpu_launches": args.steps * 2,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -182,10 +182,11 @@ fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
 
 /* Record caller-created CUDA events (cudaEvent_t) at the stage boundaries
  * of every later fconv_run / fconv_run_accumulators on this plan, on the
- * run's stream: events[0] before the filter pack, events[1] after it,
- * events[2] after the int8 -> fp16 input widening (same point as events[1]
- * for bf16 plans), events[3] after the convolution kernel.  NULL disables.
- * The events must outlive the runs that record them. */
+ * run's stream: events[0] before the operand preparation (filter pack and,
+ * for int8 plans, the int8 -> fp16 input widening, one launch), events[1]
+ * after it, events[2] before the convolution kernel (the same point as
+ * events[1]), events[3] after the convolution kernel.  NULL disables.  The
+ * events must outlive the runs that record them. */
 fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]);
 
 /* fconv_run for callers that cannot allocate device memory: a plugin inside

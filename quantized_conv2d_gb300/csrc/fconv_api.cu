@@ -240,18 +240,16 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
 
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
-  if (!skip_pack) {
-    e = fconv::launch_pack_filter(is_int8, w, wt, p->Ktot, p->K, p->Kpad, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "filter pack launch");
-  }
-  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
+  // filter pack and (int8) input widening in one launch
   const void *act = x;
-  if (is_int8) {
-    const long long n = static_cast<long long>(p->N) * p->H * p->W * p->C;
-    e = fconv::launch_widen_i8(static_cast<const int8_t *>(x), xh, n, sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "input widen launch");
-    act = xh;
+  const long long n = static_cast<long long>(p->N) * p->H * p->W * p->C;
+  if (!skip_pack || is_int8) {
+    e = fconv::launch_prep(is_int8, skip_pack ? nullptr : w, wt, p->Ktot, skip_pack ? 0 : p->K,
+                           p->Kpad, static_cast<const int8_t *>(x), xh, n, sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
   }
+  if (is_int8) act = xh;
+  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
 
   CUtensorMap tmap;

@@ -283,6 +283,11 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
                : "l"(p));
   return r;
 }
+__device__ __forceinline__ uint2 ldg_nc_v2(const void *p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
 __device__ __forceinline__ void stg_v4(void *p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)

@@ -50,10 +50,12 @@ cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensor
 // Whether a gather mode has a kernel for this output-channel tile; chunked
 // int8 sums on the cp.async path need a third TMEM region (BN <= 128).
 bool gather_supports(Gather gather, int block_n, bool chunked);
-cudaError_t launch_pack_filter(bool is_int8, const void *w, uint16_t *wt, int RSC, int K,
-                               int Kpad, cudaStream_t stream);
-cudaError_t launch_widen_i8(const int8_t *x, __half *xh, long long n, int sm_count,
-                            cudaStream_t stream);
+// Filter pack ([RSC][K] -> K-major 16-bit [K][Kpad]) and, for int8 plans,
+// the int8 -> fp16 widening of the input (n elements, a multiple of 16), in
+// one launch (a second, tiny one when n is not a multiple of 64).
+cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
+                        const int8_t *x, __half *xh, long long n, int sm_count,
+                        cudaStream_t stream);
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out);
 // Resource description of the kernel whose launch failed last on this thread.
 const char *last_launch_note();

@@ -713,51 +713,114 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 }
 
 // ---------------------------------------------------------------- pre-pass
-// HWIO filter [RSC][K] -> K-major 16-bit [K][Kpad] (zero for k >= RSC);
-// int8 values widen exactly to fp16, bf16 values are copied.
+// One launch prepares the operands of a run: blocks [0, pack_blocks) repack
+// the HWIO filter [RSC][K] into the K-major 16-bit [K][Kpad] the B tiles are
+// loaded from (zero for k >= RSC; int8 widened exactly to fp16, bf16
+// copied), 64 x 64 elements a block; the remaining blocks widen an int8
+// input to fp16, 64 elements a thread per step.
+
+// Four int8 values (one 32-bit word) to two fp16x2 words, exactly: with the
+// sign bit flipped a byte b is u = b + 128 in [0, 255]; the fp16 bit pattern
+// 0x6400 | u is 1024 + u, and subtracting 1152 (0x6480) leaves b.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);   // [u0, 0x64, u1, 0x64]
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);   // [u2, 0x64, u3, 0x64]
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t *>(&ha);
+  hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
+constexpr int kPrepThreads = 256;
+constexpr int kPackTile = 64;
+
 template <bool IS_INT8>
-__global__ void pack_filter_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt,
-                                   int RSC, int K, int Kpad) {
-  __shared__ uint16_t tile[32][33];
-  const int k0 = blockIdx.y * 32, rsc0 = blockIdx.x * 32;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int rsc = rsc0 + i, k = k0 + threadIdx.x;
-    uint16_t v = 0;
-    if (rsc < RSC && k < K) {
-      const long long e = static_cast<long long>(rsc) * K + k;
-      if (IS_INT8)
-        v = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<const int8_t *>(w)[e])));
-      else
-        v = static_cast<const uint16_t *>(w)[e];
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int RSC, int K, int Kpad,
+                int pack_blocks, const int8_t *__restrict__ x, __half *__restrict__ xh,
+                long long n64) {
+  if (static_cast<int>(blockIdx.x) < pack_blocks) {
+    __shared__ uint16_t tile[kPackTile][kPackTile + 2];
+    const int tiles_k = (K + kPackTile - 1) / kPackTile;
+    const int rsc0 = (blockIdx.x / tiles_k) * kPackTile;
+    const int k0 = (blockIdx.x % tiles_k) * kPackTile;
+    // load 64 (rsc) x 64 (k), k fastest: 4 consecutive k per thread
+    for (int e = threadIdx.x; e < kPackTile * kPackTile / 4; e += kPrepThreads) {
+      const int i = e / (kPackTile / 4), j = (e % (kPackTile / 4)) * 4;
+      const int rsc = rsc0 + i;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int k = k0 + j + t;
+        uint16_t v = 0;
+        if (rsc < RSC && k < K) {
+          const long long idx = static_cast<long long>(rsc) * K + k;
+          if (IS_INT8)
+            v = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<const int8_t *>(w)[idx])));
+          else
+            v = static_cast<const uint16_t *>(w)[idx];
+        }
+        tile[i][j + t] = v;
+      }
     }
-    tile[i][threadIdx.x] = v;
+    __syncthreads();
+    // store transposed: 64 (k) rows of 64 (rsc) 16-bit values, 2 per thread
+    for (int e = threadIdx.x; e < kPackTile * kPackTile / 2; e += kPrepThreads) {
+      const int kk = e / (kPackTile / 2), j = (e % (kPackTile / 2)) * 2;
+      const int k = k0 + kk, rsc = rsc0 + j;
+      if (k < K && rsc < Kpad) {
+        const uint32_t v = static_cast<uint32_t>(tile[j][kk]) |
+                           (static_cast<uint32_t>(tile[j + 1][kk]) << 16);
+        *reinterpret_cast<uint32_t *>(wt + static_cast<long long>(k) * Kpad + rsc) = v;
+      }
+    }
+    return;
   }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int k = k0 + i, rsc = rsc0 + threadIdx.x;
-    if (k < K && rsc < Kpad) wt[static_cast<long long>(k) * Kpad + rsc] = tile[threadIdx.x][i];
+  if (!IS_INT8) return;
+  // Widening, warp-contiguous: in one step a warp converts 8 x 256 bytes;
+  // for each of the 8 rounds lane l loads 8 bytes at 8*l of the round (256
+  // contiguous bytes a warp instruction) and stores their 16 fp16 bytes
+  // (512 contiguous bytes a warp instruction).
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x - pack_blocks) * (kPrepThreads / 32);
+  const long long n8 = n64 * 8;
+  for (long long base = (static_cast<long long>(blockIdx.x - pack_blocks) * (kPrepThreads / 32) +
+                         (threadIdx.x >> 5)) * 256;
+       base < n8; base += warps * 256) {
+    uint2 in[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const long long g = base + u * 32 + lane;
+      in[u] = g < n8 ? ldg_nc_v2(x + 8 * g) : make_uint2(0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const long long g = base + u * 32 + lane;
+      if (g < n8) {
+        uint4 o;
+        i8x4_to_f16x4(in[u].x, o.x, o.y);
+        i8x4_to_f16x4(in[u].y, o.z, o.w);
+        stg_v4(xh + 8 * g, o);
+      }
+    }
   }
 }
 
-// int8 -> fp16 (exact), 16 elements per thread per step; n16 = elements / 16.
-__global__ void widen_i8_kernel(const int8_t *__restrict__ x, __half *__restrict__ xh,
-                                long long n16) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint4 in = ldg_nc_v4(x + 16 * i);
-    const uint32_t w4[4] = {in.x, in.y, in.z, in.w};
-    uint32_t out[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t word = w4[e >> 1];
-      const int lo = static_cast<int8_t>((word >> (16 * (e & 1))) & 0xFFu);
-      const int hi = static_cast<int8_t>((word >> (16 * (e & 1) + 8)) & 0xFFu);
-      out[e] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(lo))) |
-               (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(hi))) << 16);
-    }
-    stg_v4(xh + 16 * i, make_uint4(out[0], out[1], out[2], out[3]));
-    stg_v4(xh + 16 * i + 8, make_uint4(out[4], out[5], out[6], out[7]));
-  }
+// int8 -> fp16 for the tail of an input whose size is not a multiple of 64
+// (16 elements a thread; sizes are multiples of 16).
+__global__ void widen_tail_kernel(const int8_t *__restrict__ x, __half *__restrict__ xh,
+                                  long long first16, long long n16) {
+  const long long i = first16 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= n16) return;
+  const uint4 in = ldg_nc_v4(x + 16 * i);
+  uint4 o0, o1;
+  i8x4_to_f16x4(in.x, o0.x, o0.y);
+  i8x4_to_f16x4(in.y, o0.z, o0.w);
+  i8x4_to_f16x4(in.z, o1.x, o1.y);
+  i8x4_to_f16x4(in.w, o1.z, o1.w);
+  stg_v4(xh + 16 * i, o0);
+  stg_v4(xh + 16 * i + 8, o1);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -840,26 +903,31 @@ cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensor
   }
 }
 
-cudaError_t launch_pack_filter(bool is_int8, const void *w, uint16_t *wt, int RSC, int K,
-                               int Kpad, cudaStream_t stream) {
-  dim3 block(32, 8);
-  dim3 grid((Kpad + 31) / 32, (K + 31) / 32);
+cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
+                        const int8_t *x, __half *xh, long long n, int sm_count,
+                        cudaStream_t stream) {
+  const int pack_blocks = ((Kpad + kPackTile - 1) / kPackTile) * ((K + kPackTile - 1) / kPackTile);
+  const long long n64 = is_int8 ? n / 64 : 0;
+  long long widen_blocks = (n64 + kPrepThreads - 1) / kPrepThreads;
+  const long long cap = static_cast<long long>(sm_count) * 4;
+  if (widen_blocks > cap) widen_blocks = cap;
+  const unsigned grid = static_cast<unsigned>(pack_blocks + widen_blocks);
   if (is_int8)
-    pack_filter_kernel<true><<<grid, block, 0, stream>>>(w, wt, RSC, K, Kpad);
+    prep_kernel<true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks, x, xh,
+                                                          n64);
   else
-    pack_filter_kernel<false><<<grid, block, 0, stream>>>(w, wt, RSC, K, Kpad);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_widen_i8(const int8_t *x, __half *xh, long long n, int sm_count,
-                            cudaStream_t stream) {
-  const long long n16 = n / 16;
-  if (n16 == 0) return cudaSuccess;
-  long long blocks = (n16 + 255) / 256;
-  const long long cap = static_cast<long long>(sm_count) * 8;
-  if (blocks > cap) blocks = cap;
-  widen_i8_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, xh, n16);
-  return cudaGetLastError();
+    prep_kernel<false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
+                                                           nullptr, nullptr, 0);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !is_int8) return e;
+  const long long n16 = n / 16, first16 = n64 * 4;
+  if (n16 > first16) {
+    const long long rest = n16 - first16;
+    widen_tail_kernel<<<static_cast<unsigned>((rest + 255) / 256), 256, 0, stream>>>(x, xh, first16,
+                                                                                     n16);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out) {
