@@ -139,6 +139,31 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- ranks
+def reduce_max(value: float, device=None) -> float:
+    """Maximum of a per-rank number over all ranks (the value itself when no
+    process group is running).  Works with any torch.distributed backend."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as tdist
+    if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
+        tdist.barrier()
+
+
+def weak_scaling_tops(world: int, steps: int, ops_per_step: float, max_ms: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of its own batch;
+    the job takes as long as the slowest rank."""
+    return world * steps * ops_per_step / (max_ms / 1e3) / 1e12
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 def time_oracle(wl, P, Q, target_s: float, max_images: int):
     """Time the CPU oracle on a bounded sample (whole images of the workload,
@@ -168,17 +193,19 @@ def run_reference(args, rank, world):
     wl = FI.WORKLOADS[args.workload]
     _, _, P, Q = ops_counts(wl)
     step_target = min(2.0, 150.0 / max(1, args.steps + args.warmup))
-    values, n_img, threads = [], 1, 1
+    values, secs, n_img, threads = [], [], 1, 1
     for i in range(args.warmup + args.steps):
-        v, n_img, _, threads = time_oracle(wl, P, Q, step_target, wl.N)
+        v, n_img, t, threads = time_oracle(wl, P, Q, step_target, wl.N)
         if i >= args.warmup:
             values.append(v)
+            secs.append(t)
     value = statistics.median(values)
     sample = f"{n_img} of {wl.N} images per step (all {wl.K} channels, full epilogue)"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
         "dtype": "int8", "data": "synthetic (seeded)", "config": config_of(wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -218,10 +245,6 @@ def run_fconv(args, rank, world, local_rank):
     x, w, bias, side = to_dev(inp["x"]), to_dev(inp["w"]), to_dev(inp["bias"]), to_dev(inp["side"])
     y = plan.new_output()
     stream = torch.cuda.current_stream(dev)
-    dist = world > 1
-    if dist:
-        import torch.distributed as tdist
-
     def step():
         plan.run(x, w, bias, side, wl.conv_scale, wl.side_scale, y=y, stream=stream)
 
@@ -237,8 +260,7 @@ def run_fconv(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local_rank)
-    if dist:
-        tdist.barrier()
+    barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.25)   # let the sampler start before the timed region
@@ -250,20 +272,16 @@ def run_fconv(args, rank, world, local_rank):
         step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
-    if dist:
-        tdist.barrier()
+    barrier()
     clk = clocks.stop()
     fc.fconv_plan_set_stage_events(plan.handle, None)
     plan.check()
     total_ms = t_start.elapsed_time(t_end)
     conv_ms = [evs[i][2].elapsed_time(evs[i][3]) for i in range(args.steps)]
     prep_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * args.steps * nominal / (total_ms / 1e3) / 1e12
+    value = weak_scaling_tops(world, args.steps, nominal, total_ms)
 
     # ------------------------------------------------ end to end, host buffers
     e2e = None
@@ -288,18 +306,13 @@ def run_fconv(args, rank, world, local_rank):
         for _ in range(3):
             host_step()
         n_e2e = max(3, min(args.steps, 50))
-        if dist:
-            tdist.barrier()
+        barrier()
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             host_step()
-        el = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([el], device=dev)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            el = float(t.item())
+        el = reduce_max(time.perf_counter() - t0, dev)
         plan.check()
-        e2e = {"value": world * n_e2e * nominal / el / 1e12, "unit": UNIT,
+        e2e = {"value": weak_scaling_tops(world, n_e2e, nominal, el * 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": n_e2e}
         del dws
