@@ -210,6 +210,11 @@ fconv_status fconv_run_no_alloc(fconv_plan *plan, const void *x, const void *w,
                                 float conv_scale, float side_scale, void *y,
                                 fconv_stream_t stream);
 
+/* Which convolution kernel the plan's next run uses: "tma-im2col" (A
+ * gathered by TMA im2col loads) or "cp-async" (the general gather).  Static
+ * text; "" for a NULL plan. */
+const char *fconv_plan_kernel(const fconv_plan *plan);
+
 /* Static text for a status code. */
 const char *fconv_status_string(fconv_status status);
 

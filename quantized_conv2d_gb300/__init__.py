@@ -80,6 +80,8 @@ def _load():
         fn.restype = i32
     lib.fconv_status_string.argtypes = [i32]
     lib.fconv_status_string.restype = ctypes.c_char_p
+    lib.fconv_plan_kernel.argtypes = [p]
+    lib.fconv_plan_kernel.restype = ctypes.c_char_p
     lib.fconv_last_error.argtypes = []
     lib.fconv_last_error.restype = ctypes.c_char_p
     _lib = lib
@@ -163,6 +165,10 @@ def fconv_run_host(plan, x_host, w_host, bias_host, side_host, conv_scale, side_
 
 def fconv_plan_set_host_chunks(plan, chunks: int) -> None:
     _check(_load().fconv_plan_set_host_chunks(plan, chunks), "fconv_plan_set_host_chunks")
+
+
+def fconv_plan_kernel(plan) -> str:
+    return _load().fconv_plan_kernel(plan).decode()
 
 
 def fconv_plan_check(plan, stream) -> None:

@@ -111,6 +111,11 @@ fconv::Gather gather_for(const fconv_plan &p, int bn, bool force_cpasync) {
   return fconv::Gather::kCpAsync;
 }
 
+// The gather the next run of a plan uses.
+fconv::Gather gather_for_run(const fconv_plan &p) {
+  return gather_for(p, p.block_n, (p.debug & FCONV_DEBUG_GATHER_CPASYNC) != 0);
+}
+
 // Output-channel tile: the candidate with the least estimated time.  A
 // k-block costs about max(2*BN, G) cycles: the 128 x BN x 64 MMA takes ~2*BN
 // and loading the 16 KB A tile costs a fixed G (~600 cycles by TMA im2col,
@@ -195,8 +200,6 @@ int device_sm_count(int *dev_out) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool force_cpasync(const fconv_plan &p) { return (p.debug & FCONV_DEBUG_GATHER_CPASYNC) != 0; }
-
 // Scratch a run needs: the packed filter, and for int8 plans the fp16 copy of
 // the input the gathers read.
 size_t workspace_need(const fconv_plan &p) { return p.wt_bytes + p.xh_bytes; }
@@ -232,7 +235,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   uint16_t *wt = static_cast<uint16_t *>(workspace);
   __half *xh = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + p->wt_bytes);
 
-  const fconv::Gather gather = gather_for(*p, p->block_n, force_cpasync(*p));
+  const fconv::Gather gather = gather_for_run(*p);
   if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb))
     return fail(FCONV_ERR_NOT_SUPPORTED,
                 "tile %d has no cp.async kernel for a sum of %d k-values (chunked sums need "
@@ -310,7 +313,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.mode = mode;
   a.debug = p->debug;
   a.timeout_ns = static_cast<unsigned long long>(p->timeout_ms) * 1000000ull;
-  const int grid = p->num_tiles < sms ? p->num_tiles : sms;
+  const int grid = a.num_tiles < sms ? a.num_tiles : sms;
   e = fconv::launch_conv(p->block_n, is_int8, gather, tmap_a, tmap, a, grid, stream);
   if (e != cudaSuccess)
     return fail(FCONV_ERR_CUDA, "convolution launch: %s (%s)", cudaGetErrorString(e),
@@ -679,6 +682,11 @@ fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]
   for (int i = 0; i < 4; ++i) plan->events[i] = static_cast<cudaEvent_t>(events[i]);
   plan->use_events = true;
   return FCONV_OK;
+}
+
+const char *fconv_plan_kernel(const fconv_plan *plan) {
+  if (!plan) return "";
+  return gather_for_run(*plan) == fconv::Gather::kTmaIm2col ? "tma-im2col" : "cp-async";
 }
 
 const char *fconv_status_string(fconv_status s) {
