@@ -116,6 +116,22 @@ fconv_status fconv_run(fconv_plan *plan, const void *x, const void *w,
                        float side_scale, void *y, void *workspace,
                        size_t workspace_bytes, fconv_stream_t stream);
 
+/* fconv_run with a per-output-channel conv_input_scale.
+ * "conv_ops_fused_int8.cc" (TensorFlow), BiasActivationOutputKernel, step
+ * (1) Scale: when the conv_input_scale tensor holds more than one element,
+ * output channel k is scaled by its k-th element; otherwise by the scalar.
+ * conv_scale: device fp32 [K], 16-byte aligned, read-only; y[..., k] is
+ * computed with conv_scale[k] in step (1), every other step as in
+ * fconv_run.  NULL conv_scale gives FCONV_ERR_INVALID_VALUE, a misaligned
+ * one FCONV_ERR_MISALIGNED.  Same ownership, workspace and stream rules as
+ * fconv_run. */
+fconv_status fconv_run_channel_scale(fconv_plan *plan, const void *x,
+                                     const void *w, const float *bias,
+                                     const void *side, const float *conv_scale,
+                                     float side_scale, void *y, void *workspace,
+                                     size_t workspace_bytes,
+                                     fconv_stream_t stream);
+
 /* The convolution sums alone, before the epilogue: int32 [N][P][Q][K] for
  * int8 plans (exact), fp32 for bf16 plans.  Same rules as fconv_run. */
 fconv_status fconv_run_accumulators(fconv_plan *plan, const void *x,

@@ -67,8 +67,8 @@ def _load():
         lib.orc_im2col.argtypes = [p, i32] + [i32] * 11 + [p]
         lib.orc_gemm_i8.argtypes = [p, p, i32, i32, i32, p]
         lib.orc_conv_i8_im2col.argtypes = [p, p] + [i32] * 13 + [p, p]
-        lib.orc_epilogue_i8.argtypes = [p, i64, i32, p, p, f32, f32, i32, p]
-        lib.orc_epilogue_f64.argtypes = [p, i64, i32, p, p, f64, f64, i32, p]
+        lib.orc_epilogue_i8.argtypes = [p, i64, i32, p, p, f32, p, f32, i32, p]
+        lib.orc_epilogue_f64.argtypes = [p, i64, i32, p, p, f64, p, f64, i32, p]
         lib.orc_num_threads.restype = i32
         for name in ("orc_conv_i8_direct", "orc_conv_i8_points",
                      "orc_conv_bf16_direct_f64", "orc_conv_bf16_points_f64",
@@ -205,9 +205,20 @@ def conv_acc_bf16_points_f64(x_bits, w_bits, idx, stride=1, padding=SAME) -> np.
     return out
 
 
+def _scale_args(conv_scale, K):
+    """(scalar, per-channel array or None): conv_scale is a number, or K
+    values, one per output channel."""
+    if np.ndim(conv_scale) == 0:
+        return float(conv_scale), None
+    sk = np.ascontiguousarray(conv_scale, dtype=np.float32)
+    assert sk.shape == (K,)
+    return 0.0, sk
+
+
 def epilogue_i8(acc: np.ndarray, bias: np.ndarray, side: np.ndarray | None,
-                conv_scale: float, side_scale: float, relu: bool) -> np.ndarray:
-    """BiasActivationOutputKernel on int32 sums shaped [..., K] -> int8."""
+                conv_scale, side_scale: float, relu: bool) -> np.ndarray:
+    """BiasActivationOutputKernel on int32 sums shaped [..., K] -> int8.
+    conv_scale: a scalar, or K fp32 values (one per output channel)."""
     acc = np.ascontiguousarray(acc, dtype=np.int32)
     K = acc.shape[-1]
     bias = np.ascontiguousarray(bias, dtype=np.float32)
@@ -215,15 +226,16 @@ def epilogue_i8(acc: np.ndarray, bias: np.ndarray, side: np.ndarray | None,
     if side is not None:
         side = np.ascontiguousarray(side, dtype=np.int8)
         assert side.shape == acc.shape
+    cs, sk = _scale_args(conv_scale, K)
     out = np.empty(acc.shape, dtype=np.int8)
     _load().orc_epilogue_i8(_ptr(acc), acc.size // K, K, _ptr(bias), _ptr(side),
-                            float(np.float32(conv_scale)), float(np.float32(side_scale)),
+                            float(np.float32(cs)), _ptr(sk), float(np.float32(side_scale)),
                             int(bool(relu)), _ptr(out))
     return out
 
 
 def epilogue_f64(acc: np.ndarray, bias: np.ndarray, side_bits: np.ndarray | None,
-                 conv_scale: float, side_scale: float, relu: bool) -> np.ndarray:
+                 conv_scale, side_scale: float, relu: bool) -> np.ndarray:
     """fp64 reference epilogue of the bf16 variant (no output rounding)."""
     acc = np.ascontiguousarray(acc, dtype=np.float64)
     K = acc.shape[-1]
@@ -231,9 +243,10 @@ def epilogue_f64(acc: np.ndarray, bias: np.ndarray, side_bits: np.ndarray | None
     if side_bits is not None:
         side_bits = np.ascontiguousarray(side_bits, dtype=np.uint16)
         assert side_bits.shape == acc.shape
+    cs, sk = _scale_args(conv_scale, K)
     out = np.empty(acc.shape, dtype=np.float64)
     _load().orc_epilogue_f64(_ptr(acc), acc.size // K, K, _ptr(bias), _ptr(side_bits),
-                             float(conv_scale), float(side_scale), int(bool(relu)), _ptr(out))
+                             cs, _ptr(sk), float(side_scale), int(bool(relu)), _ptr(out))
     return out
 
 

@@ -12,7 +12,9 @@
  *    LaunchFusedConv2DOpCpuInt8Helper: the fused op is a 2-D
  *    cross-correlation of an NHWC int8 input with an HWIO int8 filter,
  *    followed by the BiasActivationOutputKernel epilogue:
- *      (1) y = conv_output * conv_input_scale           (fp32, one rounding)
+ *      (1) y = conv_output * conv_input_scale           (fp32, one rounding;
+ *          conv_input_scale is a scalar, or one value per output channel
+ *          when its tensor holds more than one element)
  *      (2) y = fmaf(side_input, side_input_scale, y)    (only if the side
  *          input is present and side_input_scale != 0; one rounding)
  *      (3) y = y + bias[k]                               (fp32, one rounding)
@@ -278,10 +280,14 @@ void orc_conv_i8_im2col(const int8_t *x, const int8_t *w, int N, int H, int W,
 }
 
 /* The epilogue of BiasActivationOutputKernel ("conv_ops_fused_int8.cc"),
- * applied to rows x K exact int32 sums.  side may be NULL. */
+ * applied to rows x K exact int32 sums.  side may be NULL.  conv_scale_k is
+ * NULL for a scalar conv_input_scale, else its K per-channel values (the
+ * kernel's step (1) offsets the scale pointer by the output channel when the
+ * scale tensor holds more than one element). */
 void orc_epilogue_i8(const int32_t *acc, long long rows, int K,
                      const float *bias, const int8_t *side, float conv_scale,
-                     float side_scale, int relu, int8_t *out) {
+                     const float *conv_scale_k, float side_scale, int relu,
+                     int8_t *out) {
   const float lower = relu ? 0.0f : -128.0f;
   const float upper = 127.0f;
   const int use_side = (side != NULL) && (side_scale != 0.0f);
@@ -290,7 +296,8 @@ void orc_epilogue_i8(const int32_t *acc, long long rows, int K,
     for (int k = 0; k < K; ++k) {
       long long e = i * K + k;
       float v = (float)acc[e];          /* int32 -> fp32, round to nearest even */
-      v = v * conv_scale;               /* (1) scale */
+      /* (1) scale: per output channel when a [K] vector is given */
+      v = v * (conv_scale_k ? conv_scale_k[k] : conv_scale);
       if (use_side)                     /* (2) side input, one fused rounding */
         v = fmaf((float)side[e], side_scale, v);
       v = v + bias[k];                  /* (3) bias */
@@ -306,14 +313,14 @@ void orc_epilogue_i8(const int32_t *acc, long long rows, int K,
  * rounding).  side holds bf16 bit patterns and may be NULL. */
 void orc_epilogue_f64(const double *acc, long long rows, int K,
                       const float *bias, const uint16_t *side,
-                      double conv_scale, double side_scale, int relu,
-                      double *out) {
+                      double conv_scale, const float *conv_scale_k,
+                      double side_scale, int relu, double *out) {
   const int use_side = (side != NULL) && (side_scale != 0.0);
 #pragma omp parallel for schedule(static)
   for (long long i = 0; i < rows; ++i) {
     for (int k = 0; k < K; ++k) {
       long long e = i * K + k;
-      double v = acc[e] * conv_scale;
+      double v = acc[e] * (conv_scale_k ? (double)conv_scale_k[k] : conv_scale);
       if (use_side) v = bf16_value(side[e]) * side_scale + v;
       v = v + (double)bias[k];
       if (relu && v < 0.0) v = 0.0;

@@ -62,6 +62,7 @@ def _load():
         "fconv_plan_padding": [p, pi, pi, pi, pi],
         "fconv_workspace_size": [p, psz],
         "fconv_run": [p, p, p, p, p, f32, f32, p, p, sz, p],
+        "fconv_run_channel_scale": [p, p, p, p, p, p, f32, p, p, sz, p],
         "fconv_run_accumulators": [p, p, p, p, p, sz, p],
         "fconv_host_workspace_size": [p, i32, psz],
         "fconv_run_host": [p, p, p, p, p, f32, f32, p, p, sz, p],
@@ -135,6 +136,15 @@ def fconv_run(plan, x, w, bias, side, conv_scale, side_scale, y, workspace, work
               stream) -> None:
     _check(_load().fconv_run(plan, x, w, bias, side, conv_scale, side_scale, y, workspace,
                              workspace_bytes, stream), "fconv_run")
+
+
+def fconv_run_channel_scale(plan, x, w, bias, side, conv_scale, side_scale, y, workspace,
+                            workspace_bytes, stream) -> None:
+    """fconv_run with conv_scale a device fp32 [K] pointer (one scale per
+    output channel)."""
+    _check(_load().fconv_run_channel_scale(plan, x, w, bias, side, conv_scale, side_scale, y,
+                                           workspace, workspace_bytes, stream),
+           "fconv_run_channel_scale")
 
 
 def fconv_run_no_alloc(plan, x, w, bias, side, conv_scale, side_scale, y, stream) -> None:
@@ -250,14 +260,24 @@ class Conv2dPlan:
         self.ws_bytes = need
 
     def run(self, x, w, bias, side=None, conv_scale=1.0, side_scale=0.0, y=None, stream=None):
+        """conv_scale: a Python float, or a device fp32 tensor of K elements
+        (one scale per output channel)."""
         import torch
         self._ensure_workspace()
         if y is None:
             y = self.new_output()
         st = stream if stream is not None else torch.cuda.current_stream(self.device)
-        fconv_run(self.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(side), conv_scale,
-                  side_scale, _ptr(y), _ptr(self.workspace), self.workspace.numel(),
-                  _stream_handle(st))
+        if isinstance(conv_scale, torch.Tensor):
+            if conv_scale.dtype != torch.float32 or conv_scale.numel() != self.out_shape[3]:
+                raise ValueError("a per-channel conv_scale is a float32 tensor of K elements")
+            fconv_run_channel_scale(self.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(side),
+                                    _ptr(conv_scale), side_scale, _ptr(y),
+                                    _ptr(self.workspace), self.workspace.numel(),
+                                    _stream_handle(st))
+        else:
+            fconv_run(self.handle, _ptr(x), _ptr(w), _ptr(bias), _ptr(side), conv_scale,
+                      side_scale, _ptr(y), _ptr(self.workspace), self.workspace.numel(),
+                      _stream_handle(st))
         return y
 
     def accumulators(self, x, w, acc=None, stream=None):

@@ -207,14 +207,15 @@ size_t workspace_need(const fconv_plan &p) { return p.wt_bytes + p.xh_bytes; }
 fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *bias,
                      const void *side, float conv_scale, float side_scale, void *y,
                      void *workspace, size_t workspace_bytes, cudaStream_t stream, int mode,
-                     bool skip_pack = false) {
+                     bool skip_pack = false, const float *scale_k = nullptr) {
   if (!p) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
   if (!x || !w || !y) return fail(FCONV_ERR_INVALID_VALUE, "x, w and y must not be NULL");
   if (mode == fconv::kModeFused && !bias)
     return fail(FCONV_ERR_INVALID_VALUE, "bias must not be NULL");
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || (side && !aligned(side, 16)) ||
-      (bias && !aligned(bias, 16)))
-    return fail(FCONV_ERR_MISALIGNED, "x, w, y, side and bias must be 16-byte aligned");
+      (bias && !aligned(bias, 16)) || (scale_k && !aligned(scale_k, 16)))
+    return fail(FCONV_ERR_MISALIGNED,
+                "x, w, y, side, bias and the per-channel scale must be 16-byte aligned");
   const size_t need = workspace_need(*p);
   if (!workspace || workspace_bytes < need)
     return fail(FCONV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -298,6 +299,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.use_side = (mode == fconv::kModeFused && side != nullptr && side_scale != 0.0f) ? 1 : 0;
   a.side = a.use_side ? side : nullptr;
   a.bias = bias;
+  a.scale_k = mode == fconv::kModeFused ? scale_k : nullptr;
   a.y = y;
   a.N = p->N; a.H = p->H; a.W = p->W; a.C = p->C; a.K = p->K; a.R = p->R; a.S = p->S;
   a.sh = p->sh; a.sw = p->sw; a.pt = p->pt; a.pl = p->pl; a.P = p->P; a.Q = p->Q;
@@ -489,6 +491,16 @@ fconv_status fconv_run(fconv_plan *plan, const void *x, const void *w, const flo
                        void *workspace, size_t workspace_bytes, fconv_stream_t stream) {
   return enqueue(plan, x, w, bias, side, conv_scale, side_scale, y, workspace, workspace_bytes,
                  reinterpret_cast<cudaStream_t>(stream), fconv::kModeFused);
+}
+
+fconv_status fconv_run_channel_scale(fconv_plan *plan, const void *x, const void *w,
+                                     const float *bias, const void *side,
+                                     const float *conv_scale, float side_scale, void *y,
+                                     void *workspace, size_t workspace_bytes,
+                                     fconv_stream_t stream) {
+  if (!conv_scale) return fail(FCONV_ERR_INVALID_VALUE, "conv_scale must not be NULL");
+  return enqueue(plan, x, w, bias, side, 0.0f, side_scale, y, workspace, workspace_bytes,
+                 reinterpret_cast<cudaStream_t>(stream), fconv::kModeFused, false, conv_scale);
 }
 
 fconv_status fconv_run_accumulators(fconv_plan *plan, const void *x, const void *w, void *acc,

@@ -22,6 +22,7 @@ struct ConvArgs {
   const void *a;       // activations NHWC, 16-bit (fp16 widened from int8, or bf16)
   const void *side;    // side input NHWC [M][K] (int8 or bf16), or nullptr
   const float *bias;   // [K]
+  const float *scale_k;  // per-output-channel conv_input_scale [K], or nullptr (scalar)
   void *y;             // output [M][K] (int8/bf16, or int32/fp32 sums)
   int N, H, W, C, K, R, S, sh, sw, pt, pl, P, Q;
   long long M;         // N * P * Q

@@ -138,16 +138,19 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
       uint32_t out[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        // bias: every lane reads the same 16 bytes (a broadcast)
+        // bias (and per-channel scale): every lane reads the same 16 bytes
         const float4 bb = __ldg(reinterpret_cast<const float4 *>(a.bias + col + 4 * g));
         const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+        const float4 sc = a.scale_k ? __ldg(reinterpret_cast<const float4 *>(a.scale_k + col + 4 * g))
+                                    : make_float4(cs, cs, cs, cs);
+        const float sv4[4] = {sc.x, sc.y, sc.z, sc.w};
         uint32_t word = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           // (1) scale; (2) side input, one fused rounding; (3) bias.  The
           // explicit round-to-nearest intrinsics keep nvcc from contracting
           // (1) and (3) into an fma.
-          float v = __fmul_rn(vals[16 * h + 4 * g + e], cs);
+          float v = __fmul_rn(vals[16 * h + 4 * g + e], sv4[e]);
           if (use_side) {
             const float sd = static_cast<float>(static_cast<int8_t>((sw[g] >> (8 * e)) & 0xFFu));
             v = __fmaf_rn(sd, ss, v);
@@ -172,13 +175,23 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
       const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + col));
       const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + col + 4));
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      float sv8[8];
+      if (a.scale_k) {
+        const float4 s0 = __ldg(reinterpret_cast<const float4 *>(a.scale_k + col));
+        const float4 s1 = __ldg(reinterpret_cast<const float4 *>(a.scale_k + col + 4));
+        sv8[0] = s0.x; sv8[1] = s0.y; sv8[2] = s0.z; sv8[3] = s0.w;
+        sv8[4] = s1.x; sv8[5] = s1.y; sv8[6] = s1.z; sv8[7] = s1.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) sv8[t] = cs;
+      }
       uint32_t out[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t word = 0;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          float v = __fmul_rn(vals[8 * qd + 2 * g + t], cs);
+          float v = __fmul_rn(vals[8 * qd + 2 * g + t], sv8[2 * g + t]);
           if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
           v = __fadd_rn(v, bv[2 * g + t]);
           if (a.relu) v = fmaxf(v, 0.0f);

@@ -74,7 +74,10 @@ class Case:
         x, w = to_dev(self.x, self.dtype), to_dev(self.w, self.dtype)
         bias = torch.from_numpy(self.bias).cuda()
         side = to_dev(self.side, self.dtype)
-        y = p.run(x, w, bias, side, self.conv_scale, self.side_scale, stream=stream)
+        cs = self.conv_scale
+        if np.ndim(cs) > 0:   # one scale per output channel, a device [K] fp32 vector
+            cs = torch.from_numpy(np.ascontiguousarray(cs, dtype=np.float32)).cuda()
+        y = p.run(x, w, bias, side, cs, self.side_scale, stream=stream)
         p.check(stream)
         out = to_host(y)
         p.close()

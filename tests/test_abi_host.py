@@ -158,6 +158,11 @@ def test_run_argument_errors_before_any_launch():
         assert _err(fc.fconv_run, h, A, A, A, None, 1.0, 0.0, A, A, ws - 1, None) == fc.FCONV_ERR_WORKSPACE
         assert _err(fc.fconv_run, h, A, A, A, None, 1.0, 0.0, A, None, ws, None) == fc.FCONV_ERR_WORKSPACE
         assert _err(fc.fconv_run, h, A, A, A, None, 1.0, 0.0, A, A + 16, ws, None) == fc.FCONV_ERR_MISALIGNED
+        # per-channel scale: NULL vector, misaligned vector
+        assert _err(fc.fconv_run_channel_scale, h, A, A, A, None, None, 0.0, A, A, ws,
+                    None) == fc.FCONV_ERR_INVALID_VALUE
+        assert _err(fc.fconv_run_channel_scale, h, A, A, A, None, A + 4, 0.0, A, A, ws,
+                    None) == fc.FCONV_ERR_MISALIGNED
         assert _err(fc.fconv_plan_set_timeout_ms, h, 0) == fc.FCONV_ERR_INVALID_VALUE
         assert _err(fc.fconv_plan_set_debug, h, 8) == fc.FCONV_ERR_INVALID_VALUE
     finally:

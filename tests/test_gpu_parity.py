@@ -300,3 +300,43 @@ def test_misaligned_device_pointer_is_rejected():
                      torch.cuda.current_stream().cuda_stream)
     assert ei.value.status == fc.FCONV_ERR_MISALIGNED
     p.close()
+
+
+# ---------------------------------------------------------------- per-channel scale
+# (shape, dtype): TMA gather (C % 64 == 0) and cp.async gather, chunked int8
+# sums, K tails past 32/64/128-wide tiles
+CHANNEL_SCALE_SHAPES = [
+    ((2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, True), "int8"),
+    ((2, 9, 11, 48, 144, 3, 3, 2, "SAME", True, False), "int8"),
+    ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True), "int8"),
+    ((3, 8, 8, 64, 200, 3, 3, 1, "SAME", True, False), "bf16"),
+    ((2, 7, 9, 24, 40, 3, 3, 1, "VALID", False, True), "bf16"),
+]
+
+
+def _channel_scales(seed, K, dtype):
+    rng = np.random.default_rng(seed)
+    if dtype == "int8":
+        # a different binade per channel: a wrong channel index moves outputs
+        return (2.0 ** rng.integers(-13, -8, size=K) * rng.uniform(1, 2, size=K)).astype(np.float32)
+    return rng.uniform(0.25, 4.0, size=K).astype(np.float32)
+
+
+@pytest.mark.parametrize("i,item", list(enumerate(CHANNEL_SCALE_SHAPES)))
+def test_per_channel_conv_scale(i, item):
+    params, dtype = item
+    c = sweep_case(300 + i, params, dtype)
+    c.conv_scale = _channel_scales(300 + i, c.K, dtype)
+    acc_ref = c.oracle_acc()
+    c.check_output(c.run_gpu(), c.oracle_out(acc_ref))
+    if params[3] % 64 == 0:
+        c.check_output(c.run_gpu(debug=fc.FCONV_DEBUG_GATHER_CPASYNC), c.oracle_out(acc_ref))
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+def test_equal_channel_scales_equal_the_scalar_run(dtype):
+    c = sweep_case(320, (2, 10, 10, 64, 96, 3, 3, 1, "SAME", True, True), dtype)
+    scalar = c.run_gpu()
+    c.conv_scale = np.full(c.K, c.conv_scale, np.float32)
+    assert np.array_equal(c.run_gpu(), scalar)
+

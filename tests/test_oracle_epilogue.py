@@ -99,3 +99,51 @@ def test_exact_rounding_helper_pins():
     assert exact.round_half_even_int(Fraction(5, 2)) == 2
     assert exact.round_half_even_int(Fraction(-5, 2)) == -2
     assert exact.round_half_even_int(Fraction(7, 2)) == 4
+
+
+# ---------------------------------------------------------------- per-channel scale
+# BiasActivationOutputKernel, step (1) Scale: a conv_input_scale tensor of more
+# than one element is read at the output channel's offset, one value per k.
+
+def test_per_channel_scale_matches_exact_rational():
+    rng = np.random.default_rng(21)
+    rows, K = 40, 24
+    acc = rng.integers(-3_000_000, 3_000_000, size=(rows, K)).astype(np.int32)
+    side = rng.integers(-128, 128, size=(rows, K)).astype(np.int8)
+    bias = rng.normal(0.0, 3.0, size=K).astype(np.float32)
+    # scales spread over many binades so a wrong channel index changes results
+    sk = (2.0 ** rng.integers(-24, -12, size=K) * rng.uniform(1, 2, size=K)).astype(np.float32)
+    for relu in (False, True):
+        got = oracle.epilogue_i8(acc, bias, side, sk, 0.75, relu)
+        for i in range(rows):
+            for k in range(K):
+                want = exact.epilogue_i8(int(acc[i, k]), float(sk[k]), int(side[i, k]), 0.75,
+                                         float(bias[k]), relu)
+                assert got[i, k] == want, (i, k, relu)
+
+
+def test_per_channel_scale_with_equal_values_is_the_scalar_epilogue():
+    rng = np.random.default_rng(22)
+    acc = rng.integers(-2 ** 22, 2 ** 22, size=(300, 32)).astype(np.int32)
+    bias = rng.normal(0.0, 1.0, size=32).astype(np.float32)
+    side = rng.integers(-128, 128, size=acc.shape).astype(np.int8)
+    for cs in (0.002, 1.0 / 3.0, 2.0 ** -17):
+        vec = np.full(32, cs, np.float32)
+        for relu in (False, True):
+            assert np.array_equal(oracle.epilogue_i8(acc, bias, side, vec, 0.5, relu),
+                                  oracle.epilogue_i8(acc, bias, side, cs, 0.5, relu))
+
+
+def test_per_channel_scale_f64_reference():
+    rng = np.random.default_rng(23)
+    acc = rng.normal(0.0, 50.0, size=(64, 16))
+    bias = rng.normal(0.0, 0.1, size=16).astype(np.float32)
+    sk = rng.uniform(0.25, 4.0, size=16).astype(np.float32)
+    side_bits = (np.arange(64 * 16, dtype=np.uint32).reshape(64, 16) % 7 + 0x3F80).astype(np.uint16)
+    got = oracle.epilogue_f64(acc, bias, side_bits, sk, 0.5, False)
+    side = oracle.bf16_bits_to_f64(side_bits)
+    # written out per element in fp64: acc*s[k] + side*0.5 + bias[k]
+    for i in range(64):
+        for k in range(16):
+            want = acc[i, k] * float(sk[k]) + side[i, k] * 0.5 + float(bias[k])
+            assert got[i, k] == want
