@@ -38,7 +38,11 @@
  * only bind buffers.
  *
  * Ownership and errors: the caller owns every buffer and the stream; a plan
- * owns only host memory.  Every call returns a status and never aborts.
+ * owns only host memory (its settings and the TMA descriptors of its last
+ * run, re-encoded when a tensor's address changes).  A plan is used by one
+ * host thread at a time; different plans are independent.  Runs capture
+ * into CUDA graphs (after one run outside the capture on that device).
+ * Every call returns a status and never aborts.
  * Device pointers must be device-accessible memory of the current device.
  * Runs are asynchronous on the given stream; a kernel that gives up waiting
  * (a stalled pipeline) records FCONV_ERR_TIMEOUT in a per-device word that

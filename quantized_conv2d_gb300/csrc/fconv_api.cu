@@ -35,6 +35,14 @@ struct fconv_plan {
   int pipe_dev;     // device the streams/events below belong to, -1 = none
   cudaStream_t s_in, s_out;
   cudaEvent_t ev_entry, ev_out, ev_in[16], ev_comp[16];
+  // tensor maps of the last run, reused while what they encode is unchanged
+  // (the tensor's address, the batch size, the tile)
+  struct MapCache {
+    bool valid;
+    const void *base;
+    int n, block_n;
+    CUtensorMap map;
+  } map_a, map_b;
 };
 
 constexpr int kMaxHostChunks = 16;
@@ -256,21 +264,32 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
 
-  CUtensorMap tmap;
-  memset(&tmap, 0, sizeof tmap);
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->Kpad), static_cast<cuuint64_t>(p->K)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->Kpad) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(p->block_n)};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult cr = encode(&tmap, is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                       2, wt, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
+  fconv_plan::MapCache &mb = p->map_b;
+  if (!(mb.valid && mb.base == wt && mb.block_n == p->block_n)) {
+    mb.valid = false;
+    memset(&mb.map, 0, sizeof mb.map);
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->Kpad), static_cast<cuuint64_t>(p->K)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->Kpad) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(p->block_n)};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult cr = encode(&mb.map,
+                         is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, wt, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS)
+      return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
+    mb.base = wt;
+    mb.block_n = p->block_n;
+    mb.valid = true;
+  }
+  const CUtensorMap &tmap = mb.map;
 
-  CUtensorMap tmap_a;
-  memset(&tmap_a, 0, sizeof tmap_a);
-  if (gather == fconv::Gather::kTmaIm2col) {
+  fconv_plan::MapCache &ma = p->map_a;
+  if (gather == fconv::Gather::kTmaIm2col && !(ma.valid && ma.base == act && ma.n == p->N)) {
+    ma.valid = false;
+    memset(&ma.map, 0, sizeof ma.map);
+    CUtensorMap &tmap_a = ma.map;
     PFN_cuTensorMapEncodeIm2col_v12000 enc_a = encode_im2col_fn();
     if (!enc_a) return fail(FCONV_ERR_CUDA, "cuTensorMapEncodeIm2col is unavailable");
     // NHWC, innermost first: C, W, H, N.  The bounding box of filter-window
@@ -291,7 +310,12 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cra != CUDA_SUCCESS)
       return fail(FCONV_ERR_INTERNAL, "im2col tensor map encode failed (%d)", (int)cra);
+    ma.base = act;
+    ma.n = p->N;
+    ma.valid = true;
   }
+  static const CUtensorMap kNoMap = {};
+  const CUtensorMap &tmap_a = gather == fconv::Gather::kTmaIm2col ? ma.map : kNoMap;
 
   fconv::ConvArgs a;
   memset(&a, 0, sizeof a);

@@ -30,6 +30,7 @@
 //              three fp32 steps, rounding, saturation, 16-byte stores.
 // The accumulator is double-buffered in TMEM so the epilogue of one tile
 // overlaps the mainloop of the next.
+#include <atomic>
 #include <cstdio>
 
 #include "fconv_device.cuh"
@@ -837,12 +838,27 @@ __global__ void widen_tail_kernel(const int8_t *__restrict__ x, __half *__restri
 }
 
 // ---------------------------------------------------------------- launchers
+// Raise a kernel's dynamic shared-memory limit once per device (the
+// attribute call costs host time on every launch otherwise, and is best kept
+// out of CUDA-graph captures).  `done` holds one bit per device ordinal.
+template <typename Kern>
+static cudaError_t ensure_smem_limit(Kern kern, int smem, std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 template <int BN, bool IS_INT8>
 static cudaError_t launch_cpasync_t(const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
                                     cudaStream_t stream) {
   auto kern = conv_fprop_cpasync_kernel<BN, IS_INT8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<BN>::kSmemBytes);
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = ensure_smem_limit(kern, Cfg<BN>::kSmemBytes, configured);
   if (e == cudaSuccess) {
     kern<<<grid, kThreads, Cfg<BN>::kSmemBytes, stream>>>(tmap_b, args);
     e = cudaGetLastError();
@@ -870,8 +886,8 @@ template <int BN, bool IS_INT8>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                                 const ConvArgs &args, int grid, cudaStream_t stream) {
   auto kern = conv_fprop_tma_kernel<BN, IS_INT8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TmaCfg<BN>::kSmemBytes);
+  static std::atomic<unsigned long long> configured{0};
+  cudaError_t e = ensure_smem_limit(kern, TmaCfg<BN>::kSmemBytes, configured);
   if (e == cudaSuccess) {
     kern<<<grid, kTmaThreads, TmaCfg<BN>::kSmemBytes, stream>>>(tmap_a, tmap_b, args);
     e = cudaGetLastError();

@@ -340,3 +340,29 @@ def test_equal_channel_scales_equal_the_scalar_run(dtype):
     c.conv_scale = np.full(c.K, c.conv_scale, np.float32)
     assert np.array_equal(c.run_gpu(), scalar)
 
+
+
+def test_run_replays_from_a_cuda_graph():
+    """A captured fconv_run replays on new contents of the same buffers."""
+    params = (2, 10, 10, 64, 96, 3, 3, 1, "SAME", True, True)
+    first, second = sweep_case(330, params, "int8"), sweep_case(331, params, "int8")
+    p = first.plan()
+    x, w = to_dev(first.x, "int8"), to_dev(first.w, "int8")
+    bias, side = torch.from_numpy(first.bias).cuda(), to_dev(first.side, "int8")
+    y = p.new_output()
+    p.run(x, w, bias, side, first.conv_scale, first.side_scale, y=y)   # outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        p.run(x, w, bias, side, first.conv_scale, first.side_scale, y=y)
+    for c in (second, first):
+        x.copy_(to_dev(c.x, "int8"))
+        w.copy_(to_dev(c.w, "int8"))
+        bias.copy_(torch.from_numpy(c.bias).cuda())
+        side.copy_(to_dev(c.side, "int8"))
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        p.check()
+        c.check_output(to_host(y), c.oracle_out())
+    p.close()
