@@ -126,8 +126,11 @@ fconv::Gather gather_for_run(const fconv_plan &p) {
 
 // Output-channel tile: the candidate with the least estimated time.  A
 // k-block costs about max(2*BN, G) cycles: the 128 x BN x 64 MMA takes ~2*BN
-// and loading the 16 KB A tile costs a fixed G (~600 cycles by TMA im2col,
-// ~800 by cp.async) whatever BN is; tiles run in waves over the SMs.
+// on the tensor core, and the issuing threads' per-k-block work (barrier
+// waits, copy and MMA issue) a fixed G whatever BN is (~360 on the TMA path,
+// ~800 on the cp.async path, measured).  Tiles run in waves over the SMs;
+// the epilogue of a CTA's last tile (~8 cycles per output column) is not
+// hidden behind a next tile's mainloop.
 int choose_block_n(const fconv_plan &p, int sms) {
   const long long m_tiles = (p.M + 127) / 128;
   const bool chunked = p.kb_chunk < p.num_kb;
@@ -138,10 +141,10 @@ int choose_block_n(const fconv_plan &p, int sms) {
     if (bn > kp) continue;
     const fconv::Gather g = gather_for(p, bn, false);
     if (!fconv::gather_supports(g, bn, chunked)) continue;
-    const long long fixed = g == fconv::Gather::kTmaIm2col ? 600 : 800;
+    const long long fixed = g == fconv::Gather::kTmaIm2col ? 360 : 800;
     const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
     const long long waves = (tiles + sms - 1) / sms;
-    const long long cost = waves * (2 * bn > fixed ? 2 * bn : fixed);
+    const long long cost = waves * p.num_kb * (2 * bn > fixed ? 2 * bn : fixed) + 8LL * bn;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = bn;

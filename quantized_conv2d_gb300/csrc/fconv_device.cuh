@@ -82,6 +82,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// mbar_wait executed by every lane of a warp, which then takes lane 0's
+// answer: the loop around it stays warp-uniform, so the descriptors and
+// coordinates computed from its state stay warp-uniform too.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int *abort_flag,
+                                               uint64_t timeout_ns) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, timeout_ns);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Two phases at once (the second only if `both`): in the steady state,
+// where neither has to wait, the ready test of both barriers costs one
+// round trip.
+__device__ __forceinline__ bool mbar_wait2_warp(uint32_t bar0, uint32_t parity0, uint32_t bar1,
+                                                uint32_t parity1, bool both,
+                                                volatile int *abort_flag,
+                                                uint64_t timeout_ns) {
+  const bool r0 = mbar_try_wait(bar0, parity0);
+  const bool r1 = !both || mbar_try_wait(bar1, parity1);
+  if (__shfl_sync(0xffffffffu, (r0 && r1) ? 1 : 0, 0) != 0) return true;
+  if (!mbar_wait_warp(bar0, parity0, abort_flag, timeout_ns)) return false;
+  return !both || mbar_wait_warp(bar1, parity1, abort_flag, timeout_ns);
+}
+
 // A wait used only while shutting down after an abort: ignores the abort
 // flag, gives up silently after timeout_ns.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,

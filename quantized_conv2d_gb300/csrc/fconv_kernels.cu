@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem *bars = reinterpret_cast<Smem *>(smem + C::kBarOffset);
   volatile int *abort_flag = &bars->abort_flag;
 
-  const int warp = threadIdx.x >> 5;
+  // taken from lane 0 so that the compiler sees a warp-uniform value and the
+  // role branches below are uniform
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = args.timeout_ns;
 
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = bars->tmem_base;
+  const uint32_t tmem_base = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
 
   const int num_kb = args.num_kb;
   const int kb_chunk = args.kb_chunk;
@@ -356,38 +358,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
-        for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kb_chunk) {
-          const int kb1 = min(kb0 + kb_chunk, num_kb);
-          if (!mbar_wait(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo)) {
+    // The whole warp runs the loop (warp-uniform state); lane 0 issues.
+    uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+      for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kb_chunk) {
+        const int kb1 = min(kb0 + kb_chunk, num_kb);
+        if (!mbar_wait_warp(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + astage * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_warp(smem_u32(&bars->full_a[stage]), phase, abort_flag, tmo) ||
+              !mbar_wait_warp(smem_u32(&bars->full_b[stage]), phase, abort_flag, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem_base + astage * BN;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(smem_u32(&bars->full_a[stage]), phase, abort_flag, tmo) ||
-                !mbar_wait(smem_u32(&bars->full_b[stage]), phase, abort_flag, tmo)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
-            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+          if (lane == 0) {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
               umma_f16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
             umma_commit(smem_u32(&bars->empty[stage]));
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
-          if (!ok) break;
-          umma_commit(smem_u32(&bars->acc_full[astage]));
-          if (++astage == 2) { astage = 0; aphase ^= 1; }
+          __syncwarp();
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
+        if (!ok) break;
+        if (lane == 0) umma_commit(smem_u32(&bars->acc_full[astage]));
+        __syncwarp();
+        if (++astage == 2) { astage = 0; aphase ^= 1; }
       }
+    }
+    if (lane == 0) {
       // every MMA issued above has completed once this arrives
       umma_commit(smem_u32(&bars->mma_done));
       mbar_wait_drain(smem_u32(&bars->mma_done), 0, 1000000000ull);
@@ -523,7 +530,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   Smem *bars = reinterpret_cast<Smem *>(smem + C::kBarOffset);
   volatile int *abort_flag = &bars->abort_flag;
 
-  const int warp = threadIdx.x >> 5;
+  // taken from lane 0 so that the compiler sees a warp-uniform value and the
+  // role branches below are uniform
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = args.timeout_ns;
 
@@ -549,7 +558,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = bars->tmem_base;
+  const uint32_t tmem_base = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
 
   const int num_kb = args.num_kb;
   const int kb_chunk = args.kb_chunk;
@@ -559,42 +568,46 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
    setmaxnreg_dec<kTmaCtlRegs>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const long long PQ = static_cast<long long>(args.P) * args.Q;
-      const int cblocks = args.C / kBK;
-      const bool drop = (args.debug & 1) != 0;
-      uint32_t stage = 0, phase = 0, issued = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
-        const int m_tile = tile / args.num_n_tiles;
-        const int n_tile = tile - m_tile * args.num_n_tiles;
-        const long long m0 = static_cast<long long>(m_tile) * kBM;
-        const int n0 = static_cast<int>(m0 / PQ);
-        const int rem = static_cast<int>(m0 - static_cast<long long>(n0) * PQ);
-        const int p0 = rem / args.Q, q0 = rem - (rem / args.Q) * args.Q;
-        // filter-window origin of the tile's first output pixel
-        const int w0 = q0 * args.sw - args.pl, h0 = p0 * args.sh - args.pt;
-        int r = 0, s = 0, cb = 0;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
-            ok = false;
-            break;
-          }
-          if (!drop) {
+    // The whole warp runs the loop (warp-uniform state); lane 0 issues.
+    const long long PQ = static_cast<long long>(args.P) * args.Q;
+    const int cblocks = args.C / kBK;
+    const bool drop = (args.debug & 1) != 0;
+    uint32_t stage = 0, phase = 0, issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+      const int m_tile = tile / args.num_n_tiles;
+      const int n_tile = tile - m_tile * args.num_n_tiles;
+      const long long m0 = static_cast<long long>(m_tile) * kBM;
+      const int n0 = static_cast<int>(m0 / PQ);
+      const int rem = static_cast<int>(m0 - static_cast<long long>(n0) * PQ);
+      const int p0 = rem / args.Q, q0 = rem - (rem / args.Q) * args.Q;
+      // filter-window origin of the tile's first output pixel
+      const int w0 = q0 * args.sw - args.pl, h0 = p0 * args.sh - args.pt;
+      int r = 0, s = 0, cb = 0;   // filter tap and channel block of k-block kb
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        if (!drop) {
+          if (lane == 0) {
             const uint32_t fb = smem_u32(&bars->full_b[stage]);
             mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
             tma_load_im2col_4d(smem_u32(sA + stage * C::kABytes), &tmap_a, cb * kBK, w0, h0, n0,
                                static_cast<uint16_t>(s), static_cast<uint16_t>(r), fb);
             tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb * kBK, n_tile * BN, fb);
-            ++issued;
           }
-          if (++cb == cblocks) {
-            cb = 0;
-            if (++s == args.S) { s = 0; ++r; }
-          }
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          __syncwarp();
+          ++issued;
         }
+        if (++cb == cblocks) {
+          cb = 0;
+          if (++s == args.S) { s = 0; ++r; }
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
+    }
+    if (lane == 0) {
       // let any copy still in flight land before the CTA exits (after an
       // abort); on the normal path every one of them has completed
       const uint32_t first = issued > static_cast<uint32_t>(kStages) ? issued - kStages : 0;
@@ -604,37 +617,63 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
-        for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kb_chunk) {
-          const int kb1 = min(kb0 + kb_chunk, num_kb);
-          if (!mbar_wait(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo)) {
+    // The whole warp runs the loop (warp-uniform state); lane 0 issues.
+    // Two k-blocks (stages) per iteration: one wait round trip and one pass
+    // of loop control for 8 MMAs (the issuing thread, not the tensor core,
+    // bounds tiles narrower than 256).
+    uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+      for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kb_chunk) {
+        const int kb1 = min(kb0 + kb_chunk, num_kb);
+        if (!mbar_wait_warp(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + astage * BN;
+        for (int kb = kb0; kb < kb1; kb += 2) {
+          const bool pair = kb + 1 < kb1;
+          const uint32_t stage1 = stage + 1 == kStages ? 0 : stage + 1;
+          const uint32_t phase1 = stage1 == 0 ? phase ^ 1 : phase;
+          if (!mbar_wait2_warp(smem_u32(&bars->full_b[stage]), phase,
+                               smem_u32(&bars->full_b[stage1]), phase1, pair, abort_flag, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem_base + astage * BN;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(smem_u32(&bars->full_b[stage]), phase, abort_flag, tmo)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
-            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
+          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+          const uint64_t adesc1 = sw128_kmajor_desc(smem_u32(sA + stage1 * C::kABytes));
+          const uint64_t bdesc1 = sw128_kmajor_desc(smem_u32(sB + stage1 * C::kBBytes));
+          if (lane == 0) {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
               umma_f16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
             umma_commit(smem_u32(&bars->empty[stage]));
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
+            if (pair) {
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_f16(d, adesc1 + 2 * k, bdesc1 + 2 * k, kIdesc, 1u);
+              umma_commit(smem_u32(&bars->empty[stage1]));
+            }
           }
-          if (!ok) break;
-          umma_commit(smem_u32(&bars->acc_full[astage]));
-          if (++astage == 2) { astage = 0; aphase ^= 1; }
+          __syncwarp();
+          if (pair) {
+            stage = stage1 + 1 == kStages ? 0 : stage1 + 1;
+            phase = stage == 0 ? phase1 ^ 1 : phase1;
+          } else {
+            stage = stage1;
+            phase = phase1;
+          }
         }
+        if (!ok) break;
+        if (lane == 0) umma_commit(smem_u32(&bars->acc_full[astage]));
+        __syncwarp();
+        if (++astage == 2) { astage = 0; aphase ^= 1; }
       }
+    }
+    if (lane == 0) {
       // every MMA issued above has completed once this arrives
       umma_commit(smem_u32(&bars->mma_done));
       mbar_wait_drain(smem_u32(&bars->mma_done), 0, 1000000000ull);
