@@ -166,8 +166,8 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host,
                             fconv_stream_t stream);
 
 /* Number of batch chunks fconv_run_host pipelines over (1..16; 0 restores
- * the automatic choice: one chunk per >= 5 waves of output tiles, at most 8,
- * so small problems run as one). */
+ * the automatic choice: as many chunks as keep one wave of output tiles
+ * (one tile per SM) each, at most 12, so small problems run as one). */
 fconv_status fconv_plan_set_host_chunks(fconv_plan *plan, int chunks);
 
 /* Synchronize `stream`, then read and clear the current device's kernel

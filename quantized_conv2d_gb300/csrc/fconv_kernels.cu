@@ -789,11 +789,31 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
 constexpr int kPrepThreads = 256;
 constexpr int kPackTile = 64;
 
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &d) {
+  return (__umulhi(n, d.m) + n) >> d.l;
+}
+
+// Source of 8-element unit g of the subsampled copy: element 8g is channel
+// c of output pixel (n, p, q), read from x[n, p*sh, q*sw, c].  C is a
+// multiple of 16, so a unit never straddles two pixels and stays 8-byte
+// aligned; the copy holds fewer than 2^31 elements.
+__device__ __forceinline__ long long subsample_src_unit(long long g, const WidenMap &m) {
+  const uint32_t u = static_cast<uint32_t>(g);
+  const uint32_t pix = fast_div(u, m.units_per_pixel);
+  const uint32_t cu = u - pix * m.units_per_pixel.d;
+  const uint32_t n = fast_div(pix, m.pq);
+  const uint32_t rem = pix - n * m.pq.d;
+  const uint32_t p = fast_div(rem, m.q);
+  const uint32_t q = rem - p * m.q.d;
+  return ((static_cast<long long>(n) * m.H + static_cast<long long>(p) * m.sh) * m.W +
+          static_cast<long long>(q) * m.sw) * m.units_per_pixel.d + cu;
+}
+
 template <bool IS_INT8>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int RSC, int K, int Kpad,
                 int pack_blocks, const int8_t *__restrict__ x, __half *__restrict__ xh,
-                long long n64) {
+                long long n8, const WidenMap map) {
   if (static_cast<int>(blockIdx.x) < pack_blocks) {
     __shared__ uint16_t tile[kPackTile][kPackTile + 2];
     const int tiles_k = (K + kPackTile - 1) / kPackTile;
@@ -835,9 +855,9 @@ __global__ void __launch_bounds__(kPrepThreads)
   // for each of the 8 rounds lane l loads 8 bytes at 8*l of the round (256
   // contiguous bytes a warp instruction) and stores their 16 fp16 bytes
   // (512 contiguous bytes a warp instruction).
+  // (Subsampled copies: the same, with each unit read from its pixel.)
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x - pack_blocks) * (kPrepThreads / 32);
-  const long long n8 = n64 * 8;
   for (long long base = (static_cast<long long>(blockIdx.x - pack_blocks) * (kPrepThreads / 32) +
                          (threadIdx.x >> 5)) * 256;
        base < n8; base += warps * 256) {
@@ -845,7 +865,8 @@ __global__ void __launch_bounds__(kPrepThreads)
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const long long g = base + u * 32 + lane;
-      in[u] = g < n8 ? ldg_nc_v2(x + 8 * g) : make_uint2(0, 0);
+      const long long src = map.subsample ? subsample_src_unit(g, map) : g;
+      in[u] = g < n8 ? ldg_nc_v2(x + 8 * src) : make_uint2(0, 0);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -971,24 +992,42 @@ cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensor
   }
 }
 
+static FastDiv make_fast_div(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+  return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
 cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
-                        const int8_t *x, __half *xh, long long n, int sm_count,
-                        cudaStream_t stream) {
+                        const int8_t *x, __half *xh, long long n, const WidenMap &map_in,
+                        int sm_count, cudaStream_t stream) {
+  WidenMap map = map_in;
+  if (map.subsample) {
+    if (map.C % 16 != 0 || map.P <= 0 || map.Q <= 0 || n >= (1ll << 31))
+      return cudaErrorInvalidValue;
+    map.units_per_pixel = make_fast_div(static_cast<uint32_t>(map.C / 8));
+    map.pq = make_fast_div(static_cast<uint32_t>(map.P) * static_cast<uint32_t>(map.Q));
+    map.q = make_fast_div(static_cast<uint32_t>(map.Q));
+  }
   const int pack_blocks = ((Kpad + kPackTile - 1) / kPackTile) * ((K + kPackTile - 1) / kPackTile);
-  const long long n64 = is_int8 ? n / 64 : 0;
-  long long widen_blocks = (n64 + kPrepThreads - 1) / kPrepThreads;
+  // 8-element units the main loop widens: all of a subsampled copy; the
+  // whole 64-element groups of a dense one (the tail kernel does the rest)
+  const long long n8 = !is_int8 ? 0 : map.subsample ? n / 8 : (n / 64) * 8;
+  long long widen_blocks = (n8 + 8 * kPrepThreads - 1) / (8 * kPrepThreads);
   const long long cap = static_cast<long long>(sm_count) * 4;
   if (widen_blocks > cap) widen_blocks = cap;
   const unsigned grid = static_cast<unsigned>(pack_blocks + widen_blocks);
+  if (grid == 0) return cudaSuccess;
   if (is_int8)
     prep_kernel<true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks, x, xh,
-                                                          n64);
+                                                          n8, map);
   else
     prep_kernel<false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
-                                                           nullptr, nullptr, 0);
+                                                           nullptr, nullptr, 0, map);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || !is_int8) return e;
-  const long long n16 = n / 16, first16 = n64 * 4;
+  if (e != cudaSuccess || !is_int8 || map.subsample) return e;
+  const long long n16 = n / 16, first16 = (n / 64) * 4;
   if (n16 > first16) {
     const long long rest = n16 - first16;
     widen_tail_kernel<<<static_cast<unsigned>((rest + 255) / 256), 256, 0, stream>>>(x, xh, first16,

@@ -184,6 +184,12 @@ def test_workspace_sizes():
         assert fc.fconv_workspace_size(h) == 64 * 448 * 2 + 8 * 14 * 14 * 48 * 2
     finally:
         fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create(64, 28, 28, 256, 512, 1, 1, 2, 2, 1, 0, 1)
+    try:
+        # 1x1 stride 2, int8: only the strided pixels are widened ([64][14][14][256])
+        assert fc.fconv_workspace_size(h) == 512 * 256 * 2 + 64 * 14 * 14 * 256 * 2
+    finally:
+        fc.fconv_plan_destroy(h)
     h = fc.fconv_plan_create(32, 14, 14, 256, 256, 3, 3, 1, 1, 0, 1, 1)
     try:
         # bf16 plans read the input as it is: the packed filter alone

@@ -87,6 +87,8 @@ SWEEP = [
     (3, 8, 8, 128, 64, 3, 3, 2, "SAME", False, False),     # total pad 1: 0 before, 1 after
     (2, 7, 12, 192, 48, 1, 3, (2, 1), "VALID", True, True),
     (1, 20, 3, 64, 32, 4, 2, 3, "SAME", False, True),      # stride 3, even filters
+    (3, 11, 13, 64, 80, 1, 1, (2, 3), "SAME", True, True),  # 1x1 strided: subsampled copy, TMA
+    (2, 10, 9, 48, 32, 1, 1, 3, "VALID", True, False),      # 1x1 stride 3: subsampled, cp.async
 ]
 
 # shapes whose channel count lets the kernel gather A with TMA im2col loads
