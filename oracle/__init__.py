@@ -67,8 +67,8 @@ def _load():
         lib.orc_im2col.argtypes = [p, i32] + [i32] * 11 + [p]
         lib.orc_gemm_i8.argtypes = [p, p, i32, i32, i32, p]
         lib.orc_conv_i8_im2col.argtypes = [p, p] + [i32] * 13 + [p, p]
-        lib.orc_epilogue_i8.argtypes = [p, i64, i32, p, p, f32, p, f32, i32, p]
-        lib.orc_epilogue_f64.argtypes = [p, i64, i32, p, p, f64, p, f64, i32, p]
+        lib.orc_epilogue_i8.argtypes = [p, i64, i32, p, p, f32, p, f32, i32, f32, f32, p]
+        lib.orc_epilogue_f64.argtypes = [p, i64, i32, p, p, f64, p, f64, i32, f64, f64, p]
         lib.orc_num_threads.restype = i32
         for name in ("orc_conv_i8_direct", "orc_conv_i8_points",
                      "orc_conv_bf16_direct_f64", "orc_conv_bf16_points_f64",
@@ -205,6 +205,18 @@ def conv_acc_bf16_points_f64(x_bits, w_bits, idx, stride=1, padding=SAME) -> np.
     return out
 
 
+# activation codes (the C oracle's): none, Relu, leaky Relu (alpha),
+# clipped Relu (alpha), clamp to [alpha, beta]
+ACT_NONE, ACT_RELU, ACT_LEAKY_RELU, ACT_CLIPPED_RELU, ACT_CLAMP = 0, 1, 2, 3, 4
+
+
+def _act_code(relu) -> int:
+    """`relu` is a bool (BiasAdd / BiasAdd+Relu) or one of the ACT_ codes."""
+    if isinstance(relu, (bool, np.bool_)):
+        return ACT_RELU if relu else ACT_NONE
+    return int(relu)
+
+
 def _scale_args(conv_scale, K):
     """(scalar, per-channel array or None): conv_scale is a number, or K
     values, one per output channel."""
@@ -216,9 +228,11 @@ def _scale_args(conv_scale, K):
 
 
 def epilogue_i8(acc: np.ndarray, bias: np.ndarray, side: np.ndarray | None,
-                conv_scale, side_scale: float, relu: bool) -> np.ndarray:
+                conv_scale, side_scale: float, relu, alpha: float = 0.0,
+                beta: float = 0.0) -> np.ndarray:
     """BiasActivationOutputKernel on int32 sums shaped [..., K] -> int8.
-    conv_scale: a scalar, or K fp32 values (one per output channel)."""
+    conv_scale: a scalar, or K fp32 values (one per output channel).
+    relu: a bool, or an ACT_ code (alpha/beta parametrise the others)."""
     acc = np.ascontiguousarray(acc, dtype=np.int32)
     K = acc.shape[-1]
     bias = np.ascontiguousarray(bias, dtype=np.float32)
@@ -230,12 +244,14 @@ def epilogue_i8(acc: np.ndarray, bias: np.ndarray, side: np.ndarray | None,
     out = np.empty(acc.shape, dtype=np.int8)
     _load().orc_epilogue_i8(_ptr(acc), acc.size // K, K, _ptr(bias), _ptr(side),
                             float(np.float32(cs)), _ptr(sk), float(np.float32(side_scale)),
-                            int(bool(relu)), _ptr(out))
+                            _act_code(relu), float(np.float32(alpha)),
+                            float(np.float32(beta)), _ptr(out))
     return out
 
 
 def epilogue_f64(acc: np.ndarray, bias: np.ndarray, side_bits: np.ndarray | None,
-                 conv_scale, side_scale: float, relu: bool) -> np.ndarray:
+                 conv_scale, side_scale: float, relu, alpha: float = 0.0,
+                 beta: float = 0.0) -> np.ndarray:
     """fp64 reference epilogue of the bf16 variant (no output rounding)."""
     acc = np.ascontiguousarray(acc, dtype=np.float64)
     K = acc.shape[-1]
@@ -246,7 +262,8 @@ def epilogue_f64(acc: np.ndarray, bias: np.ndarray, side_bits: np.ndarray | None
     cs, sk = _scale_args(conv_scale, K)
     out = np.empty(acc.shape, dtype=np.float64)
     _load().orc_epilogue_f64(_ptr(acc), acc.size // K, K, _ptr(bias), _ptr(side_bits),
-                             cs, _ptr(sk), float(side_scale), int(bool(relu)), _ptr(out))
+                             cs, _ptr(sk), float(side_scale), _act_code(relu),
+                             float(np.float32(alpha)), float(np.float32(beta)), _ptr(out))
     return out
 
 

@@ -63,15 +63,27 @@ def f(x: float) -> Fraction:
 
 
 def epilogue_i8(acc: int, conv_scale: float, side: int | None, side_scale: float,
-                bias: float, relu: bool) -> int:
-    """int8 result of the three-step epilogue for one element, exactly."""
+                bias: float, relu, alpha: float = 0.0, beta: float = 0.0) -> int:
+    """int8 result of the three-step epilogue for one element, exactly.
+
+    relu: a bool (BiasAdd / BiasAdd+Relu) or an activation code: 2 leaky
+    (y < 0: alpha*y, rounded once), 3 clipped (min(max(y, 0), alpha)),
+    4 clamp (min(max(y, alpha), beta)), applied after the bias add."""
     v = to_f32(Fraction(acc))                       # int32 -> fp32
     v = to_f32(v * f(conv_scale))                   # (1) scale
     if side is not None and side_scale != 0.0:      # (2) side input, fused
         v = to_f32(Fraction(side) * f(side_scale) + v)
     v = to_f32(v + f(bias))                         # (3) bias
+    act = (1 if relu else 0) if isinstance(relu, bool) else int(relu)
+    a, b = f(alpha), f(beta)
+    if act == 2 and v < 0:
+        v = to_f32(v * a)
+    elif act == 3:
+        v = min(max(v, Fraction(0)), a)
+    elif act == 4:
+        v = min(max(v, a), b)
     r = round_half_even_int(v)
-    lower = 0 if relu else -128
+    lower = 0 if act == 1 else -128
     return max(lower, min(127, r))
 
 

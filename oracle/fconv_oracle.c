@@ -30,6 +30,14 @@
  *    (h, w, c) storage order, taps outside the image are zero, and the
  *    output size is (H + pad_t + pad_b - R) / stride + 1.
  *
+ *  - MIOpen's fusion page ("use-fusion-api"), tables "Convolution-based
+ *    ... fusion for inference": the activations a fused plan may end with
+ *    include Leaky Relu, Clipped Relu and CLAMP besides Relu.  The pages
+ *    name them without formulas; the readings used here are the usual ones:
+ *    leaky: y < 0 ? alpha*y : y (one fp32 rounding); clipped: min(max(y, 0),
+ *    alpha); clamp: min(max(y, alpha), beta).  Each is applied after step
+ *    (3), before the int8 rounding and clip to [-128, 127].
+ *
  * Readings where the pages leave a step open:
  *  - The conv sum is accumulated exactly in int32 (the page's "QInt8xQInt8
  *    -> QInt32" contraction), and converted to fp32 with round-to-nearest-
@@ -284,11 +292,32 @@ void orc_conv_i8_im2col(const int8_t *x, const int8_t *w, int N, int H, int W,
  * NULL for a scalar conv_input_scale, else its K per-channel values (the
  * kernel's step (1) offsets the scale pointer by the output channel when the
  * scale tensor holds more than one element). */
+/* Activation codes: 0 none (BiasAdd), 1 Relu, 2 leaky Relu (alpha),
+ * 3 clipped Relu (alpha), 4 clamp to [alpha, beta]. */
+#define ORC_ACT_NONE 0
+#define ORC_ACT_RELU 1
+#define ORC_ACT_LEAKY 2
+#define ORC_ACT_CLIPPED 3
+#define ORC_ACT_CLAMP 4
+
+static float act_f32(float v, int act, float alpha, float beta) {
+  switch (act) {
+    case ORC_ACT_LEAKY: return v < 0.0f ? v * alpha : v;
+    case ORC_ACT_CLIPPED:
+      if (v < 0.0f) v = 0.0f;
+      return v > alpha ? alpha : v;
+    case ORC_ACT_CLAMP:
+      if (v < alpha) v = alpha;
+      return v > beta ? beta : v;
+    default: return v;   /* none; Relu is the clip's lower bound */
+  }
+}
+
 void orc_epilogue_i8(const int32_t *acc, long long rows, int K,
                      const float *bias, const int8_t *side, float conv_scale,
-                     const float *conv_scale_k, float side_scale, int relu,
-                     int8_t *out) {
-  const float lower = relu ? 0.0f : -128.0f;
+                     const float *conv_scale_k, float side_scale, int act,
+                     float alpha, float beta, int8_t *out) {
+  const float lower = act == ORC_ACT_RELU ? 0.0f : -128.0f;
   const float upper = 127.0f;
   const int use_side = (side != NULL) && (side_scale != 0.0f);
 #pragma omp parallel for schedule(static)
@@ -301,6 +330,7 @@ void orc_epilogue_i8(const int32_t *acc, long long rows, int K,
       if (use_side)                     /* (2) side input, one fused rounding */
         v = fmaf((float)side[e], side_scale, v);
       v = v + bias[k];                  /* (3) bias */
+      v = act_f32(v, act, alpha, beta); /* activation other than Relu */
       float r = nearbyintf(v);          /* round half to even (default mode) */
       if (r < lower) r = lower;         /* clip to [lower, 127] */
       if (r > upper) r = upper;
@@ -314,7 +344,8 @@ void orc_epilogue_i8(const int32_t *acc, long long rows, int K,
 void orc_epilogue_f64(const double *acc, long long rows, int K,
                       const float *bias, const uint16_t *side,
                       double conv_scale, const float *conv_scale_k,
-                      double side_scale, int relu, double *out) {
+                      double side_scale, int act, double alpha, double beta,
+                      double *out) {
   const int use_side = (side != NULL) && (side_scale != 0.0);
 #pragma omp parallel for schedule(static)
   for (long long i = 0; i < rows; ++i) {
@@ -323,7 +354,13 @@ void orc_epilogue_f64(const double *acc, long long rows, int K,
       double v = acc[e] * (conv_scale_k ? (double)conv_scale_k[k] : conv_scale);
       if (use_side) v = bf16_value(side[e]) * side_scale + v;
       v = v + (double)bias[k];
-      if (relu && v < 0.0) v = 0.0;
+      switch (act) {
+        case ORC_ACT_RELU: if (v < 0.0) v = 0.0; break;
+        case ORC_ACT_LEAKY: if (v < 0.0) v = v * alpha; break;
+        case ORC_ACT_CLIPPED: if (v < 0.0) v = 0.0; if (v > alpha) v = alpha; break;
+        case ORC_ACT_CLAMP: if (v < alpha) v = alpha; if (v > beta) v = beta; break;
+        default: break;
+      }
       out[e] = v;
     }
   }

@@ -147,3 +147,92 @@ def test_per_channel_scale_f64_reference():
         for k in range(16):
             want = acc[i, k] * float(sk[k]) + side[i, k] * 0.5 + float(bias[k])
             assert got[i, k] == want
+
+
+# ---------------------------------------------------------------- activations
+# MIOpen's fusion tables list leaky Relu, clipped Relu and CLAMP as fusable
+# activations; the readings are y < 0 ? alpha*y : y, min(max(y, 0), alpha)
+# and min(max(y, alpha), beta), applied after the bias add.
+A = oracle
+
+def _run_act(acc, cs, bias, act, alpha, beta):
+    return int(oracle.epilogue_i8(np.array([[acc]], np.int32), np.array([bias], np.float32), None,
+                                  cs, 0.0, act, alpha, beta)[0, 0])
+
+
+@pytest.mark.parametrize("acc,cs,bias,act,alpha,beta,expect", [
+    # leaky, alpha 0.5: -5 -> -2.5 -> -2 (ties to even), -7 -> -3.5 -> -4, positives pass
+    (-5, 1.0, 0.0, A.ACT_LEAKY_RELU, 0.5, 0.0, -2),
+    (-7, 1.0, 0.0, A.ACT_LEAKY_RELU, 0.5, 0.0, -4),
+    (6, 1.0, 0.0, A.ACT_LEAKY_RELU, 0.5, 0.0, 6),
+    (-1000, 1.0, 0.0, A.ACT_LEAKY_RELU, 0.5, 0.0, -128),
+    # clipped at 6: 5.5 -> 6 (tie to even), 6.5 -> 6 -> 6, negatives -> 0
+    (11, 0.5, 0.0, A.ACT_CLIPPED_RELU, 6.0, 0.0, 6),
+    (13, 0.5, 0.0, A.ACT_CLIPPED_RELU, 6.0, 0.0, 6),
+    (9, 0.5, 0.0, A.ACT_CLIPPED_RELU, 6.0, 0.0, 4),
+    (-3, 1.0, 0.0, A.ACT_CLIPPED_RELU, 6.0, 0.0, 0),
+    # clipped at 2.5: 3.5 -> 2.5 -> 2
+    (7, 0.5, 0.0, A.ACT_CLIPPED_RELU, 2.5, 0.0, 2),
+    # clamp to [-3.5, 2.5]: -100 -> -3.5 -> -4, 100 -> 2.5 -> 2, 1 stays
+    (-100, 1.0, 0.0, A.ACT_CLAMP, -3.5, 2.5, -4),
+    (100, 1.0, 0.0, A.ACT_CLAMP, -3.5, 2.5, 2),
+    (1, 1.0, 0.0, A.ACT_CLAMP, -3.5, 2.5, 1),
+    # a clamp wider than int8: the int8 clip still applies
+    (1000, 1.0, 0.0, A.ACT_CLAMP, -200.0, 300.0, 127),
+    (-1000, 1.0, 0.0, A.ACT_CLAMP, -200.0, 300.0, -128),
+])
+def test_activation_hand_cases(acc, cs, bias, act, alpha, beta, expect):
+    assert _run_act(acc, cs, bias, act, alpha, beta) == expect
+    assert exact.epilogue_i8(acc, cs, None, 0.0, bias, act, alpha, beta) == expect
+
+
+@pytest.mark.parametrize("act", [A.ACT_LEAKY_RELU, A.ACT_CLIPPED_RELU, A.ACT_CLAMP])
+def test_activations_match_exact_rational(act):
+    rng = np.random.default_rng(31 + act)
+    rows, K = 60, 16
+    acc = rng.integers(-4_000_000, 4_000_000, size=(rows, K)).astype(np.int32)
+    side = rng.integers(-128, 128, size=(rows, K)).astype(np.int8)
+    bias = rng.normal(0.0, 2.0, size=K).astype(np.float32)
+    for alpha, beta in [(0.1, 0.0), (0.37, 0.0), (6.0, 0.0), (-20.5, 33.25), (2.75, 90.0)]:
+        got = oracle.epilogue_i8(acc, bias, side, 2.0 ** -15, 0.5, act, alpha, beta)
+        for i in range(rows):
+            for k in range(K):
+                want = exact.epilogue_i8(int(acc[i, k]), 2.0 ** -15, int(side[i, k]), 0.5,
+                                         float(bias[k]), act,
+                                         float(np.float32(alpha)), float(np.float32(beta)))
+                assert got[i, k] == want, (act, alpha, beta, i, k)
+
+
+def test_activations_reduce_to_relu_and_none():
+    rng = np.random.default_rng(40)
+    acc = rng.integers(-2 ** 22, 2 ** 22, size=(200, 32)).astype(np.int32)
+    bias = rng.normal(0.0, 3.0, size=32).astype(np.float32)
+    side = rng.integers(-128, 128, size=acc.shape).astype(np.int8)
+    args = (acc, bias, side, 2.0 ** -14, 0.25)
+    relu = oracle.epilogue_i8(*args, True)
+    none = oracle.epilogue_i8(*args, False)
+    assert np.array_equal(oracle.epilogue_i8(*args, A.ACT_LEAKY_RELU, 0.0), relu)
+    assert np.array_equal(oracle.epilogue_i8(*args, A.ACT_CLIPPED_RELU, 127.0), relu)
+    assert np.array_equal(oracle.epilogue_i8(*args, A.ACT_CLAMP, 0.0, 1e6), relu)
+    assert np.array_equal(oracle.epilogue_i8(*args, A.ACT_CLAMP, -128.0, 127.0), none)
+    assert np.array_equal(oracle.epilogue_i8(*args, A.ACT_LEAKY_RELU, 1.0), none)
+
+
+def test_activations_f64_reference():
+    rng = np.random.default_rng(41)
+    acc = rng.normal(0.0, 3.0, size=(50, 8))
+    bias = rng.normal(0.0, 0.5, size=8).astype(np.float32)
+    for act, alpha, beta in [(A.ACT_LEAKY_RELU, 0.2, 0.0), (A.ACT_CLIPPED_RELU, 1.5, 0.0),
+                             (A.ACT_CLAMP, -1.25, 2.0)]:
+        got = oracle.epilogue_f64(acc, bias, None, 1.0, 0.0, act, alpha, beta)
+        a, b = float(np.float32(alpha)), float(np.float32(beta))
+        for i in range(50):
+            for k in range(8):
+                v = acc[i, k] + float(bias[k])
+                if act == A.ACT_LEAKY_RELU:
+                    want = v * a if v < 0 else v
+                elif act == A.ACT_CLIPPED_RELU:
+                    want = min(max(v, 0.0), a)
+                else:
+                    want = min(max(v, a), b)
+                assert got[i, k] == want
