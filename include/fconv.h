@@ -75,8 +75,24 @@ typedef enum {
 
 typedef enum { FCONV_SAME = 0, FCONV_VALID = 1 } fconv_padding;
 typedef enum { FCONV_INT8 = 0, FCONV_BF16 = 1 } fconv_dtype;
-/* BiasAdd and BiasAdd+Relu, the two fusions the TensorFlow kernel accepts. */
-typedef enum { FCONV_ACT_NONE = 0, FCONV_ACT_RELU = 1 } fconv_act;
+/* Activation after the bias add.  BiasAdd (NONE) and BiasAdd+Relu are the
+ * two fusions the TensorFlow kernel accepts ("conv_ops_fused_int8.cc");
+ * MIOpen's fusion tables ("use-fusion-api", convolution-based fusion for
+ * inference) also list leaky Relu, clipped Relu and CLAMP, which the pages
+ * name without formulas.  Read here as, on the fp32 value y after step (3):
+ *   LEAKY_RELU:   y < 0 ? alpha * y : y   (one fp32 rounding)
+ *   CLIPPED_RELU: min(max(y, 0), alpha)
+ *   CLAMP:        min(max(y, alpha), beta)
+ * followed, for int8 output, by the usual rounding and clip to [-128, 127]
+ * (Relu keeps the TensorFlow form: clip to [0, 127]).  alpha and beta come
+ * from fconv_plan_set_activation_params (default 0, 0). */
+typedef enum {
+  FCONV_ACT_NONE = 0,
+  FCONV_ACT_RELU = 1,
+  FCONV_ACT_LEAKY_RELU = 2,
+  FCONV_ACT_CLIPPED_RELU = 3,
+  FCONV_ACT_CLAMP = 4
+} fconv_act;
 
 /* Create a plan for one convolution shape.
  * N,H,W,C: input NHWC extents; K: output channels; R,S: filter height and
@@ -91,6 +107,14 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C,
                                int K, int R, int S, int stride_h, int stride_w,
                                fconv_padding padding, fconv_dtype dtype,
                                fconv_act act);
+
+/* Parameters of the plan's activation: the slope for y < 0 (LEAKY_RELU), the
+ * upper bound (CLIPPED_RELU, alpha >= 0), or the interval [alpha, beta]
+ * (CLAMP, alpha <= beta); ignored by NONE and RELU.  Non-finite values or a
+ * violated bound give FCONV_ERR_INVALID_VALUE and leave the plan unchanged.
+ * Host only; applies to later runs. */
+fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha,
+                                              float beta);
 
 /* Free a plan (NULL is accepted).  Does not synchronize any stream. */
 fconv_status fconv_plan_destroy(fconv_plan *plan);

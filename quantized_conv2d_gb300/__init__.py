@@ -27,7 +27,8 @@ FCONV_ERR_WORKSPACE = 7
 
 FCONV_SAME, FCONV_VALID = 0, 1
 FCONV_INT8, FCONV_BF16 = 0, 1
-FCONV_ACT_NONE, FCONV_ACT_RELU = 0, 1
+FCONV_ACT_NONE, FCONV_ACT_RELU, FCONV_ACT_LEAKY_RELU, FCONV_ACT_CLIPPED_RELU, FCONV_ACT_CLAMP = (
+    0, 1, 2, 3, 4)
 FCONV_DEBUG_DROP_ARRIVE = 1
 FCONV_DEBUG_GATHER_CPASYNC = 2
 
@@ -74,6 +75,7 @@ def _load():
         "fconv_plan_set_stage_events": [p, ctypes.POINTER(ctypes.c_void_p)],
         "fconv_run_no_alloc": [p, p, p, p, p, f32, f32, p, p],
         "fconv_plan_set_host_chunks": [p, i32],
+        "fconv_plan_set_activation_params": [p, f32, f32],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -136,6 +138,11 @@ def fconv_run(plan, x, w, bias, side, conv_scale, side_scale, y, workspace, work
               stream) -> None:
     _check(_load().fconv_run(plan, x, w, bias, side, conv_scale, side_scale, y, workspace,
                              workspace_bytes, stream), "fconv_run")
+
+
+def fconv_plan_set_activation_params(plan, alpha: float, beta: float) -> None:
+    _check(_load().fconv_plan_set_activation_params(plan, alpha, beta),
+           "fconv_plan_set_activation_params")
 
 
 def fconv_run_channel_scale(plan, x, w, bias, side, conv_scale, side_scale, y, workspace,
@@ -228,14 +235,21 @@ class Conv2dPlan:
     """
 
     def __init__(self, N, H, W, C, K, R, S, stride=1, padding="SAME", dtype="int8", relu=True,
-                 device=None):
+                 device=None, alpha=0.0, beta=0.0):
+        """relu: True/False (BiasAdd+Relu / BiasAdd) or an FCONV_ACT_* code;
+        alpha, beta: that activation's parameters."""
         import torch
         sh, sw = (stride, stride) if isinstance(stride, int) else stride
         pad = {"SAME": FCONV_SAME, "VALID": FCONV_VALID}[padding]
         dt = {"int8": FCONV_INT8, "bf16": FCONV_BF16}[dtype]
         self.dtype = dtype
-        self.handle = fconv_plan_create(N, H, W, C, K, R, S, sh, sw, pad, dt,
-                                        FCONV_ACT_RELU if relu else FCONV_ACT_NONE)
+        if isinstance(relu, bool):
+            act = FCONV_ACT_RELU if relu else FCONV_ACT_NONE
+        else:
+            act = int(relu)
+        self.handle = fconv_plan_create(N, H, W, C, K, R, S, sh, sw, pad, dt, act)
+        if alpha or beta:
+            fconv_plan_set_activation_params(self.handle, alpha, beta)
         self.out_shape = fconv_plan_output_shape(self.handle)
         self.ws_bytes = fconv_workspace_size(self.handle)
         self.device = torch.device("cuda") if device is None else torch.device(device)

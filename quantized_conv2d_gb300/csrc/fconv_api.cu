@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -31,6 +32,7 @@ struct fconv_plan {
   // int8 1x1 filter with a stride above 1: only the pixels the convolution
   // reads are widened, into a compact [N][P][Q][C] copy read at stride 1
   int subsample;
+  float act_alpha, act_beta;   // activation parameters (fconv_plan_set_activation_params)
   cudaEvent_t events[4];
   bool use_events;
   // fconv_run_host pipeline: batch chunks, two copy streams and their events
@@ -353,6 +355,9 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.conv_scale = conv_scale;
   a.side_scale = side_scale;
   a.relu = p->act == FCONV_ACT_RELU ? 1 : 0;
+  a.act = static_cast<int>(p->act);
+  a.alpha = p->act_alpha;
+  a.beta = p->act_beta;
   a.mode = mode;
   a.debug = p->debug;
   a.timeout_ns = static_cast<unsigned long long>(p->timeout_ms) * 1000000ull;
@@ -446,7 +451,7 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, in
     return fail(FCONV_ERR_INVALID_VALUE, "unknown padding %d", (int)padding);
   if (dtype != FCONV_INT8 && dtype != FCONV_BF16)
     return fail(FCONV_ERR_INVALID_VALUE, "unknown dtype %d", (int)dtype);
-  if (act != FCONV_ACT_NONE && act != FCONV_ACT_RELU)
+  if (act < FCONV_ACT_NONE || act > FCONV_ACT_CLAMP)
     return fail(FCONV_ERR_INVALID_VALUE, "unknown activation %d", (int)act);
 
   fconv_plan p;
@@ -496,6 +501,19 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, in
   fconv_plan *out = new (std::nothrow) fconv_plan(p);
   if (!out) return fail(FCONV_ERR_INTERNAL, "out of host memory");
   *plan = out;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha, float beta) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (!std::isfinite(alpha) || !std::isfinite(beta))
+    return fail(FCONV_ERR_INVALID_VALUE, "activation parameters must be finite");
+  if (plan->act == FCONV_ACT_CLIPPED_RELU && alpha < 0.0f)
+    return fail(FCONV_ERR_INVALID_VALUE, "clipped Relu needs alpha >= 0, got %g", alpha);
+  if (plan->act == FCONV_ACT_CLAMP && alpha > beta)
+    return fail(FCONV_ERR_INVALID_VALUE, "clamp needs alpha <= beta, got [%g, %g]", alpha, beta);
+  plan->act_alpha = alpha;
+  plan->act_beta = beta;
   return FCONV_OK;
 }
 

@@ -12,6 +12,9 @@ namespace fconv {
 constexpr int kModeFused = 0;         // full epilogue, int8/bf16 output
 constexpr int kModeAccumulators = 1;  // raw sums: int32 (int8 plans) / fp32 (bf16 plans)
 
+// activation codes (the values of the public fconv_act)
+constexpr int kActNone = 0, kActRelu = 1, kActLeakyRelu = 2, kActClippedRelu = 3, kActClamp = 4;
+
 // Largest number of 64-wide k-blocks one fp32 accumulation may cover for
 // int8 operands: 15 * 64 = 960 products of magnitude <= 2^14 stay below
 // 2^24, so every partial sum is an exactly representable integer.
@@ -32,7 +35,9 @@ struct ConvArgs {
   int num_n_tiles;     // ceil(K / BN)
   int num_tiles;       // ceil(M / 128) * num_n_tiles
   float conv_scale, side_scale;
-  int relu;
+  int relu;            // act == kActRelu (the int8 clip's lower bound is 0)
+  int act;             // kAct*
+  float alpha, beta;   // activation parameters
   int use_side;
   int mode;
   int debug;

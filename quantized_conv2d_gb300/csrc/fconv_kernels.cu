@@ -98,6 +98,15 @@ __device__ __forceinline__ void store_i32_slice(const ConvArgs &a, long long m, 
 // groups of 16 (int8) or 8 (bf16) columns so few values are live at once.
 // vals: the 32 pre-epilogue sums as fp32 (exact integers for int8 plans).
 // Columns at or beyond K are skipped (K is a multiple of the group width).
+// Activations other than Relu, on the fp32 value after the bias add (Relu
+// is the int8 clip's lower bound, or a max with 0 for bf16 output).
+__device__ __forceinline__ float activation(float v, const ConvArgs &a) {
+  if (a.act == kActLeakyRelu) return v < 0.0f ? __fmul_rn(v, a.alpha) : v;
+  if (a.act == kActClippedRelu) return fminf(fmaxf(v, 0.0f), a.alpha);
+  if (a.act == kActClamp) return fminf(fmaxf(v, a.alpha), a.beta);
+  return v;
+}
+
 template <bool IS_INT8>
 __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
                                                const float (&vals)[32]) {
@@ -157,6 +166,7 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
             v = __fmaf_rn(sd, ss, v);
           }
           v = __fadd_rn(v, bv[e]);
+          if (a.act > kActRelu) v = activation(v, a);
           int r = __float2int_rn(v);  // round half to even, saturating
           r = min(max(r, lo), 127);
           word |= (static_cast<uint32_t>(r) & 0xFFu) << (8 * e);
@@ -196,6 +206,7 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
           if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
           v = __fadd_rn(v, bv[2 * g + t]);
           if (a.relu) v = fmaxf(v, 0.0f);
+          else if (a.act > kActRelu) v = activation(v, a);
           word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << (16 * t);
         }
         out[g] = word;

@@ -48,6 +48,7 @@ class Case:
         self.stride = (stride, stride) if isinstance(stride, int) else tuple(stride)
         self.padding, self.dtype, self.relu = padding, dtype, relu
         self.conv_scale, self.side_scale = conv_scale, side_scale
+        self.alpha, self.beta = 0.0, 0.0   # activation parameters (relu may be an act code)
         self.x, self.w, self.bias, self.side = (inputs["x"], inputs["w"], inputs["bias"],
                                                 inputs["side"])
 
@@ -57,7 +58,7 @@ class Case:
 
     def plan(self, block_n=None, debug=0):
         p = fc.Conv2dPlan(self.N, self.H, self.W, self.C, self.K, self.R, self.S, self.stride,
-                          self.padding, self.dtype, self.relu)
+                          self.padding, self.dtype, self.relu, alpha=self.alpha, beta=self.beta)
         if block_n:
             p.set_tile(block_n)
         if debug:
@@ -103,9 +104,9 @@ class Case:
             acc = self.oracle_acc()
         if self.dtype == "int8":
             return oracle.epilogue_i8(acc, self.bias, self.side, self.conv_scale,
-                                      self.side_scale, self.relu)
+                                      self.side_scale, self.relu, self.alpha, self.beta)
         return oracle.epilogue_f64(acc, self.bias, self.side, self.conv_scale, self.side_scale,
-                                   self.relu)
+                                   self.relu, self.alpha, self.beta)
 
     def check_output(self, got, ref, unit_variance_bar=False):
         """int8: bit-exact.  bf16: max relative error <= 2e-2 (|ref| floored

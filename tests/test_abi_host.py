@@ -55,7 +55,7 @@ def _err(fn, *args):
     ((1, 8, 8, 16, 16, 3, 3, 0, 1, 0, 0, 1), fc.FCONV_ERR_INVALID_VALUE),
     ((1, 8, 8, 16, 16, 3, 3, 1, 1, 7, 0, 1), fc.FCONV_ERR_INVALID_VALUE),
     ((1, 8, 8, 16, 16, 3, 3, 1, 1, 0, 5, 1), fc.FCONV_ERR_INVALID_VALUE),
-    ((1, 8, 8, 16, 16, 3, 3, 1, 1, 0, 0, 3), fc.FCONV_ERR_INVALID_VALUE),
+    ((1, 8, 8, 16, 16, 3, 3, 1, 1, 0, 0, 5), fc.FCONV_ERR_INVALID_VALUE),   # unknown activation
     ((1, 2, 8, 16, 16, 3, 3, 1, 1, 1, 0, 1), fc.FCONV_ERR_INVALID_VALUE),   # VALID, R > H
     ((1, 8, 8, 24, 16, 3, 3, 1, 1, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),   # int8 C % 16
     ((1, 8, 8, 16, 40, 3, 3, 1, 1, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),   # int8 K % 16
@@ -208,3 +208,23 @@ def test_binding_and_oracle_are_separate():
     for f in os.listdir(os.path.join(ROOT, "oracle")):
         if f.endswith((".py", ".c")):
             assert "quantized_conv2d_gb300" not in open(os.path.join(ROOT, "oracle", f)).read()
+
+
+def test_activation_params_validation():
+    for act in (fc.FCONV_ACT_LEAKY_RELU, fc.FCONV_ACT_CLIPPED_RELU, fc.FCONV_ACT_CLAMP):
+        h = fc.fconv_plan_create(1, 8, 8, 16, 16, 3, 3, 1, 1, 0, 0, act)
+        try:
+            fc.fconv_plan_set_activation_params(h, 0.5, 2.0)
+            assert _err(fc.fconv_plan_set_activation_params, h, float("nan"), 1.0) == \
+                fc.FCONV_ERR_INVALID_VALUE
+            assert _err(fc.fconv_plan_set_activation_params, h, 1.0, float("inf")) == \
+                fc.FCONV_ERR_INVALID_VALUE
+            if act == fc.FCONV_ACT_CLIPPED_RELU:
+                assert _err(fc.fconv_plan_set_activation_params, h, -1.0, 0.0) == \
+                    fc.FCONV_ERR_INVALID_VALUE
+            if act == fc.FCONV_ACT_CLAMP:
+                assert _err(fc.fconv_plan_set_activation_params, h, 3.0, 2.0) == \
+                    fc.FCONV_ERR_INVALID_VALUE
+        finally:
+            fc.fconv_plan_destroy(h)
+    assert _err(fc.fconv_plan_set_activation_params, None, 0.0, 0.0) == fc.FCONV_ERR_INVALID_VALUE

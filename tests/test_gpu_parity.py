@@ -368,3 +368,33 @@ def test_run_replays_from_a_cuda_graph():
         p.check()
         c.check_output(to_host(y), c.oracle_out())
     p.close()
+
+
+# ---------------------------------------------------------------- activations
+ACT_CASES = [
+    # (shape, dtype, act, alpha, beta)
+    ((2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, None), "int8", fc.FCONV_ACT_LEAKY_RELU, 0.1, 0.0),
+    ((2, 9, 11, 48, 144, 3, 3, 2, "SAME", True, None), "int8", fc.FCONV_ACT_CLIPPED_RELU, 6.0, 0.0),
+    ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, None), "int8", fc.FCONV_ACT_CLAMP, -20.5, 33.25),
+    ((2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, None), "int8", fc.FCONV_ACT_CLIPPED_RELU, 2.5, 0.0),
+    ((3, 8, 8, 64, 200, 3, 3, 1, "SAME", True, None), "bf16", fc.FCONV_ACT_LEAKY_RELU, 0.2, 0.0),
+    ((3, 8, 8, 64, 200, 3, 3, 1, "SAME", True, None), "bf16", fc.FCONV_ACT_CLIPPED_RELU, 1.5, 0.0),
+    ((2, 7, 9, 24, 40, 3, 3, 1, "VALID", False, None), "bf16", fc.FCONV_ACT_CLAMP, -1.25, 2.0),
+]
+
+
+@pytest.mark.parametrize("i,item", list(enumerate(ACT_CASES)))
+def test_activation_variants(i, item):
+    params, dtype, act, alpha, beta = item
+    c = sweep_case(400 + i, params, dtype)
+    c.relu, c.alpha, c.beta = act, alpha, beta
+    if dtype == "int8":
+        # sums of R*S*C products of uniform int8 values have a standard
+        # deviation of about sqrt(R*S*C) * 5461: scale them to about +-40,
+        # across the activation bounds and inside the int8 range
+        c.conv_scale = 40.0 / (np.sqrt(c.R * c.S * c.C) * 5461.0)
+        c.side_scale = 0.05
+    ref = c.oracle_out()
+    c.check_output(c.run_gpu(), ref)
+    if params[3] % 64 == 0:
+        c.check_output(c.run_gpu(debug=fc.FCONV_DEBUG_GATHER_CPASYNC), ref)
