@@ -67,13 +67,16 @@ def _load():
         lib.orc_im2col.argtypes = [p, i32] + [i32] * 11 + [p]
         lib.orc_gemm_i8.argtypes = [p, p, i32, i32, i32, p]
         lib.orc_conv_i8_im2col.argtypes = [p, p] + [i32] * 13 + [p, p]
+        lib.orc_convT_i8_direct.argtypes = [p, p] + [i32] * 13 + [p]
+        lib.orc_convT_bf16_direct_f64.argtypes = [p, p] + [i32] * 13 + [p]
         lib.orc_epilogue_i8.argtypes = [p, i64, i32, p, p, f32, p, f32, i32, f32, f32, p]
         lib.orc_epilogue_f64.argtypes = [p, i64, i32, p, p, f64, p, f64, i32, f64, f64, p]
         lib.orc_num_threads.restype = i32
         for name in ("orc_conv_i8_direct", "orc_conv_i8_points",
                      "orc_conv_bf16_direct_f64", "orc_conv_bf16_points_f64",
                      "orc_im2col", "orc_gemm_i8", "orc_conv_i8_im2col",
-                     "orc_epilogue_i8", "orc_epilogue_f64"):
+                     "orc_epilogue_i8", "orc_epilogue_f64",
+                     "orc_convT_i8_direct", "orc_convT_bf16_direct_f64"):
             getattr(lib, name).restype = None
         _lib = lib
         return lib
@@ -135,6 +138,57 @@ def conv_acc_i8(x: np.ndarray, w: np.ndarray, stride=1, padding=SAME) -> np.ndar
     acc = np.empty(g.out_shape, dtype=np.int32)
     _load().orc_conv_i8_direct(_ptr(x), _ptr(w), *g.args(), _ptr(acc))
     return acc
+
+
+def conv_acc_i8_explicit(x, w, sh, sw, pt, pl, P, Q) -> np.ndarray:
+    """The direct int32 conv sums with explicit top/left pads and output
+    extents (taps outside the image contribute zero)."""
+    x = np.ascontiguousarray(x, dtype=np.int8)
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    N, H, W, C = x.shape
+    R, S, _, K = w.shape
+    acc = np.empty((N, P, Q, K), dtype=np.int32)
+    _load().orc_conv_i8_direct(_ptr(x), _ptr(w), N, H, W, C, K, R, S, sh, sw, pt, pl, P, Q,
+                               _ptr(acc))
+    return acc
+
+
+def convT_out_size(size: int, filt: int, stride: int, pad_before: int, pad_after: int) -> int:
+    """Output extent of the transposed convolution along one axis."""
+    return (size - 1) * stride + filt - pad_before - pad_after
+
+
+def convT_acc_i8(x, w, stride, pads) -> np.ndarray:
+    """Exact int32 sums of the transposed convolution (scatter definition).
+    pads = (top, bottom, left, right)."""
+    x = np.ascontiguousarray(x, dtype=np.int8)
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    N, H, W, C = x.shape
+    R, S, Cw, K = w.shape
+    assert Cw == C
+    sh, sw = (stride, stride) if np.isscalar(stride) else stride
+    pt, pb, pl, pr = pads
+    Ho, Wo = convT_out_size(H, R, sh, pt, pb), convT_out_size(W, S, sw, pl, pr)
+    out = np.empty((N, Ho, Wo, K), dtype=np.int32)
+    _load().orc_convT_i8_direct(_ptr(x), _ptr(w), N, H, W, C, K, R, S, sh, sw, pt, pl, Ho, Wo,
+                                _ptr(out))
+    return out
+
+
+def convT_acc_bf16_f64(x_bits, w_bits, stride, pads) -> np.ndarray:
+    """fp64 sums of the transposed convolution on bf16 inputs (bit patterns)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    N, H, W, C = x.shape
+    R, S, Cw, K = w.shape
+    assert Cw == C
+    sh, sw = (stride, stride) if np.isscalar(stride) else stride
+    pt, pb, pl, pr = pads
+    Ho, Wo = convT_out_size(H, R, sh, pt, pb), convT_out_size(W, S, sw, pl, pr)
+    out = np.empty((N, Ho, Wo, K), dtype=np.float64)
+    _load().orc_convT_bf16_direct_f64(_ptr(x), _ptr(w), N, H, W, C, K, R, S, sh, sw, pt, pl, Ho,
+                                      Wo, _ptr(out))
+    return out
 
 
 def conv_acc_i8_points(x, w, idx: np.ndarray, stride=1, padding=SAME) -> np.ndarray:

@@ -287,6 +287,77 @@ void orc_conv_i8_im2col(const int8_t *x, const int8_t *w, int N, int H, int W,
   }
 }
 
+/* Transposed convolution ("cudnn_deconvolution-inl.h", MXNet, Forward: the
+ * backward-data pass of the cross-correlation with the op's pad and stride,
+ * then the bias).  Written as the scatter that defines that adjoint:
+ *   out[n, p*sh + r - pt, q*sw + s - pl, k] += x[n, p, q, c] * w[r, s, c, k]
+ * for every input pixel (p < H, q < W), tap (r, s) and channel pair whose
+ * target lies inside the Ho x Wo output; Ho = (H - 1)*sh + R - pt - pb
+ * (MXNet's symmetric pad p with output adjustment a: pt = p, pb = p - a).
+ * x: NHWC [N][H][W][C]; w: [R][S][C][K] (C input, K output channels);
+ * out: [N][Ho][Wo][K], exact int32 sums.  One image per thread: no races. */
+void orc_convT_i8_direct(const int8_t *x, const int8_t *w, int N, int H, int W,
+                         int C, int K, int R, int S, int sh, int sw, int pt,
+                         int pl, int Ho, int Wo, int32_t *out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int n = 0; n < N; ++n) {
+    int32_t *o = out + (long long)n * Ho * Wo * K;
+    for (long long i = 0; i < (long long)Ho * Wo * K; ++i) o[i] = 0;
+    for (int p = 0; p < H; ++p) {
+      for (int q = 0; q < W; ++q) {
+        const int8_t *xp = x + (((long long)n * H + p) * W + q) * C;
+        for (int r = 0; r < R; ++r) {
+          int oh = p * sh + r - pt;
+          if (oh < 0 || oh >= Ho) continue;
+          for (int s2 = 0; s2 < S; ++s2) {
+            int ow = q * sw + s2 - pl;
+            if (ow < 0 || ow >= Wo) continue;
+            int32_t *op = o + ((long long)oh * Wo + ow) * K;
+            const int8_t *wp = w + ((long long)(r * S + s2) * C) * K;
+            for (int c = 0; c < C; ++c) {
+              int32_t xv = xp[c];
+              const int8_t *wr = wp + (long long)c * K;
+              for (int k = 0; k < K; ++k) op[k] += xv * (int32_t)wr[k];
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+/* The same scatter on bf16 inputs (bit patterns), summed in fp64. */
+void orc_convT_bf16_direct_f64(const uint16_t *x, const uint16_t *w, int N,
+                               int H, int W, int C, int K, int R, int S,
+                               int sh, int sw, int pt, int pl, int Ho, int Wo,
+                               double *out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int n = 0; n < N; ++n) {
+    double *o = out + (long long)n * Ho * Wo * K;
+    for (long long i = 0; i < (long long)Ho * Wo * K; ++i) o[i] = 0.0;
+    for (int p = 0; p < H; ++p) {
+      for (int q = 0; q < W; ++q) {
+        const uint16_t *xp = x + (((long long)n * H + p) * W + q) * C;
+        for (int r = 0; r < R; ++r) {
+          int oh = p * sh + r - pt;
+          if (oh < 0 || oh >= Ho) continue;
+          for (int s2 = 0; s2 < S; ++s2) {
+            int ow = q * sw + s2 - pl;
+            if (ow < 0 || ow >= Wo) continue;
+            double *op = o + ((long long)oh * Wo + ow) * K;
+            const uint16_t *wp = w + ((long long)(r * S + s2) * C) * K;
+            for (int c = 0; c < C; ++c) {
+              double xv = bf16_value(xp[c]);
+              const uint16_t *wr = wp + (long long)c * K;
+              for (int k = 0; k < K; ++k) op[k] += xv * bf16_value(wr[k]);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 /* The epilogue of BiasActivationOutputKernel ("conv_ops_fused_int8.cc"),
  * applied to rows x K exact int32 sums.  side may be NULL.  conv_scale_k is
  * NULL for a scalar conv_input_scale, else its K per-channel values (the
