@@ -127,3 +127,10 @@ def random_case(seed: int, N, H, W, C, K, R, S, dtype: str, out_hw, with_side: b
         sd = ("uniform", -128, 127) if dtype == "int8" else ("normal", 1.0)
         side = _draw(gen, (N, P, Q, K), sd, dtype)
     return {"x": x, "w": w, "bias": bias, "side": side}
+
+
+def uniform_int8(seed: int, shape) -> np.ndarray:
+    """Seeded uniform int8 in [-128, 127] from numpy's PCG64, for inputs of
+    billions of elements (the torch CPU generator is too slow there)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.integers(-128, 128, size=shape, dtype=np.int8)

@@ -89,6 +89,8 @@ SWEEP = [
     (1, 20, 3, 64, 32, 4, 2, 3, "SAME", False, True),      # stride 3, even filters
     (3, 11, 13, 64, 80, 1, 1, (2, 3), "SAME", True, True),  # 1x1 strided: subsampled copy, TMA
     (2, 10, 9, 48, 32, 1, 1, 3, "VALID", True, False),      # 1x1 stride 3: subsampled, cp.async
+    (2, 3, 4, 16, 16, 3, 3, 5, "SAME", True, True),         # stride above the image: 1x1 output
+    (1, 2, 2, 64, 16, 5, 5, 4, "SAME", True, False),        # 5x5 on 2x2, stride 4: pads 1 and 2
 ]
 
 # shapes whose channel count lets the kernel gather A with TMA im2col loads
@@ -398,3 +400,33 @@ def test_activation_variants(i, item):
     c.check_output(c.run_gpu(), ref)
     if params[3] % 64 == 0:
         c.check_output(c.run_gpu(debug=fc.FCONV_DEBUG_GATHER_CPASYNC), ref)
+
+
+# ---------------------------------------------------------------- maximum sizes
+# Tensors of just under 2^31 elements, the plan's limit: the largest input
+# (16 x 255 x 255 x 2048 int8, an fp16 copy of 4.3 GB) and the largest output
+# (2048 x 32 x 32 x 1008).  Checked on sampled pixels, the last one included.
+@pytest.mark.parametrize("shape", [(16, 255, 255, 2048, 32), (2048, 32, 32, 16, 1008)])
+def test_maximum_tensor_sizes(shape):
+    N, H, W, C, K = shape
+    assert max(N * H * W * C, N * H * W * K) < 2 ** 31
+    x = FI.uniform_int8(600 + C, (N, H, W, C))
+    w = FI.uniform_int8(601 + C, (1, 1, C, K))
+    side = FI.uniform_int8(602 + C, (N, H, W, K))
+    bias = np.linspace(-3.0, 3.0, K, dtype=np.float32)
+    cs = 1.0 / (np.sqrt(C) * 5461.0) * 60.0
+    plan = fc.Conv2dPlan(N, H, W, C, K, 1, 1, 1, "VALID", "int8", False)
+    y = plan.run(to_dev(x, "int8"), to_dev(w, "int8"), torch.from_numpy(bias).cuda(),
+                 to_dev(side, "int8"), cs, 0.125)
+    plan.check()
+    got = to_host(y).reshape(-1, K)
+    del y
+    plan.close()
+    rng = np.random.default_rng(7)
+    M = N * H * W
+    pix = np.unique(np.concatenate([rng.choice(M, size=1500, replace=False), [0, M - 1]]))
+    idx = (pix[:, None] * K + np.arange(K)[None, :]).ravel()
+    acc = oracle.conv_acc_i8_points(x, w, idx, 1, oracle.VALID).reshape(-1, K)
+    ref = oracle.epilogue_i8(acc, bias, side.reshape(-1, K)[pix], cs, 0.125, False)
+    bad = np.argwhere(got[pix] != ref)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
