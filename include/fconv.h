@@ -116,6 +116,27 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C,
 fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha,
                                               float beta);
 
+/* Create a plan for a transposed convolution (the forward pass of a
+ * deconvolution layer): "cudnn_deconvolution-inl.h" (MXNet), Forward, runs
+ * cuDNN's backward-data pass of the cross-correlation with the op's pad and
+ * stride and then adds the bias; here the bias and the rest of fconv_run's
+ * epilogue are fused.  The sums are
+ *   acc[n, p*sh + r - pad_top, q*sw + s - pad_left, k] += x[n, p, q, c] * w[r, s, c, k]
+ * over input pixels p < H, q < W and taps whose target lies in the output,
+ * which is Ho = (H-1)*sh + R - pad_top - pad_bottom by Wo (likewise).
+ * MXNet's symmetric pad with output adjustment a is pad_top = pad,
+ * pad_bottom = pad - a.  x: NHWC [N][H][W][C]; w: [R][S][C][K] (C input and
+ * K output channels); y and side: [N][Ho][Wo][K].  Runs through every
+ * fconv_run* entry point like any plan.  Stride 1 and pads in [0, filter-1]
+ * only (else FCONV_ERR_NOT_SUPPORTED); pads that leave no output give
+ * FCONV_ERR_INVALID_VALUE.  Pure host work. */
+fconv_status fconv_plan_create_transposed(fconv_plan **plan, int N, int H, int W,
+                                          int C, int K, int R, int S,
+                                          int stride_h, int stride_w,
+                                          int pad_top, int pad_bottom,
+                                          int pad_left, int pad_right,
+                                          fconv_dtype dtype, fconv_act act);
+
 /* Free a plan (NULL is accepted).  Does not synchronize any stream. */
 fconv_status fconv_plan_destroy(fconv_plan *plan);
 

@@ -58,6 +58,7 @@ def _load():
     psz = ctypes.POINTER(ctypes.c_size_t)
     sigs = {
         "fconv_plan_create": [pp] + [i32] * 12,
+        "fconv_plan_create_transposed": [pp] + [i32] * 15,
         "fconv_plan_destroy": [p],
         "fconv_plan_output_shape": [p, pi, pi, pi, pi],
         "fconv_plan_padding": [p, pi, pi, pi, pi],
@@ -108,6 +109,16 @@ def fconv_plan_create(N, H, W, C, K, R, S, stride_h, stride_w, padding, dtype, a
     plan = ctypes.c_void_p()
     _check(_load().fconv_plan_create(ctypes.byref(plan), N, H, W, C, K, R, S, stride_h,
                                      stride_w, padding, dtype, act), "fconv_plan_create")
+    return plan.value
+
+
+def fconv_plan_create_transposed(N, H, W, C, K, R, S, stride_h, stride_w, pad_top, pad_bottom,
+                                 pad_left, pad_right, dtype, act) -> int:
+    plan = ctypes.c_void_p()
+    _check(_load().fconv_plan_create_transposed(ctypes.byref(plan), N, H, W, C, K, R, S, stride_h,
+                                                stride_w, pad_top, pad_bottom, pad_left,
+                                                pad_right, dtype, act),
+           "fconv_plan_create_transposed")
     return plan.value
 
 
@@ -235,19 +246,25 @@ class Conv2dPlan:
     """
 
     def __init__(self, N, H, W, C, K, R, S, stride=1, padding="SAME", dtype="int8", relu=True,
-                 device=None, alpha=0.0, beta=0.0):
+                 device=None, alpha=0.0, beta=0.0, transposed_pads=None):
         """relu: True/False (BiasAdd+Relu / BiasAdd) or an FCONV_ACT_* code;
-        alpha, beta: that activation's parameters."""
+        alpha, beta: that activation's parameters.  transposed_pads =
+        (top, bottom, left, right) makes a transposed-convolution plan
+        (padding is then ignored)."""
         import torch
         sh, sw = (stride, stride) if isinstance(stride, int) else stride
-        pad = {"SAME": FCONV_SAME, "VALID": FCONV_VALID}[padding]
         dt = {"int8": FCONV_INT8, "bf16": FCONV_BF16}[dtype]
         self.dtype = dtype
         if isinstance(relu, bool):
             act = FCONV_ACT_RELU if relu else FCONV_ACT_NONE
         else:
             act = int(relu)
-        self.handle = fconv_plan_create(N, H, W, C, K, R, S, sh, sw, pad, dt, act)
+        if transposed_pads is not None:
+            self.handle = fconv_plan_create_transposed(N, H, W, C, K, R, S, sh, sw,
+                                                       *transposed_pads, dt, act)
+        else:
+            pad = {"SAME": FCONV_SAME, "VALID": FCONV_VALID}[padding]
+            self.handle = fconv_plan_create(N, H, W, C, K, R, S, sh, sw, pad, dt, act)
         if alpha or beta:
             fconv_plan_set_activation_params(self.handle, alpha, beta)
         self.out_shape = fconv_plan_output_shape(self.handle)

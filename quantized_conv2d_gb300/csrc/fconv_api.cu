@@ -32,6 +32,12 @@ struct fconv_plan {
   // int8 1x1 filter with a stride above 1: only the pixels the convolution
   // reads are widened, into a compact [N][P][Q][C] copy read at stride 1
   int subsample;
+  // transposed convolution: the filter is packed flipped in both spatial axes
+  int transposed;
+  // transposed convolution with a stride above 1: the prep launch copies x
+  // with stride-1 zero rows/columns inserted ((H-1)*sh+1 x (W-1)*sw+1), and
+  // the convolution runs at stride 1 on that copy
+  int upsample;
   float act_alpha, act_beta;   // activation parameters (fconv_plan_set_activation_params)
   cudaEvent_t events[4];
   bool use_events;
@@ -103,12 +109,23 @@ int sm_count_of_current_device(int fallback) {
   return v;
 }
 
+// The input as the convolution kernels read it: extents and strides.
+struct InputView {
+  int H, W, sh, sw;
+};
+InputView input_view(const fconv_plan &p) {
+  if (p.subsample) return {p.P, p.Q, 1, 1};   // compact copy of the strided pixels
+  if (p.upsample) return {(p.H - 1) * p.sh + 1, (p.W - 1) * p.sw + 1, 1, 1};
+  return {p.H, p.W, p.sh, p.sw};
+}
+
 // The A tile can be loaded by one TMA im2col copy when a k-block never
 // straddles two filter taps (C % 64 == 0) and the convolution fits the
 // tensor map's limits for a 4-D tensor: bounding-box corners in [-128, 127],
 // traversal strides <= 8, filter offsets small.
 bool im2col_ok(const fconv_plan &p) {
-  const int sh = p.subsample ? 1 : p.sh, sw = p.subsample ? 1 : p.sw;
+  const InputView v = input_view(p);
+  const int sh = v.sh, sw = v.sw;
   if (p.C % 64 != 0 || sh > 8 || sw > 8 || p.R > 16 || p.S > 16) return false;
   const int corners[4] = {-p.pl, -p.pt, p.pr - (p.S - 1), p.pb - (p.R - 1)};
   for (int c : corners)
@@ -217,6 +234,7 @@ int device_sm_count(int *dev_out) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+
 // Scratch a run needs: the packed filter, and for int8 plans the fp16 copy of
 // the input the gathers read.
 size_t workspace_need(const fconv_plan &p) { return p.wt_bytes + p.xh_bytes; }
@@ -261,25 +279,27 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
 
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
-  // filter pack and (int8) input widening in one launch
-  // the input as the convolution reads it: a subsampled plan reads its
-  // compact copy as a P x Q image at stride 1 (a 1x1 filter has no padding)
-  const bool sub = p->subsample != 0;
-  const int gH = sub ? p->P : p->H, gW = sub ? p->Q : p->W;
-  const int gsh = sub ? 1 : p->sh, gsw = sub ? 1 : p->sw;
+  // filter pack and input copy (int8 widening; subsampled or upsampled
+  // copies) in one launch; the convolution reads the copy when there is one
+  const InputView view = input_view(*p);
+  const int gH = view.H, gW = view.W, gsh = view.sh, gsw = view.sw;
+  const bool copy = is_int8 || p->upsample;
   const void *act = x;
   const long long n = static_cast<long long>(p->N) * gH * gW * p->C;
-  if (!skip_pack || is_int8) {
+  if (!skip_pack || copy) {
     fconv::WidenMap map;
     memset(&map, 0, sizeof map);
-    map.subsample = p->subsample;
-    map.C = p->C; map.H = p->H; map.W = p->W; map.P = p->P; map.Q = p->Q;
+    map.mode = p->subsample ? fconv::kCopySubsample
+                            : p->upsample ? fconv::kCopyUpsample : fconv::kCopyDense;
+    map.C = p->C; map.H = p->H; map.W = p->W; map.P = gH; map.Q = gW;
     map.sh = p->sh; map.sw = p->sw;
+    map.flip_R = p->transposed ? p->R : 0;
+    map.flip_S = p->transposed ? p->S : 0;
     e = fconv::launch_prep(is_int8, skip_pack ? nullptr : w, wt, p->Ktot, skip_pack ? 0 : p->K,
-                           p->Kpad, static_cast<const int8_t *>(x), xh, n, map, sms, stream);
+                           p->Kpad, x, xh, copy ? n : 0, map, sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
   }
-  if (is_int8) act = xh;
+  if (copy) act = xh;
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -437,6 +457,10 @@ fconv_status enqueue_fused(fconv_plan *p, const void *x, const void *w, const fl
 }
 }  // namespace fconv
 
+namespace {
+fconv_status finish_plan(fconv_plan &p, fconv_plan **plan);
+}  // namespace
+
 extern "C" {
 
 fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, int K, int R, int S,
@@ -463,6 +487,18 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, in
       !axis_geometry(W, S, stride_w, padding, &p.Q, &p.pl, &p.pr))
     return fail(FCONV_ERR_INVALID_VALUE, "VALID padding with a filter larger than the input");
 
+  return finish_plan(p, plan);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Everything after the geometry: limits, k-blocks, tile, workspace.
+fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
+  const int N = p.N, H = p.H, W = p.W, C = p.C, K = p.K, R = p.R, S = p.S;
+  const fconv_dtype dtype = p.dtype;
+  const int stride_h = p.sh, stride_w = p.sw;
   const int vec = dtype == FCONV_INT8 ? 16 : 8;
   if (C % vec != 0 || K % vec != 0)
     return fail(FCONV_ERR_NOT_SUPPORTED,
@@ -494,14 +530,64 @@ fconv_status fconv_plan_create(fconv_plan **plan, int N, int H, int W, int C, in
   p.host_chunks = 0;
   p.pipe_dev = -1;
   p.wt_bytes = align_up(static_cast<size_t>(K) * p.Kpad * 2, 256);
-  const long long xh_elems =
-      p.subsample ? static_cast<long long>(N) * p.P * p.Q * C : in_elems;
-  p.xh_bytes = dtype == FCONV_INT8 ? align_up(static_cast<size_t>(xh_elems) * 2, 256) : 0;
+  const InputView view = input_view(p);
+  const long long xh_elems = static_cast<long long>(N) * view.H * view.W * C;
+  if (xh_elems > kLimit) return fail(FCONV_ERR_NOT_SUPPORTED, "a tensor has 2^31 or more elements");
+  p.xh_bytes = (dtype == FCONV_INT8 || p.upsample)
+                   ? align_up(static_cast<size_t>(xh_elems) * 2, 256) : 0;
 
   fconv_plan *out = new (std::nothrow) fconv_plan(p);
   if (!out) return fail(FCONV_ERR_INTERNAL, "out of host memory");
   *plan = out;
   return FCONV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fconv_status fconv_plan_create_transposed(fconv_plan **plan, int N, int H, int W, int C, int K,
+                                          int R, int S, int stride_h, int stride_w, int pad_top,
+                                          int pad_bottom, int pad_left, int pad_right,
+                                          fconv_dtype dtype, fconv_act act) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan output pointer is NULL");
+  *plan = nullptr;
+  if (N <= 0 || H <= 0 || W <= 0 || C <= 0 || K <= 0 || R <= 0 || S <= 0)
+    return fail(FCONV_ERR_INVALID_VALUE, "every extent must be positive");
+  if (stride_h <= 0 || stride_w <= 0) return fail(FCONV_ERR_INVALID_VALUE, "strides must be >= 1");
+  if (dtype != FCONV_INT8 && dtype != FCONV_BF16)
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown dtype %d", (int)dtype);
+  if (act < FCONV_ACT_NONE || act > FCONV_ACT_CLAMP)
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown activation %d", (int)act);
+  const long long Ho = static_cast<long long>(H - 1) * stride_h + R - pad_top - pad_bottom;
+  const long long Wo = static_cast<long long>(W - 1) * stride_w + S - pad_left - pad_right;
+  if (Ho <= 0 || Wo <= 0) return fail(FCONV_ERR_INVALID_VALUE, "the pads leave no output");
+  // pads in [0, filter-1]; the bottom/right pad may go down to 1-stride
+  // (an output adjustment larger than the pad)
+  if (pad_top < 0 || pad_top > R - 1 || pad_bottom < 1 - stride_h || pad_bottom > R - 1 ||
+      pad_left < 0 || pad_left > S - 1 || pad_right < 1 - stride_w || pad_right > S - 1)
+    return fail(FCONV_ERR_NOT_SUPPORTED,
+                "transposed-convolution pads must lie in [0, filter-1] (bottom/right down to "
+                "1-stride)");
+  if (stride_h > 8 || stride_w > 8)
+    return fail(FCONV_ERR_NOT_SUPPORTED, "transposed-convolution strides above 8");
+  // Stride 1: out[h, w] = sum over taps of x[h - r + pad_top, w - s + pad_left] w[r, s]
+  // is the cross-correlation of x with the filter flipped in both spatial
+  // axes and padded by filter-1-pad on each side.  Stride s: the same on x
+  // with s-1 zero rows (columns) inserted between its rows (columns).
+  fconv_plan p;
+  memset(&p, 0, sizeof p);
+  p.N = N; p.H = H; p.W = W; p.C = C; p.K = K; p.R = R; p.S = S;
+  p.sh = stride_h; p.sw = stride_w;
+  p.upsample = (stride_h > 1 || stride_w > 1) ? 1 : 0;
+  p.padding = FCONV_VALID;   // unused: the pads are explicit
+  p.dtype = dtype; p.act = act;
+  p.transposed = 1;
+  p.pt = R - 1 - pad_top; p.pb = R - 1 - pad_bottom;
+  p.pl = S - 1 - pad_left; p.pr = S - 1 - pad_right;
+  p.P = static_cast<int>(Ho);
+  p.Q = static_cast<int>(Wo);
+  return finish_plan(p, plan);
 }
 
 fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha, float beta) {

@@ -56,11 +56,16 @@ cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensor
 // Whether a gather mode has a kernel for this output-channel tile; chunked
 // int8 sums on the cp.async path need a third TMEM region (BN <= 128).
 bool gather_supports(Gather gather, int block_n, bool chunked);
-// Which input elements the int8 -> fp16 widening copies.  Dense (subsample
-// 0): all of x, in place order.  Subsampled (1): for a 1x1 filter with a
-// stride above 1 the convolution reads only x[n, p*sh, q*sw, :], so only
-// those pixels are widened, into a compact [N][P][Q][C] copy that the
-// convolution then reads as a 1x1 stride-1 input.
+// Which input elements the prep launch copies (int8 widened to fp16, bf16
+// as it is) into the [N][P][Q][C] copy the convolution reads.  Dense
+// (mode 0, int8 only): all of x, P x Q = H x W.  Subsampled (1): for a 1x1
+// filter with a stride above 1 the convolution reads only
+// x[n, p*sh, q*sw, :], so only those pixels are copied, and the convolution
+// reads the copy as a 1x1 stride-1 input.  Upsampled (2): a transposed
+// convolution with stride (sh, sw) is the stride-1 one on x with sh-1 zero
+// rows (sw-1 zero columns) inserted between its rows (columns): copy pixel
+// (n, a, b) is x[n, a/sh, b/sw, :] when sh divides a and sw divides b, else
+// zero; P = (H-1)*sh + 1, Q = (W-1)*sw + 1.
 // Division by an invariant d >= 1 of any n < 2^31: q = (umulhi(n, m) + n) >> l
 // with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1 (the
 // multiply-high method of Granlund and Montgomery, "Division by invariant
@@ -68,17 +73,21 @@ bool gather_supports(Gather gather, int block_n, bool chunked);
 struct FastDiv {
   uint32_t d, m, l;
 };
+constexpr int kCopyDense = 0, kCopySubsample = 1, kCopyUpsample = 2;
 struct WidenMap {
-  int subsample;
+  int mode;
   int C, H, W, P, Q, sh, sw;
-  FastDiv units_per_pixel, pq, q;   // filled in by launch_prep
+  FastDiv units_per_pixel, pq, q, div_sh, div_sw;   // filled in by launch_prep
+  // filter pack: flip_R, flip_S > 0 read w[R-1-r][S-1-s] (transposed
+  // convolution); 0 reads it as it is
+  int flip_R, flip_S;
 };
 // Filter pack ([RSC][K] -> K-major 16-bit [K][Kpad]) and, for int8 plans,
 // the int8 -> fp16 widening of the input (n elements of the copy, a multiple
 // of 16), in one launch (a second, tiny one when a dense n is not a multiple
 // of 64).
 cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
-                        const int8_t *x, __half *xh, long long n, const WidenMap &map,
+                        const void *x, __half *xh, long long n, const WidenMap &map,
                         int sm_count, cudaStream_t stream);
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out);
 // Resource description of the kernel whose launch failed last on this thread.

@@ -804,26 +804,34 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &d) {
   return (__umulhi(n, d.m) + n) >> d.l;
 }
 
-// Source of 8-element unit g of the subsampled copy: element 8g is channel
-// c of output pixel (n, p, q), read from x[n, p*sh, q*sw, c].  C is a
-// multiple of 16, so a unit never straddles two pixels and stays 8-byte
+// Source of 8-element unit g of a subsampled or upsampled copy (-1: a zero
+// unit): element 8g is channel c of copy pixel (n, a, b).  C is a multiple
+// of 8 (16 for int8), so a unit never straddles two pixels and stays
 // aligned; the copy holds fewer than 2^31 elements.
-__device__ __forceinline__ long long subsample_src_unit(long long g, const WidenMap &m) {
+__device__ __forceinline__ long long copy_src_unit(long long g, const WidenMap &m) {
   const uint32_t u = static_cast<uint32_t>(g);
   const uint32_t pix = fast_div(u, m.units_per_pixel);
   const uint32_t cu = u - pix * m.units_per_pixel.d;
   const uint32_t n = fast_div(pix, m.pq);
   const uint32_t rem = pix - n * m.pq.d;
-  const uint32_t p = fast_div(rem, m.q);
-  const uint32_t q = rem - p * m.q.d;
-  return ((static_cast<long long>(n) * m.H + static_cast<long long>(p) * m.sh) * m.W +
-          static_cast<long long>(q) * m.sw) * m.units_per_pixel.d + cu;
+  const uint32_t a = fast_div(rem, m.q);
+  const uint32_t b = rem - a * m.q.d;
+  uint32_t h, w;
+  if (m.mode == kCopySubsample) {
+    h = a * static_cast<uint32_t>(m.sh);
+    w = b * static_cast<uint32_t>(m.sw);
+  } else {
+    h = fast_div(a, m.div_sh);
+    w = fast_div(b, m.div_sw);
+    if (h * m.div_sh.d != a || w * m.div_sw.d != b) return -1;
+  }
+  return ((static_cast<long long>(n) * m.H + h) * m.W + w) * m.units_per_pixel.d + cu;
 }
 
 template <bool IS_INT8>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int RSC, int K, int Kpad,
-                int pack_blocks, const int8_t *__restrict__ x, __half *__restrict__ xh,
+                int pack_blocks, const void *__restrict__ xv, __half *__restrict__ xh,
                 long long n8, const WidenMap map) {
   if (static_cast<int>(blockIdx.x) < pack_blocks) {
     __shared__ uint16_t tile[kPackTile][kPackTile + 2];
@@ -839,7 +847,15 @@ __global__ void __launch_bounds__(kPrepThreads)
         const int k = k0 + j + t;
         uint16_t v = 0;
         if (rsc < RSC && k < K) {
-          const long long idx = static_cast<long long>(rsc) * K + k;
+          int src = rsc;
+          if (map.flip_R > 0) {
+            // (r, s, c) -> (R-1-r, S-1-s, c)
+            const int C = RSC / (map.flip_R * map.flip_S);
+            const int c = rsc % C, rs = rsc / C;
+            const int r = rs / map.flip_S, s2 = rs - r * map.flip_S;
+            src = ((map.flip_R - 1 - r) * map.flip_S + (map.flip_S - 1 - s2)) * C + c;
+          }
+          const long long idx = static_cast<long long>(src) * K + k;
           if (IS_INT8)
             v = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<const int8_t *>(w)[idx])));
           else
@@ -861,32 +877,49 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
     return;
   }
-  if (!IS_INT8) return;
-  // Widening, warp-contiguous: in one step a warp converts 8 x 256 bytes;
-  // for each of the 8 rounds lane l loads 8 bytes at 8*l of the round (256
-  // contiguous bytes a warp instruction) and stores their 16 fp16 bytes
-  // (512 contiguous bytes a warp instruction).
-  // (Subsampled copies: the same, with each unit read from its pixel.)
+  // Input copy, warp-contiguous: in one step a warp handles 8 x 32 units of
+  // 8 elements; for each of the 8 rounds lane l takes unit 32*round + l, so
+  // a warp instruction loads 256 contiguous int8 bytes (or 512 bf16 bytes)
+  // of a dense copy and stores 512 contiguous fp16 bytes.  Subsampled and
+  // upsampled copies read each unit from its own pixel (or write zeros).
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x - pack_blocks) * (kPrepThreads / 32);
   for (long long base = (static_cast<long long>(blockIdx.x - pack_blocks) * (kPrepThreads / 32) +
                          (threadIdx.x >> 5)) * 256;
        base < n8; base += warps * 256) {
-    uint2 in[8];
+    if constexpr (IS_INT8) {
+      const int8_t *x = static_cast<const int8_t *>(xv);
+      uint2 in[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const long long g = base + u * 32 + lane;
-      const long long src = map.subsample ? subsample_src_unit(g, map) : g;
-      in[u] = g < n8 ? ldg_nc_v2(x + 8 * src) : make_uint2(0, 0);
-    }
+      for (int u = 0; u < 8; ++u) {
+        const long long g = base + u * 32 + lane;
+        const long long src = map.mode == kCopyDense ? g : copy_src_unit(g, map);
+        // a zero byte widens to +0.0
+        in[u] = (g < n8 && src >= 0) ? ldg_nc_v2(x + 8 * src) : make_uint2(0, 0);
+      }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const long long g = base + u * 32 + lane;
-      if (g < n8) {
-        uint4 o;
-        i8x4_to_f16x4(in[u].x, o.x, o.y);
-        i8x4_to_f16x4(in[u].y, o.z, o.w);
-        stg_v4(xh + 8 * g, o);
+      for (int u = 0; u < 8; ++u) {
+        const long long g = base + u * 32 + lane;
+        if (g < n8) {
+          uint4 o;
+          i8x4_to_f16x4(in[u].x, o.x, o.y);
+          i8x4_to_f16x4(in[u].y, o.z, o.w);
+          stg_v4(xh + 8 * g, o);
+        }
+      }
+    } else {
+      const uint16_t *x = static_cast<const uint16_t *>(xv);
+      uint4 in[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const long long g = base + u * 32 + lane;
+        const long long src = map.mode == kCopyDense ? g : copy_src_unit(g, map);
+        in[u] = (g < n8 && src >= 0) ? ldg_nc_v4(x + 8 * src) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const long long g = base + u * 32 + lane;
+        if (g < n8) stg_v4(xh + 8 * g, in[u]);
       }
     }
   }
@@ -1011,20 +1044,25 @@ static FastDiv make_fast_div(uint32_t d) {
 }
 
 cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
-                        const int8_t *x, __half *xh, long long n, const WidenMap &map_in,
+                        const void *x, __half *xh, long long n, const WidenMap &map_in,
                         int sm_count, cudaStream_t stream) {
   WidenMap map = map_in;
-  if (map.subsample) {
-    if (map.C % 16 != 0 || map.P <= 0 || map.Q <= 0 || n >= (1ll << 31))
+  if (map.mode != kCopyDense) {
+    if (map.C % 8 != 0 || map.P <= 0 || map.Q <= 0 || map.sh <= 0 || map.sw <= 0 ||
+        n >= (1ll << 31))
       return cudaErrorInvalidValue;
     map.units_per_pixel = make_fast_div(static_cast<uint32_t>(map.C / 8));
     map.pq = make_fast_div(static_cast<uint32_t>(map.P) * static_cast<uint32_t>(map.Q));
     map.q = make_fast_div(static_cast<uint32_t>(map.Q));
+    map.div_sh = make_fast_div(static_cast<uint32_t>(map.sh));
+    map.div_sw = make_fast_div(static_cast<uint32_t>(map.sw));
+  } else if (!is_int8) {
+    n = 0;   // bf16 plans read a dense input as it is
   }
   const int pack_blocks = ((Kpad + kPackTile - 1) / kPackTile) * ((K + kPackTile - 1) / kPackTile);
   // 8-element units the main loop widens: all of a subsampled copy; the
   // whole 64-element groups of a dense one (the tail kernel does the rest)
-  const long long n8 = !is_int8 ? 0 : map.subsample ? n / 8 : (n / 64) * 8;
+  const long long n8 = map.mode != kCopyDense ? n / 8 : (n / 64) * 8;
   long long widen_blocks = (n8 + 8 * kPrepThreads - 1) / (8 * kPrepThreads);
   const long long cap = static_cast<long long>(sm_count) * 4;
   if (widen_blocks > cap) widen_blocks = cap;
@@ -1034,14 +1072,15 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int 
     prep_kernel<true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks, x, xh,
                                                           n8, map);
   else
-    prep_kernel<false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
-                                                           nullptr, nullptr, 0, map);
+    prep_kernel<false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks, x,
+                                                           xh, n8, map);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || !is_int8 || map.subsample) return e;
+  if (e != cudaSuccess || !is_int8 || map.mode != kCopyDense) return e;
   const long long n16 = n / 16, first16 = (n / 64) * 4;
   if (n16 > first16) {
     const long long rest = n16 - first16;
-    widen_tail_kernel<<<static_cast<unsigned>((rest + 255) / 256), 256, 0, stream>>>(x, xh, first16,
+    widen_tail_kernel<<<static_cast<unsigned>((rest + 255) / 256), 256, 0, stream>>>(
+        static_cast<const int8_t *>(x), xh, first16,
                                                                                      n16);
     e = cudaGetLastError();
   }

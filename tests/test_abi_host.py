@@ -228,3 +228,42 @@ def test_activation_params_validation():
         finally:
             fc.fconv_plan_destroy(h)
     assert _err(fc.fconv_plan_set_activation_params, None, 0.0, 0.0) == fc.FCONV_ERR_INVALID_VALUE
+
+
+def test_transposed_plan_geometry_and_limits():
+    # Ho = (H-1)*s + R - pt - pb
+    h = fc.fconv_plan_create_transposed(2, 7, 9, 16, 32, 3, 5, 1, 1, 1, 0, 2, 1, 0, 1)
+    try:
+        assert fc.fconv_plan_output_shape(h) == (2, 7 - 1 + 3 - 1 - 0, 9 - 1 + 5 - 2 - 1, 32)
+        assert fc.fconv_plan_output_shape(h)[1:3] == (
+            oracle.convT_out_size(7, 3, 1, 1, 0), oracle.convT_out_size(9, 5, 1, 2, 1))
+    finally:
+        fc.fconv_plan_destroy(h)
+    bad = [
+        ((2, 7, 9, 16, 32, 3, 3, 2, 2, 1, 1, 1, 1, 0, 1), None),                        # stride 2
+        ((2, 7, 9, 16, 32, 3, 3, 2, 2, 1, 0, 1, 0, 0, 1), None),        # output adjustment 1
+        ((2, 7, 9, 16, 32, 3, 3, 2, 2, 1, -1, 1, 0, 0, 1), None),       # pad_bottom 1 - stride
+        ((2, 7, 9, 16, 32, 3, 3, 2, 2, 1, -2, 1, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),
+        ((2, 7, 9, 16, 32, 3, 3, 9, 1, 1, 1, 1, 1, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),  # stride 9
+        ((2, 7, 9, 16, 32, 3, 3, 1, 1, 3, 0, 0, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),  # pad > R-1
+        ((2, 7, 9, 16, 32, 3, 3, 1, 1, -1, 0, 0, 0, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),
+        ((2, 1, 1, 16, 32, 1, 1, 1, 1, 0, 0, 0, 0, 0, 1), None),                        # 1x1 output
+        ((2, 7, 9, 24, 32, 3, 3, 1, 1, 1, 1, 1, 1, 0, 1), fc.FCONV_ERR_NOT_SUPPORTED),  # int8 C % 16
+        ((0, 7, 9, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1, 0, 1), fc.FCONV_ERR_INVALID_VALUE),
+    ]
+    for args, status in bad:
+        if status is None:
+            fc.fconv_plan_destroy(fc.fconv_plan_create_transposed(*args))
+        else:
+            assert _err(fc.fconv_plan_create_transposed, *args) == status
+
+
+def test_transposed_workspace_holds_the_upsampled_copy():
+    # stride 2, bf16: x with zero rows/columns inserted, (7-1)*2+1 x (9-1)*2+1
+    h = fc.fconv_plan_create_transposed(2, 7, 9, 16, 32, 3, 3, 2, 2, 1, 1, 1, 1, 1, 1)
+    try:
+        assert fc.fconv_plan_output_shape(h) == (2, 13, 17, 32)
+        xh = 2 * 13 * 17 * 16 * 2
+        assert fc.fconv_workspace_size(h) == 32 * 192 * 2 + (xh + 255) // 256 * 256
+    finally:
+        fc.fconv_plan_destroy(h)
