@@ -56,7 +56,17 @@ def axis(in_, filt, stride, padding):
 
 
 def ops_counts(wl):
-    """(nominal ops 2*M*N*K with padded taps, ops over in-bounds taps only)."""
+    """(nominal ops 2*M*N*K with padded taps, ops over in-bounds taps only).
+    Transposed convolutions: nominal = 2 * every input pixel x tap x channel
+    pair of the scatter; in-bounds = those whose target is in the output."""
+    if wl.transposed_pads is not None:
+        pt, pb, pl, pr = wl.transposed_pads
+        P = (wl.H - 1) * wl.stride + wl.R - pt - pb
+        Q = (wl.W - 1) * wl.stride + wl.S - pl - pr
+        nominal = 2 * wl.N * wl.H * wl.W * wl.C * wl.K * wl.R * wl.S
+        rows = sum(1 for p in range(wl.H) for r in range(wl.R) if 0 <= p * wl.stride + r - pt < P)
+        cols = sum(1 for q in range(wl.W) for s in range(wl.S) if 0 <= q * wl.stride + s - pl < Q)
+        return nominal, 2 * wl.N * wl.C * wl.K * rows * cols, P, Q
     P, pt = axis(wl.H, wl.R, wl.stride, wl.padding)
     Q, pl = axis(wl.W, wl.S, wl.stride, wl.padding)
     nominal = 2 * wl.N * P * Q * wl.K * wl.R * wl.S * wl.C
@@ -175,14 +185,25 @@ def time_oracle(wl, P, Q, target_s: float, max_images: int):
     def run(n):
         inp = FI.generate(wl, (P, Q), batch=n)
         t0 = time.perf_counter()
-        acc = oracle.conv_acc_i8(inp["x"], inp["w"], wl.stride, pad)
-        oracle.epilogue_i8(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale, wl.relu)
+        if wl.transposed_pads is not None:
+            acc = (oracle.convT_acc_i8 if wl.dtype == "int8" else oracle.convT_acc_bf16_f64)(
+                inp["x"], inp["w"], wl.stride, wl.transposed_pads)
+        elif wl.dtype == "int8":
+            acc = oracle.conv_acc_i8(inp["x"], inp["w"], wl.stride, pad)
+        else:
+            acc = oracle.conv_acc_bf16_f64(inp["x"], inp["w"], wl.stride, pad)
+        if wl.dtype == "int8":
+            oracle.epilogue_i8(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale,
+                               wl.relu)
+        else:
+            oracle.epilogue_f64(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale,
+                                wl.relu)
         return time.perf_counter() - t0
 
     t1 = run(1)
     n = int(max(1, min(max_images, target_s / max(t1, 1e-6))))
     t = run(n) if n > 1 else t1
-    per_image = 2 * P * Q * wl.K * wl.R * wl.S * wl.C
+    per_image = ops_counts(wl)[0] / wl.N
     return per_image * n / t / 1e12, n, t, oracle.num_threads()
 
 
@@ -190,7 +211,7 @@ def time_oracle(wl, P, Q, target_s: float, max_images: int):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    wl = FI.WORKLOADS[args.workload]
+    wl = FI.workload(args.workload)
     _, _, P, Q = ops_counts(wl)
     step_target = min(2.0, 150.0 / max(1, args.steps + args.warmup))
     values, secs, n_img, threads = [], [], 1, 1
@@ -206,7 +227,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8", "data": "synthetic (seeded)", "config": config_of(wl),
+        "dtype": wl.dtype, "data": "synthetic (seeded)", "config": config_of(wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -215,9 +236,24 @@ def run_reference(args, rank, world):
 
 
 def config_of(wl):
-    return {"workload": f"{wl.name}: {wl.note}", "N": wl.N, "H": wl.H, "W": wl.W, "C": wl.C,
-            "K": wl.K, "R": wl.R, "S": wl.S, "stride": wl.stride, "padding": wl.padding,
-            "dtype": wl.dtype, "side_input": wl.has_side, "relu": wl.relu}
+    cfg = {"workload": f"{wl.name}: {wl.note}", "N": wl.N, "H": wl.H, "W": wl.W, "C": wl.C,
+           "K": wl.K, "R": wl.R, "S": wl.S, "stride": wl.stride, "padding": wl.padding,
+           "dtype": wl.dtype, "side_input": wl.has_side, "relu": wl.relu}
+    if wl.transposed_pads is not None:
+        cfg["transposed"] = True
+        cfg["padding"] = "explicit (top, bottom, left, right) = " + str(tuple(wl.transposed_pads))
+    return cfg
+
+
+# epilogue variants: (activation code or None for the workload's own, alpha, beta,
+# per-channel conv scale)
+VARIANTS = {
+    "plain": (None, 0.0, 0.0, False),
+    "channel_scale": (None, 0.0, 0.0, True),
+    "leaky_relu": (2, 0.1, 0.0, False),
+    "clipped_relu": (3, 6.0, 0.0, False),
+    "clamp": (4, -20.0, 20.0, False),
+}
 
 
 def run_fconv(args, rank, world, local_rank):
@@ -226,10 +262,12 @@ def run_fconv(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    wl = FI.WORKLOADS[args.workload]
+    wl = FI.workload(args.workload)
     nominal, inbounds, P, Q = ops_counts(wl)
+    act, alpha, beta, per_channel = VARIANTS[args.variant]
     plan = fc.Conv2dPlan(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.padding,
-                         wl.dtype, wl.relu, device=dev)
+                         wl.dtype, wl.relu if act is None else act, device=dev, alpha=alpha,
+                         beta=beta, transposed_pads=wl.transposed_pads)
     if args.tile:
         plan.set_tile(args.tile)
     assert plan.out_shape == (wl.N, P, Q, wl.K)
@@ -245,8 +283,14 @@ def run_fconv(args, rank, world, local_rank):
     x, w, bias, side = to_dev(inp["x"]), to_dev(inp["w"]), to_dev(inp["bias"]), to_dev(inp["side"])
     y = plan.new_output()
     stream = torch.cuda.current_stream(dev)
+    # a per-channel scale spreads the workload's scalar over [0.5, 1.5] x
+    cs = wl.conv_scale
+    if per_channel:
+        cs = torch.linspace(0.5 * wl.conv_scale, 1.5 * wl.conv_scale, wl.K,
+                            dtype=torch.float32, device=dev)
+
     def step():
-        plan.run(x, w, bias, side, wl.conv_scale, wl.side_scale, y=y, stream=stream)
+        plan.run(x, w, bias, side, cs, wl.side_scale, y=y, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -264,10 +308,18 @@ def run_fconv(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.25)   # let the sampler start before the timed region
+    # inputs smaller than L2: flush it before every timed step (a 256 MB
+    # write), outside the step's own events, and time the steps by those
+    footprint = sum(t.numel() * t.element_size() for t in (x, w, side, y) if t is not None) \
+        + plan.ws_bytes
+    flush = None if footprint > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8,
+                                                          device=dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
         fc.fconv_plan_set_stage_events(plan.handle, [e.cuda_event for e in evs[i]])
         step()
     t_end.record(stream)
@@ -277,6 +329,8 @@ def run_fconv(args, rank, world, local_rank):
     fc.fconv_plan_set_stage_events(plan.handle, None)
     plan.check()
     total_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        total_ms = sum(evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps))
     conv_ms = [evs[i][2].elapsed_time(evs[i][3]) for i in range(args.steps)]
     prep_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
     total_ms = reduce_max(total_ms, dev)
@@ -285,13 +339,15 @@ def run_fconv(args, rank, world, local_rank):
 
     # ------------------------------------------------ end to end, host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not per_channel:   # the host-buffer entry takes a scalar scale
         nbytes = fc.fconv_host_workspace_size(plan.handle, side is not None)
         dws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        hx = torch.from_numpy(inp["x"]).pin_memory()
-        hw = torch.from_numpy(inp["w"]).pin_memory()
-        hb = torch.from_numpy(inp["bias"]).pin_memory()
-        hs = torch.from_numpy(inp["side"]).pin_memory() if inp["side"] is not None else None
+        def pinned(a):
+            if a is None:
+                return None
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+
+        hx, hw, hb, hs = pinned(inp["x"]), pinned(inp["w"]), pinned(inp["bias"]), pinned(inp["side"])
         hy = torch.empty(plan.out_shape, dtype=plan.torch_dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in (hx, hw, hb, hs) if t is not None)
         d2h = hy.numel() * hy.element_size()
@@ -334,7 +390,8 @@ def run_fconv(args, rank, world, local_rank):
         pass
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": f"conv_fprop_kernel<{plan.config()[0]}, int8> (tcgen05.mma kind::f16)",
+                "kernel": f"conv_fprop_kernel<{plan.config()[0]}, {wl.dtype}> "
+                          f"({fc.fconv_plan_kernel(plan.handle)}, tcgen05.mma kind::f16)",
                 "peak_source": f"{'sustained' if long_run else 'burst'} bf16 dense of {src} "
                                f"(fp16 rate = bf16 rate; no int8 tensor-core MMA on sm_103a)",
                 "ops_per_launch": inbounds, "ops_definition": "2*MAC over in-bounds taps"}
@@ -342,10 +399,12 @@ def run_fconv(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded)",
-        "config": dict(config_of(wl), block_n=plan.config()[0],
-                       l2="inputs larger than L2: x+side+y+workspace = "
-                          f"{(x.numel() + (side.numel() if side is not None else 0) + y.numel() + plan.ws_bytes) / 1e6:.0f} MB > 129 MB"),
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded)",
+        "config": dict(config_of(wl), block_n=plan.config()[0], variant=args.variant,
+                       l2=(f"inputs larger than L2: x+w+side+y+workspace = {footprint / 1e6:.0f} MB"
+                           f" > {L2_BYTES / 1e6:.0f} MB") if flush is None else
+                          (f"L2 flushed before every step (x+w+side+y+workspace = "
+                           f"{footprint / 1e6:.0f} MB); steps timed by their own events")),
         "stage_ms": {"prep (filter pack + int8->fp16 widening)": statistics.mean(prep_ms),
                      "conv": statistics.mean(conv_ms)},
         "roofline": roofline,
@@ -369,7 +428,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fconv", "reference"], default="fconv")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(FI.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=list(FI.WORKLOADS) + list(FI.VARIANT_WORKLOADS))
+    ap.add_argument("--variant", default="plain", choices=list(VARIANTS),
+                    help="epilogue variant: per-channel conv scale or another activation")
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

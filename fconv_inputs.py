@@ -41,6 +41,9 @@ class Workload:
     relu: bool
     seed: int
     note: str = field(default="", compare=False)
+    # (top, bottom, left, right) for a transposed convolution (deconvolution
+    # forward, stride `stride`); None for a forward convolution
+    transposed_pads: tuple | None = field(default=None, compare=False)
 
 
 # The five workload shapes of the fused int8/bf16 conv benchmark suite.
@@ -68,6 +71,26 @@ WORKLOADS = {
 }
 
 ORDER = list(WORKLOADS)
+
+# Further shapes for the paths beyond the five (measured, not the headline):
+# transposed convolutions of a decoder / generator, one upsampling by 2.
+VARIANT_WORKLOADS = {
+    "deconv_bf16_16x16x256_s2": Workload(
+        "deconv_bf16_16x16x256_s2", "bf16", 64, 16, 16, 256, 128, 4, 4, 2, "VALID",
+        ("normal", 1.0), ("normal", 1.0 / 32.0), 0.1, 1.0, 0.0, False, True, 5,
+        "bf16 transposed conv, N=64 16x16x256 -> 32x32x128, 4x4 stride 2 pad 1, bias+ReLU",
+        transposed_pads=(1, 1, 1, 1)),
+    "deconv_i8_14x14x512_s1": Workload(
+        "deconv_i8_14x14x512_s1", "int8", 64, 14, 14, 512, 256, 3, 3, 1, "VALID",
+        ("uniform", -128, 127), ("uniform", -128, 127), 1.0, 0.0005, 0.0, False, True, 6,
+        "int8 transposed conv, N=64 14x14x512 -> 14x14x256, 3x3 stride 1 pad 1, bias+ReLU",
+        transposed_pads=(1, 1, 1, 1)),
+}
+
+
+def workload(name: str) -> Workload:
+    """A workload by name, from either table."""
+    return WORKLOADS[name] if name in WORKLOADS else VARIANT_WORKLOADS[name]
 
 
 def _draw(gen: torch.Generator, shape, dist, dtype: str) -> np.ndarray:

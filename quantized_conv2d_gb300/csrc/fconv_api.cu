@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <limits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -374,10 +375,18 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.num_tiles = p->num_tiles;
   a.conv_scale = conv_scale;
   a.side_scale = side_scale;
-  a.relu = p->act == FCONV_ACT_RELU ? 1 : 0;
   a.act = static_cast<int>(p->act);
-  a.alpha = p->act_alpha;
-  a.beta = p->act_beta;
+  {
+    const float inf = std::numeric_limits<float>::infinity();
+    a.slope = 1.0f; a.lo = -inf; a.hi = inf;
+    switch (p->act) {
+      case FCONV_ACT_RELU: a.lo = 0.0f; break;
+      case FCONV_ACT_LEAKY_RELU: a.slope = p->act_alpha; break;
+      case FCONV_ACT_CLIPPED_RELU: a.lo = 0.0f; a.hi = p->act_alpha; break;
+      case FCONV_ACT_CLAMP: a.lo = p->act_alpha; a.hi = p->act_beta; break;
+      default: break;
+    }
+  }
   a.mode = mode;
   a.debug = p->debug;
   a.timeout_ns = static_cast<unsigned long long>(p->timeout_ms) * 1000000ull;

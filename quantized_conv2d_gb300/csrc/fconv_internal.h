@@ -35,9 +35,8 @@ struct ConvArgs {
   int num_n_tiles;     // ceil(K / BN)
   int num_tiles;       // ceil(M / 128) * num_n_tiles
   float conv_scale, side_scale;
-  int relu;            // act == kActRelu (the int8 clip's lower bound is 0)
   int act;             // kAct*
-  float alpha, beta;   // activation parameters
+  float slope, lo, hi; // the activation as slope-then-clamp (see the epilogue)
   int use_side;
   int mode;
   int debug;

@@ -98,13 +98,16 @@ __device__ __forceinline__ void store_i32_slice(const ConvArgs &a, long long m, 
 // groups of 16 (int8) or 8 (bf16) columns so few values are live at once.
 // vals: the 32 pre-epilogue sums as fp32 (exact integers for int8 plans).
 // Columns at or beyond K are skipped (K is a multiple of the group width).
-// Activations other than Relu, on the fp32 value after the bias add (Relu
-// is the int8 clip's lower bound, or a max with 0 for bf16 output).
+// The activation on the fp32 value after the bias add, branch-free: a
+// slope for negative values (one rounding; 1 is exact), then a clamp to
+// [lo, hi] (infinite bounds are exact).  The host sets slope, lo and hi:
+// none (1, -inf, inf), Relu (1, 0, inf), leaky (alpha, -inf, inf), clipped
+// (1, 0, alpha), clamp (1, alpha, beta).  For v < 0 the first line is
+// round(v * slope) + 0, for v >= 0 it is 0 * slope + v: the same value as
+// "v < 0 ? v * slope : v".
 __device__ __forceinline__ float activation(float v, const ConvArgs &a) {
-  if (a.act == kActLeakyRelu) return v < 0.0f ? __fmul_rn(v, a.alpha) : v;
-  if (a.act == kActClippedRelu) return fminf(fmaxf(v, 0.0f), a.alpha);
-  if (a.act == kActClamp) return fminf(fmaxf(v, a.alpha), a.beta);
-  return v;
+  v = __fadd_rn(__fmul_rn(fminf(v, 0.0f), a.slope), fmaxf(v, 0.0f));
+  return fminf(fmaxf(v, a.lo), a.hi);
 }
 
 template <bool IS_INT8>
@@ -137,7 +140,6 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
   const float cs = a.conv_scale, ss = a.side_scale;
   const bool use_side = a.use_side != 0;
   if (IS_INT8) {
-    const int lo = a.relu ? 0 : -128;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int col = col0 + 16 * h;
@@ -165,10 +167,9 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
             const float sd = static_cast<float>(static_cast<int8_t>((sw[g] >> (8 * e)) & 0xFFu));
             v = __fmaf_rn(sd, ss, v);
           }
-          v = __fadd_rn(v, bv[e]);
-          if (a.act > kActRelu) v = activation(v, a);
+          v = activation(__fadd_rn(v, bv[e]), a);
           int r = __float2int_rn(v);  // round half to even, saturating
-          r = min(max(r, lo), 127);
+          r = min(max(r, -128), 127);
           word |= (static_cast<uint32_t>(r) & 0xFFu) << (8 * e);
         }
         out[g] = word;
@@ -204,9 +205,7 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
         for (int t = 0; t < 2; ++t) {
           float v = __fmul_rn(vals[8 * qd + 2 * g + t], sv8[2 * g + t]);
           if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
-          v = __fadd_rn(v, bv[2 * g + t]);
-          if (a.relu) v = fmaxf(v, 0.0f);
-          else if (a.act > kActRelu) v = activation(v, a);
+          v = activation(__fadd_rn(v, bv[2 * g + t]), a);
           word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << (16 * t);
         }
         out[g] = word;
@@ -828,7 +827,7 @@ __device__ __forceinline__ long long copy_src_unit(long long g, const WidenMap &
   return ((static_cast<long long>(n) * m.H + h) * m.W + w) * m.units_per_pixel.d + cu;
 }
 
-template <bool IS_INT8>
+template <bool IS_INT8, bool MAPPED>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int RSC, int K, int Kpad,
                 int pack_blocks, const void *__restrict__ xv, __half *__restrict__ xh,
@@ -893,7 +892,7 @@ __global__ void __launch_bounds__(kPrepThreads)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const long long g = base + u * 32 + lane;
-        const long long src = map.mode == kCopyDense ? g : copy_src_unit(g, map);
+        const long long src = MAPPED ? copy_src_unit(g, map) : g;
         // a zero byte widens to +0.0
         in[u] = (g < n8 && src >= 0) ? ldg_nc_v2(x + 8 * src) : make_uint2(0, 0);
       }
@@ -913,7 +912,7 @@ __global__ void __launch_bounds__(kPrepThreads)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const long long g = base + u * 32 + lane;
-        const long long src = map.mode == kCopyDense ? g : copy_src_unit(g, map);
+        const long long src = MAPPED ? copy_src_unit(g, map) : g;
         in[u] = (g < n8 && src >= 0) ? ldg_nc_v4(x + 8 * src) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
@@ -1068,12 +1067,19 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int 
   if (widen_blocks > cap) widen_blocks = cap;
   const unsigned grid = static_cast<unsigned>(pack_blocks + widen_blocks);
   if (grid == 0) return cudaSuccess;
-  if (is_int8)
-    prep_kernel<true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks, x, xh,
-                                                          n8, map);
+  const bool mapped = map.mode != kCopyDense;
+  if (is_int8 && mapped)
+    prep_kernel<true, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
+                                                                x, xh, n8, map);
+  else if (is_int8)
+    prep_kernel<true, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
+                                                                 x, xh, n8, map);
+  else if (mapped)
+    prep_kernel<false, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
+                                                                 x, xh, n8, map);
   else
-    prep_kernel<false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks, x,
-                                                           xh, n8, map);
+    prep_kernel<false, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad,
+                                                                  pack_blocks, x, xh, n8, map);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !is_int8 || map.mode != kCopyDense) return e;
   const long long n16 = n / 16, first16 = (n / 64) * 4;
