@@ -300,9 +300,11 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 }
 
 // ---------------------------------------------------------------- globals
+// Read-only loads: not volatile, so the compiler may hoist them above
+// unrelated stores and keep several in flight.
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
   uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
@@ -312,6 +314,14 @@ __device__ __forceinline__ uint2 ldg_nc_v2(const void *p) {
   asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
+// Bring the 128-byte lines of [p, p + bytes) into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void *p, int bytes) {
+  const uintptr_t first = reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(127);
+  const uintptr_t last = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes) - 1;
+  for (uintptr_t a = first; a <= last; a += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 __device__ __forceinline__ void stg_v4(void *p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)

@@ -110,9 +110,32 @@ __device__ __forceinline__ float activation(float v, const ConvArgs &a) {
   return fminf(fmaxf(v, a.lo), a.hi);
 }
 
+// Side-input words of one 32-column slice: int8 2 x 16 columns, bf16 4 x 8.
+template <bool IS_INT8>
+struct SideWords {
+  static constexpr int kWords = IS_INT8 ? 2 : 4;
+  static constexpr int kCols = IS_INT8 ? 16 : 8;
+};
+
+template <bool IS_INT8>
+__device__ __forceinline__ void load_side_words(const ConvArgs &a, long long m, int col0,
+                                                uint4 *words) {
+#pragma unroll
+  for (int h = 0; h < SideWords<IS_INT8>::kWords; ++h) {
+    const int col = col0 + h * SideWords<IS_INT8>::kCols;
+    words[h] = (a.use_side && col < a.K)
+                   ? ldg_nc_v4(static_cast<const uint8_t *>(a.side) +
+                               (m * a.K + col) * (IS_INT8 ? 1 : 2))
+                   : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// side_pre: the slice's side words loaded ahead (load_side_words), or
+// nullptr to load them here.
 template <bool IS_INT8>
 __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
-                                               const float (&vals)[32]) {
+                                               const float (&vals)[32],
+                                               const uint4 *side_pre = nullptr) {
   const int K = a.K;
   if (a.mode == kModeAccumulators) {
     // raw sums: int32 for int8 plans, fp32 for bf16 plans; 4 columns per store
@@ -145,7 +168,8 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
       const int col = col0 + 16 * h;
       if (col >= K) continue;
       uint4 sv = make_uint4(0, 0, 0, 0);
-      if (use_side) sv = ldg_nc_v4(static_cast<const int8_t *>(a.side) + m * K + col);
+      if (side_pre) sv = side_pre[h];
+      else if (use_side) sv = ldg_nc_v4(static_cast<const int8_t *>(a.side) + m * K + col);
       const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
       uint32_t out[4];
 #pragma unroll
@@ -182,7 +206,8 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
       const int col = col0 + 8 * qd;
       if (col >= K) continue;
       uint4 sv = make_uint4(0, 0, 0, 0);
-      if (use_side) sv = ldg_nc_v4(static_cast<const __nv_bfloat16 *>(a.side) + m * K + col);
+      if (side_pre) sv = side_pre[qd];
+      else if (use_side) sv = ldg_nc_v4(static_cast<const __nv_bfloat16 *>(a.side) + m * K + col);
       const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
       const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + col));
       const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + col + 4));
@@ -423,6 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long m = static_cast<long long>(m_tile) * kBM + row;
       const bool mvalid = m < args.M;
       const int n0 = n_tile * BN;
+      // the side input this thread reads after the tile's last chunk: into
+      // L2 now, so the final epilogue does not wait on DRAM
+      if (args.use_side && mvalid && n0 < args.K)
+        prefetch_l2(static_cast<const uint8_t *>(args.side) + (m * args.K + n0) * (IS_INT8 ? 1 : 2),
+                    min(BN, args.K - n0) * (IS_INT8 ? 1 : 2));
       for (int ch = 0; ch < n_chunks; ++ch) {
         if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
           ok = false;
@@ -707,7 +737,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const long long m = static_cast<long long>(m_tile) * kBM + row;
       const bool mvalid = m < args.M;
       const int c0 = n_tile * BN + cbase;
+      // the side input this thread reads after the tile's last chunk: into
+      // L2 now, so the final epilogue does not wait on DRAM
+      if (args.use_side && mvalid && c0 < args.K)
+        prefetch_l2(static_cast<const uint8_t *>(args.side) + (m * args.K + c0) * (IS_INT8 ? 1 : 2),
+                    min(C::kHalfCols, args.K - c0) * (IS_INT8 ? 1 : 2));
+      // the side words of the whole row segment, loaded before the wait for
+      // the accumulator the outputs come from, so their latency overlaps it
+      constexpr int kSideWords = C::kSlices * SideWords<IS_INT8>::kWords;
+      uint4 side_pre[kSideWords];
+      const bool preload = args.use_side && mvalid && args.mode == kModeFused;
       for (int ch = 0; ch < n_chunks; ++ch) {
+        if (ch == n_chunks - 1 && preload) {
+#pragma unroll
+          for (int jj = 0; jj < C::kSlices; ++jj)
+            load_side_words<IS_INT8>(args, m, c0 + jj * 32,
+                                     side_pre + jj * SideWords<IS_INT8>::kWords);
+        }
         if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
           ok = false;
           break;
@@ -725,7 +771,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             // + 0.0f turns a -0 sum into the +0 that float(int32 0) gives
 #pragma unroll
             for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
-            if (mvalid) epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals);
+            if (mvalid)
+              epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals,
+                                      preload ? side_pre + jj * SideWords<IS_INT8>::kWords
+                                              : nullptr);
           }
           tc_fence_before();
           __syncwarp();
@@ -759,7 +808,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 float vals[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(sums[jj * 32 + i]);
-                epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals);
+                epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals,
+                                        preload ? side_pre + jj * SideWords<IS_INT8>::kWords
+                                                : nullptr);
               }
             }
           }
