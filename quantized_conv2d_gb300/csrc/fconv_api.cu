@@ -35,10 +35,22 @@ struct fconv_plan {
   int subsample;
   // transposed convolution: the filter is packed flipped in both spatial axes
   int transposed;
-  // transposed convolution with a stride above 1: the prep launch copies x
-  // with stride-1 zero rows/columns inserted ((H-1)*sh+1 x (W-1)*sw+1), and
-  // the convolution runs at stride 1 on that copy
+  // transposed convolution with a stride above the filter: the prep launch
+  // copies x with stride-1 zero rows/columns inserted ((H-1)*sh+1 x
+  // (W-1)*sw+1), and the convolution runs at stride 1 on that copy
   int upsample;
+  int tpad[4];   // a transposed plan's pads as given (top, bottom, left, right)
+  // the packed filter's taps (see fconv::WidenMap); tap_nR == 0: as given
+  int tap_nR, tap_nS, tap_R, tap_S, tap_r0, tap_s0, tap_rstep, tap_sstep;
+  // output pixel map (see fconv::ConvArgs); omap == 0: GEMM row = pixel
+  int omap, out_H, out_W, o_sh, o_sw, o_h0, o_w0;
+  // where this plan's packed filter and input copy sit in the workspace
+  size_t ws_wt_off, ws_xh_off;
+  // a strided transposed convolution runs as sh*sw phases, each a forward
+  // plan over x with every stride-th filter tap, writing every stride-th
+  // output row and column (owned by this plan)
+  int num_phases;
+  fconv_plan *phase[64];
   float act_alpha, act_beta;   // activation parameters (fconv_plan_set_activation_params)
   cudaEvent_t events[4];
   bool use_events;
@@ -127,6 +139,7 @@ InputView input_view(const fconv_plan &p) {
 bool im2col_ok(const fconv_plan &p) {
   const InputView v = input_view(p);
   const int sh = v.sh, sw = v.sw;
+  if (p.pt < 0 || p.pl < 0) return false;   // window origins starting inside the image
   if (p.C % 64 != 0 || sh > 8 || sw > 8 || p.R > 16 || p.S > 16) return false;
   const int corners[4] = {-p.pl, -p.pt, p.pr - (p.S - 1), p.pb - (p.R - 1)};
   for (int c : corners)
@@ -238,12 +251,18 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // Scratch a run needs: the packed filter, and for int8 plans the fp16 copy of
 // the input the gathers read.
-size_t workspace_need(const fconv_plan &p) { return p.wt_bytes + p.xh_bytes; }
+size_t workspace_need(const fconv_plan &p) {
+  const size_t a = p.ws_wt_off + p.wt_bytes, b = p.ws_xh_off + p.xh_bytes;
+  return a > b ? a : b;
+}
+
+fconv_plan batch_slice(const fconv_plan &p, int n);
 
 fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *bias,
                      const void *side, float conv_scale, float side_scale, void *y,
                      void *workspace, size_t workspace_bytes, cudaStream_t stream, int mode,
-                     bool skip_pack = false, const float *scale_k = nullptr) {
+                     bool skip_pack = false, const float *scale_k = nullptr,
+                     bool skip_copy = false) {
   if (!p) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
   if (!x || !w || !y) return fail(FCONV_ERR_INVALID_VALUE, "x, w and y must not be NULL");
   if (mode == fconv::kModeFused && !bias)
@@ -269,8 +288,38 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   auto mark = [&](int i) -> cudaError_t {
     return p->use_events ? cudaEventRecord(p->events[i], stream) : cudaSuccess;
   };
-  uint16_t *wt = static_cast<uint16_t *>(workspace);
-  __half *xh = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + p->wt_bytes);
+  uint16_t *wt = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(workspace) + p->ws_wt_off);
+  __half *xh = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + p->ws_xh_off);
+
+  if (p->num_phases > 0) {
+    // one forward plan per phase, in order; the first one widens the input
+    // (int8) for all of them
+    cudaError_t e0 = mark(0);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "event record");
+    for (int i = 0; i < p->num_phases; ++i) {
+      fconv_plan *q = p->phase[i];
+      fconv_plan tmp;
+      if (q->N != p->N) {
+        tmp = batch_slice(*q, p->N);
+        q = &tmp;
+      }
+      q->act = p->act;
+      q->act_alpha = p->act_alpha;
+      q->act_beta = p->act_beta;
+      q->debug = p->debug;
+      q->timeout_ms = p->timeout_ms;
+      fconv_status st = enqueue(q, x, w, bias, side, conv_scale, side_scale, y, workspace,
+                                workspace_bytes, stream, mode, skip_pack, scale_k,
+                                skip_copy || i > 0);
+      if (st != FCONV_OK) return st;
+      if (i == 0) {
+        if ((e0 = mark(1)) != cudaSuccess || (e0 = mark(2)) != cudaSuccess)
+          return cuda_fail(e0, "event record");
+      }
+    }
+    if ((e0 = mark(3)) != cudaSuccess) return cuda_fail(e0, "event record");
+    return FCONV_OK;
+  }
 
   const fconv::Gather gather = gather_for_run(*p);
   if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb))
@@ -284,20 +333,22 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   // copies) in one launch; the convolution reads the copy when there is one
   const InputView view = input_view(*p);
   const int gH = view.H, gW = view.W, gsh = view.sh, gsw = view.sw;
-  const bool copy = is_int8 || p->upsample;
+  const bool copy = is_int8 || p->upsample;          // the convolution reads a copy
+  const bool do_copy = copy && !skip_copy;            // ... made by this launch
   const void *act = x;
   const long long n = static_cast<long long>(p->N) * gH * gW * p->C;
-  if (!skip_pack || copy) {
+  if (!skip_pack || do_copy) {
     fconv::WidenMap map;
     memset(&map, 0, sizeof map);
     map.mode = p->subsample ? fconv::kCopySubsample
                             : p->upsample ? fconv::kCopyUpsample : fconv::kCopyDense;
     map.C = p->C; map.H = p->H; map.W = p->W; map.P = gH; map.Q = gW;
     map.sh = p->sh; map.sw = p->sw;
-    map.flip_R = p->transposed ? p->R : 0;
-    map.flip_S = p->transposed ? p->S : 0;
+    map.tap_nR = p->tap_nR; map.tap_nS = p->tap_nS; map.tap_R = p->tap_R; map.tap_S = p->tap_S;
+    map.tap_r0 = p->tap_r0; map.tap_s0 = p->tap_s0;
+    map.tap_rstep = p->tap_rstep; map.tap_sstep = p->tap_sstep;
     e = fconv::launch_prep(is_int8, skip_pack ? nullptr : w, wt, p->Ktot, skip_pack ? 0 : p->K,
-                           p->Kpad, x, xh, copy ? n : 0, map, sms, stream);
+                           p->Kpad, x, xh, do_copy ? n : 0, map, sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
   }
   if (copy) act = xh;
@@ -376,6 +427,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.conv_scale = conv_scale;
   a.side_scale = side_scale;
   a.act = static_cast<int>(p->act);
+  a.omap = p->omap; a.out_H = p->out_H; a.out_W = p->out_W;
+  a.o_sh = p->o_sh; a.o_sw = p->o_sw; a.o_h0 = p->o_h0; a.o_w0 = p->o_w0;
   {
     const float inf = std::numeric_limits<float>::infinity();
     a.slope = 1.0f; a.lo = -inf; a.hi = inf;
@@ -532,7 +585,9 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   const long long m_tiles = (p.M + 127) / 128;
   if (m_tiles * ((K + 31) / 32) > kLimit)
     return fail(FCONV_ERR_NOT_SUPPORTED, "too many output tiles");
-  p.subsample = (dtype == FCONV_INT8 && R == 1 && S == 1 && (stride_h > 1 || stride_w > 1)) ? 1 : 0;
+  p.subsample =
+      (!p.transposed && dtype == FCONV_INT8 && R == 1 && S == 1 && (stride_h > 1 || stride_w > 1))
+          ? 1 : 0;
   p.auto_block_n = choose_block_n(p, sm_count_of_current_device(148));
   set_tiling(p, p.auto_block_n);
   p.timeout_ms = 2000;
@@ -544,6 +599,8 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   if (xh_elems > kLimit) return fail(FCONV_ERR_NOT_SUPPORTED, "a tensor has 2^31 or more elements");
   p.xh_bytes = (dtype == FCONV_INT8 || p.upsample)
                    ? align_up(static_cast<size_t>(xh_elems) * 2, 256) : 0;
+  p.ws_wt_off = 0;
+  p.ws_xh_off = p.wt_bytes;
 
   fconv_plan *out = new (std::nothrow) fconv_plan(p);
   if (!out) return fail(FCONV_ERR_INTERNAL, "out of host memory");
@@ -582,21 +639,102 @@ fconv_status fconv_plan_create_transposed(fconv_plan **plan, int N, int H, int W
     return fail(FCONV_ERR_NOT_SUPPORTED, "transposed-convolution strides above 8");
   // Stride 1: out[h, w] = sum over taps of x[h - r + pad_top, w - s + pad_left] w[r, s]
   // is the cross-correlation of x with the filter flipped in both spatial
-  // axes and padded by filter-1-pad on each side.  Stride s: the same on x
-  // with s-1 zero rows (columns) inserted between its rows (columns).
+  // axes and padded by filter-1-pad on each side.  Stride s <= filter: the
+  // output splits into s*s phases (rows ho with (ho + pad_top) % sh = a,
+  // columns likewise with b); phase (a, b) gets only the taps r = a + sh*j,
+  // s = b + sw*l, and is the stride-1 cross-correlation of x with those taps
+  // flipped, writing every sh-th row and sw-th column.  Stride > filter: the
+  // stride-1 case on x with zero rows/columns inserted (some outputs get no
+  // tap at all there).
   fconv_plan p;
   memset(&p, 0, sizeof p);
   p.N = N; p.H = H; p.W = W; p.C = C; p.K = K; p.R = R; p.S = S;
   p.sh = stride_h; p.sw = stride_w;
-  p.upsample = (stride_h > 1 || stride_w > 1) ? 1 : 0;
+  const bool strided = stride_h > 1 || stride_w > 1;
+  const bool phased = strided && R >= stride_h && S >= stride_w;
+  p.upsample = (strided && !phased) ? 1 : 0;
   p.padding = FCONV_VALID;   // unused: the pads are explicit
   p.dtype = dtype; p.act = act;
   p.transposed = 1;
+  p.tpad[0] = pad_top; p.tpad[1] = pad_bottom; p.tpad[2] = pad_left; p.tpad[3] = pad_right;
   p.pt = R - 1 - pad_top; p.pb = R - 1 - pad_bottom;
   p.pl = S - 1 - pad_left; p.pr = S - 1 - pad_right;
   p.P = static_cast<int>(Ho);
   p.Q = static_cast<int>(Wo);
-  return finish_plan(p, plan);
+  p.tap_nR = R; p.tap_nS = S; p.tap_R = R; p.tap_S = S;   // flipped filter
+  p.tap_rstep = 1; p.tap_sstep = 1;
+  if (!phased) return finish_plan(p, plan);
+
+  // the phases: forward plans over x (stride 1, explicit pads)
+  auto floor_div = [](long long a, long long b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
+  auto ceil_div = [&](long long a, long long b) { return -floor_div(-a, b); };
+  fconv_plan *phases[64];
+  int np = 0;
+  auto cleanup = [&]() {
+    for (int i = 0; i < np; ++i) delete phases[i];
+  };
+  size_t wt_total = 0;
+  for (int a = 0; a < stride_h; ++a) {
+    for (int b = 0; b < stride_w; ++b) {
+      const int Ra = (R - a + stride_h - 1) / stride_h, Sb = (S - b + stride_w - 1) / stride_w;
+      const long long u_lo = ceil_div(pad_top - a, stride_h);
+      const long long u_hi = floor_div(Ho - 1 + pad_top - a, stride_h);
+      const long long v_lo = ceil_div(pad_left - b, stride_w);
+      const long long v_hi = floor_div(Wo - 1 + pad_left - b, stride_w);
+      if (u_hi < u_lo || v_hi < v_lo) continue;   // no output row or column in this phase
+      fconv_plan q;
+      memset(&q, 0, sizeof q);
+      q.N = N; q.H = H; q.W = W; q.C = C; q.K = K; q.R = Ra; q.S = Sb;
+      q.sh = 1; q.sw = 1;
+      q.padding = FCONV_VALID; q.dtype = dtype; q.act = act; q.transposed = 1;
+      q.P = static_cast<int>(u_hi - u_lo + 1);
+      q.Q = static_cast<int>(v_hi - v_lo + 1);
+      // output p of the phase reads input rows p + j - pt, j < Ra
+      q.pt = static_cast<int>(Ra - 1 - u_lo);
+      q.pl = static_cast<int>(Sb - 1 - v_lo);
+      q.pb = q.P - H - q.pt + Ra - 1;
+      q.pr = q.Q - W - q.pl + Sb - 1;
+      q.tap_nR = Ra; q.tap_nS = Sb; q.tap_R = R; q.tap_S = S;
+      q.tap_r0 = a; q.tap_s0 = b; q.tap_rstep = stride_h; q.tap_sstep = stride_w;
+      q.omap = 1; q.out_H = static_cast<int>(Ho); q.out_W = static_cast<int>(Wo);
+      q.o_sh = stride_h; q.o_sw = stride_w;
+      q.o_h0 = static_cast<int>(stride_h * u_lo + a - pad_top);
+      q.o_w0 = static_cast<int>(stride_w * v_lo + b - pad_left);
+      fconv_plan *made = nullptr;
+      const fconv_status st = finish_plan(q, &made);
+      if (st != FCONV_OK) {
+        cleanup();
+        return st;
+      }
+      made->ws_wt_off = wt_total;
+      wt_total += made->wt_bytes;
+      phases[np++] = made;
+    }
+  }
+  // the whole plan: the geometry above for checks and reports; its
+  // workspace is the phases' packed filters, then one input copy (int8)
+  fconv_plan *whole = nullptr;
+  const fconv_status st = finish_plan(p, &whole);
+  if (st != FCONV_OK) {
+    cleanup();
+    return st;
+  }
+  whole->num_phases = np;
+  for (int i = 0; i < np; ++i) {
+    whole->phase[i] = phases[i];
+    phases[i]->ws_xh_off = wt_total;
+  }
+  whole->wt_bytes = wt_total;
+  whole->ws_wt_off = 0;
+  whole->ws_xh_off = wt_total;
+  whole->xh_bytes = dtype == FCONV_INT8 ? align_up(static_cast<size_t>(N) * H * W * C * 2, 256) : 0;
+  for (int i = 0; i < np; ++i) phases[i]->xh_bytes = whole->xh_bytes;
+  whole->num_tiles = 0;
+  for (int i = 0; i < np; ++i) whole->num_tiles += phases[i]->num_tiles;
+  whole->block_n = phases[0]->block_n;
+  whole->kb_chunk = phases[0]->kb_chunk;
+  *plan = whole;
+  return FCONV_OK;
 }
 
 fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha, float beta) {
@@ -613,7 +751,10 @@ fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha, flo
 }
 
 fconv_status fconv_plan_destroy(fconv_plan *plan) {
-  if (plan) destroy_pipeline(plan);
+  if (plan) {
+    destroy_pipeline(plan);
+    for (int i = 0; i < plan->num_phases; ++i) delete plan->phase[i];
+  }
   delete plan;
   return FCONV_OK;
 }
@@ -630,10 +771,11 @@ fconv_status fconv_plan_output_shape(const fconv_plan *plan, int *N, int *P, int
 fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top, int *pad_bottom,
                                 int *pad_left, int *pad_right) {
   if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
-  if (pad_top) *pad_top = plan->pt;
-  if (pad_bottom) *pad_bottom = plan->pb;
-  if (pad_left) *pad_left = plan->pl;
-  if (pad_right) *pad_right = plan->pr;
+  const bool t = plan->transposed != 0;   // report the pads the caller gave
+  if (pad_top) *pad_top = t ? plan->tpad[0] : plan->pt;
+  if (pad_bottom) *pad_bottom = t ? plan->tpad[1] : plan->pb;
+  if (pad_left) *pad_left = t ? plan->tpad[2] : plan->pl;
+  if (pad_right) *pad_right = t ? plan->tpad[3] : plan->pr;
   return FCONV_OK;
 }
 
@@ -807,6 +949,17 @@ fconv_status fconv_plan_check(fconv_plan *plan, fconv_stream_t stream) {
 
 fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
   if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (plan->num_phases > 0) {
+    // every phase takes the tile (or its own automatic choice for 0)
+    for (int i = 0; i < plan->num_phases; ++i) {
+      const fconv_status st = fconv_plan_set_tile(plan->phase[i], block_n);
+      if (st != FCONV_OK) return st;
+    }
+    plan->block_n = plan->phase[0]->block_n;
+    plan->num_tiles = 0;
+    for (int i = 0; i < plan->num_phases; ++i) plan->num_tiles += plan->phase[i]->num_tiles;
+    return FCONV_OK;
+  }
   if (block_n == 0) {
     set_tiling(*plan, plan->auto_block_n);
     return FCONV_OK;
@@ -859,6 +1012,7 @@ fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]
 
 const char *fconv_plan_kernel(const fconv_plan *plan) {
   if (!plan) return "";
+  if (plan->num_phases > 0) plan = plan->phase[0];
   return gather_for_run(*plan) == fconv::Gather::kTmaIm2col ? "tma-im2col" : "cp-async";
 }
 

@@ -36,6 +36,10 @@ struct ConvArgs {
   int num_tiles;       // ceil(M / 128) * num_n_tiles
   float conv_scale, side_scale;
   int act;             // kAct*
+  // output pixel of GEMM row m (a phase of a strided transposed convolution
+  // writes every o_sh-th row and o_sw-th column of an out_H x out_W output,
+  // from (o_h0, o_w0)); omap == 0: row m is output pixel m
+  int omap, out_H, out_W, o_sh, o_sw, o_h0, o_w0;
   float slope, lo, hi; // the activation as slope-then-clamp (see the epilogue)
   int use_side;
   int mode;
@@ -77,9 +81,12 @@ struct WidenMap {
   int mode;
   int C, H, W, P, Q, sh, sw;
   FastDiv units_per_pixel, pq, q, div_sh, div_sw;   // filled in by launch_prep
-  // filter pack: flip_R, flip_S > 0 read w[R-1-r][S-1-s] (transposed
-  // convolution); 0 reads it as it is
-  int flip_R, flip_S;
+  // filter pack: with tap_nR > 0 the packed filter is [tap_nR][tap_nS][C][K]
+  // whose tap (j, l) is w[tap_r0 + tap_rstep*(tap_nR-1-j)][tap_s0 +
+  // tap_sstep*(tap_nS-1-l)] of the caller's [tap_R][tap_S][C][K] filter
+  // (flipped, and for a phase of a strided transposed convolution every
+  // stride-th tap); tap_nR == 0 packs the filter as it is
+  int tap_nR, tap_nS, tap_R, tap_S, tap_r0, tap_s0, tap_rstep, tap_sstep;
 };
 // Filter pack ([RSC][K] -> K-major 16-bit [K][Kpad]) and, for int8 plans,
 // the int8 -> fp16 widening of the input (n elements of the copy, a multiple

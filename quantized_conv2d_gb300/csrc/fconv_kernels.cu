@@ -110,6 +110,17 @@ __device__ __forceinline__ float activation(float v, const ConvArgs &a) {
   return fminf(fmaxf(v, a.lo), a.hi);
 }
 
+// Output pixel (flat [N][out_H][out_W] index) of GEMM row m.
+__device__ __forceinline__ long long out_pixel(const ConvArgs &a, long long m) {
+  if (!a.omap) return m;
+  const long long PQ = static_cast<long long>(a.P) * a.Q;
+  const long long n = m / PQ;
+  const int rem = static_cast<int>(m - n * PQ);
+  const int p = rem / a.Q, q = rem - p * a.Q;
+  return (n * a.out_H + a.o_h0 + static_cast<long long>(p) * a.o_sh) * a.out_W + a.o_w0 +
+         static_cast<long long>(q) * a.o_sw;
+}
+
 // Side-input words of one 32-column slice: int8 2 x 16 columns, bf16 4 x 8.
 template <bool IS_INT8>
 struct SideWords {
@@ -447,11 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_tile = tile - m_tile * args.num_n_tiles;
       const long long m = static_cast<long long>(m_tile) * kBM + row;
       const bool mvalid = m < args.M;
+      const long long mo = out_pixel(args, m);   // the output pixel row m writes
       const int n0 = n_tile * BN;
       // the side input this thread reads after the tile's last chunk: into
       // L2 now, so the final epilogue does not wait on DRAM
       if (args.use_side && mvalid && n0 < args.K)
-        prefetch_l2(static_cast<const uint8_t *>(args.side) + (m * args.K + n0) * (IS_INT8 ? 1 : 2),
+        prefetch_l2(static_cast<const uint8_t *>(args.side) + (mo * args.K + n0) * (IS_INT8 ? 1 : 2),
                     min(BN, args.K - n0) * (IS_INT8 ? 1 : 2));
       for (int ch = 0; ch < n_chunks; ++ch) {
         if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
@@ -487,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               continue;
             }
             if (args.mode == kModeAccumulators) {
-              if (mvalid) store_i32_slice(args, m, n0 + jj * 32, sacc);
+              if (mvalid) store_i32_slice(args, mo, n0 + jj * 32, sacc);
               continue;
             }
 #pragma unroll
@@ -497,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
           }
-          if (mvalid) epilogue_slice<IS_INT8>(args, m, n0 + jj * 32, vals);
+          if (mvalid) epilogue_slice<IS_INT8>(args, mo, n0 + jj * 32, vals);
         }
         if (!last) tmem_wait_st();
         tc_fence_before();
@@ -736,11 +748,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const int n_tile = tile - m_tile * args.num_n_tiles;
       const long long m = static_cast<long long>(m_tile) * kBM + row;
       const bool mvalid = m < args.M;
+      const long long mo = out_pixel(args, m);   // the output pixel row m writes
       const int c0 = n_tile * BN + cbase;
       // the side input this thread reads after the tile's last chunk: into
       // L2 now, so the final epilogue does not wait on DRAM
       if (args.use_side && mvalid && c0 < args.K)
-        prefetch_l2(static_cast<const uint8_t *>(args.side) + (m * args.K + c0) * (IS_INT8 ? 1 : 2),
+        prefetch_l2(static_cast<const uint8_t *>(args.side) + (mo * args.K + c0) * (IS_INT8 ? 1 : 2),
                     min(C::kHalfCols, args.K - c0) * (IS_INT8 ? 1 : 2));
       // the side words of the whole row segment, loaded before the wait for
       // the accumulator the outputs come from, so their latency overlaps it
@@ -751,7 +764,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (ch == n_chunks - 1 && preload) {
 #pragma unroll
           for (int jj = 0; jj < C::kSlices; ++jj)
-            load_side_words<IS_INT8>(args, m, c0 + jj * 32,
+            load_side_words<IS_INT8>(args, mo, c0 + jj * 32,
                                      side_pre + jj * SideWords<IS_INT8>::kWords);
         }
         if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
@@ -772,7 +785,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
             if (mvalid)
-              epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals,
+              epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals,
                                       preload ? side_pre + jj * SideWords<IS_INT8>::kWords
                                               : nullptr);
           }
@@ -803,12 +816,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 uint32_t u[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) u[i] = static_cast<uint32_t>(sums[jj * 32 + i]);
-                store_i32_slice(args, m, c0 + jj * 32, u);
+                store_i32_slice(args, mo, c0 + jj * 32, u);
               } else {
                 float vals[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(sums[jj * 32 + i]);
-                epilogue_slice<IS_INT8>(args, m, c0 + jj * 32, vals,
+                epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals,
                                         preload ? side_pre + jj * SideWords<IS_INT8>::kWords
                                                 : nullptr);
               }
@@ -898,12 +911,14 @@ __global__ void __launch_bounds__(kPrepThreads)
         uint16_t v = 0;
         if (rsc < RSC && k < K) {
           int src = rsc;
-          if (map.flip_R > 0) {
-            // (r, s, c) -> (R-1-r, S-1-s, c)
-            const int C = RSC / (map.flip_R * map.flip_S);
-            const int c = rsc % C, rs = rsc / C;
-            const int r = rs / map.flip_S, s2 = rs - r * map.flip_S;
-            src = ((map.flip_R - 1 - r) * map.flip_S + (map.flip_S - 1 - s2)) * C + c;
+          if (map.tap_nR > 0) {
+            // (j, l, c) of the packed filter -> (r, s, c) of the caller's
+            const int C = RSC / (map.tap_nR * map.tap_nS);
+            const int c = rsc % C, jl = rsc / C;
+            const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
+            const int r = map.tap_r0 + map.tap_rstep * (map.tap_nR - 1 - j);
+            const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
+            src = (r * map.tap_S + s2) * C + c;
           }
           const long long idx = static_cast<long long>(src) * K + k;
           if (IS_INT8)

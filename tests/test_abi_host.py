@@ -258,12 +258,29 @@ def test_transposed_plan_geometry_and_limits():
             assert _err(fc.fconv_plan_create_transposed, *args) == status
 
 
-def test_transposed_workspace_holds_the_upsampled_copy():
-    # stride 2, bf16: x with zero rows/columns inserted, (7-1)*2+1 x (9-1)*2+1
+def test_transposed_workspace_layouts():
+    # stride 2, 3x3, bf16: four phases (taps 2x2, 2x1, 1x2, 1x1 of 16 channels,
+    # each packed as [32][64]); bf16 reads x as it is
     h = fc.fconv_plan_create_transposed(2, 7, 9, 16, 32, 3, 3, 2, 2, 1, 1, 1, 1, 1, 1)
     try:
         assert fc.fconv_plan_output_shape(h) == (2, 13, 17, 32)
+        assert fc.fconv_plan_padding(h) == (1, 1, 1, 1)
+        assert fc.fconv_workspace_size(h) == 4 * 32 * 64 * 2
+    finally:
+        fc.fconv_plan_destroy(h)
+    # 1x1 filter, stride 2: no phase has more than one tap and some outputs
+    # none, so x is copied with zero rows/columns inserted (13 x 17)
+    h = fc.fconv_plan_create_transposed(2, 7, 9, 16, 32, 1, 1, 2, 2, 0, 0, 0, 0, 1, 1)
+    try:
+        assert fc.fconv_plan_output_shape(h) == (2, 13, 17, 32)
         xh = 2 * 13 * 17 * 16 * 2
-        assert fc.fconv_workspace_size(h) == 32 * 192 * 2 + (xh + 255) // 256 * 256
+        assert fc.fconv_workspace_size(h) == 32 * 64 * 2 + (xh + 255) // 256 * 256
+    finally:
+        fc.fconv_plan_destroy(h)
+    # int8, stride 2, 4x4: four phases of 2x2 taps, then one fp16 copy of x
+    h = fc.fconv_plan_create_transposed(2, 7, 9, 64, 32, 4, 4, 2, 2, 1, 1, 1, 1, 0, 1)
+    try:
+        xh = 2 * 7 * 9 * 64 * 2
+        assert fc.fconv_workspace_size(h) == 4 * 32 * 256 * 2 + (xh + 255) // 256 * 256
     finally:
         fc.fconv_plan_destroy(h)

@@ -86,6 +86,9 @@ STRIDED = [
     (1, 5, 6, 48, 32, 5, 3, (3, 2), (2, -2, 0, -1), "int8", False, True),   # cp.async, pb < 0
     (2, 6, 6, 128, 64, 2, 2, (2, 2), (0, 0, 0, 0), "bf16", True, True),     # 2x2/2: no overlap
     (2, 4, 5, 32, 24, 3, 3, (2, 3), (1, 1, 2, 0), "bf16", False, False),
+    (2, 6, 7, 64, 32, 3, 3, (2, 2), (2, 2, 2, 2), "int8", True, True),     # phases starting inside
+    (2, 5, 5, 32, 32, 2, 2, (3, 3), (0, 0, 0, 0), "int8", True, False),    # stride > filter: zeros inserted
+    (2, 5, 6, 16, 16, 1, 1, (2, 2), (0, -1, 0, 0), "bf16", True, True),    # 1x1 upsampling
 ]
 
 
