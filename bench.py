@@ -409,7 +409,7 @@ def run_fconv(args, rank, world, local_rank):
                      "conv": statistics.mean(conv_ms)},
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * 2,
+        "gpu_launches": args.steps * fc.fconv_plan_launch_count(plan.handle),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -275,6 +275,12 @@ fconv_status fconv_run_no_alloc(fconv_plan *plan, const void *x, const void *w,
                                 float conv_scale, float side_scale, void *y,
                                 fconv_stream_t stream);
 
+/* Number of kernel launches one fconv_run (or fconv_run_channel_scale,
+ * fconv_run_accumulators) on this plan enqueues: the operand preparation and
+ * the convolution, per phase for a strided transposed plan, plus a small
+ * widening launch for int8 inputs whose size is not a multiple of 64. */
+fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches);
+
 /* Which convolution kernel the plan's next run uses: "tma-im2col" (A
  * gathered by TMA im2col loads) or "cp-async" (the general gather).  Static
  * text; "" for a NULL plan. */

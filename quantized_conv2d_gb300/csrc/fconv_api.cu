@@ -1010,6 +1010,28 @@ fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]
   return FCONV_OK;
 }
 
+fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches) {
+  if (!plan || !launches) return fail(FCONV_ERR_INVALID_VALUE, "plan and launches must not be NULL");
+  // per forward plan: the prep launch, a tail widening launch when a dense
+  // int8 input is not a multiple of 64 elements, and the convolution
+  auto one = [](const fconv_plan &p) {
+    const long long n = static_cast<long long>(p.N) * p.H * p.W * p.C;
+    const bool tail = p.dtype == FCONV_INT8 && !p.subsample && !p.upsample && n % 64 != 0;
+    return 2 + (tail ? 1 : 0);
+  };
+  int total = 0;
+  if (plan->num_phases > 0) {
+    for (int i = 0; i < plan->num_phases; ++i) {
+      const fconv_plan &q = *plan->phase[i];
+      total += i == 0 ? one(q) : 2;
+    }
+  } else {
+    total = one(*plan);
+  }
+  *launches = total;
+  return FCONV_OK;
+}
+
 const char *fconv_plan_kernel(const fconv_plan *plan) {
   if (!plan) return "";
   if (plan->num_phases > 0) plan = plan->phase[0];

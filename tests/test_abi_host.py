@@ -284,3 +284,23 @@ def test_transposed_workspace_layouts():
         assert fc.fconv_workspace_size(h) == 4 * 32 * 256 * 2 + (xh + 255) // 256 * 256
     finally:
         fc.fconv_plan_destroy(h)
+
+
+def test_launch_counts():
+    cases = [
+        ((256, 28, 28, 512, 512, 3, 3, 1, 1, 0, 0, 1), 2),     # prep + conv
+        ((1, 3, 3, 16, 16, 3, 3, 1, 1, 0, 0, 1), 3),           # 144 int8 inputs: a tail launch
+        ((1, 3, 3, 16, 16, 3, 3, 1, 1, 0, 1, 1), 2),           # bf16 reads x as it is
+    ]
+    for args, n in cases:
+        h = fc.fconv_plan_create(*args)
+        try:
+            assert fc.fconv_plan_launch_count(h) == n
+        finally:
+            fc.fconv_plan_destroy(h)
+    # stride 2, 4x4 transposed: four phases, each prep + conv
+    h = fc.fconv_plan_create_transposed(2, 8, 8, 64, 32, 4, 4, 2, 2, 1, 1, 1, 1, 0, 1)
+    try:
+        assert fc.fconv_plan_launch_count(h) == 8
+    finally:
+        fc.fconv_plan_destroy(h)
