@@ -142,11 +142,12 @@ __device__ __forceinline__ void load_side_words(const ConvArgs &a, long long m, 
 }
 
 // side_pre: the slice's side words loaded ahead (load_side_words), or
-// nullptr to load them here.
-template <bool IS_INT8>
-__device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
-                                               const float (&vals)[32],
-                                               const uint4 *side_pre = nullptr) {
+// nullptr to load them here.  GENERAL_ACT: the slope-then-clamp activation;
+// otherwise (no activation or Relu) only the lower bound a.lo (-inf or 0).
+template <bool IS_INT8, bool GENERAL_ACT>
+__device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m, int col0,
+                                                 const float (&vals)[32],
+                                                 const uint4 *side_pre) {
   const int K = a.K;
   if (a.mode == kModeAccumulators) {
     // raw sums: int32 for int8 plans, fp32 for bf16 plans; 4 columns per store
@@ -202,7 +203,8 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
             const float sd = static_cast<float>(static_cast<int8_t>((sw[g] >> (8 * e)) & 0xFFu));
             v = __fmaf_rn(sd, ss, v);
           }
-          v = activation(__fadd_rn(v, bv[e]), a);
+          v = __fadd_rn(v, bv[e]);
+          v = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
           int r = __float2int_rn(v);  // round half to even, saturating
           r = min(max(r, -128), 127);
           word |= (static_cast<uint32_t>(r) & 0xFFu) << (8 * e);
@@ -241,7 +243,8 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
         for (int t = 0; t < 2; ++t) {
           float v = __fmul_rn(vals[8 * qd + 2 * g + t], sv8[2 * g + t]);
           if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
-          v = activation(__fadd_rn(v, bv[2 * g + t]), a);
+          v = __fadd_rn(v, bv[2 * g + t]);
+          v = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
           word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << (16 * t);
         }
         out[g] = word;
@@ -250,6 +253,16 @@ __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, i
              make_uint4(out[0], out[1], out[2], out[3]));
     }
   }
+}
+
+template <bool IS_INT8>
+__device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
+                                               const float (&vals)[32],
+                                               const uint4 *side_pre = nullptr) {
+  if (a.act > kActRelu)
+    epilogue_slice_t<IS_INT8, true>(a, m, col0, vals, side_pre);
+  else
+    epilogue_slice_t<IS_INT8, false>(a, m, col0, vals, side_pre);
 }
 
 // General path: cp.async gather of A by 4 loader warps, 4 epilogue warps.
