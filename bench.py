@@ -289,8 +289,8 @@ def run_fconv(args, rank, world, local_rank):
         cs = torch.linspace(0.5 * wl.conv_scale, 1.5 * wl.conv_scale, wl.K,
                             dtype=torch.float32, device=dev)
 
-    def step():
-        plan.run(x, w, bias, side, cs, wl.side_scale, y=y, stream=stream)
+    def step(st=None):
+        plan.run(x, w, bias, side, cs, wl.side_scale, y=y, stream=stream if st is None else st)
 
     for _ in range(args.warmup):
         step()
@@ -336,6 +336,45 @@ def run_fconv(args, rank, world, local_rank):
     total_ms = reduce_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = weak_scaling_tops(world, args.steps, nominal, total_ms)
+
+    # ------------------------------------------------ the same steps from a CUDA graph
+    # (GPU time without the host's launch gaps, which small workloads feel;
+    # L2 flushed by a memset node before each step when the tensors fit in it)
+    graph = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            if flush is not None:
+                flush.zero_()
+            step(torch.cuda.current_stream(dev))   # the capture stream
+        g.replay()
+        torch.cuda.synchronize(dev)
+        flush_ms = 0.0
+        if flush is not None:
+            gf = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gf):
+                flush.zero_()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(args.steps):
+                gf.replay()
+            f1.record(stream)
+            torch.cuda.synchronize(dev)
+            flush_ms = f0.elapsed_time(f1)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        plan.check()
+        graph_ms = reduce_max(max(g0.elapsed_time(g1) - flush_ms, 1e-6), dev)
+        graph = {"value": weak_scaling_tops(world, args.steps, nominal, graph_ms), "unit": UNIT,
+                 "ms_per_step": graph_ms / args.steps,
+                 "how": "one step captured in a CUDA graph, replayed steps times"
+                        + (" after an L2-flush node, flush time subtracted" if flush is not None
+                           else "")}
 
     # ------------------------------------------------ end to end, host buffers
     e2e = None
@@ -409,6 +448,7 @@ def run_fconv(args, rank, world, local_rank):
                      "conv": statistics.mean(conv_ms)},
         "roofline": roofline,
         "e2e": e2e,
+        "graph": graph,
         "gpu_launches": args.steps * fc.fconv_plan_launch_count(plan.handle),
         "clocks": clk,
     }
@@ -434,6 +474,8 @@ def main():
                     help="epilogue variant: per-channel conv scale or another activation")
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the steps replayed from a CUDA graph (GPU time alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

@@ -131,3 +131,31 @@ def test_transposed_host_buffers():
     p.check()
     c.check_output(y, c.oracle_out())
     p.close()
+
+
+def test_phased_plan_replays_from_a_cuda_graph():
+    """A strided transposed plan is several launches (a prep and a conv per
+    phase); captured once, it replays on new contents of the same buffers."""
+    first = TCase(760, 2, 8, 8, 64, 64, 4, 4, (1, 1, 1, 1), "int8", True, True, stride=(2, 2))
+    second = TCase(761, 2, 8, 8, 64, 64, 4, 4, (1, 1, 1, 1), "int8", True, True, stride=(2, 2))
+    p = first.plan()
+    assert fc.fconv_plan_launch_count(p.handle) == 8
+    x, w = to_dev(first.x, "int8"), to_dev(first.w, "int8")
+    bias, side = torch.from_numpy(first.bias).cuda(), to_dev(first.side, "int8")
+    y = p.new_output()
+    p.run(x, w, bias, side, first.conv_scale, first.side_scale, y=y)   # outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        p.run(x, w, bias, side, first.conv_scale, first.side_scale, y=y)
+    for c in (second, first):
+        x.copy_(to_dev(c.x, "int8"))
+        w.copy_(to_dev(c.w, "int8"))
+        bias.copy_(torch.from_numpy(c.bias).cuda())
+        side.copy_(to_dev(c.side, "int8"))
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        p.check()
+        c.check_output(to_host(y), c.oracle_out())
+    p.close()
