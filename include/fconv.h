@@ -225,6 +225,13 @@ fconv_status fconv_plan_check(fconv_plan *plan, fconv_stream_t stream);
  * k-values) accept at most 128.  For benchmarking and tests. */
 fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n);
 
+/* Override the tile with `pixels` output pixels (128 or 256) x `channels`
+ * output channels.  256-pixel tiles (two 128-pixel halves sharing each
+ * filter tile) exist on the TMA im2col gather for 64 or 128 channels; other
+ * shapes give FCONV_ERR_NOT_SUPPORTED.  fconv_plan_set_tile(plan, 0)
+ * restores the automatic choice.  Host only. */
+fconv_status fconv_plan_set_tile_shape(fconv_plan *plan, int pixels, int channels);
+
 /* The plan's kernel configuration: output-channel tile, k-blocks summed in
  * one fp32 accumulator before they are folded into int32 (int8 plans), and
  * the number of output tiles. */

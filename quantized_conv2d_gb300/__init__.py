@@ -76,6 +76,7 @@ def _load():
         "fconv_plan_set_stage_events": [p, ctypes.POINTER(ctypes.c_void_p)],
         "fconv_run_no_alloc": [p, p, p, p, p, f32, f32, p, p],
         "fconv_plan_set_host_chunks": [p, i32],
+        "fconv_plan_set_tile_shape": [p, i32, i32],
         "fconv_plan_launch_count": [p, pi],
         "fconv_plan_set_activation_params": [p, f32, f32],
     }
@@ -194,6 +195,10 @@ def fconv_run_host(plan, x_host, w_host, bias_host, side_host, conv_scale, side_
 
 def fconv_plan_set_host_chunks(plan, chunks: int) -> None:
     _check(_load().fconv_plan_set_host_chunks(plan, chunks), "fconv_plan_set_host_chunks")
+
+
+def fconv_plan_set_tile_shape(plan, pixels: int, channels: int) -> None:
+    _check(_load().fconv_plan_set_tile_shape(plan, pixels, channels), "fconv_plan_set_tile_shape")
 
 
 def fconv_plan_launch_count(plan) -> int:

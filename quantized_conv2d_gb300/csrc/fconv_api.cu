@@ -26,7 +26,8 @@ struct fconv_plan {
   long long M;
   int Ktot, num_kb, Kpad;
   int block_n, kb_chunk, num_n_tiles, num_tiles;
-  int auto_block_n;
+  int m_sub;            // 128-pixel sub-tiles per output tile (1 or 2)
+  int auto_block_n, auto_m_sub;
   uint32_t timeout_ms;
   int debug;
   size_t wt_bytes, xh_bytes;
@@ -161,39 +162,48 @@ fconv::Gather gather_for_run(const fconv_plan &p) {
   return gather_for(p, p.block_n, (p.debug & FCONV_DEBUG_GATHER_CPASYNC) != 0);
 }
 
-// Output-channel tile: the candidate with the least estimated time.  A
-// k-block costs about max(2*BN, G) cycles: the 128 x BN x 64 MMA takes ~2*BN
-// on the tensor core, and the issuing threads' per-k-block work (barrier
-// waits, copy and MMA issue) a fixed G whatever BN is (~360 on the TMA path,
-// ~800 on the cp.async path, measured).  Tiles run in waves over the SMs;
-// the epilogue of a CTA's last tile (~8 cycles per output column) is not
-// hidden behind a next tile's mainloop.
-int choose_block_n(const fconv_plan &p, int sms) {
-  const long long m_tiles = (p.M + 127) / 128;
+// Tile: the candidate (BN output channels x 128*MS output pixels) with the
+// least estimated time.  A k-block costs about max(2*BN*MS, G) cycles: the
+// MMAs of a 128 x BN x 64 block take ~2*BN on the tensor core, and the
+// issuing threads' per-k-block work (barrier waits, copy and MMA issue) a
+// fixed G whatever BN is (~360 on the TMA path with one 128-pixel sub-tile,
+// ~450 with two, ~800 on the cp.async path; measured).  Tiles run in waves
+// over the SMs; the epilogue of a CTA's last tile (~8 cycles per output
+// column per 128 pixels) is not hidden behind a next tile's mainloop.
+struct TileChoice {
+  int bn, ms;
+};
+TileChoice choose_tile(const fconv_plan &p, int sms) {
   const bool chunked = p.kb_chunk < p.num_kb;
   const int kp = (p.K + 31) / 32 * 32;
-  int best = 32;
+  TileChoice best = {32, 1};
   long long best_cost = -1;
   for (int bn : {256, 128, 64, 32}) {
-    if (bn > kp) continue;
-    const fconv::Gather g = gather_for(p, bn, false);
-    if (!fconv::gather_supports(g, bn, chunked)) continue;
-    const long long fixed = g == fconv::Gather::kTmaIm2col ? 360 : 800;
-    const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
-    const long long waves = (tiles + sms - 1) / sms;
-    const long long cost = waves * p.num_kb * (2 * bn > fixed ? 2 * bn : fixed) + 8LL * bn;
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = bn;
+    for (int ms : {1, 2}) {
+      if (bn > kp) continue;
+      fconv::Gather g = gather_for(p, bn, false);
+      if (!fconv::gather_supports(g, bn, chunked, ms)) continue;
+      const long long fixed =
+          g == fconv::Gather::kTmaIm2col ? (ms == 2 ? 450 : 360) : 800;
+      const long long m_tiles = (p.M + 128LL * ms - 1) / (128LL * ms);
+      const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
+      const long long waves = (tiles + sms - 1) / sms;
+      const long long work = 2LL * bn * ms;
+      const long long cost = waves * p.num_kb * (work > fixed ? work : fixed) + 8LL * bn * ms;
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best = {bn, ms};
+      }
     }
   }
   return best;
 }
 
-void set_tiling(fconv_plan &p, int bn) {
+void set_tiling(fconv_plan &p, int bn, int ms = 1) {
   p.block_n = bn;
+  p.m_sub = ms;
   p.num_n_tiles = (p.K + bn - 1) / bn;
-  p.num_tiles = static_cast<int>((p.M + 127) / 128) * p.num_n_tiles;
+  p.num_tiles = static_cast<int>((p.M + 128LL * ms - 1) / (128LL * ms)) * p.num_n_tiles;
 }
 
 PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col_fn() {
@@ -322,7 +332,10 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   }
 
   const fconv::Gather gather = gather_for_run(*p);
-  if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb))
+  // two 128-pixel sub-tiles exist on the TMA gather only: a plan forced onto
+  // the cp.async gather (a test hook) runs one
+  if (gather == fconv::Gather::kCpAsync && p->m_sub != 1) set_tiling(*p, p->block_n, 1);
+  if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb, p->m_sub))
     return fail(FCONV_ERR_NOT_SUPPORTED,
                 "tile %d has no cp.async kernel for a sum of %d k-values (chunked sums need "
                 "BN <= 128 there)", p->block_n, p->Ktot);
@@ -444,7 +457,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.debug = p->debug;
   a.timeout_ns = static_cast<unsigned long long>(p->timeout_ms) * 1000000ull;
   const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-  e = fconv::launch_conv(p->block_n, is_int8, gather, tmap_a, tmap, a, grid, stream);
+  e = fconv::launch_conv(p->block_n, p->m_sub, is_int8, gather, tmap_a, tmap, a, grid, stream);
   if (e != cudaSuccess)
     return fail(FCONV_ERR_CUDA, "convolution launch: %s (%s)", cudaGetErrorString(e),
                 fconv::last_launch_note());
@@ -462,7 +475,7 @@ fconv_plan batch_slice(const fconv_plan &p, int n) {
   fconv_plan q = p;
   q.N = n;
   q.M = static_cast<long long>(n) * p.P * p.Q;
-  q.num_tiles = static_cast<int>((q.M + 127) / 128) * p.num_n_tiles;
+  q.num_tiles = static_cast<int>((q.M + 128LL * p.m_sub - 1) / (128LL * p.m_sub)) * p.num_n_tiles;
   q.use_events = false;
   return q;
 }
@@ -588,8 +601,10 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   p.subsample =
       (!p.transposed && dtype == FCONV_INT8 && R == 1 && S == 1 && (stride_h > 1 || stride_w > 1))
           ? 1 : 0;
-  p.auto_block_n = choose_block_n(p, sm_count_of_current_device(148));
-  set_tiling(p, p.auto_block_n);
+  const TileChoice tile = choose_tile(p, sm_count_of_current_device(148));
+  p.auto_block_n = tile.bn;
+  p.auto_m_sub = tile.ms;
+  set_tiling(p, tile.bn, tile.ms);
   p.timeout_ms = 2000;
   p.host_chunks = 0;
   p.pipe_dev = -1;
@@ -961,7 +976,7 @@ fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
     return FCONV_OK;
   }
   if (block_n == 0) {
-    set_tiling(*plan, plan->auto_block_n);
+    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub);
     return FCONV_OK;
   }
   if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256)
@@ -971,6 +986,29 @@ fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
     return fail(FCONV_ERR_NOT_SUPPORTED,
                 "tile %d leaves no tensor memory for the int32 sums this plan needs", block_n);
   set_tiling(*plan, block_n);
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_tile_shape(fconv_plan *plan, int pixels, int channels) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (pixels != 128 && pixels != 256)
+    return fail(FCONV_ERR_NOT_SUPPORTED, "tiles of %d output pixels: 128 or 256", pixels);
+  if (plan->num_phases > 0) {
+    for (int i = 0; i < plan->num_phases; ++i) {
+      const fconv_status st = fconv_plan_set_tile_shape(plan->phase[i], pixels, channels);
+      if (st != FCONV_OK) return st;
+    }
+    plan->block_n = plan->phase[0]->block_n;
+    plan->num_tiles = 0;
+    for (int i = 0; i < plan->num_phases; ++i) plan->num_tiles += plan->phase[i]->num_tiles;
+    return FCONV_OK;
+  }
+  const int ms = pixels / 128;
+  if (!fconv::gather_supports(gather_for(*plan, channels, false), channels,
+                              plan->kb_chunk < plan->num_kb, ms))
+    return fail(FCONV_ERR_NOT_SUPPORTED, "no kernel for %d x %d tiles on this plan", pixels,
+                channels);
+  set_tiling(*plan, channels, ms);
   return FCONV_OK;
 }
 
@@ -1035,6 +1073,8 @@ fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches) {
 const char *fconv_plan_kernel(const fconv_plan *plan) {
   if (!plan) return "";
   if (plan->num_phases > 0) plan = plan->phase[0];
+  if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col && plan->m_sub == 2)
+    return "tma-im2col-m256";
   return gather_for_run(*plan) == fconv::Gather::kTmaIm2col ? "tma-im2col" : "cp-async";
 }
 

@@ -53,12 +53,14 @@ enum class Gather {
   kTmaIm2col = 1 // one TMA im2col load of 128 pixels x 64 channels; needs C % 64 == 0
 };
 
-cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensorMap &tmap_a,
-                        const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
-                        cudaStream_t stream);
+// m_sub: 128-pixel sub-tiles per output tile (1, or 2 on the TMA gather
+// with block_n <= 128; args.num_tiles counts tiles of 128 * m_sub pixels).
+cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
+                        const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
+                        const ConvArgs &args, int grid, cudaStream_t stream);
 // Whether a gather mode has a kernel for this output-channel tile; chunked
 // int8 sums on the cp.async path need a third TMEM region (BN <= 128).
-bool gather_supports(Gather gather, int block_n, bool chunked);
+bool gather_supports(Gather gather, int block_n, bool chunked, int m_sub = 1);
 // Which input elements the prep launch copies (int8 widened to fp16, bf16
 // as it is) into the [N][P][Q][C] copy the convolution reads.  Dense
 // (mode 0, int8 only): all of x, P x Q = H x W.  Subsampled (1): for a 1x1

@@ -563,35 +563,47 @@ constexpr int kTmaEpiRegs = 224;
 static_assert(128 * kTmaCtlRegs + 256 * kTmaEpiRegs <= kTmaThreads * 168,
               "register split exceeds the launch allocation");
 
-template <int BN>
+// MS: M sub-tiles of 128 output pixels per tile.  MS = 2 gives a tile of
+// 256 pixels x BN channels whose two halves share each B stage (one wait,
+// one commit and one B copy per k-block for twice the MMA work), for tiles
+// narrower than 256 channels, where the issuing threads' fixed per-k-block
+// work, not the tensor cores, sets the pace.
+template <int BN, int MS = 1>
 struct TmaCfg {
-  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kABytes = kBM * kBK * 2;        // one sub-tile's A
+  static constexpr int kAStage = MS * kABytes;
   static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStageBytes = kAStage + kBBytes;
   static constexpr int kStages0 = (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kTmemCols = 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  static constexpr int kAccCols = MS * BN;             // one accumulator buffer
+  static constexpr int kTmemCols = 2 * kAccCols <= 128 ? 128 : 2 * kAccCols <= 256 ? 256 : 512;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
-  static constexpr int kHalfCols = BN / 2;   // columns per epilogue thread
+  // columns per epilogue thread: MS = 1 splits a row's BN columns between
+  // two warps; MS = 2 gives each warp half one sub-tile's whole rows
+  static constexpr int kHalfCols = MS == 1 ? BN / 2 : BN;
   static constexpr int kSlices = kHalfCols / 32;
   static_assert(BN == 64 || BN == 128 || BN == 256, "TMA path tile");
+  static_assert(MS == 1 || (MS == 2 && BN <= 128), "two sub-tiles need BN <= 128");
+  static_assert(2 * kAccCols <= 512, "tensor memory");
   static_assert(kStages >= 3, "pipeline too shallow");
 };
 
-template <int BN, bool IS_INT8>
+template <int BN, bool IS_INT8, int MS>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     conv_fprop_tma_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
-  using C = TmaCfg<BN>;
+  using C = TmaCfg<BN, MS>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8);
+  constexpr int kTileM = kBM * MS;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *sA = smem;
-  uint8_t *sB = smem + kStages * C::kABytes;
+  uint8_t *sA = smem;   // per stage: MS sub-tiles of A, 16 KB each
+  uint8_t *sB = smem + kStages * C::kAStage;
   Smem *bars = reinterpret_cast<Smem *>(smem + C::kBarOffset);
   volatile int *abort_flag = &bars->abort_flag;
 
@@ -642,12 +654,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
       const int m_tile = tile / args.num_n_tiles;
       const int n_tile = tile - m_tile * args.num_n_tiles;
-      const long long m0 = static_cast<long long>(m_tile) * kBM;
-      const int n0 = static_cast<int>(m0 / PQ);
-      const int rem = static_cast<int>(m0 - static_cast<long long>(n0) * PQ);
-      const int p0 = rem / args.Q, q0 = rem - (rem / args.Q) * args.Q;
-      // filter-window origin of the tile's first output pixel
-      const int w0 = q0 * args.sw - args.pl, h0 = p0 * args.sh - args.pt;
+      // filter-window origin of each sub-tile's first output pixel (a
+      // sub-tile past the last pixel reads images beyond N: zero-filled)
+      int w0[MS], h0[MS], n0[MS];
+#pragma unroll
+      for (int u = 0; u < MS; ++u) {
+        const long long m0 = static_cast<long long>(m_tile) * kTileM + u * kBM;
+        n0[u] = static_cast<int>(m0 / PQ);
+        const int rem = static_cast<int>(m0 - static_cast<long long>(n0[u]) * PQ);
+        const int p0 = rem / args.Q, q0 = rem - (rem / args.Q) * args.Q;
+        w0[u] = q0 * args.sw - args.pl;
+        h0[u] = p0 * args.sh - args.pt;
+      }
       int r = 0, s = 0, cb = 0;   // filter tap and channel block of k-block kb
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
@@ -657,9 +675,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (!drop) {
           if (lane == 0) {
             const uint32_t fb = smem_u32(&bars->full_b[stage]);
-            mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
-            tma_load_im2col_4d(smem_u32(sA + stage * C::kABytes), &tmap_a, cb * kBK, w0, h0, n0,
-                               static_cast<uint16_t>(s), static_cast<uint16_t>(r), fb);
+            mbar_arrive_expect_tx(fb, C::kAStage + C::kBBytes);
+#pragma unroll
+            for (int u = 0; u < MS; ++u)
+              tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage + u * C::kABytes), &tmap_a,
+                                 cb * kBK, w0[u], h0[u], n0[u], static_cast<uint16_t>(s),
+                                 static_cast<uint16_t>(r), fb);
             tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb * kBK, n_tile * BN, fb);
           }
           __syncwarp();
@@ -696,7 +717,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + astage * BN;
+        const uint32_t d = tmem_base + astage * C::kAccCols;   // sub-tile u at d + u * BN
         for (int kb = kb0; kb < kb1; kb += 2) {
           const bool pair = kb + 1 < kb1;
           const uint32_t stage1 = stage + 1 == kStages ? 0 : stage + 1;
@@ -707,19 +728,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
+          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kAStage));
           const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
-          const uint64_t adesc1 = sw128_kmajor_desc(smem_u32(sA + stage1 * C::kABytes));
+          const uint64_t adesc1 = sw128_kmajor_desc(smem_u32(sA + stage1 * C::kAStage));
           const uint64_t bdesc1 = sw128_kmajor_desc(smem_u32(sB + stage1 * C::kBBytes));
+          // a sub-tile's A is 16 KB further: + (16384 >> 4) in the descriptor
+          constexpr uint64_t kSubStep = static_cast<uint64_t>(C::kABytes >> 4);
           if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              umma_f16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int u = 0; u < MS; ++u)
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                umma_f16(d + u * BN, adesc + u * kSubStep + 2 * k, bdesc + 2 * k, kIdesc,
+                         (kb > kb0 || k > 0) ? 1u : 0u);
             umma_commit(smem_u32(&bars->empty[stage]));
             if (pair) {
 #pragma unroll
-              for (int k = 0; k < kBK / 16; ++k)
-                umma_f16(d, adesc1 + 2 * k, bdesc1 + 2 * k, kIdesc, 1u);
+              for (int u = 0; u < MS; ++u)
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                  umma_f16(d + u * BN, adesc1 + u * kSubStep + 2 * k, bdesc1 + 2 * k, kIdesc, 1u);
               umma_commit(smem_u32(&bars->empty[stage1]));
             }
           }
@@ -749,17 +777,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     setmaxnreg_inc<kTmaEpiRegs>();
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
-    const int half = (warp - kTmaEpiWarp0) >> 2;  // which half of the BN columns
-    const int row = quarter * 32 + lane;
+    const int half = (warp - kTmaEpiWarp0) >> 2;  // MS = 1: which half of the BN columns;
+                                                  // MS = 2: which sub-tile
+    const int row = (MS == 2 ? half * kBM : 0) + quarter * 32 + lane;   // in the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int cbase = half * C::kHalfCols;
+    const int cbase = MS == 2 ? 0 : half * C::kHalfCols;        // first column, in the tile
+    const int tcol = (MS == 2 ? half * BN : 0) + cbase;          // its TMEM column offset
     int32_t sums[IS_INT8 ? C::kHalfCols : 1];  // int32 running sums across chunks
     uint32_t astage = 0, aphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
       const int m_tile = tile / args.num_n_tiles;
       const int n_tile = tile - m_tile * args.num_n_tiles;
-      const long long m = static_cast<long long>(m_tile) * kBM + row;
+      const long long m = static_cast<long long>(m_tile) * kTileM + row;
       const bool mvalid = m < args.M;
       const long long mo = out_pixel(args, m);   // the output pixel row m writes
       const int c0 = n_tile * BN + cbase;
@@ -785,7 +815,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t t_acc = tmem_base + lane_off + astage * BN + cbase;
+        const uint32_t t_acc = tmem_base + lane_off + astage * C::kAccCols + tcol;
         if (n_chunks == 1) {
           // the whole sum is in TMEM: epilogue straight from it
 #pragma unroll 1
@@ -1064,42 +1094,55 @@ static void note_attributes(Kern kern, int threads, int smem) {
 
 const char *last_launch_note() { return t_kernel_note; }
 
-template <int BN, bool IS_INT8>
+template <int BN, bool IS_INT8, int MS>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                                 const ConvArgs &args, int grid, cudaStream_t stream) {
-  auto kern = conv_fprop_tma_kernel<BN, IS_INT8>;
+  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS>;
+  using Cfg = TmaCfg<BN, MS>;
   static std::atomic<unsigned long long> configured{0};
-  cudaError_t e = ensure_smem_limit(kern, TmaCfg<BN>::kSmemBytes, configured);
+  cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
   if (e == cudaSuccess) {
-    kern<<<grid, kTmaThreads, TmaCfg<BN>::kSmemBytes, stream>>>(tmap_a, tmap_b, args);
+    kern<<<grid, kTmaThreads, Cfg::kSmemBytes, stream>>>(tmap_a, tmap_b, args);
     e = cudaGetLastError();
   }
-  if (e != cudaSuccess) note_attributes(kern, kTmaThreads, TmaCfg<BN>::kSmemBytes);
+  if (e != cudaSuccess) note_attributes(kern, kTmaThreads, Cfg::kSmemBytes);
   return e;
 }
 
-bool gather_supports(Gather gather, int block_n, bool chunked) {
-  if (gather == Gather::kTmaIm2col) return block_n == 64 || block_n == 128 || block_n == 256;
+bool gather_supports(Gather gather, int block_n, bool chunked, int m_sub) {
+  if (m_sub != 1 && m_sub != 2) return false;
+  if (gather == Gather::kTmaIm2col)
+    return m_sub == 1 ? (block_n == 64 || block_n == 128 || block_n == 256)
+                      : (block_n == 64 || block_n == 128);
+  if (m_sub != 1) return false;
   if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256) return false;
   return !chunked || 3 * block_n <= 512;
 }
 
-cudaError_t launch_conv(int block_n, bool is_int8, Gather gather, const CUtensorMap &tmap_a,
-                        const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
-                        cudaStream_t stream) {
+cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
+                        const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
+                        const ConvArgs &args, int grid, cudaStream_t stream) {
   const bool chunked = args.kb_chunk < args.num_kb;
   if (chunked && !is_int8) return cudaErrorInvalidValue;
-  if (!gather_supports(gather, block_n, chunked)) return cudaErrorInvalidValue;
+  if (!gather_supports(gather, block_n, chunked, m_sub)) return cudaErrorInvalidValue;
   if (args.kb_chunk <= 0 || grid <= 0) return cudaErrorInvalidValue;
+  if (gather == Gather::kTmaIm2col && m_sub == 2) {
+    if (args.C % kBK != 0) return cudaErrorInvalidValue;
+    if (block_n == 64)
+      return is_int8 ? launch_tma_t<64, true, 2>(tmap_a, tmap_b, args, grid, stream)
+                     : launch_tma_t<64, false, 2>(tmap_a, tmap_b, args, grid, stream);
+    return is_int8 ? launch_tma_t<128, true, 2>(tmap_a, tmap_b, args, grid, stream)
+                   : launch_tma_t<128, false, 2>(tmap_a, tmap_b, args, grid, stream);
+  }
   if (gather == Gather::kTmaIm2col) {
     if (args.C % kBK != 0) return cudaErrorInvalidValue;
     switch (block_n) {
-      case 64: return is_int8 ? launch_tma_t<64, true>(tmap_a, tmap_b, args, grid, stream)
-                              : launch_tma_t<64, false>(tmap_a, tmap_b, args, grid, stream);
-      case 128: return is_int8 ? launch_tma_t<128, true>(tmap_a, tmap_b, args, grid, stream)
-                               : launch_tma_t<128, false>(tmap_a, tmap_b, args, grid, stream);
-      default: return is_int8 ? launch_tma_t<256, true>(tmap_a, tmap_b, args, grid, stream)
-                              : launch_tma_t<256, false>(tmap_a, tmap_b, args, grid, stream);
+      case 64: return is_int8 ? launch_tma_t<64, true, 1>(tmap_a, tmap_b, args, grid, stream)
+                              : launch_tma_t<64, false, 1>(tmap_a, tmap_b, args, grid, stream);
+      case 128: return is_int8 ? launch_tma_t<128, true, 1>(tmap_a, tmap_b, args, grid, stream)
+                               : launch_tma_t<128, false, 1>(tmap_a, tmap_b, args, grid, stream);
+      default: return is_int8 ? launch_tma_t<256, true, 1>(tmap_a, tmap_b, args, grid, stream)
+                              : launch_tma_t<256, false, 1>(tmap_a, tmap_b, args, grid, stream);
     }
   }
   switch (block_n) {

@@ -304,3 +304,26 @@ def test_launch_counts():
         assert fc.fconv_plan_launch_count(h) == 8
     finally:
         fc.fconv_plan_destroy(h)
+
+
+def test_256_pixel_tile_rules():
+    h = fc.fconv_plan_create(2, 9, 11, 64, 64, 3, 3, 1, 1, 0, 0, 1)
+    try:
+        fc.fconv_plan_set_tile_shape(h, 256, 64)
+        assert fc.fconv_plan_kernel(h) == "tma-im2col-m256"
+        assert fc.fconv_plan_get_config(h)[2] == 1          # 198 pixels: one tile
+        fc.fconv_plan_set_tile_shape(h, 128, 64)
+        assert fc.fconv_plan_get_config(h)[2] == 2
+        assert _err(fc.fconv_plan_set_tile_shape, h, 512, 64) == fc.FCONV_ERR_NOT_SUPPORTED
+    finally:
+        fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create(1, 8, 8, 64, 256, 3, 3, 1, 1, 0, 0, 1)
+    try:   # 2 x 256 columns of accumulators would not fit in tensor memory twice
+        assert _err(fc.fconv_plan_set_tile_shape, h, 256, 256) == fc.FCONV_ERR_NOT_SUPPORTED
+    finally:
+        fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create(1, 8, 8, 48, 64, 3, 3, 1, 1, 0, 0, 1)
+    try:   # C % 64 != 0: the cp.async gather, which has no 256-pixel tiles
+        assert _err(fc.fconv_plan_set_tile_shape, h, 256, 64) == fc.FCONV_ERR_NOT_SUPPORTED
+    finally:
+        fc.fconv_plan_destroy(h)

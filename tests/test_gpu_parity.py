@@ -430,3 +430,37 @@ def test_maximum_tensor_sizes(shape):
     ref = oracle.epilogue_i8(acc, bias, side.reshape(-1, K)[pix], cs, 0.125, False)
     bad = np.argwhere(got[pix] != ref)
     assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+# ---------------------------------------------------------------- 256-pixel tiles
+# two 128-pixel halves sharing each filter tile (TMA gather, 64 or 128
+# channels); ragged ends leave the second half partly or wholly past the
+# last pixel
+M256_CASES = [
+    ((2, 9, 11, 64, 64, 3, 3, 1, "SAME", True, True), "int8", 64),       # M = 198
+    ((1, 10, 13, 64, 128, 3, 3, 1, "SAME", True, False), "int8", 128),   # M = 130
+    ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True), "int8", 128),   # chunked sums, K tail
+    ((4, 14, 14, 128, 96, 3, 3, 2, "SAME", False, True), "int8", 64),    # stride 2, K tail
+    ((3, 8, 8, 64, 200, 3, 3, 1, "SAME", True, False), "bf16", 128),
+    ((2, 9, 11, 64, 64, 3, 3, 1, "SAME", True, True), "bf16", 64),
+]
+
+
+@pytest.mark.parametrize("i,item", list(enumerate(M256_CASES)))
+def test_256_pixel_tiles(i, item):
+    params, dtype, bn = item
+    c = sweep_case(500 + i, params, dtype)
+    acc_ref = c.oracle_acc()
+    p = c.plan()
+    fc.fconv_plan_set_tile_shape(p.handle, 256, bn)
+    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-m256"
+    x, w = to_dev(c.x, dtype), to_dev(c.w, dtype)
+    bias = torch.from_numpy(c.bias).cuda()
+    side = to_dev(c.side, dtype)
+    acc = p.accumulators(x, w)
+    y = p.run(x, w, bias, side, c.conv_scale, c.side_scale)
+    p.check()
+    c.check_acc(acc.cpu().numpy(), acc_ref)
+    c.check_output(to_host(y), c.oracle_out(acc_ref))
+    p.close()
+
