@@ -116,8 +116,9 @@ def test_strided_transposed_parity(i, params):
         c.check_output(c.run_gpu(debug=fc.FCONV_DEBUG_GATHER_CPASYNC), ref)
 
 
-def test_transposed_host_buffers():
-    c = TCase(720, 6, 8, 8, 64, 32, 3, 3, (1, 1, 1, 1), "int8", True, True)
+@pytest.mark.parametrize("stride", [(1, 1), (2, 2)])
+def test_transposed_host_buffers(stride):
+    c = TCase(720, 6, 8, 8, 64, 32, 3, 3, (1, 1, 1, 1), "int8", True, True, stride=stride)
     p = c.plan()
     fc.fconv_plan_set_host_chunks(p.handle, 3)
     nbytes = fc.fconv_host_workspace_size(p.handle, True)

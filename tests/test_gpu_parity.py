@@ -267,14 +267,16 @@ def test_run_host_buffers(chunks, dtype):
 
 
 @pytest.mark.parametrize("C,K,kernel", [(16, 16, "cp-async"), (64, 64, "tma-im2col"),
-                                         (64, 256, "tma-im2col")])
+                                         (64, 256, "tma-im2col"), (64, 128, "tma-im2col-m256")])
 def test_timeout_exit_keeps_context_usable(C, K, kernel):
     """A producer that never signals 'stage full' makes the MMA issuer's wait
     run out: the kernel must stop, report FCONV_ERR_TIMEOUT, and the next run
     must work -- for the cp.async loaders and the TMA producer (64- and
-    256-wide tiles)."""
+    256-wide tiles, and 256-pixel tiles)."""
     c = sweep_case(70, (1, 8, 8, C, K, 3, 3, 1, "SAME", False, True), "int8")
     p = c.plan(block_n=256 if K == 256 else None)
+    if kernel.endswith("m256"):
+        fc.fconv_plan_set_tile_shape(p.handle, 256, K)
     assert fc.fconv_plan_kernel(p.handle) == kernel
     fc.fconv_plan_set_timeout_ms(p.handle, 50)
     fc.fconv_plan_set_debug(p.handle, fc.FCONV_DEBUG_DROP_ARRIVE)
