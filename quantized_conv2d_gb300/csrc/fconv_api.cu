@@ -52,6 +52,12 @@ struct fconv_plan {
   // output row and column (owned by this plan)
   int num_phases;
   fconv_plan *phase[64];
+  // side streams on which the phases after the first run concurrently with
+  // it (fork after the input copy, join before the run returns)
+  int fork_dev;   // device they belong to, -1 = none
+  int num_fork;
+  cudaStream_t fork_s[3];
+  cudaEvent_t fork_start, fork_done[3];
   float act_alpha, act_beta;   // activation parameters (fconv_plan_set_activation_params)
   cudaEvent_t events[4];
   bool use_events;
@@ -267,12 +273,13 @@ size_t workspace_need(const fconv_plan &p) {
 }
 
 fconv_plan batch_slice(const fconv_plan &p, int n);
+fconv_status ensure_fork(fconv_plan *p);
 
 fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *bias,
                      const void *side, float conv_scale, float side_scale, void *y,
                      void *workspace, size_t workspace_bytes, cudaStream_t stream, int mode,
                      bool skip_pack = false, const float *scale_k = nullptr,
-                     bool skip_copy = false) {
+                     bool skip_copy = false, bool prep_only = false) {
   if (!p) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
   if (!x || !w || !y) return fail(FCONV_ERR_INVALID_VALUE, "x, w and y must not be NULL");
   if (mode == fconv::kModeFused && !bias)
@@ -302,31 +309,53 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   __half *xh = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + p->ws_xh_off);
 
   if (p->num_phases > 0) {
-    // one forward plan per phase, in order; the first one widens the input
-    // (int8) for all of them
+    // one forward plan per phase: the first one's prep (which also widens
+    // the input, int8) on the caller's stream, then the other phases on
+    // side streams concurrently with the first one's convolution
+    fconv_status st = ensure_fork(p);
+    if (st != FCONV_OK) return st;
+    fconv_plan tmp[64];
+    fconv_plan *q[64];
+    for (int i = 0; i < p->num_phases; ++i) {
+      q[i] = p->phase[i];
+      if (q[i]->N != p->N) {
+        tmp[i] = batch_slice(*q[i], p->N);
+        q[i] = &tmp[i];
+      }
+      q[i]->act = p->act;
+      q[i]->act_alpha = p->act_alpha;
+      q[i]->act_beta = p->act_beta;
+      q[i]->debug = p->debug;
+      q[i]->timeout_ms = p->timeout_ms;
+    }
     cudaError_t e0 = mark(0);
     if (e0 != cudaSuccess) return cuda_fail(e0, "event record");
-    for (int i = 0; i < p->num_phases; ++i) {
-      fconv_plan *q = p->phase[i];
-      fconv_plan tmp;
-      if (q->N != p->N) {
-        tmp = batch_slice(*q, p->N);
-        q = &tmp;
-      }
-      q->act = p->act;
-      q->act_alpha = p->act_alpha;
-      q->act_beta = p->act_beta;
-      q->debug = p->debug;
-      q->timeout_ms = p->timeout_ms;
-      fconv_status st = enqueue(q, x, w, bias, side, conv_scale, side_scale, y, workspace,
-                                workspace_bytes, stream, mode, skip_pack, scale_k,
-                                skip_copy || i > 0);
-      if (st != FCONV_OK) return st;
-      if (i == 0) {
-        if ((e0 = mark(1)) != cudaSuccess || (e0 = mark(2)) != cudaSuccess)
-          return cuda_fail(e0, "event record");
-      }
+    st = enqueue(q[0], x, w, bias, side, conv_scale, side_scale, y, workspace, workspace_bytes,
+                 stream, mode, skip_pack, scale_k, skip_copy, /*prep_only=*/true);
+    if (st != FCONV_OK) return st;
+    if ((e0 = mark(1)) != cudaSuccess || (e0 = mark(2)) != cudaSuccess)
+      return cuda_fail(e0, "event record");
+    const int nf = p->num_phases > 1 ? p->num_fork : 0;
+    if (nf > 0) {
+      if ((e0 = cudaEventRecord(p->fork_start, stream)) != cudaSuccess)
+        return cuda_fail(e0, "event record");
+      for (int j = 0; j < nf; ++j)
+        if ((e0 = cudaStreamWaitEvent(p->fork_s[j], p->fork_start, 0)) != cudaSuccess)
+          return cuda_fail(e0, "stream ordering");
     }
+    for (int i = 1; i < p->num_phases; ++i) {
+      st = enqueue(q[i], x, w, bias, side, conv_scale, side_scale, y, workspace, workspace_bytes,
+                   p->fork_s[(i - 1) % nf], mode, skip_pack, scale_k, /*skip_copy=*/true);
+      if (st != FCONV_OK) return st;
+    }
+    // the first phase's convolution (its operands are ready)
+    st = enqueue(q[0], x, w, bias, side, conv_scale, side_scale, y, workspace, workspace_bytes,
+                 stream, mode, /*skip_pack=*/true, scale_k, /*skip_copy=*/true);
+    if (st != FCONV_OK) return st;
+    for (int j = 0; j < nf; ++j)
+      if ((e0 = cudaEventRecord(p->fork_done[j], p->fork_s[j])) != cudaSuccess ||
+          (e0 = cudaStreamWaitEvent(stream, p->fork_done[j], 0)) != cudaSuccess)
+        return cuda_fail(e0, "stream ordering");
     if ((e0 = mark(3)) != cudaSuccess) return cuda_fail(e0, "event record");
     return FCONV_OK;
   }
@@ -365,6 +394,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
   }
   if (copy) act = xh;
+  if (prep_only) return FCONV_OK;
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
 
@@ -493,6 +523,42 @@ void destroy_pipeline(fconv_plan *p) {
   p->pipe_dev = -1;
 }
 
+void destroy_fork(fconv_plan *p) {
+  if (p->fork_dev < 0) return;
+  for (int i = 0; i < p->num_fork; ++i) {
+    cudaStreamDestroy(p->fork_s[i]);
+    cudaEventDestroy(p->fork_done[i]);
+  }
+  cudaEventDestroy(p->fork_start);
+  p->fork_dev = -1;
+  p->num_fork = 0;
+}
+
+// Side streams and events for the phases of a strided transposed plan, on
+// the current device.
+fconv_status ensure_fork(fconv_plan *p) {
+  if (p->num_phases <= 1) return FCONV_OK;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (p->fork_dev == dev) return FCONV_OK;
+  destroy_fork(p);
+  const int n = p->num_phases - 1 < 3 ? p->num_phases - 1 : 3;
+  const unsigned ef = cudaEventDisableTiming;
+  bool ok = cudaEventCreateWithFlags(&p->fork_start, ef) == cudaSuccess;
+  int made = 0;
+  for (; ok && made < n; ++made)
+    ok = cudaStreamCreateWithFlags(&p->fork_s[made], cudaStreamNonBlocking) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->fork_done[made], ef) == cudaSuccess;
+  if (!ok) {
+    e = cudaGetLastError();
+    return cuda_fail(e, "creating the phase streams");
+  }
+  p->num_fork = n;
+  p->fork_dev = dev;
+  return FCONV_OK;
+}
+
 // Streams and events for the host-buffer pipeline, on the current device.
 fconv_status ensure_pipeline(fconv_plan *p) {
   int dev = -1;
@@ -608,6 +674,7 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   p.timeout_ms = 2000;
   p.host_chunks = 0;
   p.pipe_dev = -1;
+  p.fork_dev = -1;
   p.wt_bytes = align_up(static_cast<size_t>(K) * p.Kpad * 2, 256);
   const InputView view = input_view(p);
   const long long xh_elems = static_cast<long long>(N) * view.H * view.W * C;
@@ -768,6 +835,7 @@ fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha, flo
 fconv_status fconv_plan_destroy(fconv_plan *plan) {
   if (plan) {
     destroy_pipeline(plan);
+    destroy_fork(plan);
     for (int i = 0; i < plan->num_phases; ++i) delete plan->phase[i];
   }
   delete plan;
@@ -890,6 +958,9 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host, const void *w_
 
   fconv_status s = ensure_pipeline(plan);
   if (s != FCONV_OK) return s;
+  // the phase streams of a strided transposed plan belong to the plan, not
+  // to the per-chunk copies below
+  if ((s = ensure_fork(plan)) != FCONV_OK) return s;
   cudaError_t e;
   // the copy streams start after everything already queued on the caller's stream
   if ((e = cudaEventRecord(plan->ev_entry, st)) != cudaSuccess ||
