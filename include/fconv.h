@@ -144,13 +144,17 @@ fconv_status fconv_plan_destroy(fconv_plan *plan);
 fconv_status fconv_plan_output_shape(const fconv_plan *plan, int *N, int *P,
                                      int *Q, int *K);
 
-/* Padding the plan applies: top, bottom, left, right. */
+/* Padding of the plan: top, bottom, left, right (for a transposed plan,
+ * the pads it was created with). */
 fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top,
                                 int *pad_bottom, int *pad_left,
                                 int *pad_right);
 
-/* Device scratch bytes fconv_run needs (the filter repacked K-major in
- * 16-bit form, and for int8 plans the input widened to fp16). */
+/* Device scratch bytes fconv_run needs: the filter repacked K-major in
+ * 16-bit form (one per phase of a strided transposed plan), and a 16-bit
+ * copy of the input for int8 plans (only the strided pixels for a 1x1
+ * strided plan) and for transposed plans with a stride above the filter
+ * (zeros inserted). */
 fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes);
 
 /* Run the fused convolution on `stream`.
@@ -187,6 +191,11 @@ fconv_status fconv_run_accumulators(fconv_plan *plan, const void *x,
                                     const void *w, void *acc, void *workspace,
                                     size_t workspace_bytes,
                                     fconv_stream_t stream);
+
+/* ---- Library-side entry points and controls.  The pages have no
+ * counterpart for these: they run the operation above on host buffers,
+ * expose and override this implementation's choices (tiles, chunking,
+ * wait limits), and give tests their hooks. */
 
 /* Bytes of device memory fconv_run_host needs: the workspace plus device
  * copies of x, w, bias, side (if with_side) and y. */
@@ -257,8 +266,10 @@ fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
  * run's stream: events[0] before the operand preparation (filter pack and,
  * for int8 plans, the int8 -> fp16 input widening, one launch), events[1]
  * after it, events[2] before the convolution kernel (the same point as
- * events[1]), events[3] after the convolution kernel.  NULL disables.  The
- * events must outlive the runs that record them. */
+ * events[1]), events[3] after the convolution kernel.  For a strided
+ * transposed plan events[1] and [2] follow the first phase's preparation
+ * and events[3] the join of all phases.  NULL disables.  The events must
+ * outlive the runs that record them. */
 fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]);
 
 /* fconv_run for callers that cannot allocate device memory: a plugin inside
@@ -289,8 +300,10 @@ fconv_status fconv_run_no_alloc(fconv_plan *plan, const void *x, const void *w,
 fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches);
 
 /* Which convolution kernel the plan's next run uses: "tma-im2col" (A
- * gathered by TMA im2col loads) or "cp-async" (the general gather).  Static
- * text; "" for a NULL plan. */
+ * gathered by TMA im2col loads, 128-pixel tiles), "tma-im2col-m256" (the
+ * same with 256-pixel tiles) or "cp-async" (the general gather); for a
+ * strided transposed plan, its first phase's.  Static text; "" for a NULL
+ * plan. */
 const char *fconv_plan_kernel(const fconv_plan *plan);
 
 /* Static text for a status code. */
