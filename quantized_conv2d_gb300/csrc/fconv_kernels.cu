@@ -142,13 +142,18 @@ __device__ __forceinline__ void load_side_words(const ConvArgs &a, long long m, 
 }
 
 // side_pre: the slice's side words loaded ahead (load_side_words), or
-// nullptr to load them here.  GENERAL_ACT: the slope-then-clamp activation;
+// nullptr to load them here.  bias_c / scale_c: the slice's 32 bias and
+// per-channel scale values copied to shared memory by the caller, or nullptr
+// to read a.bias / a.scale_k.  GENERAL_ACT: the slope-then-clamp activation;
 // otherwise (no activation or Relu) only the lower bound a.lo (-inf or 0).
 template <bool IS_INT8, bool GENERAL_ACT>
 __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m, int col0,
                                                  const float (&vals)[32],
-                                                 const uint4 *side_pre) {
+                                                 const uint4 *side_pre, const float *bias_c,
+                                                 const float *scale_c) {
   const int K = a.K;
+  const float *bias_p = bias_c ? bias_c : a.bias + col0;
+  const float *scale_p = scale_c ? scale_c : a.scale_k + col0;
   if (a.mode == kModeAccumulators) {
     // raw sums: int32 for int8 plans, fp32 for bf16 plans; 4 columns per store
 #pragma unroll
@@ -175,6 +180,10 @@ __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m,
   const float cs = a.conv_scale, ss = a.side_scale;
   const bool use_side = a.use_side != 0;
   if (IS_INT8) {
+    // The clamp to [lo, 127] before rounding: the activation's lower bound
+    // (Relu 0, none -inf) merged with the int8 range.  Saturating after a
+    // round-half-even gives the same code as rounding the clamped value.
+    const float lo = GENERAL_ACT ? -128.0f : fmaxf(a.lo, -128.0f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int col = col0 + 16 * h;
@@ -182,17 +191,19 @@ __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m,
       uint4 sv = make_uint4(0, 0, 0, 0);
       if (side_pre) sv = side_pre[h];
       else if (use_side) sv = ldg_nc_v4(static_cast<const int8_t *>(a.side) + m * K + col);
-      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+      // side bytes in offset binary (b + 128, 0..255)
+      const uint32_t sw[4] = {sv.x ^ 0x80808080u, sv.y ^ 0x80808080u, sv.z ^ 0x80808080u,
+                              sv.w ^ 0x80808080u};
       uint32_t out[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         // bias (and per-channel scale): every lane reads the same 16 bytes
-        const float4 bb = __ldg(reinterpret_cast<const float4 *>(a.bias + col + 4 * g));
+        const float4 bb = *reinterpret_cast<const float4 *>(bias_p + 16 * h + 4 * g);
         const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
-        const float4 sc = a.scale_k ? __ldg(reinterpret_cast<const float4 *>(a.scale_k + col + 4 * g))
+        const float4 sc = a.scale_k ? *reinterpret_cast<const float4 *>(scale_p + 16 * h + 4 * g)
                                     : make_float4(cs, cs, cs, cs);
         const float sv4[4] = {sc.x, sc.y, sc.z, sc.w};
-        uint32_t word = 0;
+        uint32_t t[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           // (1) scale; (2) side input, one fused rounding; (3) bias.  The
@@ -200,16 +211,22 @@ __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m,
           // (1) and (3) into an fma.
           float v = __fmul_rn(vals[16 * h + 4 * g + e], sv4[e]);
           if (use_side) {
-            const float sd = static_cast<float>(static_cast<int8_t>((sw[g] >> (8 * e)) & 0xFFu));
+            // byte u = b + 128 as the mantissa of 2^23 is the float 2^23 + u;
+            // subtracting 2^23 + 128 leaves b exactly
+            const float sd = __fsub_rn(__uint_as_float(__byte_perm(sw[g], 0x4B000000u, 0x7540u + e)),
+                                       8388736.0f);
             v = __fmaf_rn(sd, ss, v);
           }
           v = __fadd_rn(v, bv[e]);
-          v = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
-          int r = __float2int_rn(v);  // round half to even, saturating
-          r = min(max(r, -128), 127);
-          word |= (static_cast<uint32_t>(r) & 0xFFu) << (8 * e);
+          if (GENERAL_ACT) v = activation(v, a);
+          v = fminf(fmaxf(v, lo), 127.0f);
+          // 1.5 * 2^23 + v, v in [-128, 127]: the fp32 ulp there is 1, so the
+          // add rounds v half to even and the low byte of the sum's bits is
+          // that integer in two's complement
+          t[e] = __float_as_uint(__fadd_rn(v, 12582912.0f));
         }
-        out[g] = word;
+        out[g] = __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x0040u),
+                             0x5410u);
       }
       stg_v4(static_cast<int8_t *>(a.y) + m * K + col, make_uint4(out[0], out[1], out[2], out[3]));
     }
@@ -222,13 +239,13 @@ __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m,
       if (side_pre) sv = side_pre[qd];
       else if (use_side) sv = ldg_nc_v4(static_cast<const __nv_bfloat16 *>(a.side) + m * K + col);
       const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-      const float4 b0 = __ldg(reinterpret_cast<const float4 *>(a.bias + col));
-      const float4 b1 = __ldg(reinterpret_cast<const float4 *>(a.bias + col + 4));
+      const float4 b0 = *reinterpret_cast<const float4 *>(bias_p + 8 * qd);
+      const float4 b1 = *reinterpret_cast<const float4 *>(bias_p + 8 * qd + 4);
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
       float sv8[8];
       if (a.scale_k) {
-        const float4 s0 = __ldg(reinterpret_cast<const float4 *>(a.scale_k + col));
-        const float4 s1 = __ldg(reinterpret_cast<const float4 *>(a.scale_k + col + 4));
+        const float4 s0 = *reinterpret_cast<const float4 *>(scale_p + 8 * qd);
+        const float4 s1 = *reinterpret_cast<const float4 *>(scale_p + 8 * qd + 4);
         sv8[0] = s0.x; sv8[1] = s0.y; sv8[2] = s0.z; sv8[3] = s0.w;
         sv8[4] = s1.x; sv8[5] = s1.y; sv8[6] = s1.z; sv8[7] = s1.w;
       } else {
@@ -238,16 +255,17 @@ __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m,
       uint32_t out[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        uint32_t word = 0;
+        float r[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           float v = __fmul_rn(vals[8 * qd + 2 * g + t], sv8[2 * g + t]);
           if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
           v = __fadd_rn(v, bv[2 * g + t]);
-          v = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
-          word |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v))) << (16 * t);
+          r[t] = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
         }
-        out[g] = word;
+        // both round to nearest even in one conversion; .x is the low half
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(r[0], r[1]);
+        out[g] = *reinterpret_cast<const uint32_t *>(&pr);
       }
       stg_v4(static_cast<__nv_bfloat16 *>(a.y) + m * K + col,
              make_uint4(out[0], out[1], out[2], out[3]));
@@ -258,11 +276,13 @@ __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m,
 template <bool IS_INT8>
 __device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
                                                const float (&vals)[32],
-                                               const uint4 *side_pre = nullptr) {
+                                               const uint4 *side_pre = nullptr,
+                                               const float *bias_c = nullptr,
+                                               const float *scale_c = nullptr) {
   if (a.act > kActRelu)
-    epilogue_slice_t<IS_INT8, true>(a, m, col0, vals, side_pre);
+    epilogue_slice_t<IS_INT8, true>(a, m, col0, vals, side_pre, bias_c, scale_c);
   else
-    epilogue_slice_t<IS_INT8, false>(a, m, col0, vals, side_pre);
+    epilogue_slice_t<IS_INT8, false>(a, m, col0, vals, side_pre, bias_c, scale_c);
 }
 
 // General path: cp.async gather of A by 4 loader warps, 4 epilogue warps.
@@ -552,14 +572,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // Registers: the register file is split over the SM's four sub-partitions,
 // so 12 warps launch at 168 a thread (384 x 168 = 64512).  Warpgroup 0 then
-// gives back down to 56 and the epilogue warpgroups take 224:
-// 128 x 56 + 256 x 224 = 64512, the launch total; per sub-partition that is
-// one warp of each warpgroup, 56 + 224 + 224 = 504 <= 512 per lane.
+// gives back down to 40 and the epilogue warpgroups take 232:
+// 128 x 40 + 256 x 232 = 64512, the launch total; per sub-partition that is
+// one warp of each warpgroup, 40 + 232 + 232 = 504 <= 512 per lane.  ptxas
+// allocates each region to its setmaxnreg budget: the int8 epilogue holds
+// 128 int32 sums, 32 side words and a 32-column slice at once.
 constexpr int kTmaThreads = 384;
 constexpr int kTmaEpiWarp0 = 4;
 constexpr int kTmaEpiWarps = 8;
-constexpr int kTmaCtlRegs = 56;
-constexpr int kTmaEpiRegs = 224;
+constexpr int kTmaCtlRegs = 40;
+constexpr int kTmaEpiRegs = 232;
 static_assert(128 * kTmaCtlRegs + 256 * kTmaEpiRegs <= kTmaThreads * 168,
               "register split exceeds the launch allocation");
 
@@ -579,11 +601,15 @@ struct TmaCfg {
   static constexpr int kAccCols = MS * BN;             // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols <= 128 ? 128 : 2 * kAccCols <= 256 ? 256 : 512;
   static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
   // columns per epilogue thread: MS = 1 splits a row's BN columns between
   // two warps; MS = 2 gives each warp half one sub-tile's whole rows
   static constexpr int kHalfCols = MS == 1 ? BN / 2 : BN;
   static constexpr int kSlices = kHalfCols / 32;
+  // after the barriers: each epilogue warp's copy of its columns' bias and
+  // per-channel scale, [warp][bias | scale][kHalfCols] floats
+  static constexpr int kParamOffset = kBarOffset + 256;
+  static constexpr int kParamBytes = kTmaEpiWarps * 2 * kHalfCols * 4;
+  static constexpr int kSmemBytes = 1024 + kParamOffset + kParamBytes;
   static_assert(BN == 64 || BN == 128 || BN == 256, "TMA path tile");
   static_assert(MS == 1 || (MS == 2 && BN <= 128), "two sub-tiles need BN <= 128");
   static_assert(2 * kAccCols <= 512, "tensor memory");
@@ -784,6 +810,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int cbase = MS == 2 ? 0 : half * C::kHalfCols;        // first column, in the tile
     const int tcol = (MS == 2 ? half * BN : 0) + cbase;          // its TMEM column offset
     int32_t sums[IS_INT8 ? C::kHalfCols : 1];  // int32 running sums across chunks
+    // this warp's copy of the bias / scale of its tile columns: read as
+    // shared-memory broadcasts by the epilogue instead of global loads that
+    // queue behind the output stores
+    float *wpar = reinterpret_cast<float *>(smem + C::kParamOffset) +
+                  (warp - kTmaEpiWarp0) * 2 * C::kHalfCols;
     uint32_t astage = 0, aphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
@@ -793,6 +824,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const bool mvalid = m < args.M;
       const long long mo = out_pixel(args, m);   // the output pixel row m writes
       const int c0 = n_tile * BN + cbase;
+      __syncwarp();   // every lane is done with the previous tile's copy
+      if (args.mode == kModeFused && args.bias) {  // no bias when only the sums are written
+        for (int j = lane; j < C::kHalfCols; j += 32) {
+          const bool in = c0 + j < args.K;
+          wpar[j] = in ? __ldg(args.bias + c0 + j) : 0.0f;
+          if (args.scale_k) wpar[C::kHalfCols + j] = in ? __ldg(args.scale_k + c0 + j) : 0.0f;
+        }
+      }
+      __syncwarp();
+      const float *wscale = args.scale_k ? wpar + C::kHalfCols : nullptr;
       // the side input this thread reads after the tile's last chunk: into
       // L2 now, so the final epilogue does not wait on DRAM
       if (args.use_side && mvalid && c0 < args.K)
@@ -818,7 +859,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint32_t t_acc = tmem_base + lane_off + astage * C::kAccCols + tcol;
         if (n_chunks == 1) {
           // the whole sum is in TMEM: epilogue straight from it
-#pragma unroll 1
+#pragma unroll
           for (int jj = 0; jj < C::kSlices; ++jj) {
             uint32_t v[32];
             tmem_ld32(t_acc + jj * 32, v);
@@ -830,7 +871,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             if (mvalid)
               epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals,
                                       preload ? side_pre + jj * SideWords<IS_INT8>::kWords
-                                              : nullptr);
+                                              : nullptr,
+                                      wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr);
           }
           tc_fence_before();
           __syncwarp();
@@ -866,7 +908,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(sums[jj * 32 + i]);
                 epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals,
                                         preload ? side_pre + jj * SideWords<IS_INT8>::kWords
-                                                : nullptr);
+                                                : nullptr,
+                                        wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr);
               }
             }
           }
