@@ -141,11 +141,103 @@ __device__ __forceinline__ void load_side_words(const ConvArgs &a, long long m, 
   }
 }
 
+// One 16-byte group of a fused epilogue slice: int8 columns 16 * gi .. +15
+// or bf16 columns 8 * gi .. +7 of the slice, packed as they are stored.
+// sv: the group's side-input word; bias_p / scale_p: the slice's first
+// column.  GENERAL_ACT: the slope-then-clamp activation; otherwise (no
+// activation or Relu) only the lower bound a.lo (-inf or 0).
+template <bool IS_INT8, bool GENERAL_ACT>
+__device__ __forceinline__ uint4 fused_group(const ConvArgs &a, const float (&vals)[32], int gi,
+                                             uint4 sv, const float *bias_p,
+                                             const float *scale_p) {
+  const float cs = a.conv_scale, ss = a.side_scale;
+  const bool use_side = a.use_side != 0;
+  uint32_t out[4];
+  if (IS_INT8) {
+    // The clamp to [lo, 127] before rounding: the activation's lower bound
+    // (Relu 0, none -inf) merged with the int8 range.  Saturating after a
+    // round-half-even gives the same code as rounding the clamped value.
+    const float lo = GENERAL_ACT ? -128.0f : fmaxf(a.lo, -128.0f);
+    // side bytes in offset binary (b + 128, 0..255)
+    const uint32_t sw[4] = {sv.x ^ 0x80808080u, sv.y ^ 0x80808080u, sv.z ^ 0x80808080u,
+                            sv.w ^ 0x80808080u};
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      // bias (and per-channel scale): every lane reads the same 16 bytes
+      const float4 bb = *reinterpret_cast<const float4 *>(bias_p + 16 * gi + 4 * g);
+      const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+      const float4 sc = a.scale_k ? *reinterpret_cast<const float4 *>(scale_p + 16 * gi + 4 * g)
+                                  : make_float4(cs, cs, cs, cs);
+      const float sv4[4] = {sc.x, sc.y, sc.z, sc.w};
+      uint32_t t[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // (1) scale; (2) side input, one fused rounding; (3) bias.  The
+        // explicit round-to-nearest intrinsics keep nvcc from contracting
+        // (1) and (3) into an fma.
+        float v = __fmul_rn(vals[16 * gi + 4 * g + e], sv4[e]);
+        if (use_side) {
+          // byte u = b + 128 as the mantissa of 2^23 is the float 2^23 + u;
+          // subtracting 2^23 + 128 leaves b exactly
+          const float sd = __fsub_rn(__uint_as_float(__byte_perm(sw[g], 0x4B000000u, 0x7540u + e)),
+                                     8388736.0f);
+          v = __fmaf_rn(sd, ss, v);
+        }
+        v = __fadd_rn(v, bv[e]);
+        if (GENERAL_ACT) v = activation(v, a);
+        v = fminf(fmaxf(v, lo), 127.0f);
+        // 1.5 * 2^23 + v, v in [-128, 127]: the fp32 ulp there is 1, so the
+        // add rounds v half to even and the low byte of the sum's bits is
+        // that integer in two's complement
+        t[e] = __float_as_uint(__fadd_rn(v, 12582912.0f));
+      }
+      out[g] = __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x0040u),
+                           0x5410u);
+    }
+  } else {
+    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+    const float4 b0 = *reinterpret_cast<const float4 *>(bias_p + 8 * gi);
+    const float4 b1 = *reinterpret_cast<const float4 *>(bias_p + 8 * gi + 4);
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    float sv8[8];
+    if (a.scale_k) {
+      const float4 s0 = *reinterpret_cast<const float4 *>(scale_p + 8 * gi);
+      const float4 s1 = *reinterpret_cast<const float4 *>(scale_p + 8 * gi + 4);
+      sv8[0] = s0.x; sv8[1] = s0.y; sv8[2] = s0.z; sv8[3] = s0.w;
+      sv8[4] = s1.x; sv8[5] = s1.y; sv8[6] = s1.z; sv8[7] = s1.w;
+    } else {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) sv8[t] = cs;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float r[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float v = __fmul_rn(vals[8 * gi + 2 * g + t], sv8[2 * g + t]);
+        if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
+        v = __fadd_rn(v, bv[2 * g + t]);
+        r[t] = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
+      }
+      // both round to nearest even in one conversion; .x is the low half
+      const __nv_bfloat162 pr = __floats2bfloat162_rn(r[0], r[1]);
+      out[g] = *reinterpret_cast<const uint32_t *>(&pr);
+    }
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Groups of 16 bytes in a 32-column slice: int8 2, bf16 4.
+template <bool IS_INT8>
+struct SliceGroups {
+  static constexpr int kGroups = IS_INT8 ? 2 : 4;
+  static constexpr int kCols = IS_INT8 ? 16 : 8;   // columns per group
+};
+
 // side_pre: the slice's side words loaded ahead (load_side_words), or
 // nullptr to load them here.  bias_c / scale_c: the slice's 32 bias and
 // per-channel scale values copied to shared memory by the caller, or nullptr
-// to read a.bias / a.scale_k.  GENERAL_ACT: the slope-then-clamp activation;
-// otherwise (no activation or Relu) only the lower bound a.lo (-inf or 0).
+// to read a.bias / a.scale_k.  Each thread stores its own row's groups.
 template <bool IS_INT8, bool GENERAL_ACT>
 __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m, int col0,
                                                  const float (&vals)[32],
@@ -177,100 +269,96 @@ __device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m,
     }
     return;
   }
-  const float cs = a.conv_scale, ss = a.side_scale;
-  const bool use_side = a.use_side != 0;
-  if (IS_INT8) {
-    // The clamp to [lo, 127] before rounding: the activation's lower bound
-    // (Relu 0, none -inf) merged with the int8 range.  Saturating after a
-    // round-half-even gives the same code as rounding the clamped value.
-    const float lo = GENERAL_ACT ? -128.0f : fmaxf(a.lo, -128.0f);
+  using G = SliceGroups<IS_INT8>;
+  constexpr int elt = IS_INT8 ? 1 : 2;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = col0 + 16 * h;
-      if (col >= K) continue;
-      uint4 sv = make_uint4(0, 0, 0, 0);
-      if (side_pre) sv = side_pre[h];
-      else if (use_side) sv = ldg_nc_v4(static_cast<const int8_t *>(a.side) + m * K + col);
-      // side bytes in offset binary (b + 128, 0..255)
-      const uint32_t sw[4] = {sv.x ^ 0x80808080u, sv.y ^ 0x80808080u, sv.z ^ 0x80808080u,
-                              sv.w ^ 0x80808080u};
-      uint32_t out[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        // bias (and per-channel scale): every lane reads the same 16 bytes
-        const float4 bb = *reinterpret_cast<const float4 *>(bias_p + 16 * h + 4 * g);
-        const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
-        const float4 sc = a.scale_k ? *reinterpret_cast<const float4 *>(scale_p + 16 * h + 4 * g)
-                                    : make_float4(cs, cs, cs, cs);
-        const float sv4[4] = {sc.x, sc.y, sc.z, sc.w};
-        uint32_t t[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // (1) scale; (2) side input, one fused rounding; (3) bias.  The
-          // explicit round-to-nearest intrinsics keep nvcc from contracting
-          // (1) and (3) into an fma.
-          float v = __fmul_rn(vals[16 * h + 4 * g + e], sv4[e]);
-          if (use_side) {
-            // byte u = b + 128 as the mantissa of 2^23 is the float 2^23 + u;
-            // subtracting 2^23 + 128 leaves b exactly
-            const float sd = __fsub_rn(__uint_as_float(__byte_perm(sw[g], 0x4B000000u, 0x7540u + e)),
-                                       8388736.0f);
-            v = __fmaf_rn(sd, ss, v);
-          }
-          v = __fadd_rn(v, bv[e]);
-          if (GENERAL_ACT) v = activation(v, a);
-          v = fminf(fmaxf(v, lo), 127.0f);
-          // 1.5 * 2^23 + v, v in [-128, 127]: the fp32 ulp there is 1, so the
-          // add rounds v half to even and the low byte of the sum's bits is
-          // that integer in two's complement
-          t[e] = __float_as_uint(__fadd_rn(v, 12582912.0f));
-        }
-        out[g] = __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x0040u),
-                             0x5410u);
-      }
-      stg_v4(static_cast<int8_t *>(a.y) + m * K + col, make_uint4(out[0], out[1], out[2], out[3]));
-    }
-  } else {
-#pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-      const int col = col0 + 8 * qd;
-      if (col >= K) continue;
-      uint4 sv = make_uint4(0, 0, 0, 0);
-      if (side_pre) sv = side_pre[qd];
-      else if (use_side) sv = ldg_nc_v4(static_cast<const __nv_bfloat16 *>(a.side) + m * K + col);
-      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-      const float4 b0 = *reinterpret_cast<const float4 *>(bias_p + 8 * qd);
-      const float4 b1 = *reinterpret_cast<const float4 *>(bias_p + 8 * qd + 4);
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-      float sv8[8];
-      if (a.scale_k) {
-        const float4 s0 = *reinterpret_cast<const float4 *>(scale_p + 8 * qd);
-        const float4 s1 = *reinterpret_cast<const float4 *>(scale_p + 8 * qd + 4);
-        sv8[0] = s0.x; sv8[1] = s0.y; sv8[2] = s0.z; sv8[3] = s0.w;
-        sv8[4] = s1.x; sv8[5] = s1.y; sv8[6] = s1.z; sv8[7] = s1.w;
-      } else {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) sv8[t] = cs;
-      }
-      uint32_t out[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float r[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          float v = __fmul_rn(vals[8 * qd + 2 * g + t], sv8[2 * g + t]);
-          if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
-          v = __fadd_rn(v, bv[2 * g + t]);
-          r[t] = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
-        }
-        // both round to nearest even in one conversion; .x is the low half
-        const __nv_bfloat162 pr = __floats2bfloat162_rn(r[0], r[1]);
-        out[g] = *reinterpret_cast<const uint32_t *>(&pr);
-      }
-      stg_v4(static_cast<__nv_bfloat16 *>(a.y) + m * K + col,
-             make_uint4(out[0], out[1], out[2], out[3]));
-    }
+  for (int gi = 0; gi < G::kGroups; ++gi) {
+    const int col = col0 + G::kCols * gi;
+    if (col >= K) continue;
+    uint4 sv = make_uint4(0, 0, 0, 0);
+    if (side_pre) sv = side_pre[gi];
+    else if (a.use_side) sv = ldg_nc_v4(static_cast<const uint8_t *>(a.side) + (m * K + col) * elt);
+    stg_v4(static_cast<uint8_t *>(a.y) + (m * K + col) * elt,
+           fused_group<IS_INT8, GENERAL_ACT>(a, vals, gi, sv, bias_p, scale_p));
   }
+}
+
+// The same slice for a whole warp (all 32 lanes call it; lane l holds row
+// l), with the stores coalesced: the rows' 16-byte groups pass through the
+// warp's shared-memory buffer `stage` (32 rows x kGroups x 16 bytes) so that
+// each store instruction writes whole 32-byte row segments of consecutive
+// lanes (kGroups lanes per row).  Groups sit in the buffer rotated by the
+// row's position within its eight-row bank window, so neither the writes
+// nor the reads conflict.  mo / valid: this lane's output pixel and whether
+// its row exists; side_pre as above, loaded only for valid rows.  st_mo /
+// st_ok: output pixel and existence of the row this lane stores in store
+// round k (row (32 k + lane) / kGroups), from coalesced_rows.
+template <bool IS_INT8, bool GENERAL_ACT>
+__device__ __forceinline__ void epilogue_slice_coalesced(const ConvArgs &a, long long mo,
+                                                         bool valid, int col0,
+                                                         const float (&vals)[32],
+                                                         const uint4 *side_pre,
+                                                         const float *bias_c,
+                                                         const float *scale_c, uint4 *stage,
+                                                         const long long *st_mo,
+                                                         const bool *st_ok) {
+  using G = SliceGroups<IS_INT8>;
+  constexpr int kG = G::kGroups;
+  constexpr int elt = IS_INT8 ? 1 : 2;
+  const int lane = threadIdx.x & 31;
+  const int K = a.K;
+  const float *scale_p = scale_c ? scale_c : a.scale_k + col0;
+  // swizzle of row r: 8 / kG consecutive rows share a 128-byte bank window
+  auto swz = [](int r) { return (r / (8 / kG)) % kG; };
+#pragma unroll
+  for (int gi = 0; gi < kG; ++gi) {
+    uint4 sv = make_uint4(0, 0, 0, 0);
+    if (side_pre) sv = side_pre[gi];
+    else if (a.use_side && valid && col0 + G::kCols * gi < K)
+      sv = ldg_nc_v4(static_cast<const uint8_t *>(a.side) + (mo * K + col0 + G::kCols * gi) * elt);
+    stage[lane * kG + (gi ^ swz(lane))] =
+        fused_group<IS_INT8, GENERAL_ACT>(a, vals, gi, sv, bias_c, scale_p);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < kG; ++k) {
+    const int piece = k * 32 + lane;
+    const int r = piece / kG, q = piece % kG;   // row and group this lane stores
+    const uint4 v = stage[r * kG + (q ^ swz(r))];
+    const int col = col0 + G::kCols * q;
+    if (st_ok[k] && col < K) stg_v4(static_cast<uint8_t *>(a.y) + (st_mo[k] * K + col) * elt, v);
+  }
+  __syncwarp();   // the buffer is free for the next slice
+}
+
+// The rows a lane stores in the coalesced rounds: round k stores row
+// (32 k + lane) / kGroups, whose output pixel and existence its own lane
+// holds.  The whole warp calls this, once per tile.
+template <bool IS_INT8>
+__device__ __forceinline__ void coalesced_rows(long long mo, bool valid, long long *st_mo,
+                                               bool *st_ok) {
+  constexpr int kG = SliceGroups<IS_INT8>::kGroups;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < kG; ++k) {
+    const int r = (k * 32 + lane) / kG;
+    st_mo[k] = __shfl_sync(0xffffffffu, mo, r);
+    st_ok[k] = __shfl_sync(0xffffffffu, static_cast<int>(valid), r) != 0;
+  }
+}
+
+template <bool IS_INT8>
+__device__ __forceinline__ void epilogue_slice_warp(const ConvArgs &a, long long mo, bool valid,
+                                                    int col0, const float (&vals)[32],
+                                                    const uint4 *side_pre, const float *bias_c,
+                                                    const float *scale_c, uint4 *stage,
+                                                    const long long *st_mo, const bool *st_ok) {
+  if (a.act > kActRelu)
+    epilogue_slice_coalesced<IS_INT8, true>(a, mo, valid, col0, vals, side_pre, bias_c, scale_c,
+                                            stage, st_mo, st_ok);
+  else
+    epilogue_slice_coalesced<IS_INT8, false>(a, mo, valid, col0, vals, side_pre, bias_c, scale_c,
+                                             stage, st_mo, st_ok);
 }
 
 template <bool IS_INT8>
@@ -609,7 +697,12 @@ struct TmaCfg {
   // per-channel scale, [warp][bias | scale][kHalfCols] floats
   static constexpr int kParamOffset = kBarOffset + 256;
   static constexpr int kParamBytes = kTmaEpiWarps * 2 * kHalfCols * 4;
-  static constexpr int kSmemBytes = 1024 + kParamOffset + kParamBytes;
+  // then each epilogue warp's output staging: 32 rows x 64 bytes (a bf16
+  // slice; an int8 slice uses half)
+  static constexpr int kOutOffset = kParamOffset + kParamBytes;
+  static constexpr int kOutWarpBytes = 32 * 64;
+  static constexpr int kSmemBytes = 1024 + kOutOffset + kTmaEpiWarps * kOutWarpBytes;
+  static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
   static_assert(BN == 64 || BN == 128 || BN == 256, "TMA path tile");
   static_assert(MS == 1 || (MS == 2 && BN <= 128), "two sub-tiles need BN <= 128");
   static_assert(2 * kAccCols <= 512, "tensor memory");
@@ -815,6 +908,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // queue behind the output stores
     float *wpar = reinterpret_cast<float *>(smem + C::kParamOffset) +
                   (warp - kTmaEpiWarp0) * 2 * C::kHalfCols;
+    // this warp's staging buffer for the coalesced output stores
+    uint4 *ostage = reinterpret_cast<uint4 *>(smem + C::kOutOffset) +
+                    (warp - kTmaEpiWarp0) * C::kOutWarpBytes / 16;
     uint32_t astage = 0, aphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
@@ -823,6 +919,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const long long m = static_cast<long long>(m_tile) * kTileM + row;
       const bool mvalid = m < args.M;
       const long long mo = out_pixel(args, m);   // the output pixel row m writes
+      long long st_mo[SliceGroups<IS_INT8>::kGroups];
+      bool st_ok[SliceGroups<IS_INT8>::kGroups];
+      coalesced_rows<IS_INT8>(mo, mvalid, st_mo, st_ok);
       const int c0 = n_tile * BN + cbase;
       __syncwarp();   // every lane is done with the previous tile's copy
       if (args.mode == kModeFused && args.bias) {  // no bias when only the sums are written
@@ -851,7 +950,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             load_side_words<IS_INT8>(args, mo, c0 + jj * 32,
                                      side_pre + jj * SideWords<IS_INT8>::kWords);
         }
-        if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
+        // one outcome for the whole warp: the stores below are warp-wide
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo))) {
           ok = false;
           break;
         }
@@ -868,11 +969,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             // + 0.0f turns a -0 sum into the +0 that float(int32 0) gives
 #pragma unroll
             for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
-            if (mvalid)
-              epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals,
-                                      preload ? side_pre + jj * SideWords<IS_INT8>::kWords
-                                              : nullptr,
-                                      wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr);
+            if (args.mode == kModeFused)
+              epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals,
+                                           preload ? side_pre + jj * SideWords<IS_INT8>::kWords
+                                                   : nullptr,
+                                           wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
+                                           ostage, st_mo, st_ok);
+            else if (mvalid)
+              epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals);
           }
           tc_fence_before();
           __syncwarp();
@@ -894,22 +998,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[astage]));
-          if (ch == n_chunks - 1 && mvalid) {
+          if (ch == n_chunks - 1) {   // the whole warp: the fused stores are coalesced
 #pragma unroll
             for (int jj = 0; jj < C::kSlices; ++jj) {
               if (args.mode == kModeAccumulators) {
                 uint32_t u[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) u[i] = static_cast<uint32_t>(sums[jj * 32 + i]);
-                store_i32_slice(args, mo, c0 + jj * 32, u);
+                if (mvalid) store_i32_slice(args, mo, c0 + jj * 32, u);
               } else {
                 float vals[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(sums[jj * 32 + i]);
-                epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals,
-                                        preload ? side_pre + jj * SideWords<IS_INT8>::kWords
-                                                : nullptr,
-                                        wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr);
+                epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals,
+                                             preload ? side_pre + jj * SideWords<IS_INT8>::kWords
+                                                     : nullptr,
+                                             wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
+                                             ostage, st_mo, st_ok);
               }
             }
           }
