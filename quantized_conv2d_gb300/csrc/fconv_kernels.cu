@@ -62,7 +62,15 @@ struct Cfg {
                                    : kColsNeeded <= 256 ? 256
                                                         : 512;
   static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
+  // after the barriers: each of the 4 epilogue warps' copy of the tile's
+  // bias and per-channel scale ([warp][bias | scale][BN] floats), then its
+  // output staging buffer (32 rows x 64 bytes)
+  static constexpr int kParamOffset = kBarOffset + 256;
+  static constexpr int kParamBytes = 4 * 2 * BN * 4;
+  static constexpr int kOutOffset = kParamOffset + kParamBytes;
+  static constexpr int kOutWarpBytes = 32 * 64;
+  static constexpr int kSmemBytes = 1024 + kOutOffset + 4 * kOutWarpBytes;
+  static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
   static_assert(kLag >= 2, "pipeline too shallow");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
 };
@@ -572,6 +580,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int ew = warp - kMmaWarp - 1;   // epilogue warp 0..3
+    // this warp's copy of the tile columns' bias / scale, and its staging
+    // buffer for the coalesced output stores
+    float *wpar = reinterpret_cast<float *>(smem + C::kParamOffset) + ew * 2 * BN;
+    uint4 *ostage = reinterpret_cast<uint4 *>(smem + C::kOutOffset) + ew * C::kOutWarpBytes / 16;
     uint32_t astage = 0, aphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
@@ -581,13 +594,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool mvalid = m < args.M;
       const long long mo = out_pixel(args, m);   // the output pixel row m writes
       const int n0 = n_tile * BN;
+      long long st_mo[SliceGroups<IS_INT8>::kGroups];
+      bool st_ok[SliceGroups<IS_INT8>::kGroups];
+      coalesced_rows<IS_INT8>(mo, mvalid, st_mo, st_ok);
+      __syncwarp();   // every lane is done with the previous tile's copy
+      if (args.mode == kModeFused && args.bias) {  // no bias when only the sums are written
+        for (int j = lane; j < BN; j += 32) {
+          const bool in = n0 + j < args.K;
+          wpar[j] = in ? __ldg(args.bias + n0 + j) : 0.0f;
+          if (args.scale_k) wpar[BN + j] = in ? __ldg(args.scale_k + n0 + j) : 0.0f;
+        }
+      }
+      __syncwarp();
+      const float *wscale = args.scale_k ? wpar + BN : nullptr;
       // the side input this thread reads after the tile's last chunk: into
       // L2 now, so the final epilogue does not wait on DRAM
       if (args.use_side && mvalid && n0 < args.K)
         prefetch_l2(static_cast<const uint8_t *>(args.side) + (mo * args.K + n0) * (IS_INT8 ? 1 : 2),
                     min(BN, args.K - n0) * (IS_INT8 ? 1 : 2));
       for (int ch = 0; ch < n_chunks; ++ch) {
-        if (!mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo)) {
+        // one outcome for the whole warp: the stores below are warp-wide
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bars->acc_full[astage]), aphase, abort_flag, tmo))) {
           ok = false;
           break;
         }
@@ -630,7 +658,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
           }
-          if (mvalid) epilogue_slice<IS_INT8>(args, mo, n0 + jj * 32, vals);
+          if (args.mode == kModeFused)
+            epilogue_slice_warp<IS_INT8>(args, mo, mvalid, n0 + jj * 32, vals, nullptr,
+                                         wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
+                                         ostage, st_mo, st_ok);
+          else if (mvalid)
+            epilogue_slice<IS_INT8>(args, mo, n0 + jj * 32, vals);
         }
         if (!last) tmem_wait_st();
         tc_fence_before();
