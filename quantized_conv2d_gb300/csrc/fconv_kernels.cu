@@ -129,19 +129,20 @@ __device__ __forceinline__ long long out_pixel(const ConvArgs &a, long long m) {
          static_cast<long long>(q) * a.o_sw;
 }
 
-// Side-input words of one 32-column slice: int8 2 x 16 columns, bf16 4 x 8.
+// 16-byte groups of a 32-column slice (of outputs, or of side-input words):
+// int8 2 x 16 columns, bf16 4 x 8.
 template <bool IS_INT8>
-struct SideWords {
-  static constexpr int kWords = IS_INT8 ? 2 : 4;
-  static constexpr int kCols = IS_INT8 ? 16 : 8;
+struct SliceGroups {
+  static constexpr int kGroups = IS_INT8 ? 2 : 4;
+  static constexpr int kCols = IS_INT8 ? 16 : 8;   // columns per group
 };
 
 template <bool IS_INT8>
 __device__ __forceinline__ void load_side_words(const ConvArgs &a, long long m, int col0,
                                                 uint4 *words) {
 #pragma unroll
-  for (int h = 0; h < SideWords<IS_INT8>::kWords; ++h) {
-    const int col = col0 + h * SideWords<IS_INT8>::kCols;
+  for (int h = 0; h < SliceGroups<IS_INT8>::kGroups; ++h) {
+    const int col = col0 + h * SliceGroups<IS_INT8>::kCols;
     words[h] = (a.use_side && col < a.K)
                    ? ldg_nc_v4(static_cast<const uint8_t *>(a.side) +
                                (m * a.K + col) * (IS_INT8 ? 1 : 2))
@@ -235,72 +236,47 @@ __device__ __forceinline__ uint4 fused_group(const ConvArgs &a, const float (&va
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// Groups of 16 bytes in a 32-column slice: int8 2, bf16 4.
+// Raw sums of one 32-column slice of row m (the accumulator-only mode):
+// int32 for int8 plans, fp32 for bf16 plans; 4 columns per store.
 template <bool IS_INT8>
-struct SliceGroups {
-  static constexpr int kGroups = IS_INT8 ? 2 : 4;
-  static constexpr int kCols = IS_INT8 ? 16 : 8;   // columns per group
-};
-
-// side_pre: the slice's side words loaded ahead (load_side_words), or
-// nullptr to load them here.  bias_c / scale_c: the slice's 32 bias and
-// per-channel scale values copied to shared memory by the caller, or nullptr
-// to read a.bias / a.scale_k.  Each thread stores its own row's groups.
-template <bool IS_INT8, bool GENERAL_ACT>
-__device__ __forceinline__ void epilogue_slice_t(const ConvArgs &a, long long m, int col0,
-                                                 const float (&vals)[32],
-                                                 const uint4 *side_pre, const float *bias_c,
-                                                 const float *scale_c) {
+__device__ __forceinline__ void store_raw_slice(const ConvArgs &a, long long m, int col0,
+                                                const float (&vals)[32]) {
   const int K = a.K;
-  const float *bias_p = bias_c ? bias_c : a.bias + col0;
-  const float *scale_p = scale_c ? scale_c : a.scale_k + col0;
-  if (a.mode == kModeAccumulators) {
-    // raw sums: int32 for int8 plans, fp32 for bf16 plans; 4 columns per store
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int col = col0 + 4 * g;
-      if (col < K) {
-        uint4 o;
-        if (IS_INT8) {
-          o.x = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 0]));
-          o.y = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 1]));
-          o.z = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 2]));
-          o.w = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 3]));
-        } else {
-          o.x = __float_as_uint(vals[4 * g + 0]);
-          o.y = __float_as_uint(vals[4 * g + 1]);
-          o.z = __float_as_uint(vals[4 * g + 2]);
-          o.w = __float_as_uint(vals[4 * g + 3]);
-        }
-        stg_v4(static_cast<uint32_t *>(a.y) + m * K + col, o);
+  for (int g = 0; g < 8; ++g) {
+    const int col = col0 + 4 * g;
+    if (col < K) {
+      uint4 o;
+      if (IS_INT8) {
+        o.x = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 0]));
+        o.y = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 1]));
+        o.z = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 2]));
+        o.w = static_cast<uint32_t>(__float2int_rn(vals[4 * g + 3]));
+      } else {
+        o.x = __float_as_uint(vals[4 * g + 0]);
+        o.y = __float_as_uint(vals[4 * g + 1]);
+        o.z = __float_as_uint(vals[4 * g + 2]);
+        o.w = __float_as_uint(vals[4 * g + 3]);
       }
+      stg_v4(static_cast<uint32_t *>(a.y) + m * K + col, o);
     }
-    return;
-  }
-  using G = SliceGroups<IS_INT8>;
-  constexpr int elt = IS_INT8 ? 1 : 2;
-#pragma unroll
-  for (int gi = 0; gi < G::kGroups; ++gi) {
-    const int col = col0 + G::kCols * gi;
-    if (col >= K) continue;
-    uint4 sv = make_uint4(0, 0, 0, 0);
-    if (side_pre) sv = side_pre[gi];
-    else if (a.use_side) sv = ldg_nc_v4(static_cast<const uint8_t *>(a.side) + (m * K + col) * elt);
-    stg_v4(static_cast<uint8_t *>(a.y) + (m * K + col) * elt,
-           fused_group<IS_INT8, GENERAL_ACT>(a, vals, gi, sv, bias_p, scale_p));
   }
 }
 
-// The same slice for a whole warp (all 32 lanes call it; lane l holds row
-// l), with the stores coalesced: the rows' 16-byte groups pass through the
-// warp's shared-memory buffer `stage` (32 rows x kGroups x 16 bytes) so that
-// each store instruction writes whole 32-byte row segments of consecutive
-// lanes (kGroups lanes per row).  Groups sit in the buffer rotated by the
-// row's position within its eight-row bank window, so neither the writes
-// nor the reads conflict.  mo / valid: this lane's output pixel and whether
-// its row exists; side_pre as above, loaded only for valid rows.  st_mo /
-// st_ok: output pixel and existence of the row this lane stores in store
-// round k (row (32 k + lane) / kGroups), from coalesced_rows.
+// The fused epilogue of one 32-column slice for a whole warp (all 32 lanes
+// call it; lane l holds row l), with the stores coalesced: the rows'
+// 16-byte groups pass through the warp's shared-memory buffer `stage` (32
+// rows x kGroups x 16 bytes) so that each store instruction writes whole
+// 32-byte row segments of consecutive lanes (kGroups lanes per row).
+// Groups sit in the buffer rotated by the row's position within its
+// eight-row bank window, so neither the writes nor the reads conflict.
+// mo / valid: this lane's output pixel and whether its row exists.
+// side_pre: the slice's side words loaded ahead (load_side_words), or
+// nullptr to load them here (valid rows only).  bias_c / scale_c: the
+// slice's 32 bias and per-channel scale values in shared memory (scale_c
+// nullptr: the scalar a.conv_scale).  st_mo / st_ok: output pixel and
+// existence of the row this lane stores in store round k (row
+// (32 k + lane) / kGroups), from coalesced_rows.
 template <bool IS_INT8, bool GENERAL_ACT>
 __device__ __forceinline__ void epilogue_slice_coalesced(const ConvArgs &a, long long mo,
                                                          bool valid, int col0,
@@ -367,18 +343,6 @@ __device__ __forceinline__ void epilogue_slice_warp(const ConvArgs &a, long long
   else
     epilogue_slice_coalesced<IS_INT8, false>(a, mo, valid, col0, vals, side_pre, bias_c, scale_c,
                                              stage, st_mo, st_ok);
-}
-
-template <bool IS_INT8>
-__device__ __forceinline__ void epilogue_slice(const ConvArgs &a, long long m, int col0,
-                                               const float (&vals)[32],
-                                               const uint4 *side_pre = nullptr,
-                                               const float *bias_c = nullptr,
-                                               const float *scale_c = nullptr) {
-  if (a.act > kActRelu)
-    epilogue_slice_t<IS_INT8, true>(a, m, col0, vals, side_pre, bias_c, scale_c);
-  else
-    epilogue_slice_t<IS_INT8, false>(a, m, col0, vals, side_pre, bias_c, scale_c);
 }
 
 // General path: cp.async gather of A by 4 loader warps, 4 epilogue warps.
@@ -663,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
                                          ostage, st_mo, st_ok);
           else if (mvalid)
-            epilogue_slice<IS_INT8>(args, mo, n0 + jj * 32, vals);
+            store_raw_slice<IS_INT8>(args, mo, n0 + jj * 32, vals);
         }
         if (!last) tmem_wait_st();
         tc_fence_before();
@@ -973,7 +937,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                     min(C::kHalfCols, args.K - c0) * (IS_INT8 ? 1 : 2));
       // the side words of the whole row segment, loaded before the wait for
       // the accumulator the outputs come from, so their latency overlaps it
-      constexpr int kSideWords = C::kSlices * SideWords<IS_INT8>::kWords;
+      constexpr int kSideWords = C::kSlices * SliceGroups<IS_INT8>::kGroups;
       uint4 side_pre[kSideWords];
       const bool preload = args.use_side && mvalid && args.mode == kModeFused;
       for (int ch = 0; ch < n_chunks; ++ch) {
@@ -981,7 +945,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < C::kSlices; ++jj)
             load_side_words<IS_INT8>(args, mo, c0 + jj * 32,
-                                     side_pre + jj * SideWords<IS_INT8>::kWords);
+                                     side_pre + jj * SliceGroups<IS_INT8>::kGroups);
         }
         // one outcome for the whole warp: the stores below are warp-wide
         if (!__all_sync(0xffffffffu,
@@ -1004,12 +968,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
             if (args.mode == kModeFused)
               epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals,
-                                           preload ? side_pre + jj * SideWords<IS_INT8>::kWords
+                                           preload ? side_pre + jj * SliceGroups<IS_INT8>::kGroups
                                                    : nullptr,
                                            wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
                                            ostage, st_mo, st_ok);
             else if (mvalid)
-              epilogue_slice<IS_INT8>(args, mo, c0 + jj * 32, vals);
+              store_raw_slice<IS_INT8>(args, mo, c0 + jj * 32, vals);
           }
           tc_fence_before();
           __syncwarp();
@@ -1044,7 +1008,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(sums[jj * 32 + i]);
                 epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals,
-                                             preload ? side_pre + jj * SideWords<IS_INT8>::kWords
+                                             preload ? side_pre + jj * SliceGroups<IS_INT8>::kGroups
                                                      : nullptr,
                                              wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
                                              ostage, st_mo, st_ok);
