@@ -1092,30 +1092,33 @@ __global__ void __launch_bounds__(kPrepThreads)
     // load 64 (rsc) x 64 (k), k fastest: 4 consecutive k per thread
     for (int e = threadIdx.x; e < kPackTile * kPackTile / 4; e += kPrepThreads) {
       const int i = e / (kPackTile / 4), j = (e % (kPackTile / 4)) * 4;
-      const int rsc = rsc0 + i;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int k = k0 + j + t;
-        uint16_t v = 0;
-        if (rsc < RSC && k < K) {
-          int src = rsc;
-          if (map.tap_nR > 0) {
-            // (j, l, c) of the packed filter -> (r, s, c) of the caller's
-            const int C = RSC / (map.tap_nR * map.tap_nS);
-            const int c = rsc % C, jl = rsc / C;
-            const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
-            const int r = map.tap_r0 + map.tap_rstep * (map.tap_nR - 1 - j);
-            const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
-            src = (r * map.tap_S + s2) * C + c;
-          }
-          const long long idx = static_cast<long long>(src) * K + k;
-          if (IS_INT8)
-            v = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<const int8_t *>(w)[idx])));
-          else
-            v = static_cast<const uint16_t *>(w)[idx];
+      const int rsc = rsc0 + i, k = k0 + j;
+      // K is a multiple of 8, so the 4 values are all in range or all out
+      uint16_t v[4] = {0, 0, 0, 0};
+      if (rsc < RSC && k < K) {
+        int src = rsc;
+        if (map.tap_nR > 0) {
+          // (j, l, c) of the packed filter -> (r, s, c) of the caller's
+          const int C = RSC / (map.tap_nR * map.tap_nS);
+          const int c = rsc % C, jl = rsc / C;
+          const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
+          const int r = map.tap_r0 + map.tap_rstep * (map.tap_nR - 1 - j);
+          const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
+          src = (r * map.tap_S + s2) * C + c;
         }
-        tile[i][j + t] = v;
+        const long long idx = static_cast<long long>(src) * K + k;   // a multiple of 4
+        if (IS_INT8) {
+          const uint32_t b4 = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const int8_t *>(w) + idx));
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            v[t] = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<int8_t>(b4 >> (8 * t)))));
+        } else {
+          const uint2 h4 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(w) + idx));
+          v[0] = h4.x & 0xFFFFu; v[1] = h4.x >> 16; v[2] = h4.y & 0xFFFFu; v[3] = h4.y >> 16;
+        }
       }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) tile[i][j + t] = v[t];
     }
     __syncthreads();
     // store transposed: 64 (k) rows of 64 (rsc) 16-bit values, 2 per thread
