@@ -192,6 +192,29 @@ fconv_status fconv_run_accumulators(fconv_plan *plan, const void *x,
                                     size_t workspace_bytes,
                                     fconv_stream_t stream);
 
+/* Batch-norm inference folded into fconv_run_channel_scale's arguments.
+ * "use-fusion-api" (MIOpen), fusion plans: BatchNorm inference is one of
+ * the fusable operators and the convolution-bias-batchnorm-activation
+ * (CBNA) combination is listed for inference; the page gives no formula.
+ * Read as the usual per-channel ("spatial") inference form applied to the
+ * biased conv output, y_k -> gamma_k * (y_k - mean_k) / sqrt(var_k + eps)
+ * + beta_k, which on y_k = acc * conv_scale + bias_k is again an affine map
+ * of acc:
+ *   g_k       = gamma_k / sqrt(var_k + eps)
+ *   scale_out = conv_scale * g_k
+ *   bias_out  = (bias_k - mean_k) * g_k + beta_k
+ * each computed in double and rounded once to float.  A side input keeps
+ * its own scale and is added after the normalisation (the residual add of
+ * a conv-BN-add-Relu block).  All arrays are HOST fp32 [K] and are only
+ * read (bias may be NULL: zero); scale_out and bias_out receive K values
+ * each, for fconv_run_channel_scale's conv_scale and bias (after copying
+ * them to the device).  FCONV_ERR_INVALID_VALUE for K <= 0, a NULL
+ * required pointer, a non-finite or negative eps, or var_k + eps <= 0. */
+fconv_status fconv_fold_batchnorm(int K, float conv_scale, const float *bias,
+                                  const float *gamma, const float *beta,
+                                  const float *mean, const float *var, float eps,
+                                  float *scale_out, float *bias_out);
+
 /* ---- Library-side entry points and controls.  The pages have no
  * counterpart for these: they run the operation above on host buffers,
  * expose and override this implementation's choices (tiles, chunking,

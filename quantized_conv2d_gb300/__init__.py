@@ -79,6 +79,7 @@ def _load():
         "fconv_plan_set_tile_shape": [p, i32, i32],
         "fconv_plan_launch_count": [p, pi],
         "fconv_plan_set_activation_params": [p, f32, f32],
+        "fconv_fold_batchnorm": [i32, f32, p, p, p, p, p, f32, p, p],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -133,6 +134,26 @@ def fconv_plan_output_shape(plan: int):
     _check(_load().fconv_plan_output_shape(plan, *[ctypes.byref(x) for x in v]),
            "fconv_plan_output_shape")
     return tuple(x.value for x in v)
+
+
+def fconv_fold_batchnorm(conv_scale: float, gamma, beta, mean, var, eps: float, bias=None):
+    """fconv_fold_batchnorm on host fp32 vectors [K]: returns (conv_scale_k,
+    bias_k) numpy arrays for fconv_run_channel_scale."""
+    import numpy as np
+    arrs = [np.ascontiguousarray(a, dtype=np.float32) for a in (gamma, beta, mean, var)]
+    K = arrs[0].shape[0]
+    if any(a.shape != (K,) for a in arrs):
+        raise ValueError("gamma, beta, mean and var must be vectors of one length")
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if b is not None and b.shape != (K,):
+        raise ValueError("bias must have the length of gamma")
+    scale_out = np.empty(K, np.float32)
+    bias_out = np.empty(K, np.float32)
+    ptr = lambda a: None if a is None else a.ctypes.data
+    _check(_load().fconv_fold_batchnorm(K, float(conv_scale), ptr(b), *[ptr(a) for a in arrs],
+                                        float(eps), ptr(scale_out), ptr(bias_out)),
+           "fconv_fold_batchnorm")
+    return scale_out, bias_out
 
 
 def fconv_plan_padding(plan: int):

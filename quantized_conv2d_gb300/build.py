@@ -48,7 +48,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    # host arithmetic (the batch-norm fold) rounds every operation on x86
+    # and on Arm alike: no fused multiply-adds from the host compiler
     common = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+              "-Xcompiler", "-ffp-contract=off",
               "-I", os.path.join(ROOT, "include"), "-I", CSRC]
     if verbose:
         common += ["-Xptxas", "-v"]

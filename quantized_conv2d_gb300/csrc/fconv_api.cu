@@ -842,6 +842,25 @@ fconv_status fconv_plan_destroy(fconv_plan *plan) {
   return FCONV_OK;
 }
 
+fconv_status fconv_fold_batchnorm(int K, float conv_scale, const float *bias, const float *gamma,
+                                  const float *beta, const float *mean, const float *var,
+                                  float eps, float *scale_out, float *bias_out) {
+  if (K <= 0) return fail(FCONV_ERR_INVALID_VALUE, "K must be positive");
+  if (!gamma || !beta || !mean || !var || !scale_out || !bias_out)
+    return fail(FCONV_ERR_INVALID_VALUE, "gamma, beta, mean, var and the outputs must not be NULL");
+  if (!std::isfinite(eps) || eps < 0.0f) return fail(FCONV_ERR_INVALID_VALUE, "eps must be >= 0");
+  for (int k = 0; k < K; ++k)
+    if (!(static_cast<double>(var[k]) + eps > 0.0))
+      return fail(FCONV_ERR_INVALID_VALUE, "var + eps must be positive");
+  for (int k = 0; k < K; ++k) {
+    const double g = static_cast<double>(gamma[k]) / std::sqrt(static_cast<double>(var[k]) + eps);
+    const double b = bias ? static_cast<double>(bias[k]) : 0.0;
+    scale_out[k] = static_cast<float>(static_cast<double>(conv_scale) * g);
+    bias_out[k] = static_cast<float>((b - static_cast<double>(mean[k])) * g + beta[k]);
+  }
+  return FCONV_OK;
+}
+
 fconv_status fconv_plan_output_shape(const fconv_plan *plan, int *N, int *P, int *Q, int *K) {
   if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
   if (N) *N = plan->N;

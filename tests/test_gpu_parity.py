@@ -340,6 +340,38 @@ def test_per_channel_conv_scale(i, item):
 
 
 @pytest.mark.parametrize("dtype", ["int8", "bf16"])
+def test_batchnorm_folded_block(dtype):
+    """A conv-BN-add-Relu block: batch-norm inference folded on the host
+    (fconv_fold_batchnorm) into the per-channel scale and bias, then one fused
+    run.  Bit-exact (int8) against the oracle epilogue with the folded
+    parameters, and within one output step of the unfused normalisation
+    evaluated in double."""
+    c = sweep_case(325, (2, 10, 12, 64, 80, 3, 3, 1, "SAME", True, True), dtype)
+    rng = np.random.default_rng(325)
+    K = c.K
+    acc_ref = c.oracle_acc()
+    y_conv = acc_ref.astype(np.float64) * np.float32(c.conv_scale) + c.bias.astype(np.float64)
+    # the batch's own statistics, and a gamma that spreads the int8 outputs
+    mean = y_conv.reshape(-1, K).mean(axis=0).astype(np.float32)
+    var = y_conv.reshape(-1, K).var(axis=0).astype(np.float32)
+    gamma = rng.uniform(10.0, 40.0, K).astype(np.float32) if dtype == "int8" else \
+        rng.uniform(0.5, 2.0, K).astype(np.float32)
+    beta = rng.normal(0, 2.0 if dtype == "int8" else 0.5, K).astype(np.float32)
+    scale_k, bias_k = fc.fconv_fold_batchnorm(c.conv_scale, gamma, beta, mean, var, 1e-5,
+                                              bias=c.bias)
+    c.conv_scale, c.bias = scale_k, bias_k
+    got = c.run_gpu()
+    c.check_output(got, c.oracle_out(acc_ref))
+    if dtype == "int8":
+        # the unfused block in double: normalise, add the scaled side, Relu, round
+        g = gamma.astype(np.float64) / np.sqrt(var.astype(np.float64) + np.float32(1e-5))
+        z = g * (y_conv - mean) + beta + c.side.astype(np.float64) * np.float32(c.side_scale)
+        want = np.clip(np.rint(np.maximum(z, 0.0)), 0, 127)
+        diff = np.abs(got.astype(np.int64) - want.astype(np.int64))
+        assert diff.max() <= 1 and (diff == 0).mean() > 0.99
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
 def test_equal_channel_scales_equal_the_scalar_run(dtype):
     c = sweep_case(320, (2, 10, 10, 64, 96, 3, 3, 1, "SAME", True, True), dtype)
     scalar = c.run_gpu()
