@@ -141,6 +141,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch: a convolution launch may begin (barrier
+// set-up, tensor-memory allocation, descriptor prefetch) while the prep
+// launch before it in the stream still runs.  griddep_wait blocks until that
+// grid has completed and its writes are visible; threads that read what it
+// wrote call it first.  griddep_launch_dependents lets the next launch start
+// once every block of this grid has called it (or finished).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

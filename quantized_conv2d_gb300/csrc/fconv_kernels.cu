@@ -33,6 +33,8 @@
 #include <atomic>
 #include <cstdio>
 
+#include <utility>
+
 #include "fconv_device.cuh"
 #include "fconv_internal.h"
 
@@ -410,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pending = 0;
     bool ok = true;
     const bool drop = (args.debug & 1) != 0;
+    griddep_wait();   // the widened input and packed filter of the prep launch
 
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
       const int m_tile = tile / args.num_n_tiles;
@@ -765,6 +768,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const long long PQ = static_cast<long long>(args.P) * args.Q;
     const int cblocks = args.C / kBK;
     const bool drop = (args.debug & 1) != 0;
+    griddep_wait();   // the widened input and packed filter of the prep launch
     uint32_t stage = 0, phase = 0, issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
@@ -1084,6 +1088,9 @@ __global__ void __launch_bounds__(kPrepThreads)
     prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int RSC, int K, int Kpad,
                 int pack_blocks, const void *__restrict__ xv, __half *__restrict__ xh,
                 long long n8, const WidenMap map) {
+  // the convolution launch behind this one may start its set-up now; it
+  // waits for this grid before reading what it writes
+  griddep_launch_dependents();
   if (static_cast<int>(blockIdx.x) < pack_blocks) {
     __shared__ uint16_t tile[kPackTile][kPackTile + 2];
     const int tiles_k = (K + kPackTile - 1) / kPackTile;
@@ -1213,6 +1220,25 @@ static cudaError_t ensure_smem_limit(Kern kern, int smem, std::atomic<unsigned l
   return e;
 }
 
+// A convolution launch that may overlap the tail of the launch before it in
+// the stream (programmatic stream serialization; the kernels wait for that
+// grid before reading its output).
+template <typename... ExpTypes, typename... ActTypes>
+static cudaError_t launch_overlapping(void (*kern)(ExpTypes...), int grid, int threads, int smem,
+                                     cudaStream_t stream, ActTypes &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<ActTypes>(args)...);
+}
+
 template <int BN, bool IS_INT8>
 static cudaError_t launch_cpasync_t(const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
                                     cudaStream_t stream) {
@@ -1220,8 +1246,7 @@ static cudaError_t launch_cpasync_t(const CUtensorMap &tmap_b, const ConvArgs &a
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg<BN>::kSmemBytes, configured);
   if (e == cudaSuccess) {
-    kern<<<grid, kThreads, Cfg<BN>::kSmemBytes, stream>>>(tmap_b, args);
-    e = cudaGetLastError();
+    e = launch_overlapping(kern, grid, kThreads, Cfg<BN>::kSmemBytes, stream, tmap_b, args);
   }
   if (e != cudaSuccess) note_attributes(kern, kThreads, Cfg<BN>::kSmemBytes);
   return e;
@@ -1250,8 +1275,7 @@ static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tm
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
   if (e == cudaSuccess) {
-    kern<<<grid, kTmaThreads, Cfg::kSmemBytes, stream>>>(tmap_a, tmap_b, args);
-    e = cudaGetLastError();
+    e = launch_overlapping(kern, grid, kTmaThreads, Cfg::kSmemBytes, stream, tmap_a, tmap_b, args);
   }
   if (e != cudaSuccess) note_attributes(kern, kTmaThreads, Cfg::kSmemBytes);
   return e;
