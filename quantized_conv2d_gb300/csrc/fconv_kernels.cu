@@ -1096,12 +1096,12 @@ __global__ void __launch_bounds__(kPrepThreads)
     const int tiles_k = (K + kPackTile - 1) / kPackTile;
     const int rsc0 = (blockIdx.x / tiles_k) * kPackTile;
     const int k0 = (blockIdx.x % tiles_k) * kPackTile;
-    // load 64 (rsc) x 64 (k), k fastest: 4 consecutive k per thread
-    for (int e = threadIdx.x; e < kPackTile * kPackTile / 4; e += kPrepThreads) {
-      const int i = e / (kPackTile / 4), j = (e % (kPackTile / 4)) * 4;
+    // load 64 (rsc) x 64 (k), k fastest: 8 consecutive k per thread (K is a
+    // multiple of 8, so the 8 values are all in range or all out)
+    for (int e = threadIdx.x; e < kPackTile * kPackTile / 8; e += kPrepThreads) {
+      const int i = e / (kPackTile / 8), j = (e % (kPackTile / 8)) * 8;
       const int rsc = rsc0 + i, k = k0 + j;
-      // K is a multiple of 8, so the 4 values are all in range or all out
-      uint16_t v[4] = {0, 0, 0, 0};
+      uint32_t v[4] = {0, 0, 0, 0};   // 8 16-bit values, low half first
       if (rsc < RSC && k < K) {
         int src = rsc;
         if (map.tap_nR > 0) {
@@ -1113,29 +1113,42 @@ __global__ void __launch_bounds__(kPrepThreads)
           const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
           src = (r * map.tap_S + s2) * C + c;
         }
-        const long long idx = static_cast<long long>(src) * K + k;   // a multiple of 4
+        const long long idx = static_cast<long long>(src) * K + k;   // a multiple of 8
         if (IS_INT8) {
-          const uint32_t b4 = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const int8_t *>(w) + idx));
+          const uint2 b8 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(w) + idx));
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            v[t] = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<int8_t>(b4 >> (8 * t)))));
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t word = t < 2 ? b8.x : b8.y;
+            const int sh = 16 * (t & 1);
+            const uint32_t lo = __half_as_ushort(
+                __int2half_rn(static_cast<int>(static_cast<int8_t>(word >> sh))));
+            const uint32_t hi = __half_as_ushort(
+                __int2half_rn(static_cast<int>(static_cast<int8_t>(word >> (sh + 8)))));
+            v[t] = lo | (hi << 16);
+          }
         } else {
-          const uint2 h4 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(w) + idx));
-          v[0] = h4.x & 0xFFFFu; v[1] = h4.x >> 16; v[2] = h4.y & 0xFFFFu; v[3] = h4.y >> 16;
+          const uint4 h8 = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(w) + idx));
+          v[0] = h8.x; v[1] = h8.y; v[2] = h8.z; v[3] = h8.w;
         }
       }
+      // a row is 66 halves (132 bytes): j even keeps the words 4-byte aligned
+      uint32_t *row = reinterpret_cast<uint32_t *>(&tile[i][j]);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) tile[i][j + t] = v[t];
+      for (int t = 0; t < 4; ++t) row[t] = v[t];
     }
     __syncthreads();
-    // store transposed: 64 (k) rows of 64 (rsc) 16-bit values, 2 per thread
-    for (int e = threadIdx.x; e < kPackTile * kPackTile / 2; e += kPrepThreads) {
-      const int kk = e / (kPackTile / 2), j = (e % (kPackTile / 2)) * 2;
+    // store transposed: 64 (k) rows of 64 (rsc) 16-bit values, 8 per thread
+    // (one 16-byte store; Kpad and rsc0 are multiples of 64)
+    for (int e = threadIdx.x; e < kPackTile * kPackTile / 8; e += kPrepThreads) {
+      const int kk = e / (kPackTile / 8), j = (e % (kPackTile / 8)) * 8;
       const int k = k0 + kk, rsc = rsc0 + j;
       if (k < K && rsc < Kpad) {
-        const uint32_t v = static_cast<uint32_t>(tile[j][kk]) |
-                           (static_cast<uint32_t>(tile[j + 1][kk]) << 16);
-        *reinterpret_cast<uint32_t *>(wt + static_cast<long long>(k) * Kpad + rsc) = v;
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          o[t] = static_cast<uint32_t>(tile[j + 2 * t][kk]) |
+                 (static_cast<uint32_t>(tile[j + 2 * t + 1][kk]) << 16);
+        stg_v4(wt + static_cast<long long>(k) * Kpad + rsc, make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
     return;
