@@ -376,23 +376,29 @@ def run_fconv(args, rank, world, local_rank):
                         + (" after an L2-flush node, flush time subtracted" if flush is not None
                            else "")}
         if flush is not None:
-            # the same replay without the flush: inputs left in L2 by the step before
+            # the same steps without the flush, inputs left in L2 by the step
+            # before; 20 steps a graph so that the host's replay calls do not
+            # pace the GPU
+            per = 20
             gw = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gw):
-                step(torch.cuda.current_stream(dev))
+                for _ in range(per):
+                    step(torch.cuda.current_stream(dev))
             gw.replay()
             torch.cuda.synchronize(dev)
+            reps = max(1, args.steps // per)
             w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier()
             w0.record(stream)
-            for _ in range(args.steps):
+            for _ in range(reps):
                 gw.replay()
             w1.record(stream)
             torch.cuda.synchronize(dev)
             plan.check()
             warm_ms = reduce_max(w0.elapsed_time(w1), dev)
-            graph["warm_l2"] = {"value": weak_scaling_tops(world, args.steps, nominal, warm_ms),
-                                "ms_per_step": warm_ms / args.steps}
+            graph["warm_l2"] = {"value": weak_scaling_tops(world, reps * per, nominal, warm_ms),
+                                "ms_per_step": warm_ms / (reps * per),
+                                "how": f"{per} steps a graph, replayed {reps} times"}
 
     # ------------------------------------------------ end to end, host buffers
     e2e = None
