@@ -175,36 +175,57 @@ def weak_scaling_tops(world: int, steps: int, ops_per_step: float, max_ms: float
 
 
 # ---------------------------------------------------------------- CPU oracle timing
+class OracleSample:
+    """The CPU oracle on a bounded sample of a workload: whole images, all
+    channels, full epilogue.  Inputs are drawn once per sample size (their
+    generation is not timed)."""
+
+    def __init__(self, wl, P, Q):
+        import oracle
+        oracle.build()
+        self.oracle, self.wl, self.P, self.Q = oracle, wl, P, Q
+        self.pad = oracle.SAME if wl.padding == "SAME" else oracle.VALID
+        self.inputs = {}
+
+    def run(self, n):
+        """Seconds for one oracle pass over n images."""
+        orc, wl = self.oracle, self.wl
+        if n not in self.inputs:
+            self.inputs = {n: FI.generate(wl, (self.P, self.Q), batch=n)}
+        inp = self.inputs[n]
+        t0 = time.perf_counter()
+        if wl.transposed_pads is not None:
+            acc = (orc.convT_acc_i8 if wl.dtype == "int8" else orc.convT_acc_bf16_f64)(
+                inp["x"], inp["w"], wl.stride, wl.transposed_pads)
+        elif wl.dtype == "int8":
+            acc = orc.conv_acc_i8(inp["x"], inp["w"], wl.stride, self.pad)
+        else:
+            acc = orc.conv_acc_bf16_f64(inp["x"], inp["w"], wl.stride, self.pad)
+        if wl.dtype == "int8":
+            orc.epilogue_i8(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale, wl.relu)
+        else:
+            orc.epilogue_f64(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale, wl.relu)
+        return time.perf_counter() - t0
+
+    def images_for(self, target_s: float) -> int:
+        """Whole images whose oracle pass takes about target_s (at least 1)."""
+        t1 = self.run(1)
+        return int(max(1, min(self.wl.N, target_s / max(t1, 1e-6))))
+
+    def tops(self, n: int, seconds: float) -> float:
+        return ops_counts(self.wl)[0] / self.wl.N * n / seconds / 1e12
+
+    def threads(self) -> int:
+        return self.oracle.num_threads()
+
+
 def time_oracle(wl, P, Q, target_s: float, max_images: int):
     """Time the CPU oracle on a bounded sample (whole images of the workload,
     all channels, full epilogue).  Returns (TOPS nominal, images, seconds, threads)."""
-    import oracle
-    oracle.build()
-    pad = oracle.SAME if wl.padding == "SAME" else oracle.VALID
-
-    def run(n):
-        inp = FI.generate(wl, (P, Q), batch=n)
-        t0 = time.perf_counter()
-        if wl.transposed_pads is not None:
-            acc = (oracle.convT_acc_i8 if wl.dtype == "int8" else oracle.convT_acc_bf16_f64)(
-                inp["x"], inp["w"], wl.stride, wl.transposed_pads)
-        elif wl.dtype == "int8":
-            acc = oracle.conv_acc_i8(inp["x"], inp["w"], wl.stride, pad)
-        else:
-            acc = oracle.conv_acc_bf16_f64(inp["x"], inp["w"], wl.stride, pad)
-        if wl.dtype == "int8":
-            oracle.epilogue_i8(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale,
-                               wl.relu)
-        else:
-            oracle.epilogue_f64(acc, inp["bias"], inp["side"], wl.conv_scale, wl.side_scale,
-                                wl.relu)
-        return time.perf_counter() - t0
-
-    t1 = run(1)
-    n = int(max(1, min(max_images, target_s / max(t1, 1e-6))))
-    t = run(n) if n > 1 else t1
-    per_image = ops_counts(wl)[0] / wl.N
-    return per_image * n / t / 1e12, n, t, oracle.num_threads()
+    sample = OracleSample(wl, P, Q)
+    n = min(max_images, sample.images_for(target_s))
+    t = sample.run(n)
+    return sample.tops(n, t), n, t, sample.threads()
 
 
 # ---------------------------------------------------------------- arms
@@ -213,12 +234,17 @@ def run_reference(args, rank, world):
         return
     wl = FI.workload(args.workload)
     _, _, P, Q = ops_counts(wl)
+    # each step one oracle pass over the same bounded sample, sized so that
+    # all steps together take about 150 s
     step_target = min(2.0, 150.0 / max(1, args.steps + args.warmup))
-    values, secs, n_img, threads = [], [], 1, 1
+    sample = OracleSample(wl, P, Q)
+    n_img = sample.images_for(step_target)
+    threads = sample.threads()
+    values, secs = [], []
     for i in range(args.warmup + args.steps):
-        v, n_img, t, threads = time_oracle(wl, P, Q, step_target, wl.N)
+        t = sample.run(n_img)
         if i >= args.warmup:
-            values.append(v)
+            values.append(sample.tops(n_img, t))
             secs.append(t)
     value = statistics.median(values)
     sample = f"{n_img} of {wl.N} images per step (all {wl.K} channels, full epilogue)"
