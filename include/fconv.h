@@ -163,7 +163,12 @@ fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes);
  * conv_scale, side_scale: host scalars (the TensorFlow GPU helper reads
  * them as host scalars too).  workspace: device, 256-byte aligned,
  * workspace_bytes >= fconv_workspace_size().  x/w must not alias y or
- * the workspace.  Asynchronous; returns after enqueueing. */
+ * the workspace.  Asynchronous; returns after enqueueing.  A run is a
+ * prep launch and the convolution launch (fconv_plan_launch_count); the
+ * second is a programmatic dependent of the first, which lets it start
+ * its set-up while the first finishes; it reads nothing the first writes
+ * before that grid has completed, and ordering against the caller's other
+ * work on the stream is that of two plain launches. */
 fconv_status fconv_run(fconv_plan *plan, const void *x, const void *w,
                        const float *bias, const void *side, float conv_scale,
                        float side_scale, void *y, void *workspace,
