@@ -380,6 +380,29 @@ def test_equal_channel_scales_equal_the_scalar_run(dtype):
 
 
 
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+def test_back_to_back_runs_share_the_workspace(dtype):
+    """Runs enqueued back to back on one stream reuse the plan's workspace:
+    each convolution (launched as a dependent of its prep launch) must read
+    its own prep's output, and finish before the next prep overwrites it.
+    Two input sets alternate over 16 runs without a synchronisation."""
+    params = (2, 10, 10, 64, 96, 3, 3, 1, "SAME", True, True)
+    cases = [sweep_case(340, params, dtype), sweep_case(341, params, dtype)]
+    p = cases[0].plan()
+    ins = [(to_dev(c.x, dtype), to_dev(c.w, dtype), torch.from_numpy(c.bias).cuda(),
+            to_dev(c.side, dtype)) for c in cases]
+    ys = [p.new_output() for _ in range(16)]
+    for i, y in enumerate(ys):
+        x, w, bias, side = ins[i % 2]
+        p.run(x, w, bias, side, cases[0].conv_scale, cases[0].side_scale, y=y)
+    torch.cuda.synchronize()
+    p.check()
+    refs = [c.oracle_out(c.oracle_acc()) for c in cases]
+    for i, y in enumerate(ys):
+        cases[i % 2].check_output(to_host(y), refs[i % 2])
+    p.close()
+
+
 def test_run_replays_from_a_cuda_graph():
     """A captured fconv_run replays on new contents of the same buffers."""
     params = (2, 10, 10, 64, 96, 3, 3, 1, "SAME", True, True)
