@@ -321,6 +321,19 @@ fconv_status fconv_run_no_alloc(fconv_plan *plan, const void *x, const void *w,
                                 float conv_scale, float side_scale, void *y,
                                 fconv_stream_t stream);
 
+/* Split-K for the plan's current tile: each output tile's k-blocks are
+ * divided over `splits` CTAs (1: none; 0: the automatic choice made at
+ * plan creation, tile included); every unit writes its partial sums to the
+ * workspace and the last of a tile's units to finish adds them in split
+ * order (int32 sums exactly, fp32 sums in that fixed order) and runs the
+ * epilogue, so no CTA waits on another.  Forward plans on the TMA im2col
+ * gather with 128-pixel tiles only (FCONV_ERR_NOT_SUPPORTED otherwise, and
+ * for more splits than the plan has k-blocks); at most 8.  fconv_plan_set_tile and
+ * fconv_plan_set_tile_shape reset it to 1.  The workspace size changes with
+ * it: query fconv_workspace_size after setting it. */
+fconv_status fconv_plan_set_splits(fconv_plan *plan, int splits);
+fconv_status fconv_plan_get_splits(const fconv_plan *plan, int *splits);
+
 /* Number of kernel launches one fconv_run (or fconv_run_channel_scale,
  * fconv_run_accumulators) on this plan enqueues: the operand preparation and
  * the convolution, per phase for a strided transposed plan, plus a small

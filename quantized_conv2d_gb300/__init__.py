@@ -80,6 +80,8 @@ def _load():
         "fconv_plan_launch_count": [p, pi],
         "fconv_plan_set_activation_params": [p, f32, f32],
         "fconv_fold_batchnorm": [i32, f32, p, p, p, p, p, f32, p, p],
+        "fconv_plan_set_splits": [p, i32],
+        "fconv_plan_get_splits": [p, pi],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -234,6 +236,16 @@ def fconv_plan_kernel(plan) -> str:
 
 def fconv_plan_check(plan, stream) -> None:
     _check(_load().fconv_plan_check(plan, stream), "fconv_plan_check")
+
+
+def fconv_plan_set_splits(plan, splits: int) -> None:
+    _check(_load().fconv_plan_set_splits(plan, splits), "fconv_plan_set_splits")
+
+
+def fconv_plan_get_splits(plan) -> int:
+    v = ctypes.c_int()
+    _check(_load().fconv_plan_get_splits(plan, ctypes.byref(v)), "fconv_plan_get_splits")
+    return v.value
 
 
 def fconv_plan_set_tile(plan, block_n: int) -> None:

@@ -27,7 +27,9 @@ struct fconv_plan {
   int Ktot, num_kb, Kpad;
   int block_n, kb_chunk, num_n_tiles, num_tiles;
   int m_sub;            // 128-pixel sub-tiles per output tile (1 or 2)
-  int auto_block_n, auto_m_sub;
+  int splits;           // split-K units per tile (1: none; TMA gather only)
+  int auto_splits;
+  int auto_block_n, auto_m_sub;  // the automatic tile (and auto_splits)
   uint32_t timeout_ms;
   int debug;
   size_t wt_bytes, xh_bytes;
@@ -98,6 +100,12 @@ fconv_status cuda_fail(cudaError_t e, const char *what) {
 
 constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 constexpr long long kLimit = 0x7FFFFFFFLL;
+// split-K: at most this many units per tile, each of at least
+// kMinSplitKBlocks k-blocks; one completion counter per tile and TMA
+// epilogue warp
+constexpr int kMaxSplits = 8;
+constexpr int kMinSplitKBlocks = 4;
+constexpr int kSplitCountersPerTile = 8;
 
 // Output extent and padding split of one axis under TensorFlow's rule:
 // SAME keeps ceil(in / stride) outputs and pads max(0, (out-1)*stride +
@@ -176,13 +184,18 @@ fconv::Gather gather_for_run(const fconv_plan &p) {
 // ~450 with two, ~800 on the cp.async path; measured).  Tiles run in waves
 // over the SMs; the epilogue of a CTA's last tile (~8 cycles per output
 // column per 128 pixels) is not hidden behind a next tile's mainloop.
+// Split-K (splits > 1 units per tile, TMA gather, forward plans): a unit
+// runs ceil(num_kb / splits) k-blocks; every unit writes its partial sums
+// (128*MS x BN 32-bit words) and the last to finish reads all of them
+// back, ~8 cycles per output column per 128 pixels per split at an SM's
+// ~64 bytes per cycle from L2, before the epilogue.
 struct TileChoice {
-  int bn, ms;
+  int bn, ms, splits;
 };
 TileChoice choose_tile(const fconv_plan &p, int sms) {
   const bool chunked = p.kb_chunk < p.num_kb;
   const int kp = (p.K + 31) / 32 * 32;
-  TileChoice best = {32, 1};
+  TileChoice best = {32, 1, 1};
   long long best_cost = -1;
   for (int bn : {256, 128, 64, 32}) {
     for (int ms : {1, 2}) {
@@ -193,21 +206,35 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
           g == fconv::Gather::kTmaIm2col ? (ms == 2 ? 450 : 360) : 800;
       const long long m_tiles = (p.M + 128LL * ms - 1) / (128LL * ms);
       const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
-      const long long waves = (tiles + sms - 1) / sms;
       const long long work = 2LL * bn * ms;
-      const long long cost = waves * p.num_kb * (work > fixed ? work : fixed) + 8LL * bn * ms;
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best = {bn, ms};
+      const bool can_split = g == fconv::Gather::kTmaIm2col && !p.transposed && ms == 1;
+      for (int sp = 1; sp <= (can_split ? kMaxSplits : 1); ++sp) {
+        if (sp > 1 && (tiles * sp > sms || p.num_kb < kMinSplitKBlocks * sp)) break;
+        const long long units = tiles * sp;
+        const long long waves = (units + sms - 1) / sms;
+        const long long kbs = (p.num_kb + sp - 1) / sp;
+        const long long cost = waves * kbs * (work > fixed ? work : fixed) + 8LL * bn * ms +
+                               (sp > 1 ? 8LL * bn * ms * (sp + 1) : 0);
+        if (best_cost < 0 || cost < best_cost) {
+          best_cost = cost;
+          best = {bn, ms, sp};
+        }
       }
     }
   }
   return best;
 }
 
-void set_tiling(fconv_plan &p, int bn, int ms = 1) {
+void set_tiling(fconv_plan &p, int bn, int ms = 1, int splits = 1) {
   p.block_n = bn;
   p.m_sub = ms;
+  // no empty unit: with ceil(num_kb / splits) k-blocks a unit, that many
+  // units cover the tile (9 k-blocks asked in 4 splits run as 3 of 3)
+  if (splits > 1) {
+    const int per = (p.num_kb + splits - 1) / splits;
+    splits = (p.num_kb + per - 1) / per;
+  }
+  p.splits = splits < 1 ? 1 : splits;
   p.num_n_tiles = (p.K + bn - 1) / bn;
   p.num_tiles = static_cast<int>((p.M + 128LL * ms - 1) / (128LL * ms)) * p.num_n_tiles;
 }
@@ -267,8 +294,21 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // Scratch a run needs: the packed filter, and for int8 plans the fp16 copy of
 // the input the gathers read.
+// Split-K scratch after the operand copies: every unit's partial block
+// (128 * m_sub * block_n 32-bit words), then one counter per tile and
+// epilogue warp.
+size_t split_partial_offset(const fconv_plan &p) {
+  const size_t a = p.ws_wt_off + p.wt_bytes, b = p.ws_xh_off + p.xh_bytes;
+  return align_up(a > b ? a : b, 256);
+}
+size_t split_partial_bytes(const fconv_plan &p) {
+  return align_up(static_cast<size_t>(p.num_tiles) * p.splits * 128 * p.m_sub * p.block_n * 4, 256);
+}
 size_t workspace_need(const fconv_plan &p) {
   const size_t a = p.ws_wt_off + p.wt_bytes, b = p.ws_xh_off + p.xh_bytes;
+  if (p.splits > 1)
+    return split_partial_offset(p) + split_partial_bytes(p) +
+           align_up(static_cast<size_t>(p.num_tiles) * kSplitCountersPerTile * 4, 256);
   return a > b ? a : b;
 }
 
@@ -363,7 +403,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   const fconv::Gather gather = gather_for_run(*p);
   // two 128-pixel sub-tiles exist on the TMA gather only: a plan forced onto
   // the cp.async gather (a test hook) runs one
-  if (gather == fconv::Gather::kCpAsync && p->m_sub != 1) set_tiling(*p, p->block_n, 1);
+  if (gather == fconv::Gather::kCpAsync && (p->m_sub != 1 || p->splits != 1))
+    set_tiling(*p, p->block_n, 1, 1);
   if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb, p->m_sub))
     return fail(FCONV_ERR_NOT_SUPPORTED,
                 "tile %d has no cp.async kernel for a sum of %d k-values (chunked sums need "
@@ -379,6 +420,17 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   const bool do_copy = copy && !skip_copy;            // ... made by this launch
   const void *act = x;
   const long long n = static_cast<long long>(p->N) * gH * gW * p->C;
+  // split-K scratch: partial sums, then the completion counters (zeroed by
+  // the prep launch of every run)
+  uint32_t *split_partial = nullptr;
+  int *split_counters = nullptr;
+  if (p->splits > 1) {
+    uint8_t *base = static_cast<uint8_t *>(workspace) + split_partial_offset(*p);
+    split_partial = reinterpret_cast<uint32_t *>(base);
+    split_counters = reinterpret_cast<int *>(base + split_partial_bytes(*p));
+    if (skip_pack && !do_copy)
+      return fail(FCONV_ERR_INTERNAL, "a split-K run needs its prep launch");
+  }
   if (!skip_pack || do_copy) {
     fconv::WidenMap map;
     memset(&map, 0, sizeof map);
@@ -390,7 +442,9 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     map.tap_r0 = p->tap_r0; map.tap_s0 = p->tap_s0;
     map.tap_rstep = p->tap_rstep; map.tap_sstep = p->tap_sstep;
     e = fconv::launch_prep(is_int8, skip_pack ? nullptr : w, wt, p->Ktot, skip_pack ? 0 : p->K,
-                           p->Kpad, x, xh, do_copy ? n : 0, map, sms, stream);
+                           p->Kpad, x, xh, do_copy ? n : 0, map, split_counters,
+                           split_counters ? p->num_tiles * kSplitCountersPerTile : 0, sms,
+                           stream);
     if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
   }
   if (copy) act = xh;
@@ -486,7 +540,12 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.mode = mode;
   a.debug = p->debug;
   a.timeout_ns = static_cast<unsigned long long>(p->timeout_ms) * 1000000ull;
-  const int grid = a.num_tiles < sms ? a.num_tiles : sms;
+  a.splits = p->splits;
+  a.kb_per_split = (p->num_kb + p->splits - 1) / p->splits;
+  a.partial = split_partial;
+  a.counters = split_counters;
+  const long long units = static_cast<long long>(a.num_tiles) * a.splits;
+  const int grid = units < sms ? static_cast<int>(units) : sms;
   e = fconv::launch_conv(p->block_n, p->m_sub, is_int8, gather, tmap_a, tmap, a, grid, stream);
   if (e != cudaSuccess)
     return fail(FCONV_ERR_CUDA, "convolution launch: %s (%s)", cudaGetErrorString(e),
@@ -670,7 +729,8 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   const TileChoice tile = choose_tile(p, sm_count_of_current_device(148));
   p.auto_block_n = tile.bn;
   p.auto_m_sub = tile.ms;
-  set_tiling(p, tile.bn, tile.ms);
+  p.auto_splits = tile.splits;
+  set_tiling(p, tile.bn, tile.ms, tile.splits);
   p.timeout_ms = 2000;
   p.host_chunks = 0;
   p.pipe_dev = -1;
@@ -1066,7 +1126,7 @@ fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
     return FCONV_OK;
   }
   if (block_n == 0) {
-    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub);
+    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits);
     return FCONV_OK;
   }
   if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256)
@@ -1099,6 +1159,34 @@ fconv_status fconv_plan_set_tile_shape(fconv_plan *plan, int pixels, int channel
     return fail(FCONV_ERR_NOT_SUPPORTED, "no kernel for %d x %d tiles on this plan", pixels,
                 channels);
   set_tiling(*plan, channels, ms);
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_splits(fconv_plan *plan, int splits) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (splits < 0 || splits > kMaxSplits)
+    return fail(FCONV_ERR_INVALID_VALUE, "splits %d: 0 (automatic) or 1 to %d", splits, kMaxSplits);
+  if (splits == 0) {
+    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits);
+    return FCONV_OK;
+  }
+  if (splits > 1) {
+    if (plan->transposed || plan->num_phases > 0)
+      return fail(FCONV_ERR_NOT_SUPPORTED, "split-K is for forward convolution plans");
+    if (gather_for(*plan, plan->block_n, false) != fconv::Gather::kTmaIm2col)
+      return fail(FCONV_ERR_NOT_SUPPORTED, "split-K runs on the TMA im2col gather only");
+    if (plan->m_sub != 1)
+      return fail(FCONV_ERR_NOT_SUPPORTED, "split-K runs on 128-pixel tiles");
+    if (splits > plan->num_kb)
+      return fail(FCONV_ERR_NOT_SUPPORTED, "%d splits of %d k-blocks", splits, plan->num_kb);
+  }
+  set_tiling(*plan, plan->block_n, plan->m_sub, splits);
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_get_splits(const fconv_plan *plan, int *splits) {
+  if (!plan || !splits) return fail(FCONV_ERR_INVALID_VALUE, "plan and splits must not be NULL");
+  *splits = plan->splits > 0 ? plan->splits : 1;
   return FCONV_OK;
 }
 

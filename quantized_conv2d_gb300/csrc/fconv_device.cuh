@@ -336,6 +336,17 @@ __device__ __forceinline__ void prefetch_l2(const void *p, int bytes) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
 }
 
+// A load served from L2 (not a possibly stale L1 line): data another SM
+// wrote in this launch.  Volatile, so it stays after the fence before it.
+__device__ __forceinline__ uint4 ldcg_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+
 __device__ __forceinline__ void stg_v4(void *p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)

@@ -45,6 +45,14 @@ struct ConvArgs {
   int mode;
   int debug;
   unsigned long long timeout_ns;
+  // split-K (TMA kernel): each tile's k-blocks in `splits` units of
+  // kb_per_split; every unit writes its 32-bit partial sums (int32 for int8
+  // plans, fp32 for bf16) to `partial`, and the last unit of a tile portion
+  // to arrive (counted in `counters`, zeroed by the prep launch) adds them
+  // in split order and runs the epilogue.  splits == 1: no partials.
+  int splits, kb_per_split;
+  uint32_t *partial;
+  int *counters;
 };
 
 // How the kernel gathers the A (activation) tile of each k-block.
@@ -94,9 +102,10 @@ struct WidenMap {
 // the int8 -> fp16 widening of the input (n elements of the copy, a multiple
 // of 16), in one launch (a second, tiny one when a dense n is not a multiple
 // of 64).
+// zero / zero_n: split-K counters the launch clears (nullptr, 0: none).
 cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
                         const void *x, __half *xh, long long n, const WidenMap &map,
-                        int sm_count, cudaStream_t stream);
+                        int *zero, int zero_n, int sm_count, cudaStream_t stream);
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out);
 // Resource description of the kernel whose launch failed last on this thread.
 const char *last_launch_note();

@@ -709,7 +709,9 @@ struct TmaCfg {
   static_assert(kStages >= 3, "pipeline too shallow");
 };
 
-template <int BN, bool IS_INT8, int MS>
+// SPLITK: the split-K form (units of kb_per_split k-blocks, partial sums
+// and the last unit's reduction); the other instance keeps one unit a tile.
+template <int BN, bool IS_INT8, int MS, bool SPLITK>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     conv_fprop_tma_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
@@ -757,8 +759,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t tmem_base = __shfl_sync(0xffffffffu, bars->tmem_base, 0);
 
   const int num_kb = args.num_kb;
+  const int splits = SPLITK ? args.splits : 1;
+  const int kb_per_split = SPLITK ? args.kb_per_split : num_kb;
   const int kb_chunk = args.kb_chunk;
-  const int n_chunks = (num_kb + kb_chunk - 1) / kb_chunk;
 
   if (warp < kTmaEpiWarp0) {
    setmaxnreg_dec<kTmaCtlRegs>();
@@ -771,7 +774,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     griddep_wait();   // the widened input and packed filter of the prep launch
     uint32_t stage = 0, phase = 0, issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+    const int num_units = args.num_tiles * splits;
+    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      // unit: one split (a run of k-blocks) of one tile
+      const int tile = unit / splits;
+      const int ukb0 = (unit - tile * splits) * kb_per_split;
+      const int ukb1 = min(num_kb, ukb0 + kb_per_split);
       const int m_tile = tile / args.num_n_tiles;
       const int n_tile = tile - m_tile * args.num_n_tiles;
       // filter-window origin of each sub-tile's first output pixel (a
@@ -786,8 +794,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         w0[u] = q0 * args.sw - args.pl;
         h0[u] = p0 * args.sh - args.pt;
       }
-      int r = 0, s = 0, cb = 0;   // filter tap and channel block of k-block kb
-      for (int kb = 0; kb < num_kb; ++kb) {
+      // filter tap and channel block of k-block kb (tap-major, channels fastest)
+      int cb = ukb0 % cblocks, s = (ukb0 / cblocks) % args.S, r = ukb0 / cblocks / args.S;
+      for (int kb = ukb0; kb < ukb1; ++kb) {
         if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
           ok = false;
           break;
@@ -829,9 +838,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // bounds tiles narrower than 256).
     uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
-      for (int kb0 = 0; kb0 < num_kb && ok; kb0 += kb_chunk) {
-        const int kb1 = min(kb0 + kb_chunk, num_kb);
+    const int num_units = args.num_tiles * splits;
+    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      const int ukb0 = (unit % splits) * kb_per_split;
+      const int ukb1 = min(num_kb, ukb0 + kb_per_split);
+      for (int kb0 = ukb0; kb0 < ukb1 && ok; kb0 += kb_chunk) {
+        const int kb1 = min(kb0 + kb_chunk, ukb1);
         if (!mbar_wait_warp(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo)) {
           ok = false;
           break;
@@ -912,9 +924,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // this warp's staging buffer for the coalesced output stores
     uint4 *ostage = reinterpret_cast<uint4 *>(smem + C::kOutOffset) +
                     (warp - kTmaEpiWarp0) * C::kOutWarpBytes / 16;
+    const int ew = warp - kTmaEpiWarp0;
+    const int num_units = args.num_tiles * splits;
     uint32_t astage = 0, aphase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
+    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      const int tile = unit / splits;
+      const int ukb0 = (unit - tile * splits) * kb_per_split;
+      const int uchunks = (min(num_kb, ukb0 + kb_per_split) - ukb0 + kb_chunk - 1) / kb_chunk;
+      // split-K: this unit's block of partial sums (this warp's rows and
+      // columns; slice jj, 4-column group g, lane l at ((jj*8 + g)*32 + l)*4)
+      uint32_t *const wpart =
+          args.partial + (static_cast<size_t>(unit) * kTmaEpiWarps + ew) * 32 * C::kHalfCols;
       const int m_tile = tile / args.num_n_tiles;
       const int n_tile = tile - m_tile * args.num_n_tiles;
       const long long m = static_cast<long long>(m_tile) * kTileM + row;
@@ -943,9 +964,63 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       // the accumulator the outputs come from, so their latency overlaps it
       constexpr int kSideWords = C::kSlices * SliceGroups<IS_INT8>::kGroups;
       uint4 side_pre[kSideWords];
-      const bool preload = args.use_side && mvalid && args.mode == kModeFused;
-      for (int ch = 0; ch < n_chunks; ++ch) {
-        if (ch == n_chunks - 1 && preload) {
+      const bool preload = args.use_side && mvalid && args.mode == kModeFused && splits == 1;
+      // split-K: count this warp's partial in; the last unit of the tile
+      // portion to arrive adds all partials in split order and stores
+      auto finish_split = [&]() {
+        __threadfence();   // this lane's partial words before the count
+        __syncwarp();
+        int* const counter = args.counters + tile * kTmaEpiWarps + ew;
+        int old = 0;
+        if (lane == 0) old = atomicAdd(counter, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != splits - 1) return;   // a later unit finishes this portion
+        if (lane == 0) atomicExch(counter, 0);   // zero again for the next run
+        __threadfence();   // the other units' partial words after the count
+        __syncwarp();
+        const uint32_t *part0 =
+            args.partial + (static_cast<size_t>(tile) * splits * kTmaEpiWarps + ew) * 32 *
+                               C::kHalfCols;
+        const size_t split_words = static_cast<size_t>(kTmaEpiWarps) * 32 * C::kHalfCols;
+#pragma unroll 1
+        for (int jj = 0; jj < C::kSlices; ++jj) {
+          uint32_t t[32];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const size_t off = static_cast<size_t>((jj * 8 + g) * 32 + lane) * 4;
+            uint4 acc = ldcg_v4(part0 + off);
+            for (int j = 1; j < splits; ++j) {
+              const uint4 q = ldcg_v4(part0 + j * split_words + off);
+              if (IS_INT8) {   // int32 sums: exact in any order
+                acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+              } else {         // fp32 sums: added in split order
+                acc.x = __float_as_uint(__fadd_rn(__uint_as_float(acc.x), __uint_as_float(q.x)));
+                acc.y = __float_as_uint(__fadd_rn(__uint_as_float(acc.y), __uint_as_float(q.y)));
+                acc.z = __float_as_uint(__fadd_rn(__uint_as_float(acc.z), __uint_as_float(q.z)));
+                acc.w = __float_as_uint(__fadd_rn(__uint_as_float(acc.w), __uint_as_float(q.w)));
+              }
+            }
+            t[4 * g + 0] = acc.x; t[4 * g + 1] = acc.y; t[4 * g + 2] = acc.z; t[4 * g + 3] = acc.w;
+          }
+          float vals[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            vals[i] = IS_INT8 ? __int2float_rn(static_cast<int>(t[i]))
+                              : __fadd_rn(__uint_as_float(t[i]), 0.0f);
+          if (args.mode == kModeAccumulators) {
+            if (mvalid) {
+              if (IS_INT8) store_i32_slice(args, mo, c0 + jj * 32, t);
+              else store_raw_slice<IS_INT8>(args, mo, c0 + jj * 32, vals);
+            }
+          } else {
+            epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals, nullptr,
+                                         wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
+                                         ostage, st_mo, st_ok);
+          }
+        }
+      };
+      for (int ch = 0; ch < uchunks; ++ch) {
+        if (ch == uchunks - 1 && preload) {
 #pragma unroll
           for (int jj = 0; jj < C::kSlices; ++jj)
             load_side_words<IS_INT8>(args, mo, c0 + jj * 32,
@@ -959,7 +1034,29 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         tc_fence_after();
         const uint32_t t_acc = tmem_base + lane_off + astage * C::kAccCols + tcol;
-        if (n_chunks == 1) {
+        if (SPLITK && uchunks == 1) {
+          // split-K, one chunk: the unit's sums (int32 for int8 plans, exact
+          // here) from TMEM to its partial block, then the count
+#pragma unroll
+          for (int jj = 0; jj < C::kSlices; ++jj) {
+            uint32_t v[32];
+            tmem_ld32(t_acc + jj * 32, v);
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = IS_INT8 ? static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[4 * g + e])))
+                                : v[4 * g + e];
+              stg_v4(wpart + ((jj * 8 + g) * 32 + lane) * 4, make_uint4(w4[0], w4[1], w4[2], w4[3]));
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[astage]));
+          finish_split();
+        } else if (uchunks == 1) {
           // the whole sum is in TMEM: epilogue straight from it
 #pragma unroll
           for (int jj = 0; jj < C::kSlices; ++jj) {
@@ -999,7 +1096,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[astage]));
-          if (ch == n_chunks - 1) {   // the whole warp: the fused stores are coalesced
+          if (SPLITK && ch == uchunks - 1) {
+            // split-K: the unit's int32 sums to its partial block, then the count
+#pragma unroll
+            for (int jj = 0; jj < C::kSlices; ++jj)
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                const int b = jj * 32 + 4 * g;
+                stg_v4(wpart + ((jj * 8 + g) * 32 + lane) * 4,
+                       make_uint4(static_cast<uint32_t>(sums[b]), static_cast<uint32_t>(sums[b + 1]),
+                                  static_cast<uint32_t>(sums[b + 2]),
+                                  static_cast<uint32_t>(sums[b + 3])));
+              }
+            finish_split();
+          } else if (ch == uchunks - 1) {   // the whole warp: the fused stores are coalesced
 #pragma unroll
             for (int jj = 0; jj < C::kSlices; ++jj) {
               if (args.mode == kModeAccumulators) {
@@ -1087,10 +1197,12 @@ template <bool IS_INT8, bool MAPPED>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int RSC, int K, int Kpad,
                 int pack_blocks, const void *__restrict__ xv, __half *__restrict__ xh,
-                long long n8, const WidenMap map) {
+                long long n8, const WidenMap map, int *__restrict__ zero, int zero_n) {
   // the convolution launch behind this one may start its set-up now; it
   // waits for this grid before reading what it writes
   griddep_launch_dependents();
+  if (blockIdx.x == 0)   // the split-K counters of the convolution
+    for (int i = threadIdx.x; i < zero_n; i += kPrepThreads) zero[i] = 0;
   if (static_cast<int>(blockIdx.x) < pack_blocks) {
     __shared__ uint16_t tile[kPackTile][kPackTile + 2];
     const int tiles_k = (K + kPackTile - 1) / kPackTile;
@@ -1280,10 +1392,10 @@ static void note_attributes(Kern kern, int threads, int smem) {
 
 const char *last_launch_note() { return t_kernel_note; }
 
-template <int BN, bool IS_INT8, int MS>
+template <int BN, bool IS_INT8, int MS, bool SPLITK = false>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                                 const ConvArgs &args, int grid, cudaStream_t stream) {
-  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS>;
+  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK>;
   using Cfg = TmaCfg<BN, MS>;
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
@@ -1319,6 +1431,21 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
     return is_int8 ? launch_tma_t<128, true, 2>(tmap_a, tmap_b, args, grid, stream)
                    : launch_tma_t<128, false, 2>(tmap_a, tmap_b, args, grid, stream);
   }
+  if (gather == Gather::kTmaIm2col && args.splits > 1) {
+    // split-K: 128-pixel tiles of 64, 128 or 256 channels
+    if (args.C % kBK != 0 || m_sub != 1 || block_n < 64 || args.partial == nullptr ||
+        args.counters == nullptr || args.kb_per_split <= 0 ||
+        (args.splits - 1) * args.kb_per_split >= args.num_kb)
+      return cudaErrorInvalidValue;
+    switch (block_n) {
+      case 64: return is_int8 ? launch_tma_t<64, true, 1, true>(tmap_a, tmap_b, args, grid, stream)
+                              : launch_tma_t<64, false, 1, true>(tmap_a, tmap_b, args, grid, stream);
+      case 128: return is_int8 ? launch_tma_t<128, true, 1, true>(tmap_a, tmap_b, args, grid, stream)
+                               : launch_tma_t<128, false, 1, true>(tmap_a, tmap_b, args, grid, stream);
+      default: return is_int8 ? launch_tma_t<256, true, 1, true>(tmap_a, tmap_b, args, grid, stream)
+                              : launch_tma_t<256, false, 1, true>(tmap_a, tmap_b, args, grid, stream);
+    }
+  }
   if (gather == Gather::kTmaIm2col) {
     if (args.C % kBK != 0) return cudaErrorInvalidValue;
     switch (block_n) {
@@ -1351,7 +1478,7 @@ static FastDiv make_fast_div(uint32_t d) {
 
 cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
                         const void *x, __half *xh, long long n, const WidenMap &map_in,
-                        int sm_count, cudaStream_t stream) {
+                        int *zero, int zero_n, int sm_count, cudaStream_t stream) {
   WidenMap map = map_in;
   if (map.mode != kCopyDense) {
     if (map.C % 8 != 0 || map.P <= 0 || map.Q <= 0 || map.sh <= 0 || map.sw <= 0 ||
@@ -1375,21 +1502,23 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int 
   // 16 at ~96 %)
   const long long cap = static_cast<long long>(sm_count) * 16;
   if (widen_blocks > cap) widen_blocks = cap;
-  const unsigned grid = static_cast<unsigned>(pack_blocks + widen_blocks);
+  unsigned grid = static_cast<unsigned>(pack_blocks + widen_blocks);
+  if (grid == 0 && zero_n > 0) grid = 1;
   if (grid == 0) return cudaSuccess;
   const bool mapped = map.mode != kCopyDense;
   if (is_int8 && mapped)
     prep_kernel<true, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
-                                                                x, xh, n8, map);
+                                                                x, xh, n8, map, zero, zero_n);
   else if (is_int8)
     prep_kernel<true, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
-                                                                 x, xh, n8, map);
+                                                                 x, xh, n8, map, zero, zero_n);
   else if (mapped)
     prep_kernel<false, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
-                                                                 x, xh, n8, map);
+                                                                 x, xh, n8, map, zero, zero_n);
   else
     prep_kernel<false, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad,
-                                                                  pack_blocks, x, xh, n8, map);
+                                                                  pack_blocks, x, xh, n8, map,
+                                                                  zero, zero_n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !is_int8 || map.mode != kCopyDense) return e;
   const long long n16 = n / 16, first16 = (n / 64) * 4;

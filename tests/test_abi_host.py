@@ -327,3 +327,53 @@ def test_256_pixel_tile_rules():
         assert _err(fc.fconv_plan_set_tile_shape, h, 256, 64) == fc.FCONV_ERR_NOT_SUPPORTED
     finally:
         fc.fconv_plan_destroy(h)
+
+
+def test_split_k_rules():
+    """Split-K: forward plans on the TMA gather, no empty unit, workspace
+    grown by the partial sums and counters, reset by an explicit tile."""
+    h = fc.fconv_plan_create(2, 9, 11, 64, 80, 3, 3, 1, 1, 0, 0, 1)   # 9 k-blocks
+    try:
+        base = fc.fconv_workspace_size(h)
+        fc.fconv_plan_set_tile_shape(h, 128, 64)
+        tiles = fc.fconv_plan_get_config(h)[2]
+        assert fc.fconv_plan_get_splits(h) == 1
+        fc.fconv_plan_set_splits(h, 3)
+        assert fc.fconv_plan_get_splits(h) == 3
+        part = tiles * 3 * 128 * 64 * 4
+        assert fc.fconv_workspace_size(h) >= base + part + tiles * 8 * 4
+        for asked, runs in [(4, 3), (5, 5), (8, 5), (9, 5), (2, 2)]:   # 9 k-blocks
+            if asked <= 8:
+                fc.fconv_plan_set_splits(h, asked)
+                assert fc.fconv_plan_get_splits(h) == runs, asked
+        assert _err(fc.fconv_plan_set_splits, h, 9) == fc.FCONV_ERR_INVALID_VALUE
+        assert _err(fc.fconv_plan_set_splits, h, -1) == fc.FCONV_ERR_INVALID_VALUE
+        fc.fconv_plan_set_tile(h, 128)
+        assert fc.fconv_plan_get_splits(h) == 1
+        fc.fconv_plan_set_splits(h, 0)   # the automatic choice again
+        assert fc.fconv_workspace_size(h) == base
+    finally:
+        fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create(2, 9, 11, 64, 64, 3, 3, 1, 1, 0, 0, 1)
+    try:   # 256-pixel tiles have no split-K
+        fc.fconv_plan_set_tile_shape(h, 256, 64)
+        assert _err(fc.fconv_plan_set_splits, h, 2) == fc.FCONV_ERR_NOT_SUPPORTED
+    finally:
+        fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create(1, 8, 8, 48, 64, 3, 3, 1, 1, 0, 0, 1)
+    try:   # C % 64 != 0: the cp.async gather, which has no split-K
+        assert _err(fc.fconv_plan_set_splits, h, 2) == fc.FCONV_ERR_NOT_SUPPORTED
+        fc.fconv_plan_set_splits(h, 1)
+    finally:
+        fc.fconv_plan_destroy(h)
+    h = fc.fconv_plan_create_transposed(2, 8, 8, 64, 32, 4, 4, 2, 2, 1, 1, 1, 1, 0, 1)
+    try:
+        assert _err(fc.fconv_plan_set_splits, h, 2) == fc.FCONV_ERR_NOT_SUPPORTED
+    finally:
+        fc.fconv_plan_destroy(h)
+    # a batch-one deep layer: few tiles, long K, split on its own
+    h = fc.fconv_plan_create(1, 7, 7, 512, 512, 3, 3, 1, 1, 0, 0, 1)
+    try:
+        assert fc.fconv_plan_get_splits(h) > 1
+    finally:
+        fc.fconv_plan_destroy(h)

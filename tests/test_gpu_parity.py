@@ -308,6 +308,76 @@ def test_misaligned_device_pointer_is_rejected():
     p.close()
 
 
+# ---------------------------------------------------------------- split-K
+# each tile's k-blocks over several CTAs; the last of a tile portion's units
+# adds the partial sums (int32 exactly, fp32 in split order) and stores
+SPLIT_CASES = [
+    ((2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, True), "int8", (128, 64), 3),
+    ((2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, False), "int8", (128, 128), 2),   # K tail
+    ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True), "int8", (128, 256), 2),  # chunked units
+    ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True), "int8", (128, 128), 5),  # one chunk a unit
+    ((3, 9, 11, 64, 64, 3, 3, 1, "SAME", True, True), "int8", (128, 64), 4),      # 2 of 3 k-blocks
+    ((3, 8, 8, 64, 200, 3, 3, 1, "SAME", True, False), "bf16", (128, 128), 3),
+    ((2, 9, 11, 128, 96, 3, 3, 2, "SAME", False, True), "bf16", (128, 64), 4),
+]
+
+
+@pytest.mark.parametrize("i,item", list(enumerate(SPLIT_CASES)))
+def test_split_k(i, item):
+    params, dtype, shape, splits = item
+    c = sweep_case(700 + i, params, dtype)
+    acc_ref = c.oracle_acc()
+    p = c.plan()
+    fc.fconv_plan_set_tile_shape(p.handle, *shape)
+    fc.fconv_plan_set_splits(p.handle, splits)
+    assert fc.fconv_plan_get_splits(p.handle) > 1
+    x, w = to_dev(c.x, dtype), to_dev(c.w, dtype)
+    bias = torch.from_numpy(c.bias).cuda()
+    side = to_dev(c.side, dtype)
+    acc = p.accumulators(x, w)
+    y = p.run(x, w, bias, side, c.conv_scale, c.side_scale)
+    y2 = p.run(x, w, bias, side, c.conv_scale, c.side_scale)   # counters zeroed again
+    p.check()
+    c.check_acc(acc.cpu().numpy(), acc_ref)
+    c.check_output(to_host(y), c.oracle_out(acc_ref))
+    assert torch.equal(y, y2)   # the same sums in the same order
+
+
+def test_split_k_with_channel_scale_and_graph_replay():
+    c = sweep_case(710, (2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, True), "int8")
+    c.conv_scale = _channel_scales(710, c.K, "int8")
+    p = c.plan()
+    fc.fconv_plan_set_splits(p.handle, 3)
+    assert fc.fconv_plan_get_splits(p.handle) == 3
+    ref = c.oracle_out(c.oracle_acc())
+    x, w = to_dev(c.x, "int8"), to_dev(c.w, "int8")
+    bias, side = torch.from_numpy(c.bias).cuda(), to_dev(c.side, "int8")
+    scale = torch.from_numpy(c.conv_scale).cuda()
+    y = p.new_output()
+    p.run(x, w, bias, side, scale, c.side_scale, y=y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        p.run(x, w, bias, side, scale, c.side_scale, y=y)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        p.check()
+        c.check_output(to_host(y), ref)
+    p.close()
+
+
+def test_split_k_chosen_for_a_batch_one_deep_layer():
+    """One image of 7x7x512 -> 512, 3x3: a handful of tiles and 72 k-blocks,
+    where the plan splits K on its own."""
+    c = sweep_case(720, (1, 7, 7, 512, 512, 3, 3, 1, "SAME", True, True), "int8")
+    p = c.plan()
+    assert fc.fconv_plan_get_splits(p.handle) > 1
+    c.check_output(c.run_gpu(), c.oracle_out(c.oracle_acc()))
+    p.close()
+
+
 # ---------------------------------------------------------------- per-channel scale
 # (shape, dtype): TMA gather (C % 64 == 0) and cp.async gather, chunked int8
 # sums, K tails past 32/64/128-wide tiles
