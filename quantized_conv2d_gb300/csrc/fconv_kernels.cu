@@ -982,25 +982,49 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             args.partial + (static_cast<size_t>(tile) * splits * kTmaEpiWarps + ew) * 32 *
                                C::kHalfCols;
         const size_t split_words = static_cast<size_t>(kTmaEpiWarps) * 32 * C::kHalfCols;
+        auto add4 = [](uint4 &acc, const uint4 &q) {
+          if (IS_INT8) {   // int32 sums: exact in any order
+            acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+          } else {         // fp32 sums: added in split order
+            acc.x = __float_as_uint(__fadd_rn(__uint_as_float(acc.x), __uint_as_float(q.x)));
+            acc.y = __float_as_uint(__fadd_rn(__uint_as_float(acc.y), __uint_as_float(q.y)));
+            acc.z = __float_as_uint(__fadd_rn(__uint_as_float(acc.z), __uint_as_float(q.z)));
+            acc.w = __float_as_uint(__fadd_rn(__uint_as_float(acc.w), __uint_as_float(q.w)));
+          }
+        };
 #pragma unroll 1
         for (int jj = 0; jj < C::kSlices; ++jj) {
+          // a slice's 8 groups of two splits at a time in flight (16 loads
+          // before the first add), added in split order
+          const uint32_t *sl = part0 + static_cast<size_t>(jj * 8 * 32 + lane) * 4;
+          uint4 acc[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) acc[g] = ldcg_v4(sl + g * 128);
+          int j = 1;
+          for (; j + 1 < splits; j += 2) {
+            uint4 q0[8], q1[8];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) q0[g] = ldcg_v4(sl + j * split_words + g * 128);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) q1[g] = ldcg_v4(sl + (j + 1) * split_words + g * 128);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              add4(acc[g], q0[g]);
+              add4(acc[g], q1[g]);
+            }
+          }
+          if (j < splits) {
+            uint4 q0[8];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) q0[g] = ldcg_v4(sl + j * split_words + g * 128);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) add4(acc[g], q0[g]);
+          }
           uint32_t t[32];
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
-            const size_t off = static_cast<size_t>((jj * 8 + g) * 32 + lane) * 4;
-            uint4 acc = ldcg_v4(part0 + off);
-            for (int j = 1; j < splits; ++j) {
-              const uint4 q = ldcg_v4(part0 + j * split_words + off);
-              if (IS_INT8) {   // int32 sums: exact in any order
-                acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
-              } else {         // fp32 sums: added in split order
-                acc.x = __float_as_uint(__fadd_rn(__uint_as_float(acc.x), __uint_as_float(q.x)));
-                acc.y = __float_as_uint(__fadd_rn(__uint_as_float(acc.y), __uint_as_float(q.y)));
-                acc.z = __float_as_uint(__fadd_rn(__uint_as_float(acc.z), __uint_as_float(q.z)));
-                acc.w = __float_as_uint(__fadd_rn(__uint_as_float(acc.w), __uint_as_float(q.w)));
-              }
-            }
-            t[4 * g + 0] = acc.x; t[4 * g + 1] = acc.y; t[4 * g + 2] = acc.z; t[4 * g + 3] = acc.w;
+            t[4 * g + 0] = acc[g].x; t[4 * g + 1] = acc[g].y;
+            t[4 * g + 2] = acc[g].z; t[4 * g + 3] = acc[g].w;
           }
           float vals[32];
 #pragma unroll
