@@ -428,10 +428,10 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     uint8_t *base = static_cast<uint8_t *>(workspace) + split_partial_offset(*p);
     split_partial = reinterpret_cast<uint32_t *>(base);
     split_counters = reinterpret_cast<int *>(base + split_partial_bytes(*p));
-    if (skip_pack && !do_copy)
-      return fail(FCONV_ERR_INTERNAL, "a split-K run needs its prep launch");
   }
-  if (!skip_pack || do_copy) {
+  // (a run whose filter is already packed and whose input needs no copy
+  // still launches it when split-K counters need zeroing)
+  if (!skip_pack || do_copy || split_counters) {
     fconv::WidenMap map;
     memset(&map, 0, sizeof map);
     map.mode = p->subsample ? fconv::kCopySubsample

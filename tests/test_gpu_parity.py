@@ -236,14 +236,18 @@ def test_side_stream_and_guard_bytes():
     p.close()
 
 
-@pytest.mark.parametrize("chunks", [0, 1, 3])
+@pytest.mark.parametrize("chunks,splits", [(0, 1), (1, 1), (3, 1), (3, 3)])
 @pytest.mark.parametrize("dtype", ["int8", "bf16"])
-def test_run_host_buffers(chunks, dtype):
+def test_run_host_buffers(chunks, splits, dtype):
     """fconv_run_host: host buffers in, host buffer out, the batch split into
-    pipelined chunks (7 images in 3 chunks leaves a ragged last chunk)."""
+    pipelined chunks (7 images in 3 chunks leaves a ragged last chunk), with
+    and without split-K (each chunk's tiles split over three units)."""
     c = sweep_case(90, (7, 12, 10, 64, 48, 3, 3, 1, "SAME", True, True), dtype)
     p = c.plan()
     fc.fconv_plan_set_host_chunks(p.handle, chunks)
+    if splits > 1:
+        fc.fconv_plan_set_tile_shape(p.handle, 128, 64)
+        fc.fconv_plan_set_splits(p.handle, splits)
     nbytes = fc.fconv_host_workspace_size(p.handle, True)
     dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
 
