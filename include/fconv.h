@@ -151,10 +151,12 @@ fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top,
                                 int *pad_right);
 
 /* Device scratch bytes fconv_run needs: the filter repacked K-major in
- * 16-bit form (one per phase of a strided transposed plan), and a 16-bit
- * copy of the input for int8 plans (only the strided pixels for a 1x1
- * strided plan) and for transposed plans with a stride above the filter
- * (zeros inserted). */
+ * 16-bit form (one per phase of a strided transposed plan), a 16-bit copy
+ * of the input for int8 plans (only the strided pixels for a 1x1 strided
+ * plan) and for transposed plans with a stride above the filter (zeros
+ * inserted), and for a split-K plan (fconv_plan_set_splits) every unit's
+ * 32-bit partial sums and one counter per tile and epilogue warp.  It
+ * depends on the tile and split in force: query it after changing them. */
 fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes);
 
 /* Run the fused convolution on `stream`.
