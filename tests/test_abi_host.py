@@ -377,3 +377,23 @@ def test_split_k_rules():
         assert fc.fconv_plan_get_splits(h) > 1
     finally:
         fc.fconv_plan_destroy(h)
+
+
+@pytest.mark.parametrize("shape,splits", [
+    ((1, 16, 16, 32, 32, 3, 3, 1, 0, 0), 1),        # the five benchmark workloads
+    ((32, 56, 56, 64, 64, 3, 3, 1, 0, 0), 1),
+    ((64, 28, 28, 256, 512, 1, 1, 2, 1, 0), 1),
+    ((32, 14, 14, 256, 256, 3, 3, 1, 0, 1), 1),
+    ((256, 28, 28, 512, 512, 3, 3, 1, 0, 0), 1),
+    ((1, 7, 7, 512, 512, 3, 3, 1, 0, 0), None),      # batch-one deep layers split
+    ((1, 14, 14, 256, 256, 3, 3, 1, 0, 0), None),
+    ((8, 7, 7, 2048, 512, 1, 1, 1, 0, 0), None),
+])
+def test_automatic_split_choice(shape, splits):
+    N, H, W, C, K, R, S, st, pad, dt = shape
+    h = fc.fconv_plan_create(N, H, W, C, K, R, S, st, st, pad, dt, 1)
+    try:
+        got = fc.fconv_plan_get_splits(h)
+        assert got == splits if splits is not None else got > 1
+    finally:
+        fc.fconv_plan_destroy(h)
