@@ -489,7 +489,8 @@ def run_fconv(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded)",
-        "config": dict(config_of(wl), block_n=plan.config()[0], variant=args.variant,
+        "config": dict(config_of(wl), block_n=plan.config()[0],
+                       splits=fc.fconv_plan_get_splits(plan.handle), variant=args.variant,
                        l2=(f"inputs larger than L2: x+w+side+y+workspace = {footprint / 1e6:.0f} MB"
                            f" > {L2_BYTES / 1e6:.0f} MB") if flush is None else
                           (f"L2 flushed before every step (x+w+side+y+workspace = "
