@@ -12,6 +12,12 @@ int8, 3x3 stride 1 SAME, side input, ReLU (implicit GEMM 200704 x 512 x
 included) over all ranks; the roofline block reports the convolution
 kernel alone against its own tensor-core peak.
 
+Under torchrun every rank runs its own plan on its own GPU with no exchange
+on the data path.  By default each rank convolves the whole batch (weak
+scaling); ``--strong`` splits the batch's images over the ranks
+(``shard_range``), each rank convolving its slice of x and side into its
+slice of y.
+
 ``--impl reference`` times the CPU oracle (the reference this build is
 checked against) on a bounded sample of the same workload.
 """
@@ -40,6 +46,8 @@ METRIC = "fused int8 Conv2D TOPS (1 GB300) and % of dense int8 tensor peak"
 UNIT = "TOPS"
 DEFAULT_WORKLOAD = "large_i8_28x28x512"
 L2_BYTES = 129 * 1024 * 1024
+# dense 16-bit (kind::f16) tensor-core flops per SM per cycle
+TENSOR_FLOPS_PER_CYCLE_PER_SM = 8192
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "quantized_conv2d_gb300", "csrc", f)
                   for f in ("fconv_kernels.cu", "fconv_device.cuh", "fconv_internal.h")]
@@ -174,6 +182,25 @@ def weak_scaling_tops(world: int, steps: int, ops_per_step: float, max_ms: float
     return world * steps * ops_per_step / (max_ms / 1e3) / 1e12
 
 
+def job_tops(steps: int, job_ops_per_step: float, max_ms: float) -> float:
+    """Whole-job throughput: the operations of `steps` steps of all ranks
+    together, over the slowest rank's time."""
+    return steps * job_ops_per_step / (max_ms / 1e3) / 1e12
+
+
+def shard_range(n: int, world: int, rank: int) -> tuple[int, int]:
+    """The images [lo, hi) of a batch of n that rank `rank` of `world`
+    convolves when the batch is split over the ranks (images are
+    independent, so the shards need no exchange): lo = floor(rank*n/world),
+    hi = floor((rank+1)*n/world).  Consecutive ranks get consecutive,
+    disjoint ranges covering the batch; sizes differ by at most one."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError(f"rank {rank} of {world}")
+    if n < world:
+        raise ValueError(f"a batch of {n} images cannot give {world} ranks one image each")
+    return rank * n // world, (rank + 1) * n // world
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 class OracleSample:
     """The CPU oracle on a bounded sample of a workload: whole images, all
@@ -290,14 +317,24 @@ def run_fconv(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     wl = FI.workload(args.workload)
     nominal, inbounds, P, Q = ops_counts(wl)
+    # weak scaling: every rank convolves the whole batch; strong: the batch
+    # is split over the ranks (shard_range) and each convolves its images
+    lo, hi = shard_range(wl.N, world, rank) if args.strong else (0, wl.N)
+    n_local = hi - lo
+    inbounds_local = inbounds * n_local // wl.N
+    job_ops_per_step = nominal if args.strong else world * nominal
     act, alpha, beta, per_channel = VARIANTS[args.variant]
-    plan = fc.Conv2dPlan(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.padding,
+    plan = fc.Conv2dPlan(n_local, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.padding,
                          wl.dtype, wl.relu if act is None else act, device=dev, alpha=alpha,
                          beta=beta, transposed_pads=wl.transposed_pads)
     if args.tile:
         plan.set_tile(args.tile)
-    assert plan.out_shape == (wl.N, P, Q, wl.K)
+    assert plan.out_shape == (n_local, P, Q, wl.K)
     inp = FI.generate(wl, (P, Q))
+    if n_local != wl.N:
+        for key in ("x", "side"):
+            if inp[key] is not None:
+                inp[key] = np.ascontiguousarray(inp[key][lo:hi])
 
     def to_dev(a):
         if a is None:
@@ -361,7 +398,7 @@ def run_fconv(args, rank, world, local_rank):
     prep_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)]
     total_ms = reduce_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = weak_scaling_tops(world, args.steps, nominal, total_ms)
+    value = job_tops(args.steps, job_ops_per_step, total_ms)
 
     # ------------------------------------------------ the same steps from a CUDA graph
     # (GPU time without the host's launch gaps, which small workloads feel;
@@ -396,7 +433,7 @@ def run_fconv(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         plan.check()
         graph_ms = reduce_max(max(g0.elapsed_time(g1) - flush_ms, 1e-6), dev)
-        graph = {"value": weak_scaling_tops(world, args.steps, nominal, graph_ms), "unit": UNIT,
+        graph = {"value": job_tops(args.steps, job_ops_per_step, graph_ms), "unit": UNIT,
                  "ms_per_step": graph_ms / args.steps,
                  "how": "one step captured in a CUDA graph, replayed steps times"
                         + (" after an L2-flush node, flush time subtracted" if flush is not None
@@ -422,7 +459,7 @@ def run_fconv(args, rank, world, local_rank):
             torch.cuda.synchronize(dev)
             plan.check()
             warm_ms = reduce_max(w0.elapsed_time(w1), dev)
-            graph["warm_l2"] = {"value": weak_scaling_tops(world, reps * per, nominal, warm_ms),
+            graph["warm_l2"] = {"value": job_tops(reps * per, job_ops_per_step, warm_ms),
                                 "ms_per_step": warm_ms / (reps * per),
                                 "how": f"{per} steps a graph, replayed {reps} times"}
 
@@ -457,7 +494,7 @@ def run_fconv(args, rank, world, local_rank):
             host_step()
         el = reduce_max(time.perf_counter() - t0, dev)
         plan.check()
-        e2e = {"value": weak_scaling_tops(world, n_e2e, nominal, el * 1e3), "unit": UNIT,
+        e2e = {"value": job_tops(n_e2e, job_ops_per_step, el * 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": n_e2e}
         del dws
@@ -467,7 +504,7 @@ def run_fconv(args, rank, world, local_rank):
     long_run = total_ms > 1000.0
     peak = sustained if long_run else burst
     conv_avg_s = statistics.mean(conv_ms) / 1e3
-    achieved = inbounds / conv_avg_s / 1e12
+    achieved = inbounds_local / conv_avg_s / 1e12
     traffic = None
     try:
         with open(PROFILE_TRAFFIC) as fh:
@@ -477,19 +514,34 @@ def run_fconv(args, rank, world, local_rank):
             traffic = rec["dram_bytes_per_launch"]
     except (OSError, ValueError):
         pass
+    # the same launch in SM cycles at the clock sampled during the timed
+    # steps, against the tensor pipe's dense 16-bit rate of 8192 flops per
+    # cycle per SM: a fraction that does not move with the clock the power
+    # cap allows
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clk.get("sm_mhz") if clk else None
+    cycles = conv_avg_s * mhz * 1e6 if mhz else None
+    ideal_cycles = inbounds_local / (TENSOR_FLOPS_PER_CYCLE_PER_SM * sms)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
+                "frac_burst": achieved / burst, "frac_sustained": achieved / sustained,
+                "sm_mhz": mhz, "cycles_per_launch": cycles,
+                "ideal_tensor_cycles": ideal_cycles,
+                "tensor_cycle_frac": ideal_cycles / cycles if cycles else None,
                 "kernel": f"conv_fprop_kernel<{plan.config()[0]}, {wl.dtype}> "
                           f"({fc.fconv_plan_kernel(plan.handle)}, tcgen05.mma kind::f16)",
                 "peak_source": f"{'sustained' if long_run else 'burst'} bf16 dense of {src} "
                                f"(fp16 rate = bf16 rate; no int8 tensor-core MMA on sm_103a)",
-                "ops_per_launch": inbounds, "ops_definition": "2*MAC over in-bounds taps"}
+                "ops_per_launch": inbounds_local, "ops_definition": "2*MAC over in-bounds taps"}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded)",
+        "scaling": "strong" if args.strong else "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded)",
         "config": dict(config_of(wl), block_n=plan.config()[0],
+                       images_per_rank=(f"[{lo}, {hi}) of {wl.N} (batch split over {world} ranks)"
+                                        if args.strong else f"all {wl.N} (each rank its own batch)"),
                        splits=fc.fconv_plan_get_splits(plan.handle), variant=args.variant,
                        l2=(f"inputs larger than L2: x+w+side+y+workspace = {footprint / 1e6:.0f} MB"
                            f" > {L2_BYTES / 1e6:.0f} MB") if flush is None else
@@ -528,6 +580,9 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="also time the steps replayed from a CUDA graph (GPU time alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--strong", action="store_true",
+                    help="split the workload's batch over the ranks (strong scaling) instead of "
+                         "giving every rank the whole batch (weak scaling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

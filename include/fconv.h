@@ -127,9 +127,10 @@ fconv_status fconv_plan_set_activation_params(fconv_plan *plan, float alpha,
  * MXNet's symmetric pad with output adjustment a is pad_top = pad,
  * pad_bottom = pad - a.  x: NHWC [N][H][W][C]; w: [R][S][C][K] (C input and
  * K output channels); y and side: [N][Ho][Wo][K].  Runs through every
- * fconv_run* entry point like any plan.  Stride 1 and pads in [0, filter-1]
- * only (else FCONV_ERR_NOT_SUPPORTED); pads that leave no output give
- * FCONV_ERR_INVALID_VALUE.  Pure host work. */
+ * fconv_run* entry point like any plan.  Strides up to 8, pads in
+ * [0, filter-1] (the bottom/right pad down to 1 - stride, an output
+ * adjustment larger than the pad), else FCONV_ERR_NOT_SUPPORTED; pads that
+ * leave no output give FCONV_ERR_INVALID_VALUE.  Pure host work. */
 fconv_status fconv_plan_create_transposed(fconv_plan **plan, int N, int H, int W,
                                           int C, int K, int R, int S,
                                           int stride_h, int stride_w,
@@ -150,7 +151,12 @@ fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top,
                                 int *pad_bottom, int *pad_left,
                                 int *pad_right);
 
-/* Device scratch bytes fconv_run needs: the filter repacked K-major in
+/* Device scratch bytes fconv_run needs.  The TensorFlow GPU helper
+ * ("conv_ops_fused_int8.cc", LaunchFusedConv2DOp for the GPU: the
+ * DnnScratchAllocator and AllocateScratchOrFallback before the runner is
+ * called) gives the fused convolution a scratch buffer of the size the
+ * chosen algorithm asks for; here the caller allocates it, of this size,
+ * and passes it to every run.  It holds the filter repacked K-major in
  * 16-bit form (one per phase of a strided transposed plan), a 16-bit copy
  * of the input for int8 plans (only the strided pixels for a 1x1 strided
  * plan) and for transposed plans with a stride above the filter (zeros
@@ -254,9 +260,15 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host,
  * (one tile per SM) each, at most 12, so small problems run as one). */
 fconv_status fconv_plan_set_host_chunks(fconv_plan *plan, int chunks);
 
-/* Synchronize `stream`, then read and clear the current device's kernel
+/* Status of the runs enqueued so far.  MIOpen's fusion API ("use-fusion-api",
+ * running a fusion plan) reports an error for a run of a plan that cannot
+ * execute; the kernels here run asynchronously, so a failure inside them
+ * (a pipeline wait that ran out) is recorded on the device and read here.
+ * Synchronizes `stream`, then reads and clears the current device's kernel
  * status word: FCONV_ERR_TIMEOUT if any kernel since the last check gave up
- * waiting, FCONV_ERR_CUDA if the stream reports an error, else FCONV_OK. */
+ * waiting, FCONV_ERR_CUDA if the stream reports an error, else FCONV_OK.
+ * (fconv_run itself reports, before enqueueing anything, every error it can
+ * see on the host: bad pointers, sizes and workspace.) */
 fconv_status fconv_plan_check(fconv_plan *plan, fconv_stream_t stream);
 
 /* Override the output-channel tile: 32, 64, 128 or 256 (0 restores the
@@ -313,8 +325,9 @@ fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]
  * exceeds 32 MiB get FCONV_ERR_WORKSPACE.  The call allocates nothing: no
  * cudaMalloc, cudaFree or allocating library routine.
  * The first call on each device looks up the array's device address (a
- * one-time set-up with that device current); make that first call before
- * any stream capture.  All calls on a device share the array and it keeps
+ * one-time set-up with that device current, repeated after cudaDeviceReset
+ * gives the device a new context); make that first call before any stream
+ * capture.  All calls on a device share the array and it keeps
  * the previous call's contents; each call writes every scratch byte it
  * reads, so nothing needs clearing, but calls whose kernels overlap on the
  * GPU (other streams, other host threads) race on it: serialize them. */

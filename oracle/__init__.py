@@ -62,6 +62,7 @@ def _load():
         lib.orc_out_geometry.restype = i32
         lib.orc_conv_i8_direct.argtypes = [p, p] + geo + [p]
         lib.orc_conv_i8_points.argtypes = [p, p] + geo + [p, i64, p]
+        lib.orc_conv_i8_partial_sums.argtypes = [p, p] + geo + [p]
         lib.orc_conv_bf16_direct_f64.argtypes = [p, p] + geo + [p]
         lib.orc_conv_bf16_points_f64.argtypes = [p, p] + geo + [p, i64, p]
         lib.orc_im2col.argtypes = [p, i32] + [i32] * 11 + [p]
@@ -72,7 +73,7 @@ def _load():
         lib.orc_epilogue_i8.argtypes = [p, i64, i32, p, p, f32, p, f32, i32, f32, f32, p]
         lib.orc_epilogue_f64.argtypes = [p, i64, i32, p, p, f64, p, f64, i32, f64, f64, p]
         lib.orc_num_threads.restype = i32
-        for name in ("orc_conv_i8_direct", "orc_conv_i8_points",
+        for name in ("orc_conv_i8_direct", "orc_conv_i8_points", "orc_conv_i8_partial_sums",
                      "orc_conv_bf16_direct_f64", "orc_conv_bf16_points_f64",
                      "orc_im2col", "orc_gemm_i8", "orc_conv_i8_im2col",
                      "orc_epilogue_i8", "orc_epilogue_f64",
@@ -138,6 +139,21 @@ def conv_acc_i8(x: np.ndarray, w: np.ndarray, stride=1, padding=SAME) -> np.ndar
     acc = np.empty(g.out_shape, dtype=np.int32)
     _load().orc_conv_i8_direct(_ptr(x), _ptr(w), *g.args(), _ptr(acc))
     return acc
+
+
+def conv_i8_partial_sum_bounds(x: np.ndarray, w: np.ndarray, stride=1, padding=SAME):
+    """How large the int8 convolution's partial sums get (the page's CPU path
+    sums in fp32, which is exact while they stay below 2^24).  Returns
+    (max |acc|, max |prefix sum| with the products added in (r, s, c) patch
+    order, max sum of |x*w|) over all outputs, as Python ints."""
+    x = np.ascontiguousarray(x, dtype=np.int8)
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    g = _geom_of(x, w, stride, padding)
+    if g.R * g.S * g.C >= 2 ** 17:
+        raise ValueError("R*S*C must stay below 2^17 (int32 running sums)")
+    out = np.zeros(3, dtype=np.int64)
+    _load().orc_conv_i8_partial_sums(_ptr(x), _ptr(w), *g.args(), _ptr(out))
+    return tuple(int(v) for v in out)
 
 
 def conv_acc_i8_explicit(x, w, sh, sw, pt, pl, P, Q) -> np.ndarray:

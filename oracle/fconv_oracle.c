@@ -55,6 +55,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #ifdef _OPENMP
@@ -153,6 +154,81 @@ void orc_conv_i8_points(const int8_t *x, const int8_t *w, int N, int H, int W,
     }
     acc[t] = sum;
   }
+}
+
+/* How large the partial sums of the int8 convolution get, for deciding
+ * whether the page's CPU path, which accumulates in fp32
+ * ("conv_ops_fused_int8.cc", LaunchFusedConv2DOpCpuInt8Helper with
+ * TempT = float), reaches the same sums as the int32 reading.  Every
+ * product is an integer, so an fp32 sum is exact while every value it
+ * passes through is an integer below 2^24 in magnitude.  Over all outputs:
+ *   bounds[0] = max |acc|                       (the final sums)
+ *   bounds[1] = max |prefix sum|, the products added one at a time in the
+ *               patch order (r, s, c) of the filter's [R*S*C][K] matrix:
+ *               below 2^24, a sequential fp32 sum in that order is exact;
+ *               below 2^23, so is any sum that adds contiguous runs of that
+ *               order (a run is a difference of two prefixes)
+ *   bounds[2] = max sum of |x * w|: below 2^24, every order is exact.
+ * Same indexing and tap rule as orc_conv_i8_direct. */
+void orc_conv_i8_partial_sums(const int8_t *x, const int8_t *w, int N, int H,
+                              int W, int C, int K, int R, int S, int sh,
+                              int sw, int pt, int pl, int P, int Q,
+                              int64_t *bounds) {
+  /* int32 running values: callers keep R*S*C below 2^17, so a sum of
+   * |x * w| (each at most 2^14) stays below 2^31 */
+  long long NP = (long long)N * P;
+  int64_t g_acc = 0, g_pre = 0, g_abs = 0;
+#pragma omp parallel
+  {
+    int64_t l_acc = 0, l_pre = 0, l_abs = 0;
+    int32_t *a = (int32_t *)calloc((size_t)K * 3, sizeof(int32_t));
+    int32_t *m = a + K, *t = a + 2 * (long long)K;
+#pragma omp for schedule(dynamic, 1)
+    for (long long np = 0; np < NP; ++np) {
+      int n = (int)(np / P), p = (int)(np % P);
+      for (int q = 0; q < Q; ++q) {
+        for (int k = 0; k < K; ++k) a[k] = m[k] = t[k] = 0;
+        for (int r = 0; r < R; ++r) {
+          int ih = p * sh + r - pt;
+          if (ih < 0 || ih >= H) continue;
+          for (int s = 0; s < S; ++s) {
+            int iw = q * sw + s - pl;
+            if (iw < 0 || iw >= W) continue;
+            const int8_t *xp = x + (((long long)n * H + ih) * W + iw) * C;
+            const int8_t *wp = w + ((long long)(r * S + s) * C) * K;
+            for (int c = 0; c < C; ++c) {
+              int32_t xv = xp[c];
+              const int8_t *wr = wp + (long long)c * K;
+              for (int k = 0; k < K; ++k) {
+                int32_t prod = xv * (int32_t)wr[k];
+                int32_t sum = a[k] + prod;
+                int32_t mag = sum < 0 ? -sum : sum;
+                a[k] = sum;
+                m[k] = mag > m[k] ? mag : m[k];
+                t[k] += prod < 0 ? -prod : prod;
+              }
+            }
+          }
+        }
+        for (int k = 0; k < K; ++k) {
+          int64_t fin = a[k] < 0 ? -(int64_t)a[k] : a[k];
+          if (fin > l_acc) l_acc = fin;
+          if (m[k] > l_pre) l_pre = m[k];
+          if (t[k] > l_abs) l_abs = t[k];
+        }
+      }
+    }
+#pragma omp critical
+    {
+      if (l_acc > g_acc) g_acc = l_acc;
+      if (l_pre > g_pre) g_pre = l_pre;
+      if (l_abs > g_abs) g_abs = l_abs;
+    }
+    free(a);
+  }
+  bounds[0] = g_acc;
+  bounds[1] = g_pre;
+  bounds[2] = g_abs;
 }
 
 /* Exact value of a bf16 bit pattern (bf16 is the top half of an fp32). */

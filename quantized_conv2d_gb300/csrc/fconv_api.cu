@@ -401,10 +401,16 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   }
 
   const fconv::Gather gather = gather_for_run(*p);
-  // two 128-pixel sub-tiles exist on the TMA gather only: a plan forced onto
-  // the cp.async gather (a test hook) runs one
-  if (gather == fconv::Gather::kCpAsync && (p->m_sub != 1 || p->splits != 1))
-    set_tiling(*p, p->block_n, 1, 1);
+  // two 128-pixel sub-tiles and split-K exist on the TMA gather only: a plan
+  // forced onto the cp.async gather (a test hook) runs this launch with one
+  // unsplit 128-pixel tile, from a copy, so the caller's plan keeps its
+  // tiling (and its workspace size)
+  fconv_plan reduced;
+  if (gather == fconv::Gather::kCpAsync && (p->m_sub != 1 || p->splits != 1)) {
+    reduced = *p;
+    set_tiling(reduced, p->block_n, 1, 1);
+    p = &reduced;
+  }
   if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb, p->m_sub))
     return fail(FCONV_ERR_NOT_SUPPORTED,
                 "tile %d has no cp.async kernel for a sum of %d k-values (chunked sums need "

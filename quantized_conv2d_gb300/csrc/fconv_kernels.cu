@@ -926,6 +926,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                     (warp - kTmaEpiWarp0) * C::kOutWarpBytes / 16;
     const int ew = warp - kTmaEpiWarp0;
     const int num_units = args.num_tiles * splits;
+    // split-K: the prep launch zeroes the completion counters.  The counter
+    // atomics below already follow the producer's wait for that launch
+    // (through the stage and accumulator barriers), but they wait for it
+    // themselves too, which costs nothing by the time a unit is done.
+    if (SPLITK) griddep_wait();
     uint32_t astage = 0, aphase = 0;
     bool ok = true;
     for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {

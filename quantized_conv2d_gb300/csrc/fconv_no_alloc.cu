@@ -12,7 +12,8 @@
 //
 // Limit: kNoAllocScratchBytes (32 MiB) per device, reserved when the
 // library's module is loaded on that device and held until the process
-// exits.  Plans whose fconv_workspace_size() exceeds it are rejected with
+// exits (or until cudaDeviceReset, after which the next call finds the
+// array in the device's new context).  Plans whose fconv_workspace_size() exceeds it are rejected with
 // FCONV_ERR_WORKSPACE.
 //
 // Sharing: every call on a device uses the same array, and the array keeps
@@ -22,6 +23,7 @@
 // widening pass writes the whole input copy) before reading it.  Calls whose
 // kernels overlap on the GPU (different streams, or several host threads)
 // race on the array; serialize them, e.g. on one stream.
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -47,10 +49,44 @@ static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratc
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+  void *addr;                  // device address of the array in that context
+  unsigned long long ctx_id;   // the context it belongs to (0: not known)
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// The driver's unique id of the calling thread's current context, or 0 when
+// there is none (or the driver cannot say).  cudaDeviceReset destroys a
+// device's primary context; the next runtime call makes a new one, with a
+// new id, in which the module (and this array) is loaded afresh, possibly
+// at another address.
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 // Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// device and context (with that device current) and cached.  If the
+// context's id cannot be read, the address is looked up on every call.
 fconv_status scratch_address(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -58,17 +94,22 @@ fconv_status scratch_address(void **out) {
     return fconv::record_error(FCONV_ERR_CUDA, "no usable current CUDA device");
   }
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+  ScratchEntry &e = g_scratch[dev];
+  const unsigned long long ctx = current_context_id();
+  if (!e.addr || ctx == 0 || e.ctx_id != ctx) {
     void *ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
-    if (e != cudaSuccess || !ptr) {
+    const cudaError_t err = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
+    if (err != cudaSuccess || !ptr) {
       cudaGetLastError();
+      e.addr = nullptr;
       return fconv::record_error(FCONV_ERR_CUDA,
                                  "cudaGetSymbolAddress of the built-in scratch failed");
     }
-    g_scratch_addr[dev] = ptr;
+    e.addr = ptr;
+    // the lookup made the device's primary context current if none was
+    e.ctx_id = ctx != 0 ? ctx : current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = e.addr;
   return FCONV_OK;
 }
 

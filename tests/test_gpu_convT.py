@@ -36,6 +36,9 @@ class TCase(Case):
         super().__init__(N, H, W, C, K, R, S, 1, "VALID", dtype, relu, cs,
                          0.05 if side else 0.0, inputs)
         self.out_hw = (Ho, Wo)
+        # bf16: w ~ N(0, 1/sqrt(R*S*C)), so an output of at most R*S*C
+        # products has at most unit variance
+        self.unit_variance = dtype == "bf16"
 
     def plan(self, block_n=None, debug=0):
         p = fc.Conv2dPlan(self.N, self.H, self.W, self.C, self.K, self.R, self.S, self.tstride,

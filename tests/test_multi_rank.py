@@ -70,3 +70,66 @@ def test_reference_arm_reports_on_rank_zero_only():
     import json
     line = json.loads(res[0])
     assert line["impl"] == "reference" and line["value"] > 0 and line["n_gpus"] == 2
+
+
+# ---------------------------------------------------------------- batch shards
+def test_shard_range_covers_the_batch():
+    import bench
+    for n in (1, 2, 5, 7, 32, 256):
+        for world in range(1, min(n, 9) + 1):
+            ranges = [bench.shard_range(n, world, r) for r in range(world)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == n
+            for (lo, hi), (lo2, _) in zip(ranges, ranges[1:]):
+                assert hi == lo2                      # consecutive and disjoint
+            sizes = [hi - lo for lo, hi in ranges]
+            assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        bench.shard_range(3, 4, 0)                    # fewer images than ranks
+    with pytest.raises(ValueError):
+        bench.shard_range(8, 2, 2)                    # no such rank
+
+
+SHARD_CASE = dict(seed=9100, N=5, H=9, W=7, C=16, K=32, R=3, S=3)
+
+
+def _shard_worker(rank, world, port, out):
+    """Each rank convolves its images of one batch with the oracle; rank 0
+    gathers the shards in rank order."""
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import torch.distributed as tdist
+    import bench
+    import fconv_inputs as FI
+    import oracle
+    c = SHARD_CASE
+    P, _, _ = oracle.out_geometry(c["H"], c["R"], 1, oracle.SAME)
+    Q, _, _ = oracle.out_geometry(c["W"], c["S"], 1, oracle.SAME)
+    inp = FI.random_case(c["seed"], c["N"], c["H"], c["W"], c["C"], c["K"], c["R"], c["S"],
+                         "int8", (P, Q), True)
+    tdist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        lo, hi = bench.shard_range(c["N"], world, rank)
+        y, _ = oracle.fused_conv_i8(inp["x"][lo:hi], inp["w"], inp["bias"], inp["side"][lo:hi],
+                                    0.002, 0.5, True, 1, oracle.SAME)
+        shards = [None] * world
+        tdist.all_gather_object(shards, (lo, hi, y))
+        if rank == 0:
+            out["shards"] = shards
+            out["full"] = oracle.fused_conv_i8(inp["x"], inp["w"], inp["bias"], inp["side"],
+                                               0.002, 0.5, True, 1, oracle.SAME)[0]
+    finally:
+        tdist.destroy_process_group()
+
+
+def test_batch_shards_reassemble_the_unsharded_result():
+    import numpy as np
+    world, port = 2, _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_shard_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    shards = res["shards"]
+    assert [(lo, hi) for lo, hi, _ in shards] == [(0, 2), (2, 5)]
+    whole = np.concatenate([y for _, _, y in shards], axis=0)
+    assert np.array_equal(whole, res["full"])

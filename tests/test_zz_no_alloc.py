@@ -1,7 +1,8 @@
 """fconv_run_no_alloc: the fused run for callers that cannot allocate device
 memory (the scratch comes from the library's built-in 32 MiB array).  Its
-results must equal fconv_run's on the same inputs, call after call, although
-every call reuses the same scratch.  Collected last on purpose."""
+results must equal the oracle's and fconv_run's on the same inputs, call
+after call, although every call reuses the same scratch: plain, split-K and
+phased transposed plans.  Collected last on purpose."""
 import os
 import sys
 
@@ -60,12 +61,42 @@ def test_no_alloc_matches_fconv_run_twice(dtype):
     plan = first.plan()
     for c in (first, second):
         y_ref, y_na = _run_both(plan, c)
-        if dtype == "int8":
-            assert np.array_equal(y_na, y_ref)
-        else:
-            c.check_output(y_na, c.oracle_out())
-            c.check_output(y_ref, c.oracle_out())
-            assert np.array_equal(y_na, y_ref)
+        c.check_output(y_na, c.oracle_out())
+        c.check_output(y_ref, c.oracle_out())
+        assert np.array_equal(y_na, y_ref)
+    plan.close()
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+def test_no_alloc_split_k_plan(dtype):
+    # split-K keeps every unit's partial sums and the per-tile completion
+    # counters in the scratch: the counters must start each call at zero
+    # although the previous call's units left them there
+    first = _case(511, 2, 9, 11, 64, 80, dtype)
+    second = _case(512, 2, 9, 11, 64, 80, dtype)
+    plan = first.plan()
+    fc.fconv_plan_set_tile_shape(plan.handle, 128, 64)
+    fc.fconv_plan_set_splits(plan.handle, 3)
+    assert fc.fconv_plan_get_splits(plan.handle) == 3
+    for c in (first, second, first):
+        y_ref, y_na = _run_both(plan, c)
+        c.check_output(y_na, c.oracle_out())
+        assert np.array_equal(y_na, y_ref)
+    plan.close()
+
+
+def test_no_alloc_strided_transposed_plan():
+    # a stride-2 transposed convolution runs as four phases, three of them on
+    # the plan's side streams, each with its own packed filter in the scratch
+    from test_gpu_convT import TCase
+    first = TCase(521, 2, 8, 8, 64, 64, 4, 4, (1, 1, 1, 1), "int8", True, True, stride=(2, 2))
+    second = TCase(522, 2, 8, 8, 64, 64, 4, 4, (1, 1, 1, 1), "int8", True, True, stride=(2, 2))
+    plan = first.plan()
+    assert fc.fconv_plan_launch_count(plan.handle) > 2
+    for c in (first, second):
+        y_ref, y_na = _run_both(plan, c)
+        c.check_output(y_na, c.oracle_out())
+        assert np.array_equal(y_na, y_ref)
     plan.close()
 
 
