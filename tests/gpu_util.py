@@ -39,6 +39,13 @@ BF16_MAX_REL = 2e-2
 BF16_MEAN_ABS = 1e-3
 
 
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """fp64 values rounded once to the nearest bf16 value (8 significant
+    bits, ties to even): the best a bf16 output can be."""
+    m, e = np.frexp(np.asarray(v, dtype=np.float64))   # m in [0.5, 1)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)     # rint: half to even
+
+
 class Case:
     """One convolution problem with its inputs (numpy) and scalars."""
 
@@ -114,10 +121,16 @@ class Case:
 
     def check_output(self, got, ref, unit_variance_bar=False):
         """int8: bit-exact.  bf16: max relative error <= 2e-2 (|ref| floored
-        at 1e-2), and mean absolute error <= 1e-3 for unit-variance data
-        (``unit_variance_bar`` or the case's ``unit_variance``), else
-        <= 2^-8 * mean|ref|, the most a single bf16 rounding (8 significant
-        bits) can add on average."""
+        at 1e-2), and a mean absolute error bar:
+        * ``unit_variance_bar`` (the unit-variance ReLU workload): mean
+          |y - ref| <= 1e-3 against the unrounded fp64 reference;
+        * the case's ``unit_variance`` (unit-variance data with any
+          activation): mean |y - bf16(ref)| <= 1e-3, the error beyond the
+          output's own rounding (without a ReLU, the correctly rounded bf16
+          values of N(0,1) data are already ~1.1e-3 from the unrounded
+          reference on average);
+        * else <= 2^-8 * mean|ref|, the most a single bf16 rounding (8
+          significant bits) can add on average."""
         assert got.shape == ref.shape
         if self.dtype == "int8":
             bad = np.argwhere(got != ref)
@@ -125,9 +138,14 @@ class Case:
         else:
             mx, mean = bf16_metric(got, ref)
             assert mx <= BF16_MAX_REL, (mx, mean)
-            unit = unit_variance_bar or self.unit_variance
-            bar = BF16_MEAN_ABS if unit else 2.0 ** -8 * float(np.abs(ref).mean())
-            assert mean <= bar, (mx, mean, bar)
+            if unit_variance_bar:
+                assert mean <= BF16_MEAN_ABS, (mx, mean)
+            elif self.unit_variance:
+                beyond = float(np.abs(oracle.bf16_bits_to_f64(got) - bf16_round(ref)).mean())
+                assert beyond <= BF16_MEAN_ABS, (mx, mean, beyond)
+            else:
+                bar = 2.0 ** -8 * float(np.abs(ref).mean())
+                assert mean <= bar, (mx, mean, bar)
 
     def check_acc(self, got, ref):
         assert got.shape == ref.shape
