@@ -156,13 +156,17 @@ fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top,
  * DnnScratchAllocator and AllocateScratchOrFallback before the runner is
  * called) gives the fused convolution a scratch buffer of the size the
  * chosen algorithm asks for; here the caller allocates it, of this size,
- * and passes it to every run.  It holds the filter repacked K-major in
- * 16-bit form (one per phase of a strided transposed plan), a 16-bit copy
- * of the input for int8 plans (only the strided pixels for a 1x1 strided
- * plan) and for transposed plans with a stride above the filter (zeros
+ * and passes it to every run.  It holds a 16-bit copy of the filter in its
+ * HWIO order for int8 plans (widened to fp16) and transposed plans (the
+ * flipped taps; one per phase of a strided transposed plan) -- a bf16
+ * forward plan reads the caller's filter as it is -- a 16-bit copy of the
+ * input for int8 plans (only the strided pixels for a 1x1 strided plan)
+ * and for transposed plans with a stride above the filter (zeros
  * inserted), and for a split-K plan (fconv_plan_set_splits) every unit's
  * 32-bit partial sums and one counter per tile and epilogue warp.  It
- * depends on the tile and split in force: query it after changing them. */
+ * depends on the tile and split in force: query it after changing them.
+ * It may be 0 (an unsplit bf16 forward plan); the run then accepts a NULL
+ * workspace. */
 fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes);
 
 /* Run the fused convolution on `stream`.
@@ -172,11 +176,13 @@ fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes);
  * them as host scalars too).  workspace: device, 256-byte aligned,
  * workspace_bytes >= fconv_workspace_size().  x/w must not alias y or
  * the workspace.  Asynchronous; returns after enqueueing.  A run is a
- * prep launch and the convolution launch (fconv_plan_launch_count); the
- * second is a programmatic dependent of the first, which lets it start
- * its set-up while the first finishes; it reads nothing the first writes
- * before that grid has completed, and ordering against the caller's other
- * work on the stream is that of two plain launches. */
+ * prep launch (the filter and input copies, split-K counters) and the
+ * convolution launch, or the convolution alone for an unsplit bf16 forward
+ * plan (fconv_plan_launch_count).  After a prep launch the convolution is
+ * a programmatic dependent of it, which lets it start its set-up while the
+ * prep finishes; it reads nothing the prep writes before that grid has
+ * completed, and ordering against the caller's other work on the stream
+ * is that of plain launches. */
 fconv_status fconv_run(fconv_plan *plan, const void *x, const void *w,
                        const float *bias, const void *side, float conv_scale,
                        float side_scale, void *y, void *workspace,
@@ -271,8 +277,8 @@ fconv_status fconv_plan_set_host_chunks(fconv_plan *plan, int chunks);
  * see on the host: bad pointers, sizes and workspace.) */
 fconv_status fconv_plan_check(fconv_plan *plan, fconv_stream_t stream);
 
-/* Override the output-channel tile: 32, 64, 128 or 256 (0 restores the
- * plan's own choice).  int8 plans whose sums are chunked (more than 960
+/* Override the output-channel tile: 64, 128 or 256 (0 restores the
+ * plan's own choice; K below the tile leaves zero columns).  int8 plans whose sums are chunked (more than 960
  * k-values) accept at most 128.  For benchmarking and tests. */
 fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n);
 
@@ -305,10 +311,11 @@ fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
 
 /* Record caller-created CUDA events (cudaEvent_t) at the stage boundaries
  * of every later fconv_run / fconv_run_accumulators on this plan, on the
- * run's stream: events[0] before the operand preparation (filter pack and,
- * for int8 plans, the int8 -> fp16 input widening, one launch), events[1]
- * after it, events[2] before the convolution kernel (the same point as
- * events[1]), events[3] after the convolution kernel.  For a strided
+ * run's stream: events[0] before the operand preparation (the filter copy
+ * and, for int8 plans, the int8 -> fp16 input widening, one launch; none
+ * for an unsplit bf16 forward plan), events[1] after it, events[2] before
+ * the convolution kernel (the same point as events[1]), events[3] after
+ * the convolution kernel.  For a strided
  * transposed plan events[1] and [2] follow the first phase's preparation
  * and events[3] the join of all phases.  NULL disables.  The events must
  * outlive the runs that record them. */
@@ -350,9 +357,10 @@ fconv_status fconv_plan_set_splits(fconv_plan *plan, int splits);
 fconv_status fconv_plan_get_splits(const fconv_plan *plan, int *splits);
 
 /* Number of kernel launches one fconv_run (or fconv_run_channel_scale,
- * fconv_run_accumulators) on this plan enqueues: the operand preparation and
- * the convolution, per phase for a strided transposed plan, plus a small
- * widening launch for int8 inputs whose size is not a multiple of 64. */
+ * fconv_run_accumulators) on this plan enqueues: the operand preparation
+ * (none for an unsplit bf16 forward plan) and the convolution, per phase
+ * for a strided transposed plan, plus a small widening launch for int8
+ * inputs whose size is not a multiple of 64. */
 fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches);
 
 /* Which convolution kernel the plan's next run uses: "tma-im2col" (A

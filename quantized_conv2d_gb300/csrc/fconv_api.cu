@@ -36,6 +36,11 @@ struct fconv_plan {
   // int8 1x1 filter with a stride above 1: only the pixels the convolution
   // reads are widened, into a compact [N][P][Q][C] copy read at stride 1
   int subsample;
+  // the B tiles come from a 16-bit copy of the filter in the workspace
+  // (int8 plans: widened; transposed plans: flipped taps) written by the
+  // prep launch; otherwise (bf16 forward plans) straight from the caller's
+  // HWIO filter
+  int pack_filter;
   // transposed convolution: the filter is packed flipped in both spatial axes
   int transposed;
   // transposed convolution with a stride above the filter: the prep launch
@@ -194,10 +199,10 @@ struct TileChoice {
 };
 TileChoice choose_tile(const fconv_plan &p, int sms) {
   const bool chunked = p.kb_chunk < p.num_kb;
-  const int kp = (p.K + 31) / 32 * 32;
-  TileChoice best = {32, 1, 1};
+  const int kp = (p.K + 63) / 64 * 64;   // tiles are whole 64-channel B boxes
+  TileChoice best = {64, 1, 1};
   long long best_cost = -1;
-  for (int bn : {256, 128, 64, 32}) {
+  for (int bn : {256, 128, 64}) {
     for (int ms : {1, 2}) {
       if (bn > kp) continue;
       fconv::Gather g = gather_for(p, bn, false);
@@ -329,10 +334,10 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     return fail(FCONV_ERR_MISALIGNED,
                 "x, w, y, side, bias and the per-channel scale must be 16-byte aligned");
   const size_t need = workspace_need(*p);
-  if (!workspace || workspace_bytes < need)
+  if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(FCONV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? workspace_bytes : static_cast<size_t>(0));
-  if (!aligned(workspace, 256))
+  if (workspace && !aligned(workspace, 256))
     return fail(FCONV_ERR_MISALIGNED, "workspace must be 256-byte aligned");
 
   int dev = 0;
@@ -435,9 +440,11 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     split_partial = reinterpret_cast<uint32_t *>(base);
     split_counters = reinterpret_cast<int *>(base + split_partial_bytes(*p));
   }
-  // (a run whose filter is already packed and whose input needs no copy
-  // still launches it when split-K counters need zeroing)
-  if (!skip_pack || do_copy || split_counters) {
+  // (a run whose filter needs no copy, or has it already, and whose input
+  // needs none either still launches it when split-K counters need zeroing)
+  const bool do_pack = !skip_pack && p->pack_filter;
+  const bool prep = do_pack || do_copy || split_counters;
+  if (prep) {
     fconv::WidenMap map;
     memset(&map, 0, sizeof map);
     map.mode = p->subsample ? fconv::kCopySubsample
@@ -447,8 +454,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     map.tap_nR = p->tap_nR; map.tap_nS = p->tap_nS; map.tap_R = p->tap_R; map.tap_S = p->tap_S;
     map.tap_r0 = p->tap_r0; map.tap_s0 = p->tap_s0;
     map.tap_rstep = p->tap_rstep; map.tap_sstep = p->tap_sstep;
-    e = fconv::launch_prep(is_int8, skip_pack ? nullptr : w, wt, p->Ktot, skip_pack ? 0 : p->K,
-                           p->Kpad, x, xh, do_copy ? n : 0, map, split_counters,
+    e = fconv::launch_prep(is_int8, do_pack ? w : nullptr, wt, p->Ktot, p->K, x, xh,
+                           do_copy ? n : 0, map, split_counters,
                            split_counters ? p->num_tiles * kSplitCountersPerTile : 0, sms,
                            stream);
     if (e != cudaSuccess) return cuda_fail(e, "operand preparation launch");
@@ -458,23 +465,26 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
 
+  // B: the filter as the [R*S*C][K] matrix of its HWIO layout, 16-bit, in
+  // boxes of 64 output channels x 64 k-rows (rows past R*S*C and channels
+  // past K read as zero)
+  const void *bsrc = p->pack_filter ? static_cast<const void *>(wt) : w;
   fconv_plan::MapCache &mb = p->map_b;
-  if (!(mb.valid && mb.base == wt && mb.block_n == p->block_n)) {
+  if (!(mb.valid && mb.base == bsrc)) {
     mb.valid = false;
     memset(&mb.map, 0, sizeof mb.map);
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->Kpad), static_cast<cuuint64_t>(p->K)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->Kpad) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(p->block_n)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->Ktot)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->K) * 2};
+    const cuuint32_t box[2] = {64, 64};
     const cuuint32_t estride[2] = {1, 1};
     CUresult cr = encode(&mb.map,
                          is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                         2, wt, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         2, const_cast<void *>(bsrc), gdim, gstride, box, estride,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS)
       return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
-    mb.base = wt;
-    mb.block_n = p->block_n;
+    mb.base = bsrc;
     mb.valid = true;
   }
   const CUtensorMap &tmap = mb.map;
@@ -552,7 +562,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.counters = split_counters;
   const long long units = static_cast<long long>(a.num_tiles) * a.splits;
   const int grid = units < sms ? static_cast<int>(units) : sms;
-  e = fconv::launch_conv(p->block_n, p->m_sub, is_int8, gather, tmap_a, tmap, a, grid, stream);
+  e = fconv::launch_conv(p->block_n, p->m_sub, is_int8, gather, tmap_a, tmap, a, grid,
+                        /*overlap=*/prep, stream);
   if (e != cudaSuccess)
     return fail(FCONV_ERR_CUDA, "convolution launch: %s (%s)", cudaGetErrorString(e),
                 fconv::last_launch_note());
@@ -741,7 +752,8 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   p.host_chunks = 0;
   p.pipe_dev = -1;
   p.fork_dev = -1;
-  p.wt_bytes = align_up(static_cast<size_t>(K) * p.Kpad * 2, 256);
+  p.pack_filter = (dtype == FCONV_INT8 || p.tap_nR > 0) ? 1 : 0;
+  p.wt_bytes = p.pack_filter ? align_up(static_cast<size_t>(K) * p.Ktot * 2, 256) : 0;
   const InputView view = input_view(p);
   const long long xh_elems = static_cast<long long>(N) * view.H * view.W * C;
   if (xh_elems > kLimit) return fail(FCONV_ERR_NOT_SUPPORTED, "a tensor has 2^31 or more elements");
@@ -1135,8 +1147,8 @@ fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
     set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits);
     return FCONV_OK;
   }
-  if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256)
-    return fail(FCONV_ERR_NOT_SUPPORTED, "tile %d: this build has 32, 64, 128 and 256", block_n);
+  if (block_n != 64 && block_n != 128 && block_n != 256)
+    return fail(FCONV_ERR_NOT_SUPPORTED, "tile %d: this build has 64, 128 and 256", block_n);
   if (!fconv::gather_supports(gather_for(*plan, block_n, false), block_n,
                               plan->kb_chunk < plan->num_kb))
     return fail(FCONV_ERR_NOT_SUPPORTED,
@@ -1234,12 +1246,14 @@ fconv_status fconv_plan_set_stage_events(fconv_plan *plan, void *const events[4]
 
 fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches) {
   if (!plan || !launches) return fail(FCONV_ERR_INVALID_VALUE, "plan and launches must not be NULL");
-  // per forward plan: the prep launch, a tail widening launch when a dense
-  // int8 input is not a multiple of 64 elements, and the convolution
+  // per forward plan: the prep launch (a filter copy, an input copy or
+  // split-K counters to zero), a tail widening launch when a dense int8
+  // input is not a multiple of 64 elements, and the convolution
   auto one = [](const fconv_plan &p) {
     const long long n = static_cast<long long>(p.N) * p.H * p.W * p.C;
     const bool tail = p.dtype == FCONV_INT8 && !p.subsample && !p.upsample && n % 64 != 0;
-    return 2 + (tail ? 1 : 0);
+    const bool prep = p.pack_filter || p.dtype == FCONV_INT8 || p.upsample || p.splits > 1;
+    return (prep ? 1 : 0) + (tail ? 1 : 0) + 1;
   };
   int total = 0;
   if (plan->num_phases > 0) {

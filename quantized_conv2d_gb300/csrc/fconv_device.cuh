@@ -291,12 +291,30 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16 with fp32 accumulation, both operands
-// K-major: A and B fp16 (bf16 = false) or both bf16.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
+// Shared-memory matrix descriptor for an MN-major operand tile (the N index
+// contiguous) stored with the 128-byte swizzle, as a TMA copy of 64 x 64
+// boxes writes it: each box holds 64 consecutive N values (128 bytes) for
+// each of 64 K rows, 8-row swizzle atoms 1024 bytes apart (the stride
+// offset, along K); boxes of the next 64 N values follow 8192 bytes later
+// (the leading offset, along N).  The tile base must be 1024-byte aligned;
+// stepping K by 16 rows adds 2048 bytes, 128 in the start-address field.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;              // leading offset: next 64 N
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;              // stride offset: next 8 K rows
+  d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation: A and B fp16
+// (bf16 = false) or both bf16; A K-major, B K-major or (b_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool b_mn = false) {
   return (1u << 4)                              // D format: f32
          | ((bf16 ? 1u : 0u) << 7)              // A format
          | ((bf16 ? 1u : 0u) << 10)             // B format
+         | ((b_mn ? 1u : 0u) << 16)             // B major: 0 K, 1 MN
          | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
 }

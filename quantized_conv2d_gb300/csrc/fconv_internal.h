@@ -63,9 +63,13 @@ enum class Gather {
 
 // m_sub: 128-pixel sub-tiles per output tile (1, or 2 on the TMA gather
 // with block_n <= 128; args.num_tiles counts tiles of 128 * m_sub pixels).
+// tmap_b: the filter as a [rows][K] 16-bit matrix (HWIO order, output
+// channels contiguous), boxes of 64 x 64.  overlap: the launch directly
+// before this one on the stream is this run's prep launch, which the
+// convolution may overlap (programmatic dependent launch).
 cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
                         const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
-                        const ConvArgs &args, int grid, cudaStream_t stream);
+                        const ConvArgs &args, int grid, bool overlap, cudaStream_t stream);
 // Whether a gather mode has a kernel for this output-channel tile; chunked
 // int8 sums on the cp.async path need a third TMEM region (BN <= 128).
 bool gather_supports(Gather gather, int block_n, bool chunked, int m_sub = 1);
@@ -91,19 +95,19 @@ struct WidenMap {
   int mode;
   int C, H, W, P, Q, sh, sw;
   FastDiv units_per_pixel, pq, q, div_sh, div_sw;   // filled in by launch_prep
-  // filter pack: with tap_nR > 0 the packed filter is [tap_nR][tap_nS][C][K]
+  // filter copy: with tap_nR > 0 the packed filter is [tap_nR][tap_nS][C][K]
   // whose tap (j, l) is w[tap_r0 + tap_rstep*(tap_nR-1-j)][tap_s0 +
   // tap_sstep*(tap_nS-1-l)] of the caller's [tap_R][tap_S][C][K] filter
   // (flipped, and for a phase of a strided transposed convolution every
   // stride-th tap); tap_nR == 0 packs the filter as it is
   int tap_nR, tap_nS, tap_R, tap_S, tap_r0, tap_s0, tap_rstep, tap_sstep;
 };
-// Filter pack ([RSC][K] -> K-major 16-bit [K][Kpad]) and, for int8 plans,
-// the int8 -> fp16 widening of the input (n elements of the copy, a multiple
-// of 16), in one launch (a second, tiny one when a dense n is not a multiple
-// of 64).
+// Filter copy (w != nullptr: `rows` rows of K values into the 16-bit
+// [rows][K] wt, int8 widened to fp16, rows mapped through the map's taps)
+// and the input copy (n elements, a multiple of 16; int8 widened to fp16),
+// in one launch (a second, tiny one when a dense n is not a multiple of 64).
 // zero / zero_n: split-K counters the launch clears (nullptr, 0: none).
-cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
+cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int rows, int K,
                         const void *x, __half *xh, long long n, const WidenMap &map,
                         int *zero, int zero_n, int sm_count, cudaStream_t stream);
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int *out);

@@ -74,7 +74,7 @@ struct Cfg {
   static constexpr int kSmemBytes = 1024 + kOutOffset + 4 * kOutWarpBytes;
   static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
   static_assert(kLag >= 2, "pipeline too shallow");
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "MMA N in whole 64-channel B boxes");
 };
 
 struct Smem {
@@ -87,6 +87,20 @@ struct Smem {
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// The B (filter) tile of k-block kb and output-channel tile n_tile, MN-major:
+// the filter is read as the [R*S*C][K] matrix of its HWIO layout (output
+// channels contiguous), in BN / 64 boxes of 64 channels x 64 k-rows, each
+// 8 KB, 128-byte swizzled (see sw128_mnmajor_desc).  Rows past R*S*C and
+// channels past K read as zero.
+constexpr uint64_t kBStepK = 2048 >> 4;   // descriptor step of 16 k-rows
+template <int BN>
+__device__ __forceinline__ void load_b_tile(uint32_t dst, const CUtensorMap *map, int kb,
+                                            int n_tile, uint32_t bar) {
+#pragma unroll
+  for (int j = 0; j < BN / 64; ++j)
+    tma_load_2d(dst + j * 8192, map, n_tile * BN + 64 * j, kb * kBK, bar);
+}
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
   return __uint_as_float(b16 << 16);
@@ -355,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     conv_fprop_cpasync_kernel(const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
   using C = Cfg<BN>;
   constexpr int kStages = C::kStages;
-  constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8);
+  constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8, /*b_mn=*/true);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -451,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) {
           const uint32_t fb = smem_u32(&bars->full_b[stage]);
           mbar_arrive_expect_tx(fb, C::kBBytes);
-          tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb * kBK, n_tile * BN, fb);
+          load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, fb);
           ++issued;
         }
         const uint32_t a_base = smem_u32(sA + stage * C::kABytes);
@@ -520,11 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kABytes));
-          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+          const uint64_t bdesc = sw128_mnmajor_desc(smem_u32(sB + stage * C::kBBytes));
           if (lane == 0) {
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              umma_f16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              umma_f16(d, adesc + 2 * k, bdesc + kBStepK * k, kIdesc,
+                       (kb > kb0 || k > 0) ? 1u : 0u);
             umma_commit(smem_u32(&bars->empty[stage]));
           }
           __syncwarp();
@@ -664,14 +679,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 128 x 40 + 256 x 232 = 64512, the launch total; per sub-partition that is
 // one warp of each warpgroup, 40 + 232 + 232 = 504 <= 512 per lane.  ptxas
 // allocates each region to its setmaxnreg budget: the int8 epilogue holds
-// 128 int32 sums, 32 side words and a 32-column slice at once.
+// 128 int32 sums, 32 side words and a 32-column slice at once.  Tiles whose
+// epilogue threads hold 64 sums or fewer split 96 / 200 instead
+// (128 x 96 + 256 x 200 = 63488).
 constexpr int kTmaThreads = 384;
 constexpr int kTmaEpiWarp0 = 4;
 constexpr int kTmaEpiWarps = 8;
-constexpr int kTmaCtlRegs = 40;
-constexpr int kTmaEpiRegs = 232;
-static_assert(128 * kTmaCtlRegs + 256 * kTmaEpiRegs <= kTmaThreads * 168,
-              "register split exceeds the launch allocation");
+// Register split by tile (see TmaCfg below): an int8 epilogue thread keeps
+// kHalfCols int32 running sums; only tiles with 128 of them need 232
+// registers there, and the others leave the control warps 96 (ptxas spills
+// the 128-channel int8 instance's loop state at 40).
+template <int HALF_COLS>
+struct TmaRegs {
+  static constexpr int kCtl = HALF_COLS >= 128 ? 40 : 96;
+  static constexpr int kEpi = HALF_COLS >= 128 ? 232 : 200;
+  static_assert(128 * kCtl + 256 * kEpi <= kTmaThreads * 168,
+                "register split exceeds the launch allocation");
+};
 
 // MS: M sub-tiles of 128 output pixels per tile.  MS = 2 gives a tile of
 // 256 pixels x BN channels whose two halves share each B stage (one wait,
@@ -717,7 +741,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                           const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
   using C = TmaCfg<BN, MS>;
   constexpr int kStages = C::kStages;
-  constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8);
+  constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8, /*b_mn=*/true);
   constexpr int kTileM = kBM * MS;
 
   extern __shared__ uint8_t smem_raw[];
@@ -764,7 +788,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const int kb_chunk = args.kb_chunk;
 
   if (warp < kTmaEpiWarp0) {
-   setmaxnreg_dec<kTmaCtlRegs>();
+   setmaxnreg_dec<TmaRegs<C::kHalfCols>::kCtl>();
    if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop (warp-uniform state); lane 0 issues.
@@ -810,7 +834,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
               tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage + u * C::kABytes), &tmap_a,
                                  cb * kBK, w0[u], h0[u], n0[u], static_cast<uint16_t>(s),
                                  static_cast<uint16_t>(r), fb);
-            tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb * kBK, n_tile * BN, fb);
+            load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, fb);
           }
           __syncwarp();
           ++issued;
@@ -861,9 +885,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           }
           tc_fence_after();
           const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kAStage));
-          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::kBBytes));
+          const uint64_t bdesc = sw128_mnmajor_desc(smem_u32(sB + stage * C::kBBytes));
           const uint64_t adesc1 = sw128_kmajor_desc(smem_u32(sA + stage1 * C::kAStage));
-          const uint64_t bdesc1 = sw128_kmajor_desc(smem_u32(sB + stage1 * C::kBBytes));
+          const uint64_t bdesc1 = sw128_mnmajor_desc(smem_u32(sB + stage1 * C::kBBytes));
           // a sub-tile's A is 16 KB further: + (16384 >> 4) in the descriptor
           constexpr uint64_t kSubStep = static_cast<uint64_t>(C::kABytes >> 4);
           if (lane == 0) {
@@ -871,7 +895,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             for (int u = 0; u < MS; ++u)
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k)
-                umma_f16(d + u * BN, adesc + u * kSubStep + 2 * k, bdesc + 2 * k, kIdesc,
+                umma_f16(d + u * BN, adesc + u * kSubStep + 2 * k, bdesc + kBStepK * k, kIdesc,
                          (kb > kb0 || k > 0) ? 1u : 0u);
             umma_commit(smem_u32(&bars->empty[stage]));
             if (pair) {
@@ -879,7 +903,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
               for (int u = 0; u < MS; ++u)
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k)
-                  umma_f16(d + u * BN, adesc1 + u * kSubStep + 2 * k, bdesc1 + 2 * k, kIdesc, 1u);
+                  umma_f16(d + u * BN, adesc1 + u * kSubStep + 2 * k, bdesc1 + kBStepK * k,
+                           kIdesc, 1u);
               umma_commit(smem_u32(&bars->empty[stage1]));
             }
           }
@@ -906,7 +931,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     __syncwarp();
    }
   } else {
-    setmaxnreg_inc<kTmaEpiRegs>();
+    setmaxnreg_inc<TmaRegs<C::kHalfCols>::kEpi>();
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int half = (warp - kTmaEpiWarp0) >> 2;  // MS = 1: which half of the BN columns;
@@ -1171,11 +1196,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 }
 
 // ---------------------------------------------------------------- pre-pass
-// One launch prepares the operands of a run: blocks [0, pack_blocks) repack
-// the HWIO filter [RSC][K] into the K-major 16-bit [K][Kpad] the B tiles are
-// loaded from (zero for k >= RSC; int8 widened exactly to fp16, bf16
-// copied), 64 x 64 elements a block; the remaining blocks widen an int8
-// input to fp16, 64 elements a thread per step.
+// One launch prepares the operands of a run: blocks [0, pack_blocks) write
+// the 16-bit filter the B tiles are loaded from, [rows][K] in the HWIO
+// order (int8 widened exactly to fp16; for a transposed plan the flipped
+// taps, bf16 copied); the remaining blocks copy the input (int8 widened to
+// fp16; subsampled or upsampled copies), 64 elements a thread per step.
 
 // Four int8 values (one 32-bit word) to two fp16x2 words, exactly: with the
 // sign bit flipped a byte b is u = b + 128 in [0, 255]; the fp16 bit pattern
@@ -1192,7 +1217,6 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
 }
 
 constexpr int kPrepThreads = 256;
-constexpr int kPackTile = 64;
 
 __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &d) {
   return (__umulhi(n, d.m) + n) >> d.l;
@@ -1224,7 +1248,7 @@ __device__ __forceinline__ long long copy_src_unit(long long g, const WidenMap &
 
 template <bool IS_INT8, bool MAPPED>
 __global__ void __launch_bounds__(kPrepThreads)
-    prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int RSC, int K, int Kpad,
+    prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int rows, int K,
                 int pack_blocks, const void *__restrict__ xv, __half *__restrict__ xh,
                 long long n8, const WidenMap map, int *__restrict__ zero, int zero_n) {
   // the convolution launch behind this one may start its set-up now; it
@@ -1233,64 +1257,36 @@ __global__ void __launch_bounds__(kPrepThreads)
   if (blockIdx.x == 0)   // the split-K counters of the convolution
     for (int i = threadIdx.x; i < zero_n; i += kPrepThreads) zero[i] = 0;
   if (static_cast<int>(blockIdx.x) < pack_blocks) {
-    __shared__ uint16_t tile[kPackTile][kPackTile + 2];
-    const int tiles_k = (K + kPackTile - 1) / kPackTile;
-    const int rsc0 = (blockIdx.x / tiles_k) * kPackTile;
-    const int k0 = (blockIdx.x % tiles_k) * kPackTile;
-    // load 64 (rsc) x 64 (k), k fastest: 8 consecutive k per thread (K is a
-    // multiple of 8, so the 8 values are all in range or all out)
-    for (int e = threadIdx.x; e < kPackTile * kPackTile / 8; e += kPrepThreads) {
-      const int i = e / (kPackTile / 8), j = (e % (kPackTile / 8)) * 8;
-      const int rsc = rsc0 + i, k = k0 + j;
-      uint32_t v[4] = {0, 0, 0, 0};   // 8 16-bit values, low half first
-      if (rsc < RSC && k < K) {
-        int src = rsc;
-        if (map.tap_nR > 0) {
-          // (j, l, c) of the packed filter -> (r, s, c) of the caller's
-          const int C = RSC / (map.tap_nR * map.tap_nS);
-          const int c = rsc % C, jl = rsc / C;
-          const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
-          const int r = map.tap_r0 + map.tap_rstep * (map.tap_nR - 1 - j);
-          const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
-          src = (r * map.tap_S + s2) * C + c;
-        }
-        const long long idx = static_cast<long long>(src) * K + k;   // a multiple of 8
-        if (IS_INT8) {
-          const uint2 b8 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(w) + idx));
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t word = t < 2 ? b8.x : b8.y;
-            const int sh = 16 * (t & 1);
-            const uint32_t lo = __half_as_ushort(
-                __int2half_rn(static_cast<int>(static_cast<int8_t>(word >> sh))));
-            const uint32_t hi = __half_as_ushort(
-                __int2half_rn(static_cast<int>(static_cast<int8_t>(word >> (sh + 8)))));
-            v[t] = lo | (hi << 16);
-          }
-        } else {
-          const uint4 h8 = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(w) + idx));
-          v[0] = h8.x; v[1] = h8.y; v[2] = h8.z; v[3] = h8.w;
-        }
+    // filter rows: packed row j of [rows][K] is row src(j) of the caller's
+    // [R*S*C][K] filter (the same row for a forward plan; a flipped, for a
+    // phase every stride-th, tap for a transposed plan), in 8-element
+    // units (K is a multiple of 8; rows * K < 2^31)
+    const uint32_t per_row = static_cast<uint32_t>(K) / 8;
+    const uint32_t units = static_cast<uint32_t>(rows) * per_row;
+    for (uint32_t g = blockIdx.x * kPrepThreads + threadIdx.x; g < units;
+         g += static_cast<uint32_t>(pack_blocks) * kPrepThreads) {
+      const uint32_t row = g / per_row, cu = g - row * per_row;
+      uint32_t src = row;
+      if (map.tap_nR > 0) {
+        // (j, l, c) of the packed filter -> (r, s, c) of the caller's
+        const int C = rows / (map.tap_nR * map.tap_nS);
+        const int c = static_cast<int>(row) % C, jl = static_cast<int>(row) / C;
+        const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
+        const int r = map.tap_r0 + map.tap_rstep * (map.tap_nR - 1 - j);
+        const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
+        src = static_cast<uint32_t>((r * map.tap_S + s2) * C + c);
       }
-      // a row is 66 halves (132 bytes): j even keeps the words 4-byte aligned
-      uint32_t *row = reinterpret_cast<uint32_t *>(&tile[i][j]);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) row[t] = v[t];
-    }
-    __syncthreads();
-    // store transposed: 64 (k) rows of 64 (rsc) 16-bit values, 8 per thread
-    // (one 16-byte store; Kpad and rsc0 are multiples of 64)
-    for (int e = threadIdx.x; e < kPackTile * kPackTile / 8; e += kPrepThreads) {
-      const int kk = e / (kPackTile / 8), j = (e % (kPackTile / 8)) * 8;
-      const int k = k0 + kk, rsc = rsc0 + j;
-      if (k < K && rsc < Kpad) {
-        uint32_t o[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          o[t] = static_cast<uint32_t>(tile[j + 2 * t][kk]) |
-                 (static_cast<uint32_t>(tile[j + 2 * t + 1][kk]) << 16);
-        stg_v4(wt + static_cast<long long>(k) * Kpad + rsc, make_uint4(o[0], o[1], o[2], o[3]));
+      const long long si = static_cast<long long>(src) * K + 8 * cu;
+      const long long di = static_cast<long long>(row) * K + 8 * cu;
+      uint4 o;
+      if (IS_INT8) {
+        const uint2 b8 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(w) + si));
+        i8x4_to_f16x4(b8.x, o.x, o.y);
+        i8x4_to_f16x4(b8.y, o.z, o.w);
+      } else {
+        o = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(w) + si));
       }
+      stg_v4(wt + di, o);
     }
     return;
   }
@@ -1376,10 +1372,13 @@ static cudaError_t ensure_smem_limit(Kern kern, int smem, std::atomic<unsigned l
 
 // A convolution launch that may overlap the tail of the launch before it in
 // the stream (programmatic stream serialization; the kernels wait for that
-// grid before reading its output).
+// grid before reading its output).  Only when that launch is this run's own
+// prep launch (`overlap`): the kernels read the bias and per-channel scale
+// before that wait, which the caller's own earlier kernels may still write.
 template <typename... ExpTypes, typename... ActTypes>
-static cudaError_t launch_overlapping(void (*kern)(ExpTypes...), int grid, int threads, int smem,
-                                     cudaStream_t stream, ActTypes &&...args) {
+static cudaError_t launch_overlapping(void (*kern)(ExpTypes...), bool overlap, int grid,
+                                     int threads, int smem, cudaStream_t stream,
+                                     ActTypes &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(static_cast<unsigned>(threads));
@@ -1389,18 +1388,19 @@ static cudaError_t launch_overlapping(void (*kern)(ExpTypes...), int grid, int t
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<ActTypes>(args)...);
 }
 
 template <int BN, bool IS_INT8>
 static cudaError_t launch_cpasync_t(const CUtensorMap &tmap_b, const ConvArgs &args, int grid,
-                                    cudaStream_t stream) {
+                                    bool overlap, cudaStream_t stream) {
   auto kern = conv_fprop_cpasync_kernel<BN, IS_INT8>;
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg<BN>::kSmemBytes, configured);
   if (e == cudaSuccess) {
-    e = launch_overlapping(kern, grid, kThreads, Cfg<BN>::kSmemBytes, stream, tmap_b, args);
+    e = launch_overlapping(kern, overlap, grid, kThreads, Cfg<BN>::kSmemBytes, stream, tmap_b,
+                           args);
   }
   if (e != cudaSuccess) note_attributes(kern, kThreads, Cfg<BN>::kSmemBytes);
   return e;
@@ -1423,13 +1423,15 @@ const char *last_launch_note() { return t_kernel_note; }
 
 template <int BN, bool IS_INT8, int MS, bool SPLITK = false>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
-                                const ConvArgs &args, int grid, cudaStream_t stream) {
+                                const ConvArgs &args, int grid, bool overlap,
+                                cudaStream_t stream) {
   auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK>;
   using Cfg = TmaCfg<BN, MS>;
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
   if (e == cudaSuccess) {
-    e = launch_overlapping(kern, grid, kTmaThreads, Cfg::kSmemBytes, stream, tmap_a, tmap_b, args);
+    e = launch_overlapping(kern, overlap, grid, kTmaThreads, Cfg::kSmemBytes, stream, tmap_a,
+                           tmap_b, args);
   }
   if (e != cudaSuccess) note_attributes(kern, kTmaThreads, Cfg::kSmemBytes);
   return e;
@@ -1441,13 +1443,13 @@ bool gather_supports(Gather gather, int block_n, bool chunked, int m_sub) {
     return m_sub == 1 ? (block_n == 64 || block_n == 128 || block_n == 256)
                       : (block_n == 64 || block_n == 128);
   if (m_sub != 1) return false;
-  if (block_n != 32 && block_n != 64 && block_n != 128 && block_n != 256) return false;
+  if (block_n != 64 && block_n != 128 && block_n != 256) return false;
   return !chunked || 3 * block_n <= 512;
 }
 
 cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
                         const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
-                        const ConvArgs &args, int grid, cudaStream_t stream) {
+                        const ConvArgs &args, int grid, bool overlap, cudaStream_t stream) {
   const bool chunked = args.kb_chunk < args.num_kb;
   if (chunked && !is_int8) return cudaErrorInvalidValue;
   if (!gather_supports(gather, block_n, chunked, m_sub)) return cudaErrorInvalidValue;
@@ -1455,10 +1457,10 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
   if (gather == Gather::kTmaIm2col && m_sub == 2) {
     if (args.C % kBK != 0) return cudaErrorInvalidValue;
     if (block_n == 64)
-      return is_int8 ? launch_tma_t<64, true, 2>(tmap_a, tmap_b, args, grid, stream)
-                     : launch_tma_t<64, false, 2>(tmap_a, tmap_b, args, grid, stream);
-    return is_int8 ? launch_tma_t<128, true, 2>(tmap_a, tmap_b, args, grid, stream)
-                   : launch_tma_t<128, false, 2>(tmap_a, tmap_b, args, grid, stream);
+      return is_int8 ? launch_tma_t<64, true, 2>(tmap_a, tmap_b, args, grid, overlap, stream)
+                     : launch_tma_t<64, false, 2>(tmap_a, tmap_b, args, grid, overlap, stream);
+    return is_int8 ? launch_tma_t<128, true, 2>(tmap_a, tmap_b, args, grid, overlap, stream)
+                   : launch_tma_t<128, false, 2>(tmap_a, tmap_b, args, grid, overlap, stream);
   }
   if (gather == Gather::kTmaIm2col && args.splits > 1) {
     // split-K: 128-pixel tiles of 64, 128 or 256 channels
@@ -1467,34 +1469,32 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
         (args.splits - 1) * args.kb_per_split >= args.num_kb)
       return cudaErrorInvalidValue;
     switch (block_n) {
-      case 64: return is_int8 ? launch_tma_t<64, true, 1, true>(tmap_a, tmap_b, args, grid, stream)
-                              : launch_tma_t<64, false, 1, true>(tmap_a, tmap_b, args, grid, stream);
-      case 128: return is_int8 ? launch_tma_t<128, true, 1, true>(tmap_a, tmap_b, args, grid, stream)
-                               : launch_tma_t<128, false, 1, true>(tmap_a, tmap_b, args, grid, stream);
-      default: return is_int8 ? launch_tma_t<256, true, 1, true>(tmap_a, tmap_b, args, grid, stream)
-                              : launch_tma_t<256, false, 1, true>(tmap_a, tmap_b, args, grid, stream);
+      case 64: return is_int8 ? launch_tma_t<64, true, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                              : launch_tma_t<64, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+      case 128: return is_int8 ? launch_tma_t<128, true, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                               : launch_tma_t<128, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+      default: return is_int8 ? launch_tma_t<256, true, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                              : launch_tma_t<256, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream);
     }
   }
   if (gather == Gather::kTmaIm2col) {
     if (args.C % kBK != 0) return cudaErrorInvalidValue;
     switch (block_n) {
-      case 64: return is_int8 ? launch_tma_t<64, true, 1>(tmap_a, tmap_b, args, grid, stream)
-                              : launch_tma_t<64, false, 1>(tmap_a, tmap_b, args, grid, stream);
-      case 128: return is_int8 ? launch_tma_t<128, true, 1>(tmap_a, tmap_b, args, grid, stream)
-                               : launch_tma_t<128, false, 1>(tmap_a, tmap_b, args, grid, stream);
-      default: return is_int8 ? launch_tma_t<256, true, 1>(tmap_a, tmap_b, args, grid, stream)
-                              : launch_tma_t<256, false, 1>(tmap_a, tmap_b, args, grid, stream);
+      case 64: return is_int8 ? launch_tma_t<64, true, 1>(tmap_a, tmap_b, args, grid, overlap, stream)
+                              : launch_tma_t<64, false, 1>(tmap_a, tmap_b, args, grid, overlap, stream);
+      case 128: return is_int8 ? launch_tma_t<128, true, 1>(tmap_a, tmap_b, args, grid, overlap, stream)
+                               : launch_tma_t<128, false, 1>(tmap_a, tmap_b, args, grid, overlap, stream);
+      default: return is_int8 ? launch_tma_t<256, true, 1>(tmap_a, tmap_b, args, grid, overlap, stream)
+                              : launch_tma_t<256, false, 1>(tmap_a, tmap_b, args, grid, overlap, stream);
     }
   }
   switch (block_n) {
-    case 32: return is_int8 ? launch_cpasync_t<32, true>(tmap_b, args, grid, stream)
-                            : launch_cpasync_t<32, false>(tmap_b, args, grid, stream);
-    case 64: return is_int8 ? launch_cpasync_t<64, true>(tmap_b, args, grid, stream)
-                            : launch_cpasync_t<64, false>(tmap_b, args, grid, stream);
-    case 128: return is_int8 ? launch_cpasync_t<128, true>(tmap_b, args, grid, stream)
-                             : launch_cpasync_t<128, false>(tmap_b, args, grid, stream);
-    default: return is_int8 ? launch_cpasync_t<256, true>(tmap_b, args, grid, stream)
-                            : launch_cpasync_t<256, false>(tmap_b, args, grid, stream);
+    case 64: return is_int8 ? launch_cpasync_t<64, true>(tmap_b, args, grid, overlap, stream)
+                            : launch_cpasync_t<64, false>(tmap_b, args, grid, overlap, stream);
+    case 128: return is_int8 ? launch_cpasync_t<128, true>(tmap_b, args, grid, overlap, stream)
+                             : launch_cpasync_t<128, false>(tmap_b, args, grid, overlap, stream);
+    default: return is_int8 ? launch_cpasync_t<256, true>(tmap_b, args, grid, overlap, stream)
+                            : launch_cpasync_t<256, false>(tmap_b, args, grid, overlap, stream);
   }
 }
 
@@ -1505,7 +1505,7 @@ static FastDiv make_fast_div(uint32_t d) {
   return FastDiv{d, static_cast<uint32_t>(m), l};
 }
 
-cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int K, int Kpad,
+cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int rows, int K,
                         const void *x, __half *xh, long long n, const WidenMap &map_in,
                         int *zero, int zero_n, int sm_count, cudaStream_t stream) {
   WidenMap map = map_in;
@@ -1521,7 +1521,11 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int 
   } else if (!is_int8) {
     n = 0;   // bf16 plans read a dense input as it is
   }
-  const int pack_blocks = ((Kpad + kPackTile - 1) / kPackTile) * ((K + kPackTile - 1) / kPackTile);
+  // filter rows: 4 8-element units a thread, at most 8 blocks an SM
+  const long long pack_units = w ? static_cast<long long>(rows) * (K / 8) : 0;
+  long long pack_blocks_ll = (pack_units + 4 * kPrepThreads - 1) / (4 * kPrepThreads);
+  if (pack_blocks_ll > 8LL * sm_count) pack_blocks_ll = 8LL * sm_count;
+  const int pack_blocks = static_cast<int>(pack_blocks_ll);
   // 8-element units the main loop widens: all of a subsampled copy; the
   // whole 64-element groups of a dense one (the tail kernel does the rest)
   const long long n8 = map.mode != kCopyDense ? n / 8 : (n / 64) * 8;
@@ -1536,16 +1540,16 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int RSC, int 
   if (grid == 0) return cudaSuccess;
   const bool mapped = map.mode != kCopyDense;
   if (is_int8 && mapped)
-    prep_kernel<true, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
+    prep_kernel<true, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K, pack_blocks,
                                                                 x, xh, n8, map, zero, zero_n);
   else if (is_int8)
-    prep_kernel<true, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
+    prep_kernel<true, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K, pack_blocks,
                                                                  x, xh, n8, map, zero, zero_n);
   else if (mapped)
-    prep_kernel<false, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad, pack_blocks,
+    prep_kernel<false, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K, pack_blocks,
                                                                  x, xh, n8, map, zero, zero_n);
   else
-    prep_kernel<false, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, RSC, K, Kpad,
+    prep_kernel<false, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K,
                                                                   pack_blocks, x, xh, n8, map,
                                                                   zero, zero_n);
   cudaError_t e = cudaGetLastError();

@@ -122,7 +122,9 @@ def test_tile_override_rules():
         bn, chunk, _ = fc.fconv_plan_get_config(h)
         assert chunk < 25 and bn <= 128
         assert _err(fc.fconv_plan_set_tile, h, 256) == fc.FCONV_ERR_NOT_SUPPORTED
-        fc.fconv_plan_set_tile(h, 32)
+        fc.fconv_plan_set_tile(h, 64)
+        # tiles are whole 64-channel filter boxes: no 32-channel tile
+        assert _err(fc.fconv_plan_set_tile, h, 32) == fc.FCONV_ERR_NOT_SUPPORTED
     finally:
         fc.fconv_plan_destroy(h)
     # bf16 sums are never chunked: 256 is allowed
@@ -181,7 +183,8 @@ def test_workspace_sizes():
         fc.fconv_plan_destroy(h)
     h = fc.fconv_plan_create(8, 14, 14, 48, 64, 3, 3, 1, 1, 0, 0, 1)
     try:
-        assert fc.fconv_workspace_size(h) == 64 * 448 * 2 + 8 * 14 * 14 * 48 * 2
+        # the fp16 filter [3*3*48][64] (no padding of the 432 rows)
+        assert fc.fconv_workspace_size(h) == 432 * 64 * 2 + 8 * 14 * 14 * 48 * 2
     finally:
         fc.fconv_plan_destroy(h)
     h = fc.fconv_plan_create(64, 28, 28, 256, 512, 1, 1, 2, 2, 1, 0, 1)
@@ -192,8 +195,8 @@ def test_workspace_sizes():
         fc.fconv_plan_destroy(h)
     h = fc.fconv_plan_create(32, 14, 14, 256, 256, 3, 3, 1, 1, 0, 1, 1)
     try:
-        # bf16 plans read the input as it is: the packed filter alone
-        assert fc.fconv_workspace_size(h) == 256 * 2304 * 2
+        # bf16 forward plans read the input and the filter as they are
+        assert fc.fconv_workspace_size(h) == 0
     finally:
         fc.fconv_plan_destroy(h)
 
@@ -260,12 +263,12 @@ def test_transposed_plan_geometry_and_limits():
 
 def test_transposed_workspace_layouts():
     # stride 2, 3x3, bf16: four phases (taps 2x2, 2x1, 1x2, 1x1 of 16 channels,
-    # each packed as [32][64]); bf16 reads x as it is
+    # each copied as [taps * 16][32]); bf16 reads x as it is
     h = fc.fconv_plan_create_transposed(2, 7, 9, 16, 32, 3, 3, 2, 2, 1, 1, 1, 1, 1, 1)
     try:
         assert fc.fconv_plan_output_shape(h) == (2, 13, 17, 32)
         assert fc.fconv_plan_padding(h) == (1, 1, 1, 1)
-        assert fc.fconv_workspace_size(h) == 4 * 32 * 64 * 2
+        assert fc.fconv_workspace_size(h) == (64 + 32 + 32 + 16) * 32 * 2
     finally:
         fc.fconv_plan_destroy(h)
     # 1x1 filter, stride 2: no phase has more than one tap and some outputs
@@ -274,7 +277,7 @@ def test_transposed_workspace_layouts():
     try:
         assert fc.fconv_plan_output_shape(h) == (2, 13, 17, 32)
         xh = 2 * 13 * 17 * 16 * 2
-        assert fc.fconv_workspace_size(h) == 32 * 64 * 2 + (xh + 255) // 256 * 256
+        assert fc.fconv_workspace_size(h) == 16 * 32 * 2 + (xh + 255) // 256 * 256
     finally:
         fc.fconv_plan_destroy(h)
     # int8, stride 2, 4x4: four phases of 2x2 taps, then one fp16 copy of x
@@ -290,7 +293,7 @@ def test_launch_counts():
     cases = [
         ((256, 28, 28, 512, 512, 3, 3, 1, 1, 0, 0, 1), 2),     # prep + conv
         ((1, 3, 3, 16, 16, 3, 3, 1, 1, 0, 0, 1), 3),           # 144 int8 inputs: a tail launch
-        ((1, 3, 3, 16, 16, 3, 3, 1, 1, 0, 1, 1), 2),           # bf16 reads x as it is
+        ((1, 3, 3, 16, 16, 3, 3, 1, 1, 0, 1, 1), 1),           # bf16 reads x and w as they are
     ]
     for args, n in cases:
         h = fc.fconv_plan_create(*args)
