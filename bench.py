@@ -84,6 +84,22 @@ def ops_counts(wl):
     return nominal, inbounds, P, Q
 
 
+def algorithmic_bytes(wl):
+    """HBM bytes one step must move at least: x read once (for a 1x1 filter
+    at a stride above 1, only the pixels the convolution reads), the filter,
+    the side input, the output written once, and the bias."""
+    elt = 1 if wl.dtype == "int8" else 2
+    _, _, P, Q = ops_counts(wl)
+    if wl.transposed_pads is None and wl.R == 1 and wl.S == 1 and wl.stride > 1:
+        x = wl.N * P * Q * wl.C * elt
+    else:
+        x = wl.N * wl.H * wl.W * wl.C * elt
+    w = wl.R * wl.S * wl.C * wl.K * elt
+    y = wl.N * P * Q * wl.K * elt
+    side = y if wl.has_side else 0
+    return x + w + side + y + 4 * wl.K
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -322,6 +338,8 @@ def run_fconv(args, rank, world, local_rank):
     lo, hi = shard_range(wl.N, world, rank) if args.strong else (0, wl.N)
     n_local = hi - lo
     inbounds_local = inbounds * n_local // wl.N
+    abytes = algorithmic_bytes(wl) * n_local // wl.N   # this rank's share
+    hbm_peak = measured_peaks()[2]
     job_ops_per_step = nominal if args.strong else world * nominal
     act, alpha, beta, per_channel = VARIANTS[args.variant]
     plan = fc.Conv2dPlan(n_local, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.padding,
@@ -435,6 +453,7 @@ def run_fconv(args, rank, world, local_rank):
         graph_ms = reduce_max(max(g0.elapsed_time(g1) - flush_ms, 1e-6), dev)
         graph = {"value": job_tops(args.steps, job_ops_per_step, graph_ms), "unit": UNIT,
                  "ms_per_step": graph_ms / args.steps,
+                 "step_hbm_frac": abytes / (graph_ms / args.steps / 1e3) / 1e9 / hbm_peak,
                  "how": "one step captured in a CUDA graph, replayed steps times"
                         + (" after an L2-flush node, flush time subtracted" if flush is not None
                            else "")}
@@ -461,6 +480,8 @@ def run_fconv(args, rank, world, local_rank):
             warm_ms = reduce_max(w0.elapsed_time(w1), dev)
             graph["warm_l2"] = {"value": job_tops(reps * per, job_ops_per_step, warm_ms),
                                 "ms_per_step": warm_ms / (reps * per),
+                                "step_hbm_frac": abytes / (warm_ms / (reps * per) / 1e3) / 1e9
+                                                 / hbm_peak,
                                 "how": f"{per} steps a graph, replayed {reps} times"}
 
     # ------------------------------------------------ end to end, host buffers
@@ -522,16 +543,30 @@ def run_fconv(args, rank, world, local_rank):
     mhz = clk.get("sm_mhz") if clk else None
     cycles = conv_avg_s * mhz * 1e6 if mhz else None
     ideal_cycles = inbounds_local / (TENSOR_FLOPS_PER_CYCLE_PER_SM * sms)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
+    # HBM side: the path's algorithmic bytes over the conv kernel, and over
+    # the whole step; the bound is whichever ideal time (flops at the
+    # tensor peak, bytes at the copy bandwidth) is the longer
+    hbm_achieved = abytes / conv_avg_s / 1e9
+    hbm_bound = abytes / (hbm * 1e9) > inbounds_local / (peak * 1e12)
+    roofline = {"bound": "hbm" if hbm_bound else "tensor",
+                "achieved": hbm_achieved if hbm_bound else achieved,
+                "peak": hbm if hbm_bound else peak,
+                "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                "frac": hbm_achieved / hbm if hbm_bound else achieved / peak,
+                "traffic": traffic,
+                "tensor_tflops": achieved, "tensor_frac": achieved / peak,
                 "frac_burst": achieved / burst, "frac_sustained": achieved / sustained,
+                "hbm_gbs": hbm_achieved, "hbm_frac": hbm_achieved / hbm,
+                "algorithmic_bytes_per_launch": abytes,
+                "step_hbm_frac": abytes / (ms_per_step / 1e3) / 1e9 / hbm,
                 "sm_mhz": mhz, "cycles_per_launch": cycles,
                 "ideal_tensor_cycles": ideal_cycles,
                 "tensor_cycle_frac": ideal_cycles / cycles if cycles else None,
                 "kernel": f"conv_fprop_kernel<{plan.config()[0]}, {wl.dtype}> "
                           f"({fc.fconv_plan_kernel(plan.handle)}, tcgen05.mma kind::f16)",
-                "peak_source": f"{'sustained' if long_run else 'burst'} bf16 dense of {src} "
-                               f"(fp16 rate = bf16 rate; no int8 tensor-core MMA on sm_103a)",
+                "peak_source": (f"copy bandwidth of {src}" if hbm_bound else
+                                f"{'sustained' if long_run else 'burst'} bf16 dense of {src} "
+                                f"(fp16 rate = bf16 rate; no int8 tensor-core MMA on sm_103a)"),
                 "ops_per_launch": inbounds_local, "ops_definition": "2*MAC over in-bounds taps"}
 
     line = {

@@ -88,6 +88,22 @@ VARIANT_WORKLOADS = {
 }
 
 
+# The two shapes the page's CPU helper computes as plain matrix products
+# ("conv_ops_fused_int8.cc", LaunchFusedConv2DOpCpuInt8Helper): a 1x1 filter
+# at stride 1 ([N*H*W][C] x [C][K]) and a filter as large as the input under
+# VALID padding ([N][R*S*C] x [R*S*C][K]).
+VARIANT_WORKLOADS.update({
+    "proj1x1s1_i8_28x28x256": Workload(
+        "proj1x1s1_i8_28x28x256", "int8", 64, 28, 28, 256, 512, 1, 1, 1, "VALID",
+        ("uniform", -64, 63), ("uniform", -64, 63), 0.5, 0.004, 0.0, False, False, 7,
+        "int8 1x1 projection, N=64 28x28x256 -> 512, stride 1 (a matrix product), BiasAdd only"),
+    "fullwin_i8_7x7x512": Workload(
+        "fullwin_i8_7x7x512", "int8", 32, 7, 7, 512, 1024, 7, 7, 1, "VALID",
+        ("uniform", -128, 127), ("uniform", -128, 127), 1.0, 5e-5, 0.0, False, True, 8,
+        "int8 full-window VALID, N=32 7x7x512 -> 1x1x1024 (a matrix product), bias+ReLU"),
+})
+
+
 def workload(name: str) -> Workload:
     """A workload by name, from either table."""
     return WORKLOADS[name] if name in WORKLOADS else VARIANT_WORKLOADS[name]

@@ -49,9 +49,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     # host arithmetic (the batch-norm fold) rounds every operation on x86
-    # and on Arm alike: no fused multiply-adds from the host compiler
-    common = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-ffp-contract=off",
+    # and on Arm alike: no fused multiply-adds from the host compiler; on the
+    # device no multiply and add is contracted either (-fmad=false; the
+    # epilogue also writes its steps with explicit round-to-nearest
+    # intrinsics, each rounded once, in a fixed order)
+    common = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-fmad=false",
+              "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
               "-I", os.path.join(ROOT, "include"), "-I", CSRC]
     if verbose:
         common += ["-Xptxas", "-v"]

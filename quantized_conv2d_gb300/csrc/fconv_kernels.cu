@@ -166,90 +166,107 @@ __device__ __forceinline__ void load_side_words(const ConvArgs &a, long long m, 
   }
 }
 
-// One 16-byte group of a fused epilogue slice: int8 columns 16 * gi .. +15
-// or bf16 columns 8 * gi .. +7 of the slice, packed as they are stored.
-// sv: the group's side-input word; bias_p / scale_p: the slice's first
-// column.  GENERAL_ACT: the slope-then-clamp activation; otherwise (no
-// activation or Relu) only the lower bound a.lo (-inf or 0).
+// The fused epilogue of one 32-column slice of one output row, in the order
+// of BiasActivationOutputKernel: (1) scale, (2) side input (one fused
+// rounding), (3) bias, then the activation and the output rounding.  Each
+// step runs over 16 columns before the next, so 16 independent chains
+// interleave (two halves a slice keep the registers in bounds).  The
+// explicit round-to-nearest intrinsics keep nvcc from contracting (1) and
+// (3) into an fma.  vals: the 32 sums as fp32 (exact integers for int8
+// plans); sv: the slice's side-input words (int8 2 x 16 bytes, bf16 4 x 8
+// values); bias_p / scale_p: the slice's first column (scale_p read only
+// with a per-channel scale).  out: the slice packed as it is stored (int8
+// 2 x 16 codes, bf16 4 x 8 values).  GENERAL_ACT: the slope-then-clamp
+// activation; otherwise (no activation or Relu) only the lower bound a.lo
+// (-inf or 0).
 template <bool IS_INT8, bool GENERAL_ACT>
-__device__ __forceinline__ uint4 fused_group(const ConvArgs &a, const float (&vals)[32], int gi,
-                                             uint4 sv, const float *bias_p,
-                                             const float *scale_p) {
-  const float cs = a.conv_scale, ss = a.side_scale;
-  const bool use_side = a.use_side != 0;
-  uint32_t out[4];
-  if (IS_INT8) {
-    // The clamp to [lo, 127] before rounding: the activation's lower bound
-    // (Relu 0, none -inf) merged with the int8 range.  Saturating after a
-    // round-half-even gives the same code as rounding the clamped value.
-    const float lo = GENERAL_ACT ? -128.0f : fmaxf(a.lo, -128.0f);
-    // side bytes in offset binary (b + 128, 0..255)
-    const uint32_t sw[4] = {sv.x ^ 0x80808080u, sv.y ^ 0x80808080u, sv.z ^ 0x80808080u,
-                            sv.w ^ 0x80808080u};
+__device__ __forceinline__ void fused_slice(const ConvArgs &a, const float (&vals)[32],
+                                            const uint4 (&sv)[SliceGroups<IS_INT8>::kGroups],
+                                            const float *bias_p, const float *scale_p,
+                                            uint4 (&out)[SliceGroups<IS_INT8>::kGroups]) {
+  uint32_t sw[SliceGroups<IS_INT8>::kGroups * 4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      // bias (and per-channel scale): every lane reads the same 16 bytes
-      const float4 bb = *reinterpret_cast<const float4 *>(bias_p + 16 * gi + 4 * g);
-      const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
-      const float4 sc = a.scale_k ? *reinterpret_cast<const float4 *>(scale_p + 16 * gi + 4 * g)
-                                  : make_float4(cs, cs, cs, cs);
-      const float sv4[4] = {sc.x, sc.y, sc.z, sc.w};
-      uint32_t t[4];
+  for (int g = 0; g < SliceGroups<IS_INT8>::kGroups; ++g) {
+    sw[4 * g + 0] = sv[g].x; sw[4 * g + 1] = sv[g].y;
+    sw[4 * g + 2] = sv[g].z; sw[4 * g + 3] = sv[g].w;
+  }
+  uint32_t wd[IS_INT8 ? 8 : 16];   // the packed outputs
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // (1) scale; (2) side input, one fused rounding; (3) bias.  The
-        // explicit round-to-nearest intrinsics keep nvcc from contracting
-        // (1) and (3) into an fma.
-        float v = __fmul_rn(vals[16 * gi + 4 * g + e], sv4[e]);
-        if (use_side) {
-          // byte u = b + 128 as the mantissa of 2^23 is the float 2^23 + u;
-          // subtracting 2^23 + 128 leaves b exactly
-          const float sd = __fsub_rn(__uint_as_float(__byte_perm(sw[g], 0x4B000000u, 0x7540u + e)),
-                                     8388736.0f);
-          v = __fmaf_rn(sd, ss, v);
-        }
-        v = __fadd_rn(v, bv[e]);
-        if (GENERAL_ACT) v = activation(v, a);
-        v = fminf(fmaxf(v, lo), 127.0f);
-        // 1.5 * 2^23 + v, v in [-128, 127]: the fp32 ulp there is 1, so the
-        // add rounds v half to even and the low byte of the sum's bits is
-        // that integer in two's complement
-        t[e] = __float_as_uint(__fadd_rn(v, 12582912.0f));
+  for (int h = 0; h < 2; ++h) {
+    const int c0 = 16 * h;
+    float v[16];
+    if (a.scale_k) {   // (1) per output channel: every lane reads the same 16 bytes
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 s4 = *reinterpret_cast<const float4 *>(scale_p + c0 + 4 * q);
+        v[4 * q + 0] = __fmul_rn(vals[c0 + 4 * q + 0], s4.x);
+        v[4 * q + 1] = __fmul_rn(vals[c0 + 4 * q + 1], s4.y);
+        v[4 * q + 2] = __fmul_rn(vals[c0 + 4 * q + 2], s4.z);
+        v[4 * q + 3] = __fmul_rn(vals[c0 + 4 * q + 3], s4.w);
       }
-      out[g] = __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x0040u),
-                           0x5410u);
-    }
-  } else {
-    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-    const float4 b0 = *reinterpret_cast<const float4 *>(bias_p + 8 * gi);
-    const float4 b1 = *reinterpret_cast<const float4 *>(bias_p + 8 * gi + 4);
-    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    float sv8[8];
-    if (a.scale_k) {
-      const float4 s0 = *reinterpret_cast<const float4 *>(scale_p + 8 * gi);
-      const float4 s1 = *reinterpret_cast<const float4 *>(scale_p + 8 * gi + 4);
-      sv8[0] = s0.x; sv8[1] = s0.y; sv8[2] = s0.z; sv8[3] = s0.w;
-      sv8[4] = s1.x; sv8[5] = s1.y; sv8[6] = s1.z; sv8[7] = s1.w;
     } else {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) sv8[t] = cs;
+      for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(vals[c0 + i], a.conv_scale);
+    }
+    if (a.use_side) {   // (2)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = c0 + i;
+        float sd;
+        if (IS_INT8) {
+          // byte b in offset binary as the mantissa of 2^23 is the float
+          // 2^23 + b + 128; subtracting 2^23 + 128 leaves b exactly
+          sd = __fsub_rn(__uint_as_float(__byte_perm(sw[c / 4] ^ 0x80808080u, 0x4B000000u,
+                                                     0x7540u + (c % 4))),
+                         8388736.0f);
+        } else {
+          sd = bf16_bits_to_float((sw[c / 2] >> (16 * (c % 2))) & 0xFFFFu);
+        }
+        v[i] = __fmaf_rn(sd, a.side_scale, v[i]);
+      }
     }
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float r[2];
+    for (int q = 0; q < 4; ++q) {   // (3) every lane reads the same 16 bytes
+      const float4 b4 = *reinterpret_cast<const float4 *>(bias_p + c0 + 4 * q);
+      v[4 * q + 0] = __fadd_rn(v[4 * q + 0], b4.x);
+      v[4 * q + 1] = __fadd_rn(v[4 * q + 1], b4.y);
+      v[4 * q + 2] = __fadd_rn(v[4 * q + 2], b4.z);
+      v[4 * q + 3] = __fadd_rn(v[4 * q + 3], b4.w);
+    }
+    if (IS_INT8) {
+      // The clamp to [lo, 127] before rounding: the activation's lower
+      // bound (Relu 0, none -inf) merged with the int8 range.  Saturating
+      // after a round-half-even gives the same code as rounding the clamped
+      // value.
+      const float lo = GENERAL_ACT ? -128.0f : fmaxf(a.lo, -128.0f);
+      uint32_t t[16];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float v = __fmul_rn(vals[8 * gi + 2 * g + t], sv8[2 * g + t]);
-        if (use_side) v = __fmaf_rn(bf16_bits_to_float((sw[g] >> (16 * t)) & 0xFFFFu), ss, v);
-        v = __fadd_rn(v, bv[2 * g + t]);
-        r[t] = GENERAL_ACT ? activation(v, a) : fmaxf(v, a.lo);
+      for (int i = 0; i < 16; ++i) {
+        float x = GENERAL_ACT ? activation(v[i], a) : v[i];
+        x = fminf(fmaxf(x, lo), 127.0f);
+        // 1.5 * 2^23 + x, x in [-128, 127]: the fp32 ulp there is 1, so the
+        // add rounds x half to even and the low byte of the sum's bits is
+        // that integer in two's complement
+        t[i] = __float_as_uint(__fadd_rn(x, 12582912.0f));
       }
-      // both round to nearest even in one conversion; .x is the low half
-      const __nv_bfloat162 pr = __floats2bfloat162_rn(r[0], r[1]);
-      out[g] = *reinterpret_cast<const uint32_t *>(&pr);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        wd[4 * h + k] = __byte_perm(__byte_perm(t[4 * k], t[4 * k + 1], 0x0040u),
+                                    __byte_perm(t[4 * k + 2], t[4 * k + 3], 0x0040u), 0x5410u);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float r0 = GENERAL_ACT ? activation(v[2 * k], a) : fmaxf(v[2 * k], a.lo);
+        const float r1 = GENERAL_ACT ? activation(v[2 * k + 1], a) : fmaxf(v[2 * k + 1], a.lo);
+        // both round to nearest even in one conversion; .x is the low half
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(r0, r1);
+        wd[8 * h + k] = *reinterpret_cast<const uint32_t *>(&pr);
+      }
     }
   }
-  return make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+  for (int g = 0; g < SliceGroups<IS_INT8>::kGroups; ++g)
+    out[g] = make_uint4(wd[4 * g], wd[4 * g + 1], wd[4 * g + 2], wd[4 * g + 3]);
 }
 
 // Raw sums of one 32-column slice of row m (the accumulator-only mode):
@@ -310,15 +327,18 @@ __device__ __forceinline__ void epilogue_slice_coalesced(const ConvArgs &a, long
   const float *scale_p = scale_c ? scale_c : a.scale_k + col0;
   // swizzle of row r: 8 / kG consecutive rows share a 128-byte bank window
   auto swz = [](int r) { return (r / (8 / kG)) % kG; };
+  uint4 sv[kG], outw[kG];
 #pragma unroll
   for (int gi = 0; gi < kG; ++gi) {
-    uint4 sv = make_uint4(0, 0, 0, 0);
-    if (side_pre) sv = side_pre[gi];
+    sv[gi] = make_uint4(0, 0, 0, 0);
+    if (side_pre) sv[gi] = side_pre[gi];
     else if (a.use_side && valid && col0 + G::kCols * gi < K)
-      sv = ldg_nc_v4(static_cast<const uint8_t *>(a.side) + (mo * K + col0 + G::kCols * gi) * elt);
-    stage[lane * kG + (gi ^ swz(lane))] =
-        fused_group<IS_INT8, GENERAL_ACT>(a, vals, gi, sv, bias_c, scale_p);
+      sv[gi] = ldg_nc_v4(static_cast<const uint8_t *>(a.side) +
+                         (mo * K + col0 + G::kCols * gi) * elt);
   }
+  fused_slice<IS_INT8, GENERAL_ACT>(a, vals, sv, bias_c, scale_p, outw);
+#pragma unroll
+  for (int gi = 0; gi < kG; ++gi) stage[lane * kG + (gi ^ swz(lane))] = outw[gi];
   __syncwarp();
 #pragma unroll
   for (int k = 0; k < kG; ++k) {
@@ -636,9 +656,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) vals[i] = __int2float_rn(static_cast<int>(sacc[i]));
           } else {
-            // + 0.0f turns a -0 sum into the +0 that float(int32 0) gives
+            // bf16: + 0.0f turns a -0 sum into +0; int8: a zero of either
+            // sign gives code 0 (and the raw int32 0), so it is skipped
 #pragma unroll
-            for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
+            for (int i = 0; i < 32; ++i)
+              vals[i] = IS_INT8 ? __uint_as_float(v[i]) : __fadd_rn(__uint_as_float(v[i]), 0.0f);
           }
           if (args.mode == kModeFused)
             epilogue_slice_warp<IS_INT8>(args, mo, mvalid, n0 + jj * 32, vals, nullptr,
@@ -1118,9 +1140,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             tmem_ld32(t_acc + jj * 32, v);
             tmem_wait_ld(v);
             float vals[32];
-            // + 0.0f turns a -0 sum into the +0 that float(int32 0) gives
+            // bf16: + 0.0f turns a -0 sum into +0; int8: a zero of either
+            // sign gives code 0 (and the raw int32 0), so it is skipped
 #pragma unroll
-            for (int i = 0; i < 32; ++i) vals[i] = __fadd_rn(__uint_as_float(v[i]), 0.0f);
+            for (int i = 0; i < 32; ++i)
+              vals[i] = IS_INT8 ? __uint_as_float(v[i]) : __fadd_rn(__uint_as_float(v[i]), 0.0f);
             if (args.mode == kModeFused)
               epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals,
                                            preload ? side_pre + jj * SliceGroups<IS_INT8>::kGroups

@@ -26,7 +26,7 @@ def gpu_ready():
 
 
 def workload_case(name, batch=None):
-    wl = FI.WORKLOADS[name]
+    wl = FI.workload(name)
     g = oracle.Geometry(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.stride,
                         PAD[wl.padding])
     inputs = FI.generate(wl, (g.P, g.Q), batch=batch)
@@ -50,6 +50,17 @@ def test_workload_full_parity(name):
     assert_fp32_exact_range(c, acc_ref)
     c.check_acc(c.accumulators_gpu(), acc_ref)
     c.check_output(c.run_gpu(), c.oracle_out(acc_ref), unit_variance_bar=True)
+
+
+@pytest.mark.parametrize("name", ["proj1x1s1_i8_28x28x256", "fullwin_i8_7x7x512"])
+def test_matrix_product_workloads_full_parity(name):
+    """The two shapes the page's CPU helper computes as matrix products (a
+    1x1 filter at stride 1, a filter covering the whole input under VALID):
+    every int8 output and int32 sum against the oracle."""
+    c = workload_case(name)
+    acc_ref = c.oracle_acc()
+    c.check_acc(c.accumulators_gpu(), acc_ref)
+    c.check_output(c.run_gpu(), c.oracle_out(acc_ref))
 
 
 def test_large_workload_full_parity():
