@@ -347,6 +347,11 @@ def run_fconv(args, rank, world, local_rank):
                          beta=beta, transposed_pads=wl.transposed_pads)
     if args.tile:
         plan.set_tile(args.tile)
+    if args.tile_shape:
+        px, ch = (int(v) for v in args.tile_shape.split(","))
+        fc.fconv_plan_set_tile_shape(plan.handle, px, ch)
+    if args.splits:
+        fc.fconv_plan_set_splits(plan.handle, args.splits)
     assert plan.out_shape == (n_local, P, Q, wl.K)
     inp = FI.generate(wl, (P, Q))
     if n_local != wl.N:
@@ -611,6 +616,10 @@ def main():
     ap.add_argument("--variant", default="plain", choices=list(VARIANTS),
                     help="epilogue variant: per-channel conv scale or another activation")
     ap.add_argument("--tile", type=int, default=0)
+    ap.add_argument("--tile-shape", default="",
+                    help="PIXELS,CHANNELS: force the output tile (128 or 256 pixels)")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="force a split-K count (1: none; 0: the plan's own choice)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="also time the steps replayed from a CUDA graph (GPU time alone)")

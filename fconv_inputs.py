@@ -104,6 +104,24 @@ VARIANT_WORKLOADS.update({
 })
 
 
+# Deep layers at small batch: few output tiles over long reductions, where
+# the plan splits each tile's k-blocks over several CTAs.
+VARIANT_WORKLOADS.update({
+    "deep_b1_i8_7x7x512": Workload(
+        "deep_b1_i8_7x7x512", "int8", 1, 7, 7, 512, 512, 3, 3, 1, "SAME",
+        ("uniform", -128, 127), ("uniform", -128, 127), 1.0, 1e-4, 0.0, False, True, 9,
+        "int8 batch-one deep layer, N=1 7x7x512 -> 512, 3x3 SAME, bias+ReLU"),
+    "deep_b1_i8_14x14x256": Workload(
+        "deep_b1_i8_14x14x256", "int8", 1, 14, 14, 256, 256, 3, 3, 1, "SAME",
+        ("uniform", -128, 127), ("uniform", -128, 127), 1.0, 1.5e-4, 0.0, False, True, 10,
+        "int8 batch-one layer, N=1 14x14x256 -> 256, 3x3 SAME, bias+ReLU"),
+    "proj_b8_i8_7x7x2048": Workload(
+        "proj_b8_i8_7x7x2048", "int8", 8, 7, 7, 2048, 512, 1, 1, 1, "VALID",
+        ("uniform", -128, 127), ("uniform", -128, 127), 1.0, 1.5e-4, 0.0, False, True, 11,
+        "int8 1x1 reduction, N=8 7x7x2048 -> 512, bias+ReLU"),
+})
+
+
 def workload(name: str) -> Workload:
     """A workload by name, from either table."""
     return WORKLOADS[name] if name in WORKLOADS else VARIANT_WORKLOADS[name]

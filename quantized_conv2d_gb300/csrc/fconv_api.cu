@@ -182,11 +182,14 @@ fconv::Gather gather_for_run(const fconv_plan &p) {
 }
 
 // Tile: the candidate (BN output channels x 128*MS output pixels) with the
-// least estimated time.  A k-block costs about max(2*BN*MS, G) cycles: the
+// least estimated time.  A unit (a tile, or its split) costs the longer of
+// its mainloop and its epilogue, which runs while the next unit's mainloop
+// does.  A k-block costs about max(2*BN*MS, G) cycles: the
 // MMAs of a 128 x BN x 64 block take ~2*BN on the tensor core, and the
 // issuing threads' per-k-block work (barrier waits, copy and MMA issue) a
-// fixed G whatever BN is (~360 on the TMA path with one 128-pixel sub-tile,
-// ~450 with two, ~800 on the cp.async path; measured).  Tiles run in waves
+// fixed G whatever BN is (~500 on the TMA path with one 128-pixel sub-tile,
+// ~900 with two, ~800 on the cp.async path; measured per k-block in
+// steady state, operand traffic included).  Tiles run in waves
 // over the SMs; the epilogue of a CTA's last tile (~8 cycles per output
 // column per 128 pixels) is not hidden behind a next tile's mainloop.
 // Split-K (splits > 1 units per tile, TMA gather, forward plans): a unit
@@ -199,6 +202,8 @@ struct TileChoice {
 };
 TileChoice choose_tile(const fconv_plan &p, int sms) {
   const bool chunked = p.kb_chunk < p.num_kb;
+  // runs with a prep launch whatever the split: an input copy or a filter copy
+  const bool needs_prep = p.dtype == FCONV_INT8 || p.upsample || p.transposed;
   const int kp = (p.K + 63) / 64 * 64;   // tiles are whole 64-channel B boxes
   TileChoice best = {64, 1, 1};
   long long best_cost = -1;
@@ -208,7 +213,7 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
       fconv::Gather g = gather_for(p, bn, false);
       if (!fconv::gather_supports(g, bn, chunked, ms)) continue;
       const long long fixed =
-          g == fconv::Gather::kTmaIm2col ? (ms == 2 ? 450 : 360) : 800;
+          g == fconv::Gather::kTmaIm2col ? (ms == 2 ? 900 : 500) : 800;
       const long long m_tiles = (p.M + 128LL * ms - 1) / (128LL * ms);
       const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
       const long long work = 2LL * bn * ms;
@@ -218,8 +223,18 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
         const long long units = tiles * sp;
         const long long waves = (units + sms - 1) / sms;
         const long long kbs = (p.num_kb + sp - 1) / sp;
-        const long long cost = waves * kbs * (work > fixed ? work : fixed) + 8LL * bn * ms +
-                               (sp > 1 ? 8LL * bn * ms * (sp + 1) : 0);
+        // a tile's epilogue overlaps the next tile's mainloop, so a unit
+        // costs the longer of the two: ~1400 cycles per 32-column slice of
+        // each epilogue warp (BN / 64 slices a warp, twice that with two
+        // sub-tiles), i.e. ~22 * BN * MS
+        const long long mainloop = kbs * (work > fixed ? work : fixed);
+        const long long epilogue = 22LL * bn * ms;
+        // split-K needs its counters zeroed by a prep launch; a plan with no
+        // other prep work (bf16 forward) pays a whole launch for it (~4 us)
+        const long long split_launch = (sp > 1 && !needs_prep) ? 8000 : 0;
+        const long long cost = waves * (mainloop > epilogue ? mainloop : epilogue) +
+                               8LL * bn * ms + (sp > 1 ? 8LL * bn * ms * (sp + 1) : 0) +
+                               split_launch;
         if (best_cost < 0 || cost < best_cost) {
           best_cost = cost;
           best = {bn, ms, sp};

@@ -337,8 +337,9 @@ def test_split_k_rules():
     grown by the partial sums and counters, reset by an explicit tile."""
     h = fc.fconv_plan_create(2, 9, 11, 64, 80, 3, 3, 1, 1, 0, 0, 1)   # 9 k-blocks
     try:
-        base = fc.fconv_workspace_size(h)
+        auto = fc.fconv_workspace_size(h)       # the plan's own tile and split
         fc.fconv_plan_set_tile_shape(h, 128, 64)
+        base = fc.fconv_workspace_size(h)       # unsplit
         tiles = fc.fconv_plan_get_config(h)[2]
         assert fc.fconv_plan_get_splits(h) == 1
         fc.fconv_plan_set_splits(h, 3)
@@ -354,7 +355,7 @@ def test_split_k_rules():
         fc.fconv_plan_set_tile(h, 128)
         assert fc.fconv_plan_get_splits(h) == 1
         fc.fconv_plan_set_splits(h, 0)   # the automatic choice again
-        assert fc.fconv_workspace_size(h) == base
+        assert fc.fconv_workspace_size(h) == auto
     finally:
         fc.fconv_plan_destroy(h)
     h = fc.fconv_plan_create(2, 9, 11, 64, 64, 3, 3, 1, 1, 0, 0, 1)
