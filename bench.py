@@ -352,6 +352,8 @@ def run_fconv(args, rank, world, local_rank):
         fc.fconv_plan_set_tile_shape(plan.handle, px, ch)
     if args.splits:
         fc.fconv_plan_set_splits(plan.handle, args.splits)
+    if args.widen:
+        fc.fconv_plan_set_input_widening(plan.handle, args.widen)
     assert plan.out_shape == (n_local, P, Q, wl.K)
     inp = FI.generate(wl, (P, Q))
     if n_local != wl.N:
@@ -580,6 +582,8 @@ def run_fconv(args, rank, world, local_rank):
         "scaling": "strong" if args.strong else "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic (seeded)",
         "config": dict(config_of(wl), block_n=plan.config()[0],
+                       input_widening=("in the kernel" if fc.fconv_plan_get_input_widening(plan.handle)
+                                       else "fp16 copy" if wl.dtype == "int8" else "none (bf16)"),
                        images_per_rank=(f"[{lo}, {hi}) of {wl.N} (batch split over {world} ranks)"
                                         if args.strong else f"all {wl.N} (each rank its own batch)"),
                        splits=fc.fconv_plan_get_splits(plan.handle), variant=args.variant,
@@ -618,6 +622,8 @@ def main():
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--tile-shape", default="",
                     help="PIXELS,CHANNELS: force the output tile (128 or 256 pixels)")
+    ap.add_argument("--widen", type=int, default=0, choices=[0, 1, 2],
+                    help="int8 input widening: 0 automatic, 1 in the kernel, 2 an fp16 copy")
     ap.add_argument("--splits", type=int, default=0,
                     help="force a split-K count (1: none; 0: the plan's own choice)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -343,6 +343,23 @@ fconv_status fconv_run_no_alloc(fconv_plan *plan, const void *x, const void *w,
                                 float conv_scale, float side_scale, void *y,
                                 fconv_stream_t stream);
 
+/* Where an int8 plan widens its activations to fp16 for the tensor cores.
+ * FCONV_WIDEN_IN_KERNEL: inside the convolution kernel, from the int8 input
+ * itself (no fp16 copy in the workspace), wherever the plan's tile allows it
+ * (forward plans on the TMA im2col gather, C % 64 == 0, unsplit, 128-pixel
+ * tiles of up to 128 channels or 256-pixel tiles of 64), else in the prep
+ * launch; FCONV_WIDEN_COPY and FCONV_WIDEN_AUTO (the default, measured the
+ * faster of the two on GB300): in the prep launch, into an fp16 copy of the
+ * input in the workspace.  The workspace size depends on it
+ * (query fconv_workspace_size after setting it); results do not.
+ * fconv_plan_get_input_widening reports whether the next run widens inside
+ * the kernel (1) or copies (0).  bf16 plans have nothing to widen. */
+#define FCONV_WIDEN_AUTO 0
+#define FCONV_WIDEN_IN_KERNEL 1
+#define FCONV_WIDEN_COPY 2
+fconv_status fconv_plan_set_input_widening(fconv_plan *plan, int mode);
+fconv_status fconv_plan_get_input_widening(const fconv_plan *plan, int *in_kernel);
+
 /* Split-K for the plan's current tile: each output tile's k-blocks are
  * divided over `splits` CTAs (1: none; 0: the automatic choice made at
  * plan creation, tile included); every unit writes its partial sums to the

@@ -31,6 +31,7 @@ FCONV_ACT_NONE, FCONV_ACT_RELU, FCONV_ACT_LEAKY_RELU, FCONV_ACT_CLIPPED_RELU, FC
     0, 1, 2, 3, 4)
 FCONV_DEBUG_DROP_ARRIVE = 1
 FCONV_DEBUG_GATHER_CPASYNC = 2
+FCONV_WIDEN_AUTO, FCONV_WIDEN_IN_KERNEL, FCONV_WIDEN_COPY = 0, 1, 2
 
 
 class FconvError(RuntimeError):
@@ -82,6 +83,8 @@ def _load():
         "fconv_fold_batchnorm": [i32, f32, p, p, p, p, p, f32, p, p],
         "fconv_plan_set_splits": [p, i32],
         "fconv_plan_get_splits": [p, pi],
+        "fconv_plan_set_input_widening": [p, i32],
+        "fconv_plan_get_input_widening": [p, pi],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -245,6 +248,17 @@ def fconv_plan_set_splits(plan, splits: int) -> None:
 def fconv_plan_get_splits(plan) -> int:
     v = ctypes.c_int()
     _check(_load().fconv_plan_get_splits(plan, ctypes.byref(v)), "fconv_plan_get_splits")
+    return v.value
+
+
+def fconv_plan_set_input_widening(plan, mode: int) -> None:
+    _check(_load().fconv_plan_set_input_widening(plan, mode), "fconv_plan_set_input_widening")
+
+
+def fconv_plan_get_input_widening(plan) -> int:
+    v = ctypes.c_int()
+    _check(_load().fconv_plan_get_input_widening(plan, ctypes.byref(v)),
+           "fconv_plan_get_input_widening")
     return v.value
 
 

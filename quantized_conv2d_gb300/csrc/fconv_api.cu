@@ -36,6 +36,10 @@ struct fconv_plan {
   // int8 1x1 filter with a stride above 1: only the pixels the convolution
   // reads are widened, into a compact [N][P][Q][C] copy read at stride 1
   int subsample;
+  // int8 activations widened inside the convolution kernel (no fp16 copy
+  // of the input): widen_mode is the caller's choice (FCONV_WIDEN_*), widen
+  // whether the next run does it (see update_widen)
+  int widen_mode, widen;
   // the B tiles come from a 16-bit copy of the filter in the workspace
   // (int8 plans: widened; transposed plans: flipped taps) written by the
   // prep launch; otherwise (bf16 forward plans) straight from the caller's
@@ -78,7 +82,7 @@ struct fconv_plan {
   struct MapCache {
     bool valid;
     const void *base;
-    int n, block_n;
+    int n, form;   // A: batch size, and 1 for the int8 input itself (widening)
     CUtensorMap map;
   } map_a, map_b;
 };
@@ -147,6 +151,7 @@ struct InputView {
   int H, W, sh, sw;
 };
 InputView input_view(const fconv_plan &p) {
+  if (p.widen) return {p.H, p.W, p.sh, p.sw};  // the int8 input itself
   if (p.subsample) return {p.P, p.Q, 1, 1};   // compact copy of the strided pixels
   if (p.upsample) return {(p.H - 1) * p.sh + 1, (p.W - 1) * p.sw + 1, 1, 1};
   return {p.H, p.W, p.sh, p.sw};
@@ -180,6 +185,7 @@ fconv::Gather gather_for(const fconv_plan &p, int bn, bool force_cpasync) {
 fconv::Gather gather_for_run(const fconv_plan &p) {
   return gather_for(p, p.block_n, (p.debug & FCONV_DEBUG_GATHER_CPASYNC) != 0);
 }
+
 
 // Tile: the candidate (BN output channels x 128*MS output pixels) with the
 // least estimated time.  A unit (a tile, or its split) costs the longer of
@@ -245,6 +251,8 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
   return best;
 }
 
+void update_widen(fconv_plan &p);
+
 void set_tiling(fconv_plan &p, int bn, int ms = 1, int splits = 1) {
   p.block_n = bn;
   p.m_sub = ms;
@@ -257,6 +265,36 @@ void set_tiling(fconv_plan &p, int bn, int ms = 1, int splits = 1) {
   p.splits = splits < 1 ? 1 : splits;
   p.num_n_tiles = (p.K + bn - 1) / bn;
   p.num_tiles = static_cast<int>((p.M + 128LL * ms - 1) / (128LL * ms)) * p.num_n_tiles;
+  update_widen(p);
+}
+
+// Whether int8 activations can be widened inside the convolution kernel
+// under the plan's tile: a forward int8 plan on the TMA gather (judged on
+// the input as it is), unsplit, with epilogue threads holding at most 64
+// sums (128-pixel tiles of up to 128 channels, 256-pixel tiles of 64).
+bool widen_eligible(const fconv_plan &p) {
+  if (p.dtype != FCONV_INT8 || p.transposed || p.upsample || p.splits != 1) return false;
+  if (p.debug & FCONV_DEBUG_GATHER_CPASYNC) return false;
+  if (p.m_sub == 1 ? p.block_n > 128 : p.block_n != 64) return false;
+  fconv_plan raw = p;
+  raw.widen = 1;   // the input view of the raw input
+  return im2col_ok(raw);
+}
+
+// The widening choice and the workspace it implies: with in-kernel
+// widening there is no fp16 input copy.  FCONV_WIDEN_AUTO copies: measured
+// on the int8 workloads (CUDA graphs, GB300), the prep launch's fp16 copy
+// was faster wherever in-kernel widening applies (32x56x56x64 3x3 22.5 us
+// against 38.8; 64x28x28x256 1x1 34.0 against 43.1; the 1x1 stride-2 layer
+// 17.2 against 18.4): the two converter warps bound the mainloop and share
+// the SM with the epilogue, while HBM has room for the copy.
+void update_widen(fconv_plan &p) {
+  const bool want = p.widen_mode == FCONV_WIDEN_IN_KERNEL;
+  p.widen = (want && widen_eligible(p)) ? 1 : 0;
+  const InputView v = input_view(p);
+  const long long xh_elems = static_cast<long long>(p.N) * v.H * v.W * p.C;
+  p.xh_bytes = ((p.dtype == FCONV_INT8 && !p.widen) || p.upsample)
+                   ? align_up(static_cast<size_t>(xh_elems) * 2, 256) : 0;
 }
 
 PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col_fn() {
@@ -442,7 +480,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   // copies) in one launch; the convolution reads the copy when there is one
   const InputView view = input_view(*p);
   const int gH = view.H, gW = view.W, gsh = view.sh, gsw = view.sw;
-  const bool copy = is_int8 || p->upsample;          // the convolution reads a copy
+  const bool copy = (is_int8 && !p->widen) || p->upsample;   // the convolution reads a copy
   const bool do_copy = copy && !skip_copy;            // ... made by this launch
   const void *act = x;
   const long long n = static_cast<long long>(p->N) * gH * gW * p->C;
@@ -505,7 +543,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   const CUtensorMap &tmap = mb.map;
 
   fconv_plan::MapCache &ma = p->map_a;
-  if (gather == fconv::Gather::kTmaIm2col && !(ma.valid && ma.base == act && ma.n == p->N)) {
+  if (gather == fconv::Gather::kTmaIm2col &&
+      !(ma.valid && ma.base == act && ma.n == p->N && ma.form == (p->widen ? 1 : 0))) {
     ma.valid = false;
     memset(&ma.map, 0, sizeof ma.map);
     CUtensorMap &tmap_a = ma.map;
@@ -522,15 +561,24 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     const int upper[2] = {p->pr - (p->S - 1), p->pb - (p->R - 1)};
     const cuuint32_t traverse[4] = {1, static_cast<cuuint32_t>(gsw), static_cast<cuuint32_t>(gsh),
                                     1};
+    // widening in the kernel: the int8 input itself, 64 one-byte channels a
+    // pixel row, unswizzled (the converter warps lay it out for the MMA)
+    const int elt = p->widen ? 1 : 2;
+    const cuuint64_t astride_e[3] = {astride[0] / 2 * elt, astride[1] / 2 * elt,
+                                     astride[2] / 2 * elt};
     CUresult cra = enc_a(&tmap_a,
-                         is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                         4, const_cast<void *>(act), adim, astride, lower, upper, 64, 128, traverse,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         p->widen ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         4, const_cast<void *>(act), adim, astride_e, lower, upper, 64, 128,
+                         traverse, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         p->widen ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cra != CUDA_SUCCESS)
       return fail(FCONV_ERR_INTERNAL, "im2col tensor map encode failed (%d)", (int)cra);
     ma.base = act;
     ma.n = p->N;
+    ma.form = p->widen ? 1 : 0;
     ma.valid = true;
   }
   static const CUtensorMap kNoMap = {};
@@ -578,7 +626,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   const long long units = static_cast<long long>(a.num_tiles) * a.splits;
   const int grid = units < sms ? static_cast<int>(units) : sms;
   e = fconv::launch_conv(p->block_n, p->m_sub, is_int8, gather, tmap_a, tmap, a, grid,
-                        /*overlap=*/prep, stream);
+                        /*overlap=*/prep, stream, p->widen != 0);
   if (e != cudaSuccess)
     return fail(FCONV_ERR_CUDA, "convolution launch: %s (%s)", cudaGetErrorString(e),
                 fconv::last_launch_note());
@@ -772,8 +820,7 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   const InputView view = input_view(p);
   const long long xh_elems = static_cast<long long>(N) * view.H * view.W * C;
   if (xh_elems > kLimit) return fail(FCONV_ERR_NOT_SUPPORTED, "a tensor has 2^31 or more elements");
-  p.xh_bytes = (dtype == FCONV_INT8 || p.upsample)
-                   ? align_up(static_cast<size_t>(xh_elems) * 2, 256) : 0;
+  update_widen(p);
   p.ws_wt_off = 0;
   p.ws_xh_off = p.wt_bytes;
 
@@ -1243,6 +1290,23 @@ fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags) {
   if (flags & ~(FCONV_DEBUG_DROP_ARRIVE | FCONV_DEBUG_GATHER_CPASYNC))
     return fail(FCONV_ERR_INVALID_VALUE, "unknown flags");
   plan->debug = flags;
+  if (plan->num_phases == 0) update_widen(*plan);
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_input_widening(fconv_plan *plan, int mode) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (mode != FCONV_WIDEN_AUTO && mode != FCONV_WIDEN_IN_KERNEL && mode != FCONV_WIDEN_COPY)
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown widening mode %d", mode);
+  plan->widen_mode = mode;
+  if (plan->num_phases == 0) update_widen(*plan);
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_get_input_widening(const fconv_plan *plan, int *in_kernel) {
+  if (!plan || !in_kernel)
+    return fail(FCONV_ERR_INVALID_VALUE, "plan and in_kernel must not be NULL");
+  *in_kernel = plan->widen;
   return FCONV_OK;
 }
 
@@ -1266,7 +1330,8 @@ fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches) {
   // input is not a multiple of 64 elements, and the convolution
   auto one = [](const fconv_plan &p) {
     const long long n = static_cast<long long>(p.N) * p.H * p.W * p.C;
-    const bool tail = p.dtype == FCONV_INT8 && !p.subsample && !p.upsample && n % 64 != 0;
+    const bool tail =
+        p.dtype == FCONV_INT8 && !p.widen && !p.subsample && !p.upsample && n % 64 != 0;
     const bool prep = p.pack_filter || p.dtype == FCONV_INT8 || p.upsample || p.splits > 1;
     return (prep ? 1 : 0) + (tail ? 1 : 0) + 1;
   };

@@ -67,9 +67,12 @@ enum class Gather {
 // channels contiguous), boxes of 64 x 64.  overlap: the launch directly
 // before this one on the stream is this run's prep launch, which the
 // convolution may overlap (programmatic dependent launch).
+// widen: int8 plans on the TMA gather, unsplit, block_n <= 128: tmap_a maps
+// the int8 input itself (64-byte pixel rows) and the kernel widens it.
 cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
                         const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
-                        const ConvArgs &args, int grid, bool overlap, cudaStream_t stream);
+                        const ConvArgs &args, int grid, bool overlap, cudaStream_t stream,
+                        bool widen = false);
 // Whether a gather mode has a kernel for this output-channel tile; chunked
 // int8 sums on the cp.async path need a third TMEM region (BN <= 128).
 bool gather_supports(Gather gather, int block_n, bool chunked, int m_sub = 1);

@@ -102,6 +102,20 @@ __device__ __forceinline__ void load_b_tile(uint32_t dst, const CUtensorMap *map
     tma_load_2d(dst + j * 8192, map, n_tile * BN + 64 * j, kb * kBK, bar);
 }
 
+// Four int8 values (one 32-bit word) to two fp16x2 words, exactly: with the
+// sign bit flipped a byte b is u = b + 128 in [0, 255]; the fp16 bit pattern
+// 0x6400 | u is 1024 + u, and subtracting 1152 (0x6480) leaves b.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);   // [u0, 0x64, u1, 0x64]
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);   // [u2, 0x64, u3, 0x64]
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+  const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+  lo = *reinterpret_cast<const uint32_t *>(&ha);
+  hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
   return __uint_as_float(b16 << 16);
 }
@@ -724,17 +738,24 @@ struct TmaRegs {
 // one commit and one B copy per k-block for twice the MMA work), for tiles
 // narrower than 256 channels, where the issuing threads' fixed per-k-block
 // work, not the tensor cores, sets the pace.
-template <int BN, int MS = 1>
+// WIDEN: int8 activations are loaded as they are (64 bytes a pixel) into a
+// staging ring and widened to fp16 inside the kernel (see the converter
+// role below), instead of being read from a widened copy in global memory.
+template <int BN, int MS = 1, bool WIDEN = false>
 struct TmaCfg {
   static constexpr int kABytes = kBM * kBK * 2;        // one sub-tile's A
   static constexpr int kAStage = MS * kABytes;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kAStage + kBBytes;
-  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+  // staging of the int8 A tiles (WIDEN): 128 pixels x 64 bytes a sub-tile
+  static constexpr int kStgBytes = WIDEN ? MS * kBM * kBK : 0;
+  static constexpr int kStgStages = WIDEN ? (MS == 2 ? 3 : 4) : 0;
+  static constexpr int kStages0 = (200 * 1024 - kStgStages * kStgBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kAccCols = MS * BN;             // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols <= 128 ? 128 : 2 * kAccCols <= 256 ? 256 : 512;
-  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kStgOffset = kStages * kStageBytes;
+  static constexpr int kBarOffset = kStgOffset + kStgStages * kStgBytes;
   // columns per epilogue thread: MS = 1 splits a row's BN columns between
   // two warps; MS = 2 gives each warp half one sub-tile's whole rows
   static constexpr int kHalfCols = MS == 1 ? BN / 2 : BN;
@@ -753,15 +774,19 @@ struct TmaCfg {
   static_assert(MS == 1 || (MS == 2 && BN <= 128), "two sub-tiles need BN <= 128");
   static_assert(2 * kAccCols <= 512, "tensor memory");
   static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(!WIDEN || kHalfCols <= 64, "in-kernel widening needs the 96-register control warps");
 };
 
 // SPLITK: the split-K form (units of kb_per_split k-blocks, partial sums
 // and the last unit's reduction); the other instance keeps one unit a tile.
-template <int BN, bool IS_INT8, int MS, bool SPLITK>
+// WIDEN (int8, unsplit, BN <= 128): tmap_a is an im2col map of the int8
+// input itself; warps 2-3 widen each staged A tile into the fp16 stage.
+template <int BN, bool IS_INT8, int MS, bool SPLITK, bool WIDEN = false>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     conv_fprop_tma_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
-  using C = TmaCfg<BN, MS>;
+  static_assert(!WIDEN || (IS_INT8 && !SPLITK), "widening: int8, unsplit");
+  using C = TmaCfg<BN, MS, WIDEN>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8, /*b_mn=*/true);
   constexpr int kTileM = kBM * MS;
@@ -771,7 +796,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *sA = smem;   // per stage: MS sub-tiles of A, 16 KB each
   uint8_t *sB = smem + kStages * C::kAStage;
+  uint8_t *sStg = smem + C::kStgOffset;   // WIDEN: the int8 A staging ring
   Smem *bars = reinterpret_cast<Smem *>(smem + C::kBarOffset);
+  // WIDEN: the staging ring's barriers (the TMA kernel has no other use for
+  // full_a): full_a[i] = staged tile i landed, full_a[4 + i] = slot i read
+  uint64_t *stg_full = bars->full_a;
+  uint64_t *stg_empty = bars->full_a + 4;
   volatile int *abort_flag = &bars->abort_flag;
 
   // taken from lane 0 so that the compiler sees a warp-uniform value and the
@@ -782,8 +812,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars->full_b[s]), 1);
+      // WIDEN: the stage is full once the producer's B copy has landed and
+      // both converter warps have written the A tile
+      mbar_init(smem_u32(&bars->full_b[s]), WIDEN ? 3 : 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int i = 0; i < C::kStgStages; ++i) {
+      mbar_init(smem_u32(&stg_full[i]), 1);
+      mbar_init(smem_u32(&stg_empty[i]), 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars->acc_full[s]), 1);
@@ -819,6 +855,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const bool drop = (args.debug & 1) != 0;
     griddep_wait();   // the widened input and packed filter of the prep launch
     uint32_t stage = 0, phase = 0, issued = 0;
+    uint32_t sstage = 0, sphase = 0;   // WIDEN: the staging ring
     bool ok = true;
     const int num_units = args.num_tiles * splits;
     for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
@@ -843,19 +880,33 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       // filter tap and channel block of k-block kb (tap-major, channels fastest)
       int cb = ukb0 % cblocks, s = (ukb0 / cblocks) % args.S, r = ukb0 / cblocks / args.S;
       for (int kb = ukb0; kb < ukb1; ++kb) {
-        if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
+        if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo) ||
+            (WIDEN && !mbar_wait_warp(smem_u32(&stg_empty[sstage]), sphase ^ 1, abort_flag, tmo))) {
           ok = false;
           break;
         }
         if (!drop) {
           if (lane == 0) {
             const uint32_t fb = smem_u32(&bars->full_b[stage]);
-            mbar_arrive_expect_tx(fb, C::kAStage + C::kBBytes);
+            if (WIDEN) {
+              // int8 A (64 bytes a pixel) into the staging slot; the
+              // converter warps widen it into the stage
+              const uint32_t sf = smem_u32(&stg_full[sstage]);
+              mbar_arrive_expect_tx(sf, C::kStgBytes);
 #pragma unroll
-            for (int u = 0; u < MS; ++u)
-              tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage + u * C::kABytes), &tmap_a,
-                                 cb * kBK, w0[u], h0[u], n0[u], static_cast<uint16_t>(s),
-                                 static_cast<uint16_t>(r), fb);
+              for (int u = 0; u < MS; ++u)
+                tma_load_im2col_4d(smem_u32(sStg + sstage * C::kStgBytes + u * kBM * kBK),
+                                   &tmap_a, cb * kBK, w0[u], h0[u], n0[u],
+                                   static_cast<uint16_t>(s), static_cast<uint16_t>(r), sf);
+              mbar_arrive_expect_tx(fb, C::kBBytes);
+            } else {
+              mbar_arrive_expect_tx(fb, C::kAStage + C::kBBytes);
+#pragma unroll
+              for (int u = 0; u < MS; ++u)
+                tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage + u * C::kABytes), &tmap_a,
+                                   cb * kBK, w0[u], h0[u], n0[u], static_cast<uint16_t>(s),
+                                   static_cast<uint16_t>(r), fb);
+            }
             load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, fb);
           }
           __syncwarp();
@@ -866,6 +917,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           if (++s == args.S) { s = 0; ++r; }
         }
         if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (WIDEN && ++sstage == C::kStgStages) { sstage = 0; sphase ^= 1; }
       }
     }
     if (lane == 0) {
@@ -874,8 +926,64 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const uint32_t first = issued > static_cast<uint32_t>(kStages) ? issued - kStages : 0;
       for (uint32_t i = first; i < issued; ++i)
         mbar_wait_drain(smem_u32(&bars->full_b[i % kStages]), (i / kStages) & 1u, 100000000ull);
+      if constexpr (WIDEN) {
+        const uint32_t sfirst =
+            issued > static_cast<uint32_t>(C::kStgStages) ? issued - C::kStgStages : 0;
+        for (uint32_t i = sfirst; i < issued; ++i)
+          mbar_wait_drain(smem_u32(&stg_full[i % C::kStgStages]), (i / C::kStgStages) & 1u,
+                          100000000ull);
+      }
     }
     __syncwarp();
+  } else if (WIDEN && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ converters
+    // Widen each staged int8 A tile into the fp16 stage the MMA reads, in the
+    // 128-byte-swizzled K-major layout a TMA copy would have written: staged
+    // row r (a pixel, 64 bytes) becomes stage row r (128 bytes), its 16-byte
+    // chunk j at position j ^ (r & 7).  The two warps follow the producer's
+    // k-block sequence; each widens half of the tile's 16-byte pieces, then
+    // fences its writes to the async proxy and signals the stage full and
+    // the staging slot free.
+    const int ct = (warp - 2) * 32 + lane;   // 0..63
+    uint32_t stage = 0, phase = 0, sstage = 0, sphase = 0;
+    bool ok = true;
+    const int num_units = args.num_tiles * splits;
+    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      const int ukb0 = (unit % splits) * kb_per_split;
+      const int ukb1 = min(num_kb, ukb0 + kb_per_split);
+      for (int kb = ukb0; kb < ukb1; ++kb) {
+        if (!mbar_wait_warp(smem_u32(&stg_full[sstage]), sphase, abort_flag, tmo) ||
+            !mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        const uint8_t *src = sStg + sstage * C::kStgBytes;
+        uint8_t *dst = sA + stage * C::kAStage;
+#pragma unroll
+        for (int i = 0; i < MS * 8; ++i) {
+          const int q = ct + 64 * i;            // piece: sub-tile u, row r, 16 bytes p
+          const int u = q >> 9, r = (q >> 2) & 127, pc = q & 3;
+          const uint4 in = *reinterpret_cast<const uint4 *>(src + u * (kBM * kBK) + r * 64 +
+                                                            pc * 16);
+          uint4 lo, hi;
+          i8x4_to_f16x4(in.x, lo.x, lo.y);
+          i8x4_to_f16x4(in.y, lo.z, lo.w);
+          i8x4_to_f16x4(in.z, hi.x, hi.y);
+          i8x4_to_f16x4(in.w, hi.z, hi.w);
+          uint8_t *row = dst + u * C::kABytes + r * 128;
+          *reinterpret_cast<uint4 *>(row + (((2 * pc) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4 *>(row + (((2 * pc + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_proxy_async_smem();   // the stage is read by the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&bars->full_b[stage]));
+          mbar_arrive(smem_u32(&stg_empty[sstage]));
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++sstage == C::kStgStages) { sstage = 0; sphase ^= 1; }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (warp-uniform state); lane 0 issues.
@@ -1226,20 +1334,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // taps, bf16 copied); the remaining blocks copy the input (int8 widened to
 // fp16; subsampled or upsampled copies), 64 elements a thread per step.
 
-// Four int8 values (one 32-bit word) to two fp16x2 words, exactly: with the
-// sign bit flipped a byte b is u = b + 128 in [0, 255]; the fp16 bit pattern
-// 0x6400 | u is 1024 + u, and subtracting 1152 (0x6480) leaves b.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);   // [u0, 0x64, u1, 0x64]
-  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);   // [u2, 0x64, u3, 0x64]
-  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-  const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
-  const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
-  lo = *reinterpret_cast<const uint32_t *>(&ha);
-  hi = *reinterpret_cast<const uint32_t *>(&hb);
-}
-
 constexpr int kPrepThreads = 256;
 
 __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv &d) {
@@ -1445,12 +1539,12 @@ static void note_attributes(Kern kern, int threads, int smem) {
 
 const char *last_launch_note() { return t_kernel_note; }
 
-template <int BN, bool IS_INT8, int MS, bool SPLITK = false>
+template <int BN, bool IS_INT8, int MS, bool SPLITK = false, bool WIDEN = false>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                                 const ConvArgs &args, int grid, bool overlap,
                                 cudaStream_t stream) {
-  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK>;
-  using Cfg = TmaCfg<BN, MS>;
+  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK, WIDEN>;
+  using Cfg = TmaCfg<BN, MS, WIDEN>;
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
   if (e == cudaSuccess) {
@@ -1473,11 +1567,25 @@ bool gather_supports(Gather gather, int block_n, bool chunked, int m_sub) {
 
 cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
                         const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
-                        const ConvArgs &args, int grid, bool overlap, cudaStream_t stream) {
+                        const ConvArgs &args, int grid, bool overlap, cudaStream_t stream,
+                        bool widen) {
   const bool chunked = args.kb_chunk < args.num_kb;
   if (chunked && !is_int8) return cudaErrorInvalidValue;
   if (!gather_supports(gather, block_n, chunked, m_sub)) return cudaErrorInvalidValue;
   if (args.kb_chunk <= 0 || grid <= 0) return cudaErrorInvalidValue;
+  if (widen) {
+    // int8 activations widened in the kernel: TMA gather, unsplit, <= 128 channels
+    if (!is_int8 || gather != Gather::kTmaIm2col || args.splits > 1 || block_n > 128 ||
+        args.C % kBK != 0)
+      return cudaErrorInvalidValue;
+    if (m_sub == 2) {   // 256-pixel tiles of 64 channels only (64 sums an epilogue thread)
+      if (block_n != 64) return cudaErrorInvalidValue;
+      return launch_tma_t<64, true, 2, false, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+    }
+    return block_n == 64
+               ? launch_tma_t<64, true, 1, false, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+               : launch_tma_t<128, true, 1, false, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+  }
   if (gather == Gather::kTmaIm2col && m_sub == 2) {
     if (args.C % kBK != 0) return cudaErrorInvalidValue;
     if (block_n == 64)

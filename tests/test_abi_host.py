@@ -190,7 +190,14 @@ def test_workspace_sizes():
     h = fc.fconv_plan_create(64, 28, 28, 256, 512, 1, 1, 2, 2, 1, 0, 1)
     try:
         # 1x1 stride 2, int8: only the strided pixels are widened ([64][14][14][256])
+        assert fc.fconv_plan_get_input_widening(h) == 0
         assert fc.fconv_workspace_size(h) == 512 * 256 * 2 + 64 * 14 * 14 * 256 * 2
+        # widened inside the kernel instead: the fp16 filter alone
+        fc.fconv_plan_set_input_widening(h, fc.FCONV_WIDEN_IN_KERNEL)
+        assert fc.fconv_plan_get_input_widening(h) == 1
+        assert fc.fconv_workspace_size(h) == 512 * 256 * 2
+        fc.fconv_plan_set_input_widening(h, fc.FCONV_WIDEN_AUTO)
+        assert fc.fconv_plan_get_input_widening(h) == 0
     finally:
         fc.fconv_plan_destroy(h)
     h = fc.fconv_plan_create(32, 14, 14, 256, 256, 3, 3, 1, 1, 0, 1, 1)

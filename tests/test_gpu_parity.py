@@ -664,3 +664,46 @@ def test_cpasync_debug_hook_leaves_the_plan_tiling():
     p.check()
     c.check_output(to_host(y), c.oracle_out())
     p.close()
+
+
+# ---------------------------------------------------------------- in-kernel widening
+# int8 activations widened by the convolution kernel (staged int8 tiles,
+# converter warps) against the same plans with an fp16 copy of the input:
+# identical sums and outputs, both equal to the oracle
+WIDEN_CASES = [
+    ((2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, True), None),          # K tail, side input
+    ((2, 9, 11, 64, 64, 3, 3, 1, "SAME", True, True), (256, 64)),     # 256-pixel tiles
+    ((3, 8, 8, 128, 64, 3, 3, 2, "SAME", False, True), None),         # stride 2, odd pads
+    ((3, 11, 13, 64, 80, 1, 1, (2, 3), "SAME", True, True), None),    # 1x1 strided
+    ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True), (128, 128)), # chunked sums
+    ((1, 7, 7, 128, 32, 7, 7, 1, "VALID", True, True), None),         # full window
+    ((5, 6, 6, 256, 256, 1, 1, 1, "SAME", False, False), (128, 128)), # 1x1 stride 1
+]
+
+
+@pytest.mark.parametrize("i,item", list(enumerate(WIDEN_CASES)))
+def test_in_kernel_widening(i, item):
+    params, shape = item
+    c = sweep_case(980 + i, params, "int8")
+    acc_ref = c.oracle_acc()
+    ref = c.oracle_out(acc_ref)
+    got = {}
+    for mode in (fc.FCONV_WIDEN_IN_KERNEL, fc.FCONV_WIDEN_COPY):
+        p = c.plan()
+        if shape:
+            fc.fconv_plan_set_tile_shape(p.handle, *shape)
+        fc.fconv_plan_set_splits(p.handle, 1)   # widening runs unsplit
+        fc.fconv_plan_set_input_widening(p.handle, mode)
+        assert fc.fconv_plan_get_input_widening(p.handle) == (mode == fc.FCONV_WIDEN_IN_KERNEL)
+        x, w = to_dev(c.x, "int8"), to_dev(c.w, "int8")
+        bias, side = torch.from_numpy(c.bias).cuda(), to_dev(c.side, "int8")
+        acc = p.accumulators(x, w)
+        y = p.run(x, w, bias, side, c.conv_scale, c.side_scale)
+        y2 = p.run(x, w, bias, side, c.conv_scale, c.side_scale)   # the staging ring reused
+        p.check()
+        c.check_acc(acc.cpu().numpy(), acc_ref)
+        c.check_output(to_host(y), ref)
+        assert torch.equal(y, y2)
+        got[mode] = to_host(y)
+        p.close()
+    assert np.array_equal(got[fc.FCONV_WIDEN_IN_KERNEL], got[fc.FCONV_WIDEN_COPY])
