@@ -332,6 +332,11 @@ def run_fconv(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = FI.workload(args.workload)
+    if args.batch:
+        # a smaller batch of the same layer (profiling captures of a size a
+        # profiler replays quickly; not a benchmark configuration)
+        import dataclasses
+        wl = dataclasses.replace(wl, N=args.batch, note=wl.note + f" (batch {args.batch})")
     nominal, inbounds, P, Q = ops_counts(wl)
     # weak scaling: every rank convolves the whole batch; strong: the batch
     # is split over the ranks (shard_range) and each convolves its images
@@ -622,6 +627,8 @@ def main():
     ap.add_argument("--tile", type=int, default=0)
     ap.add_argument("--tile-shape", default="",
                     help="PIXELS,CHANNELS: force the output tile (128 or 256 pixels)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload's layer on this many images (profiling only)")
     ap.add_argument("--widen", type=int, default=0, choices=[0, 1, 2],
                     help="int8 input widening: 0 automatic, 1 in the kernel, 2 an fp16 copy")
     ap.add_argument("--splits", type=int, default=0,
