@@ -560,6 +560,9 @@ def run_fconv(args, rank, world, local_rank):
     # tensor peak, bytes at the copy bandwidth) is the longer
     hbm_achieved = abytes / conv_avg_s / 1e9
     hbm_bound = abytes / (hbm * 1e9) > inbounds_local / (peak * 1e12)
+    kernel_form = fc.fconv_plan_kernel(plan.handle)
+    kernel_fn = ("conv_fprop_cpasync_kernel" if kernel_form.startswith("cp-async")
+                 else "conv_fprop_tma_kernel")
     roofline = {"bound": "hbm" if hbm_bound else "tensor",
                 "achieved": hbm_achieved if hbm_bound else achieved,
                 "peak": hbm if hbm_bound else peak,
@@ -574,8 +577,8 @@ def run_fconv(args, rank, world, local_rank):
                 "sm_mhz": mhz, "cycles_per_launch": cycles,
                 "ideal_tensor_cycles": ideal_cycles,
                 "tensor_cycle_frac": ideal_cycles / cycles if cycles else None,
-                "kernel": f"conv_fprop_kernel<{plan.config()[0]}, {wl.dtype}> "
-                          f"({fc.fconv_plan_kernel(plan.handle)}, tcgen05.mma kind::f16)",
+                "kernel": (f"{kernel_fn}<{plan.config()[0]}, {wl.dtype}> "
+                           f"({kernel_form}, tcgen05.mma kind::f16)"),
                 "peak_source": (f"copy bandwidth of {src}" if hbm_bound else
                                 f"{'sustained' if long_run else 'burst'} bf16 dense of {src} "
                                 f"(fp16 rate = bf16 rate; no int8 tensor-core MMA on sm_103a)"),
@@ -596,7 +599,7 @@ def run_fconv(args, rank, world, local_rank):
                            f" > {L2_BYTES / 1e6:.0f} MB") if flush is None else
                           (f"L2 flushed before every step (x+w+side+y+workspace = "
                            f"{footprint / 1e6:.0f} MB); steps timed by their own events")),
-        "stage_ms": {"prep (filter pack + int8->fp16 widening)": statistics.mean(prep_ms),
+        "stage_ms": {"prep (filter copy + int8->fp16 widening)": statistics.mean(prep_ms),
                      "conv": statistics.mean(conv_ms)},
         "roofline": roofline,
         "e2e": e2e,

@@ -63,6 +63,7 @@ struct fconv_plan {
   // output row and column (owned by this plan)
   int num_phases;
   fconv_plan *phase[64];
+  int sm_share;   // a phase: how many phases share the SMs at once (tile choice)
   // side streams on which the phases after the first run concurrently with
   // it (fork after the input copy, join before the run returns)
   int fork_dev;   // device they belong to, -1 = none
@@ -194,8 +195,8 @@ fconv::Gather gather_for_run(const fconv_plan &p) {
 // MMAs of a 128 x BN x 64 block take ~2*BN on the tensor core, and the
 // issuing threads' per-k-block work (barrier waits, copy and MMA issue) a
 // fixed G whatever BN is (~500 on the TMA path with one 128-pixel sub-tile,
-// ~900 with two, ~800 on the cp.async path; measured per k-block in
-// steady state, operand traffic included).  Tiles run in waves
+// ~700 with two and two MMA issuers, ~800 on the cp.async path; measured
+// per k-block in steady state, operand traffic included).  Tiles run in waves
 // over the SMs; the epilogue of a CTA's last tile (~8 cycles per output
 // column per 128 pixels) is not hidden behind a next tile's mainloop.
 // Split-K (splits > 1 units per tile, TMA gather, forward plans): a unit
@@ -219,7 +220,7 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
       fconv::Gather g = gather_for(p, bn, false);
       if (!fconv::gather_supports(g, bn, chunked, ms)) continue;
       const long long fixed =
-          g == fconv::Gather::kTmaIm2col ? (ms == 2 ? 900 : 500) : 800;
+          g == fconv::Gather::kTmaIm2col ? (ms == 2 ? 700 : 500) : 800;
       const long long m_tiles = (p.M + 128LL * ms - 1) / (128LL * ms);
       const long long tiles = m_tiles * ((p.K + bn - 1) / bn);
       const long long work = 2LL * bn * ms;
@@ -476,8 +477,9 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
 
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
-  // filter pack and input copy (int8 widening; subsampled or upsampled
-  // copies) in one launch; the convolution reads the copy when there is one
+  // filter copy (int8 widened; transposed plans' taps flipped) and input
+  // copy (int8 widening; subsampled or upsampled copies) in one launch; the
+  // convolution reads the copies when there are some
   const InputView view = input_view(*p);
   const int gH = view.H, gW = view.W, gsh = view.sh, gsw = view.sw;
   const bool copy = (is_int8 && !p->widen) || p->upsample;   // the convolution reads a copy
@@ -519,32 +521,56 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
 
   // B: the filter as the [R*S*C][K] matrix of its HWIO layout, 16-bit, in
-  // boxes of 64 output channels x 64 k-rows (rows past R*S*C and channels
-  // past K read as zero)
+  // blocks of 64 output channels x 64 k-rows (rows past R*S*C and channels
+  // past K read as zero).  K a multiple of 64 (and at least block_n): the
+  // 3-D view {64 channels, rows, K / 64 blocks} (row stride K * 2 bytes,
+  // block stride 128 bytes), whose {64, 64, block_n / 64} box is a whole B
+  // tile in one copy; else the 2-D matrix in 64 x 64 boxes.
   const void *bsrc = p->pack_filter ? static_cast<const void *>(wt) : w;
+  const int b3d = (p->K % 64 == 0 && p->block_n <= p->K) ? 1 : 0;
   fconv_plan::MapCache &mb = p->map_b;
-  if (!(mb.valid && mb.base == bsrc)) {
+  if (!(mb.valid && mb.base == bsrc && mb.form == b3d && (!b3d || mb.n == p->block_n))) {
     mb.valid = false;
     memset(&mb.map, 0, sizeof mb.map);
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->K), static_cast<cuuint64_t>(p->Ktot)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->K) * 2};
-    const cuuint32_t box[2] = {64, 64};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult cr = encode(&mb.map,
-                         is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                         2, const_cast<void *>(bsrc), gdim, gstride, box, estride,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType bt =
+        is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult cr;
+    if (b3d) {
+      const cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(p->Ktot),
+                                  static_cast<cuuint64_t>(p->K / 64)};
+      const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(p->K) * 2, 128};
+      const cuuint32_t box[3] = {64, 64, static_cast<cuuint32_t>(p->block_n / 64)};
+      const cuuint32_t estride[3] = {1, 1, 1};
+      cr = encode(&mb.map, bt, 3, const_cast<void *>(bsrc), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->K),
+                                  static_cast<cuuint64_t>(p->Ktot)};
+      const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->K) * 2};
+      const cuuint32_t box[2] = {64, 64};
+      const cuuint32_t estride[2] = {1, 1};
+      cr = encode(&mb.map, bt, 2, const_cast<void *>(bsrc), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (cr != CUDA_SUCCESS)
       return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
     mb.base = bsrc;
+    mb.n = p->block_n;
+    mb.form = b3d;
     mb.valid = true;
   }
   const CUtensorMap &tmap = mb.map;
 
+  // A: one im2col copy per k-block of a whole tile's pixels (128, or 256
+  // for two sub-tiles: the second continues the first's walk); widening in
+  // the kernel copies each 128-pixel sub-tile into its own staging slot
+  const int a_pixels = p->widen ? 128 : 128 * p->m_sub;
+  const int a_form = (p->widen ? 1 : 0) | (a_pixels << 1);
   fconv_plan::MapCache &ma = p->map_a;
   if (gather == fconv::Gather::kTmaIm2col &&
-      !(ma.valid && ma.base == act && ma.n == p->N && ma.form == (p->widen ? 1 : 0))) {
+      !(ma.valid && ma.base == act && ma.n == p->N && ma.form == a_form)) {
     ma.valid = false;
     memset(&ma.map, 0, sizeof ma.map);
     CUtensorMap &tmap_a = ma.map;
@@ -570,7 +596,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
                          p->widen ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                   : is_int8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                         4, const_cast<void *>(act), adim, astride_e, lower, upper, 64, 128,
+                         4, const_cast<void *>(act), adim, astride_e, lower, upper, 64,
+                         static_cast<cuuint32_t>(a_pixels),
                          traverse, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          p->widen ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -578,7 +605,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
       return fail(FCONV_ERR_INTERNAL, "im2col tensor map encode failed (%d)", (int)cra);
     ma.base = act;
     ma.n = p->N;
-    ma.form = p->widen ? 1 : 0;
+    ma.form = a_form;
     ma.valid = true;
   }
   static const CUtensorMap kNoMap = {};
@@ -600,6 +627,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.kb_chunk = p->kb_chunk;
   a.num_n_tiles = p->num_n_tiles;
   a.num_tiles = p->num_tiles;
+  a.b3d = b3d;
   a.conv_scale = conv_scale;
   a.side_scale = side_scale;
   a.act = static_cast<int>(p->act);
@@ -806,7 +834,10 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   p.subsample =
       (!p.transposed && dtype == FCONV_INT8 && R == 1 && S == 1 && (stride_h > 1 || stride_w > 1))
           ? 1 : 0;
-  const TileChoice tile = choose_tile(p, sm_count_of_current_device(148));
+  // the phases of a strided transposed plan run concurrently (up to four
+  // streams), each on its share of the SMs
+  const int sms = sm_count_of_current_device(148);
+  const TileChoice tile = choose_tile(p, p.sm_share > 1 ? sms / p.sm_share : sms);
   p.auto_block_n = tile.bn;
   p.auto_m_sub = tile.ms;
   p.auto_splits = tile.splits;
@@ -920,6 +951,7 @@ fconv_status fconv_plan_create_transposed(fconv_plan **plan, int N, int H, int W
       q.tap_r0 = a; q.tap_s0 = b; q.tap_rstep = stride_h; q.tap_sstep = stride_w;
       q.omap = 1; q.out_H = static_cast<int>(Ho); q.out_W = static_cast<int>(Wo);
       q.o_sh = stride_h; q.o_sw = stride_w;
+      q.sm_share = stride_h * stride_w < 4 ? stride_h * stride_w : 4;
       q.o_h0 = static_cast<int>(stride_h * u_lo + a - pad_top);
       q.o_w0 = static_cast<int>(stride_w * v_lo + b - pad_left);
       fconv_plan *made = nullptr;

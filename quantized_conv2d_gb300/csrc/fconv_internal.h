@@ -34,6 +34,7 @@ struct ConvArgs {
   int kb_chunk;        // k-blocks per fp32 accumulation
   int num_n_tiles;     // ceil(K / BN)
   int num_tiles;       // ceil(M / 128) * num_n_tiles
+  int b3d;             // tmap_b is the 3-D {64, rows, K / 64} view (K % 64 == 0)
   float conv_scale, side_scale;
   int act;             // kAct*
   // output pixel of GEMM row m (a phase of a strided transposed convolution
@@ -64,7 +65,8 @@ enum class Gather {
 // m_sub: 128-pixel sub-tiles per output tile (1, or 2 on the TMA gather
 // with block_n <= 128; args.num_tiles counts tiles of 128 * m_sub pixels).
 // tmap_b: the filter as a [rows][K] 16-bit matrix (HWIO order, output
-// channels contiguous), boxes of 64 x 64.  overlap: the launch directly
+// channels contiguous), boxes of 64 x 64; with args.b3d the 3-D view
+// {64 channels, rows, K / 64 blocks} with boxes of {64, 64, block_n / 64}.  overlap: the launch directly
 // before this one on the stream is this run's prep launch, which the
 // convolution may overlap (programmatic dependent launch).
 // widen: int8 plans on the TMA gather, unsplit, block_n <= 128: tmap_a maps

@@ -90,16 +90,24 @@ struct Smem {
 
 // The B (filter) tile of k-block kb and output-channel tile n_tile, MN-major:
 // the filter is read as the [R*S*C][K] matrix of its HWIO layout (output
-// channels contiguous), in BN / 64 boxes of 64 channels x 64 k-rows, each
+// channels contiguous), as BN / 64 blocks of 64 channels x 64 k-rows, each
 // 8 KB, 128-byte swizzled (see sw128_mnmajor_desc).  Rows past R*S*C and
-// channels past K read as zero.
+// channels past K read as zero.  b3d (K a multiple of 64): the tensor map
+// views the matrix as {64 channels, rows, K / 64 channel blocks} and one
+// copy of a {64, 64, BN / 64} box writes the whole tile in that layout;
+// otherwise each block is its own 2-D copy.  The copies a producer issues,
+// not their bytes, bound how fast it fills stages, so one copy is cheaper.
 constexpr uint64_t kBStepK = 2048 >> 4;   // descriptor step of 16 k-rows
 template <int BN>
 __device__ __forceinline__ void load_b_tile(uint32_t dst, const CUtensorMap *map, int kb,
-                                            int n_tile, uint32_t bar) {
+                                            int n_tile, int b3d, uint32_t bar) {
+  if (b3d) {
+    tma_load_3d(dst, map, 0, kb * kBK, n_tile * (BN / 64), bar);
+  } else {
 #pragma unroll
-  for (int j = 0; j < BN / 64; ++j)
-    tma_load_2d(dst + j * 8192, map, n_tile * BN + 64 * j, kb * kBK, bar);
+    for (int j = 0; j < BN / 64; ++j)
+      tma_load_2d(dst + j * 8192, map, n_tile * BN + 64 * j, kb * kBK, bar);
+  }
 }
 
 // Four int8 values (one 32-bit word) to two fp16x2 words, exactly: with the
@@ -499,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) {
           const uint32_t fb = smem_u32(&bars->full_b[stage]);
           mbar_arrive_expect_tx(fb, C::kBBytes);
-          load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, fb);
+          load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, args.b3d, fb);
           ++issued;
         }
         const uint32_t a_base = smem_u32(sA + stage * C::kABytes);
@@ -701,9 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- TMA path
 // Used when C % 64 == 0 (a k-block is 64 channels of one filter tap).
-// 384 threads in three warpgroups.  Warpgroup 0: warp 0 lane 0 issues the
-// TMA loads (A by im2col, B tiled) onto one barrier per stage; warp 1
-// allocates TMEM and lane 0 issues the MMAs; warps 2-3 idle.  Warpgroups 1-2
+// 384 threads in three warpgroups.  Warpgroup 0: lane 0 of warp 0 issues
+// the A loads (im2col) and lane 0 of warp 2 the B loads (tiled) of each
+// stage onto the stage's full barrier; warp 1 allocates TMEM and lane 0
+// issues the MMAs, with lane 0 of warp 3 issuing those of the second
+// sub-tile on 256-pixel tiles (WIDEN: warp 0 issues both loads, warps 2-3
+// widen the staged A, warp 1 issues every MMA).  Warpgroups 1-2
 // (warps 4-11) run the epilogue, two warps per TMEM lane quarter, each owning
 // half of the BN columns.  int8 sums longer than one exact chunk are folded
 // into int32 registers of those threads, so all 512 TMEM columns hold a
@@ -790,6 +801,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8, /*b_mn=*/true);
   constexpr int kTileM = kBM * MS;
+  // Two MMA issuers (warps 1 and 3) for 256-pixel tiles: one thread issues a
+  // tcgen05.mma no faster than about one per 105-120 cycles, while the
+  // tensor core finishes a 128 x N x 16 MMA in about max(N / 2, 32 + N / 4)
+  // cycles, so a single issuer leaves the tensor core idle on N <= 128.
+  // Each issuer owns one 128-pixel sub-tile (its accumulator columns) and
+  // commits to the stage and accumulator barriers, which then take two
+  // arrivals.  (Splitting a 128-pixel tile's channels between two issuers,
+  // N = BN / 2 each, measured slower on every 128 x 128 workload.)
+  constexpr bool kDualMma = !WIDEN && MS == 2;
+  constexpr int kMmaArrivals = kDualMma ? 2 : 1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -812,20 +833,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // WIDEN: the stage is full once the producer's B copy has landed and
-      // both converter warps have written the A tile
-      mbar_init(smem_u32(&bars->full_b[s]), WIDEN ? 3 : 1);
-      mbar_init(smem_u32(&bars->empty[s]), 1);
+      // the stage is full once both producers' copies have landed (A from
+      // warp 0, B from warp 2); WIDEN: once the producer's B copy has landed
+      // and both converter warps have written the A tile
+      mbar_init(smem_u32(&bars->full_b[s]), WIDEN ? 3 : 2);
+      mbar_init(smem_u32(&bars->empty[s]), kMmaArrivals);
     }
     for (int i = 0; i < C::kStgStages; ++i) {
       mbar_init(smem_u32(&stg_full[i]), 1);
       mbar_init(smem_u32(&stg_empty[i]), 2);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bars->acc_full[s]), 1);
+      mbar_init(smem_u32(&bars->acc_full[s]), kMmaArrivals);
       mbar_init(smem_u32(&bars->acc_empty[s]), kTmaEpiWarps);
     }
-    mbar_init(smem_u32(&bars->mma_done), 1);
+    mbar_init(smem_u32(&bars->mma_done), kMmaArrivals);
     bars->abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmap_a);
@@ -879,6 +901,37 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       // filter tap and channel block of k-block kb (tap-major, channels fastest)
       int cb = ukb0 % cblocks, s = (ukb0 / cblocks) % args.S, r = ukb0 / cblocks / args.S;
+      if constexpr (!WIDEN) {
+        // A only: warp 2 copies each stage's B.  (Waiting for two free
+        // stages and filling both in one pass measured slower: it gives up a
+        // stage of lookahead.)
+        for (int kb = ukb0; kb < ukb1; ++kb) {
+          if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          if (!drop) {
+            if (lane == 0) {
+              // one copy of the tile's 128 * MS pixels: the tensor map's
+              // walk length is the tile's, so a second sub-tile continues
+              // the first one's walk
+              const uint32_t fb = smem_u32(&bars->full_b[stage]);
+              mbar_arrive_expect_tx(fb, C::kAStage);
+              tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage), &tmap_a, cb * kBK, w0[0],
+                                 h0[0], n0[0], static_cast<uint16_t>(s),
+                                 static_cast<uint16_t>(r), fb);
+            }
+            __syncwarp();
+            ++issued;
+          }
+          if (++cb == cblocks) {
+            cb = 0;
+            if (++s == args.S) { s = 0; ++r; }
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        continue;
+      }
       for (int kb = ukb0; kb < ukb1; ++kb) {
         if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo) ||
             (WIDEN && !mbar_wait_warp(smem_u32(&stg_empty[sstage]), sphase ^ 1, abort_flag, tmo))) {
@@ -887,27 +940,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         if (!drop) {
           if (lane == 0) {
+            // WIDEN: int8 A (64 bytes a pixel) into the staging slot, which
+            // the converter warps widen into the stage, and the stage's B
             const uint32_t fb = smem_u32(&bars->full_b[stage]);
-            if (WIDEN) {
-              // int8 A (64 bytes a pixel) into the staging slot; the
-              // converter warps widen it into the stage
-              const uint32_t sf = smem_u32(&stg_full[sstage]);
-              mbar_arrive_expect_tx(sf, C::kStgBytes);
+            const uint32_t sf = smem_u32(&stg_full[sstage]);
+            mbar_arrive_expect_tx(sf, C::kStgBytes);
 #pragma unroll
-              for (int u = 0; u < MS; ++u)
-                tma_load_im2col_4d(smem_u32(sStg + sstage * C::kStgBytes + u * kBM * kBK),
-                                   &tmap_a, cb * kBK, w0[u], h0[u], n0[u],
-                                   static_cast<uint16_t>(s), static_cast<uint16_t>(r), sf);
-              mbar_arrive_expect_tx(fb, C::kBBytes);
-            } else {
-              mbar_arrive_expect_tx(fb, C::kAStage + C::kBBytes);
-#pragma unroll
-              for (int u = 0; u < MS; ++u)
-                tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage + u * C::kABytes), &tmap_a,
-                                   cb * kBK, w0[u], h0[u], n0[u], static_cast<uint16_t>(s),
-                                   static_cast<uint16_t>(r), fb);
-            }
-            load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, fb);
+            for (int u = 0; u < MS; ++u)
+              tma_load_im2col_4d(smem_u32(sStg + sstage * C::kStgBytes + u * kBM * kBK),
+                                 &tmap_a, cb * kBK, w0[u], h0[u], n0[u],
+                                 static_cast<uint16_t>(s), static_cast<uint16_t>(r), sf);
+            mbar_arrive_expect_tx(fb, C::kBBytes);
+            load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, args.b3d,
+                            fb);
           }
           __syncwarp();
           ++issued;
@@ -933,6 +978,48 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           mbar_wait_drain(smem_u32(&stg_full[i % C::kStgStages]), (i / C::kStgStages) & 1u,
                           100000000ull);
       }
+    }
+    __syncwarp();
+  } else if (!WIDEN && warp == 2) {
+    // ------------------------------------------------------------ B producer
+    // The filter tile of every k-block, into the same stages as warp 0's A
+    // copies (each stage's full barrier takes both arrivals).  A producer's
+    // stage rate is bound by the per-stage work of its issuing thread (the
+    // barrier wait, the expect-tx arrival and each copy it issues), not by
+    // the bytes, so two issuing warps fill stages faster than one.
+    const bool drop = (args.debug & 1) != 0;
+    griddep_wait();   // the filter copy of the prep launch
+    uint32_t stage = 0, phase = 0, issued = 0;
+    bool ok = true;
+    const int num_units = args.num_tiles * splits;
+    for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
+      const int tile = unit / splits;
+      const int ukb0 = (unit - tile * splits) * kb_per_split;
+      const int ukb1 = min(num_kb, ukb0 + kb_per_split);
+      const int n_tile = tile % args.num_n_tiles;
+      for (int kb = ukb0; kb < ukb1; ++kb) {
+        if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        if (!drop) {
+          if (lane == 0) {
+            const uint32_t fb = smem_u32(&bars->full_b[stage]);
+            mbar_arrive_expect_tx(fb, C::kBBytes);
+            load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, args.b3d,
+                            fb);
+          }
+          __syncwarp();
+          ++issued;
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (lane == 0) {
+      // let any copy still in flight land before the CTA exits
+      const uint32_t first = issued > static_cast<uint32_t>(kStages) ? issued - kStages : 0;
+      for (uint32_t i = first; i < issued; ++i)
+        mbar_wait_drain(smem_u32(&bars->full_b[i % kStages]), (i / kStages) & 1u, 100000000ull);
     }
     __syncwarp();
   } else if (WIDEN && (warp == 2 || warp == 3)) {
@@ -984,12 +1071,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (++sstage == C::kStgStages) { sstage = 0; sphase ^= 1; }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (kDualMma && warp == 3)) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (warp-uniform state); lane 0 issues.
     // Two k-blocks (stages) per iteration: one wait round trip and one pass
-    // of loop control for 8 MMAs (the issuing thread, not the tensor core,
-    // bounds tiles narrower than 256).
+    // of loop control for each group of MMAs.  kDualMma: warps 1 and 3 both
+    // run this loop, each issuing its part of every k-block's MMAs.
+    const int part = warp == 3 ? 1 : 0;
     uint32_t stage = 0, phase = 0, astage = 0, aphase = 0;
     bool ok = true;
     const int num_units = args.num_tiles * splits;
@@ -1021,21 +1109,37 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           // a sub-tile's A is 16 KB further: + (16384 >> 4) in the descriptor
           constexpr uint64_t kSubStep = static_cast<uint64_t>(C::kABytes >> 4);
           if (lane == 0) {
-#pragma unroll
-            for (int u = 0; u < MS; ++u)
+            if constexpr (kDualMma && MS == 2) {
+              // this issuer's 128-pixel sub-tile
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k)
-                umma_f16(d + u * BN, adesc + u * kSubStep + 2 * k, bdesc + kBStepK * k, kIdesc,
-                         (kb > kb0 || k > 0) ? 1u : 0u);
-            umma_commit(smem_u32(&bars->empty[stage]));
-            if (pair) {
+                umma_f16(d + part * BN, adesc + part * kSubStep + 2 * k, bdesc + kBStepK * k,
+                         kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              umma_commit(smem_u32(&bars->empty[stage]));
+              if (pair) {
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                  umma_f16(d + part * BN, adesc1 + part * kSubStep + 2 * k,
+                           bdesc1 + kBStepK * k, kIdesc, 1u);
+                umma_commit(smem_u32(&bars->empty[stage1]));
+              }
+            } else {
 #pragma unroll
               for (int u = 0; u < MS; ++u)
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k)
-                  umma_f16(d + u * BN, adesc1 + u * kSubStep + 2 * k, bdesc1 + kBStepK * k,
-                           kIdesc, 1u);
-              umma_commit(smem_u32(&bars->empty[stage1]));
+                  umma_f16(d + u * BN, adesc + u * kSubStep + 2 * k, bdesc + kBStepK * k,
+                           kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              umma_commit(smem_u32(&bars->empty[stage]));
+              if (pair) {
+#pragma unroll
+                for (int u = 0; u < MS; ++u)
+#pragma unroll
+                  for (int k = 0; k < kBK / 16; ++k)
+                    umma_f16(d + u * BN, adesc1 + u * kSubStep + 2 * k, bdesc1 + kBStepK * k,
+                             kIdesc, 1u);
+                umma_commit(smem_u32(&bars->empty[stage1]));
+              }
             }
           }
           __syncwarp();

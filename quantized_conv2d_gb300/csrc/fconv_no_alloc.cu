@@ -18,9 +18,10 @@
 //
 // Sharing: every call on a device uses the same array, and the array keeps
 // whatever the previous call left in it.  Nothing needs to start at zero:
-// each call writes every scratch byte its kernels read (the filter pack
-// fills all rows including the zero padding of the last k-block, and the
-// widening pass writes the whole input copy) before reading it.  Calls whose
+// each call writes every scratch byte its kernels read (the prep launch
+// writes every row of the filter copy, the whole input copy and the split-K
+// counters; the convolution writes each partial sum before the last unit of
+// its tile reads it) before reading it.  Calls whose
 // kernels overlap on the GPU (different streams, or several host threads)
 // race on the array; serialize them, e.g. on one stream.
 #include <cudaTypedefs.h>
