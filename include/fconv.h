@@ -304,9 +304,12 @@ fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms);
  * "stage full" signal, so the MMA issuer's wait runs out and the kernel
  * exercises its timeout exit.  FCONV_DEBUG_GATHER_CPASYNC makes plans whose
  * channel count allows the TMA im2col input gather (C % 64 == 0) use the
- * general cp.async gather instead.  0 restores normal runs. */
+ * general cp.async gather instead.  FCONV_DEBUG_ONE_KBLOCK_STAGES keeps
+ * every pipeline stage at one k-block (plans that would fill two a stage,
+ * "tma-im2col-kb2", run "tma-im2col").  0 restores normal runs. */
 #define FCONV_DEBUG_DROP_ARRIVE 1
 #define FCONV_DEBUG_GATHER_CPASYNC 2
+#define FCONV_DEBUG_ONE_KBLOCK_STAGES 4
 fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
 
 /* Record caller-created CUDA events (cudaEvent_t) at the stage boundaries
@@ -381,10 +384,11 @@ fconv_status fconv_plan_get_splits(const fconv_plan *plan, int *splits);
 fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches);
 
 /* Which convolution kernel the plan's next run uses: "tma-im2col" (A
- * gathered by TMA im2col loads, 128-pixel tiles), "tma-im2col-m256" (the
- * same with 256-pixel tiles) or "cp-async" (the general gather); for a
- * strided transposed plan, its first phase's.  Static text; "" for a NULL
- * plan. */
+ * gathered by TMA im2col loads, 128-pixel tiles), "tma-im2col-kb2" (the
+ * same with two k-blocks a pipeline stage: unsplit, unchunked tiles of up to
+ * 128 channels and 12 or more k-blocks of 64), "tma-im2col-m256" (256-pixel tiles) or "cp-async" (the
+ * general gather); for a strided transposed plan, its first phase's.
+ * Static text; "" for a NULL plan. */
 const char *fconv_plan_kernel(const fconv_plan *plan);
 
 /* Static text for a status code. */

@@ -187,6 +187,22 @@ fconv::Gather gather_for_run(const fconv_plan &p) {
   return gather_for(p, p.block_n, (p.debug & FCONV_DEBUG_GATHER_CPASYNC) != 0);
 }
 
+// K-blocks a pipeline stage of the next run: 2 on the TMA gather for
+// unsplit, unchunked 128-pixel tiles of up to 128 channels and at least
+// kKps2MinKBlocks k-blocks, without in-kernel widening (a producer fills at
+// most one stage per ~550-650 cycles, so larger stages halve its cost per
+// k-block; on tiles of a few k-blocks the ring's coarser stages measured
+// slower: 64x28x28x256 1x1, 4 k-blocks, 33.5 -> 35.0 us a graph step),
+// else 1.
+constexpr int kKps2MinKBlocks = 12;
+int kblocks_per_stage(const fconv_plan &p) {
+  if (p.debug & FCONV_DEBUG_ONE_KBLOCK_STAGES) return 1;
+  const bool ok = gather_for_run(p) == fconv::Gather::kTmaIm2col && p.m_sub == 1 &&
+                  p.block_n <= 128 && p.splits == 1 && !p.widen && p.kb_chunk >= p.num_kb &&
+                  p.num_kb >= kKps2MinKBlocks;
+  return ok ? 2 : 1;
+}
+
 
 // Tile: the candidate (BN output channels x 128*MS output pixels) with the
 // least estimated time.  A unit (a tile, or its split) costs the longer of
@@ -219,6 +235,10 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
       if (bn > kp) continue;
       fconv::Gather g = gather_for(p, bn, false);
       if (!fconv::gather_supports(g, bn, chunked, ms)) continue;
+      // 128-pixel tiles of <= 128 channels, unsplit and unchunked, run two
+      // k-blocks a stage: bound by one MMA issuer (4 MMAs of ~105 cycles)
+      const bool kb2 = g == fconv::Gather::kTmaIm2col && ms == 1 && bn <= 128 && !chunked &&
+                       p.num_kb >= 12;   // kblocks_per_stage's rule
       const long long fixed =
           g == fconv::Gather::kTmaIm2col ? (ms == 2 ? 700 : 500) : 800;
       const long long m_tiles = (p.M + 128LL * ms - 1) / (128LL * ms);
@@ -234,7 +254,8 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
         // costs the longer of the two: ~1400 cycles per 32-column slice of
         // each epilogue warp (BN / 64 slices a warp, twice that with two
         // sub-tiles), i.e. ~22 * BN * MS
-        const long long mainloop = kbs * (work > fixed ? work : fixed);
+        const long long g_kb = (kb2 && sp == 1) ? 420 : fixed;
+        const long long mainloop = kbs * (work > g_kb ? work : g_kb);
         const long long epilogue = 22LL * bn * ms;
         // split-K needs its counters zeroed by a prep launch; a plan with no
         // other prep work (bf16 forward) pays a whole launch for it (~4 us)
@@ -528,8 +549,10 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   // tile in one copy; else the 2-D matrix in 64 x 64 boxes.
   const void *bsrc = p->pack_filter ? static_cast<const void *>(wt) : w;
   const int b3d = (p->K % 64 == 0 && p->block_n <= p->K) ? 1 : 0;
+  const int kps = kblocks_per_stage(*p);   // boxes of 64 * kps k-rows
+  const int b_form = b3d | (kps << 1);
   fconv_plan::MapCache &mb = p->map_b;
-  if (!(mb.valid && mb.base == bsrc && mb.form == b3d && (!b3d || mb.n == p->block_n))) {
+  if (!(mb.valid && mb.base == bsrc && mb.form == b_form && (!b3d || mb.n == p->block_n))) {
     mb.valid = false;
     memset(&mb.map, 0, sizeof mb.map);
     const CUtensorMapDataType bt =
@@ -539,7 +562,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
       const cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(p->Ktot),
                                   static_cast<cuuint64_t>(p->K / 64)};
       const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(p->K) * 2, 128};
-      const cuuint32_t box[3] = {64, 64, static_cast<cuuint32_t>(p->block_n / 64)};
+      const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(64 * kps),
+                                 static_cast<cuuint32_t>(p->block_n / 64)};
       const cuuint32_t estride[3] = {1, 1, 1};
       cr = encode(&mb.map, bt, 3, const_cast<void *>(bsrc), gdim, gstride, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -548,7 +572,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
       const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p->K),
                                   static_cast<cuuint64_t>(p->Ktot)};
       const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p->K) * 2};
-      const cuuint32_t box[2] = {64, 64};
+      const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(64 * kps)};
       const cuuint32_t estride[2] = {1, 1};
       cr = encode(&mb.map, bt, 2, const_cast<void *>(bsrc), gdim, gstride, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -558,7 +582,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
       return fail(FCONV_ERR_INTERNAL, "tensor map encode failed (%d)", (int)cr);
     mb.base = bsrc;
     mb.n = p->block_n;
-    mb.form = b3d;
+    mb.form = b_form;
     mb.valid = true;
   }
   const CUtensorMap &tmap = mb.map;
@@ -628,6 +652,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.num_n_tiles = p->num_n_tiles;
   a.num_tiles = p->num_tiles;
   a.b3d = b3d;
+  a.kps = kps;
   a.conv_scale = conv_scale;
   a.side_scale = side_scale;
   a.act = static_cast<int>(p->act);
@@ -1319,7 +1344,8 @@ fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms) {
 
 fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags) {
   if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
-  if (flags & ~(FCONV_DEBUG_DROP_ARRIVE | FCONV_DEBUG_GATHER_CPASYNC))
+  if (flags & ~(FCONV_DEBUG_DROP_ARRIVE | FCONV_DEBUG_GATHER_CPASYNC |
+                FCONV_DEBUG_ONE_KBLOCK_STAGES))
     return fail(FCONV_ERR_INVALID_VALUE, "unknown flags");
   plan->debug = flags;
   if (plan->num_phases == 0) update_widen(*plan);
@@ -1385,7 +1411,9 @@ const char *fconv_plan_kernel(const fconv_plan *plan) {
   if (plan->num_phases > 0) plan = plan->phase[0];
   if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col && plan->m_sub == 2)
     return "tma-im2col-m256";
-  return gather_for_run(*plan) == fconv::Gather::kTmaIm2col ? "tma-im2col" : "cp-async";
+  if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col)
+    return kblocks_per_stage(*plan) == 2 ? "tma-im2col-kb2" : "tma-im2col";
+  return "cp-async";
 }
 
 const char *fconv_status_string(fconv_status s) {

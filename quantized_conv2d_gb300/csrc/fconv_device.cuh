@@ -306,12 +306,14 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
 // boxes writes it: each box holds 64 consecutive N values (128 bytes) for
 // each of 64 K rows, 8-row swizzle atoms 1024 bytes apart (the stride
 // offset, along K); boxes of the next 64 N values follow 8192 bytes later
-// (the leading offset, along N).  The tile base must be 1024-byte aligned;
-// stepping K by 16 rows adds 2048 bytes, 128 in the start-address field.
-__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+// (the leading offset, along N; a box of 128 K rows puts them 16384 bytes
+// apart).  The tile base must be 1024-byte aligned; stepping K by 16 rows
+// adds 2048 bytes, 128 in the start-address field.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr,
+                                                      uint32_t n_block_bytes = 8192) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address
-  d |= static_cast<uint64_t>(8192 >> 4) << 16;              // leading offset: next 64 N
+  d |= static_cast<uint64_t>(n_block_bytes >> 4) << 16;     // leading offset: next 64 N
   d |= static_cast<uint64_t>(1024 >> 4) << 32;              // stride offset: next 8 K rows
   d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle

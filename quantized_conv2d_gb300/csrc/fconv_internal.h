@@ -35,6 +35,9 @@ struct ConvArgs {
   int num_n_tiles;     // ceil(K / BN)
   int num_tiles;       // ceil(M / 128) * num_n_tiles
   int b3d;             // tmap_b is the 3-D {64, rows, K / 64} view (K % 64 == 0)
+  int kps;             // k-blocks a pipeline stage (1, or 2: TMA gather, unsplit,
+                       // unchunked 128-pixel tiles of <= 128 channels); tmap_b's
+                       // boxes are 64 * kps k-rows deep
   float conv_scale, side_scale;
   int act;             // kAct*
   // output pixel of GEMM row m (a phase of a strided transposed convolution

@@ -97,8 +97,11 @@ struct Smem {
 // copy of a {64, 64, BN / 64} box writes the whole tile in that layout;
 // otherwise each block is its own 2-D copy.  The copies a producer issues,
 // not their bytes, bound how fast it fills stages, so one copy is cheaper.
+// KPS k-blocks a stage: the boxes are 64 * KPS k-rows deep, so each block of
+// 64 channels holds the stage's KPS k-blocks one after another (8 KB each)
+// and the blocks are 8 KB * KPS apart.
 constexpr uint64_t kBStepK = 2048 >> 4;   // descriptor step of 16 k-rows
-template <int BN>
+template <int BN, int KPS = 1>
 __device__ __forceinline__ void load_b_tile(uint32_t dst, const CUtensorMap *map, int kb,
                                             int n_tile, int b3d, uint32_t bar) {
   if (b3d) {
@@ -106,7 +109,7 @@ __device__ __forceinline__ void load_b_tile(uint32_t dst, const CUtensorMap *map
   } else {
 #pragma unroll
     for (int j = 0; j < BN / 64; ++j)
-      tma_load_2d(dst + j * 8192, map, n_tile * BN + 64 * j, kb * kBK, bar);
+      tma_load_2d(dst + j * 8192 * KPS, map, n_tile * BN + 64 * j, kb * kBK, bar);
   }
 }
 
@@ -752,11 +755,16 @@ struct TmaRegs {
 // WIDEN: int8 activations are loaded as they are (64 bytes a pixel) into a
 // staging ring and widened to fp16 inside the kernel (see the converter
 // role below), instead of being read from a widened copy in global memory.
-template <int BN, int MS = 1, bool WIDEN = false>
+// KPS: k-blocks a stage (2 on unchunked, unsplit 128-pixel tiles of up to
+// 128 channels): a producer thread fills at most one stage per ~550-650
+// cycles whatever the stage holds, so a stage of two k-blocks halves the
+// producers' cost per k-block; the MMA issuer takes the stage's MMAs after
+// one wait.
+template <int BN, int MS = 1, bool WIDEN = false, int KPS = 1>
 struct TmaCfg {
-  static constexpr int kABytes = kBM * kBK * 2;        // one sub-tile's A
-  static constexpr int kAStage = MS * kABytes;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kABytes = kBM * kBK * 2;        // one sub-tile's A of one k-block
+  static constexpr int kAStage = KPS * MS * kABytes;
+  static constexpr int kBBytes = KPS * BN * kBK * 2;
   static constexpr int kStageBytes = kAStage + kBBytes;
   // staging of the int8 A tiles (WIDEN): 128 pixels x 64 bytes a sub-tile
   static constexpr int kStgBytes = WIDEN ? MS * kBM * kBK : 0;
@@ -786,18 +794,20 @@ struct TmaCfg {
   static_assert(2 * kAccCols <= 512, "tensor memory");
   static_assert(kStages >= 3, "pipeline too shallow");
   static_assert(!WIDEN || kHalfCols <= 64, "in-kernel widening needs the 96-register control warps");
+  static_assert(KPS == 1 || (KPS == 2 && MS == 1 && !WIDEN), "two k-blocks a stage: 128-pixel tiles");
 };
 
 // SPLITK: the split-K form (units of kb_per_split k-blocks, partial sums
 // and the last unit's reduction); the other instance keeps one unit a tile.
 // WIDEN (int8, unsplit, BN <= 128): tmap_a is an im2col map of the int8
 // input itself; warps 2-3 widen each staged A tile into the fp16 stage.
-template <int BN, bool IS_INT8, int MS, bool SPLITK, bool WIDEN = false>
+template <int BN, bool IS_INT8, int MS, bool SPLITK, bool WIDEN = false, int KPS = 1>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     conv_fprop_tma_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
   static_assert(!WIDEN || (IS_INT8 && !SPLITK), "widening: int8, unsplit");
-  using C = TmaCfg<BN, MS, WIDEN>;
+  static_assert(KPS == 1 || !SPLITK, "two k-blocks a stage: unsplit");
+  using C = TmaCfg<BN, MS, WIDEN, KPS>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8, /*b_mn=*/true);
   constexpr int kTileM = kBM * MS;
@@ -905,21 +915,63 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         // A only: warp 2 copies each stage's B.  (Waiting for two free
         // stages and filling both in one pass measured slower: it gives up a
         // stage of lookahead.)
-        for (int kb = ukb0; kb < ukb1; ++kb) {
+        for (int kb = ukb0; kb < ukb1; kb += KPS) {
+          const int nk = KPS == 1 ? 1 : min(KPS, ukb1 - kb);   // the stage's k-blocks
           if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
             ok = false;
             break;
           }
           if (!drop) {
             if (lane == 0) {
-              // one copy of the tile's 128 * MS pixels: the tensor map's
-              // walk length is the tile's, so a second sub-tile continues
-              // the first one's walk
+              // per k-block one copy of the tile's 128 * MS pixels: the
+              // tensor map's walk length is the tile's, so a second
+              // sub-tile continues the first one's walk
               const uint32_t fb = smem_u32(&bars->full_b[stage]);
-              mbar_arrive_expect_tx(fb, C::kAStage);
-              tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage), &tmap_a, cb * kBK, w0[0],
-                                 h0[0], n0[0], static_cast<uint16_t>(s),
-                                 static_cast<uint16_t>(r), fb);
+              mbar_arrive_expect_tx(fb, nk * MS * C::kABytes);
+              int cq = cb, sq = s, rq = r;
+              for (int q = 0; q < nk; ++q) {
+                tma_load_im2col_4d(smem_u32(sA + stage * C::kAStage + q * C::kABytes), &tmap_a,
+                                   cq * kBK, w0[0], h0[0], n0[0], static_cast<uint16_t>(sq),
+                                   static_cast<uint16_t>(rq), fb);
+                if (++cq == cblocks) {
+                  cq = 0;
+                  if (++sq == args.S) { sq = 0; ++rq; }
+                }
+              }
+            }
+            __syncwarp();
+            ++issued;
+          }
+          for (int q = 0; q < nk; ++q) {
+            if (++cb == cblocks) {
+              cb = 0;
+              if (++s == args.S) { s = 0; ++r; }
+            }
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      } else {
+        for (int kb = ukb0; kb < ukb1; ++kb) {
+          if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo) ||
+              !mbar_wait_warp(smem_u32(&stg_empty[sstage]), sphase ^ 1, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          if (!drop) {
+            if (lane == 0) {
+              // WIDEN: int8 A (64 bytes a pixel) into the staging slot, which
+              // the converter warps widen into the stage, and the stage's B
+              const uint32_t fb = smem_u32(&bars->full_b[stage]);
+              const uint32_t sf = smem_u32(&stg_full[sstage]);
+              mbar_arrive_expect_tx(sf, C::kStgBytes);
+#pragma unroll
+              for (int u = 0; u < MS; ++u)
+                tma_load_im2col_4d(smem_u32(sStg + sstage * C::kStgBytes + u * kBM * kBK),
+                                   &tmap_a, cb * kBK, w0[u], h0[u], n0[u],
+                                   static_cast<uint16_t>(s), static_cast<uint16_t>(r), sf);
+              mbar_arrive_expect_tx(fb, C::kBBytes);
+              load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, args.b3d,
+                              fb);
             }
             __syncwarp();
             ++issued;
@@ -929,40 +981,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             if (++s == args.S) { s = 0; ++r; }
           }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++sstage == C::kStgStages) { sstage = 0; sphase ^= 1; }
         }
-        continue;
-      }
-      for (int kb = ukb0; kb < ukb1; ++kb) {
-        if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo) ||
-            (WIDEN && !mbar_wait_warp(smem_u32(&stg_empty[sstage]), sphase ^ 1, abort_flag, tmo))) {
-          ok = false;
-          break;
-        }
-        if (!drop) {
-          if (lane == 0) {
-            // WIDEN: int8 A (64 bytes a pixel) into the staging slot, which
-            // the converter warps widen into the stage, and the stage's B
-            const uint32_t fb = smem_u32(&bars->full_b[stage]);
-            const uint32_t sf = smem_u32(&stg_full[sstage]);
-            mbar_arrive_expect_tx(sf, C::kStgBytes);
-#pragma unroll
-            for (int u = 0; u < MS; ++u)
-              tma_load_im2col_4d(smem_u32(sStg + sstage * C::kStgBytes + u * kBM * kBK),
-                                 &tmap_a, cb * kBK, w0[u], h0[u], n0[u],
-                                 static_cast<uint16_t>(s), static_cast<uint16_t>(r), sf);
-            mbar_arrive_expect_tx(fb, C::kBBytes);
-            load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, args.b3d,
-                            fb);
-          }
-          __syncwarp();
-          ++issued;
-        }
-        if (++cb == cblocks) {
-          cb = 0;
-          if (++s == args.S) { s = 0; ++r; }
-        }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
-        if (WIDEN && ++sstage == C::kStgStages) { sstage = 0; sphase ^= 1; }
       }
     }
     if (lane == 0) {
@@ -997,17 +1017,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const int ukb0 = (unit - tile * splits) * kb_per_split;
       const int ukb1 = min(num_kb, ukb0 + kb_per_split);
       const int n_tile = tile % args.num_n_tiles;
-      for (int kb = ukb0; kb < ukb1; ++kb) {
+      for (int kb = ukb0; kb < ukb1; kb += KPS) {
         if (!mbar_wait_warp(smem_u32(&bars->empty[stage]), phase ^ 1, abort_flag, tmo)) {
           ok = false;
           break;
         }
         if (!drop) {
           if (lane == 0) {
+            // the stage's KPS k-blocks (a last stage of one k-block also
+            // gets the next k-block's rows, or zeros past R*S*C: unused)
             const uint32_t fb = smem_u32(&bars->full_b[stage]);
             mbar_arrive_expect_tx(fb, C::kBBytes);
-            load_b_tile<BN>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile, args.b3d,
-                            fb);
+            load_b_tile<BN, KPS>(smem_u32(sB + stage * C::kBBytes), &tmap_b, kb, n_tile,
+                                 args.b3d, fb);
           }
           __syncwarp();
           ++issued;
@@ -1092,63 +1114,95 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + astage * C::kAccCols;   // sub-tile u at d + u * BN
-        for (int kb = kb0; kb < kb1; kb += 2) {
-          const bool pair = kb + 1 < kb1;
-          const uint32_t stage1 = stage + 1 == kStages ? 0 : stage + 1;
-          const uint32_t phase1 = stage1 == 0 ? phase ^ 1 : phase;
-          if (!mbar_wait2_warp(smem_u32(&bars->full_b[stage]), phase,
-                               smem_u32(&bars->full_b[stage1]), phase1, pair, abort_flag, tmo)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kAStage));
-          const uint64_t bdesc = sw128_mnmajor_desc(smem_u32(sB + stage * C::kBBytes));
-          const uint64_t adesc1 = sw128_kmajor_desc(smem_u32(sA + stage1 * C::kAStage));
-          const uint64_t bdesc1 = sw128_mnmajor_desc(smem_u32(sB + stage1 * C::kBBytes));
-          // a sub-tile's A is 16 KB further: + (16384 >> 4) in the descriptor
-          constexpr uint64_t kSubStep = static_cast<uint64_t>(C::kABytes >> 4);
-          if (lane == 0) {
-            if constexpr (kDualMma && MS == 2) {
-              // this issuer's 128-pixel sub-tile
+        if constexpr (KPS > 1) {
+          // one stage (KPS k-blocks) a wait; A k-block q of the stage is
+          // 16 KB further, B k-block q 8 KB further within each 64-channel
+          // block (blocks 8 KB * KPS apart)
+          for (int kb = kb0; kb < kb1; kb += KPS) {
+            const int nk = min(KPS, kb1 - kb);
+            if (!mbar_wait_warp(smem_u32(&bars->full_b[stage]), phase, abort_flag, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kAStage));
+            const uint64_t bdesc =
+                sw128_mnmajor_desc(smem_u32(sB + stage * C::kBBytes), 8192 * KPS);
+            if (lane == 0) {
 #pragma unroll
-              for (int k = 0; k < kBK / 16; ++k)
-                umma_f16(d + part * BN, adesc + part * kSubStep + 2 * k, bdesc + kBStepK * k,
-                         kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
-              umma_commit(smem_u32(&bars->empty[stage]));
-              if (pair) {
-#pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)
-                  umma_f16(d + part * BN, adesc1 + part * kSubStep + 2 * k,
-                           bdesc1 + kBStepK * k, kIdesc, 1u);
-                umma_commit(smem_u32(&bars->empty[stage1]));
-              }
-            } else {
-#pragma unroll
-              for (int u = 0; u < MS; ++u)
-#pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)
-                  umma_f16(d + u * BN, adesc + u * kSubStep + 2 * k, bdesc + kBStepK * k,
-                           kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
-              umma_commit(smem_u32(&bars->empty[stage]));
-              if (pair) {
-#pragma unroll
-                for (int u = 0; u < MS; ++u)
+              for (int q = 0; q < KPS; ++q) {
+                if (q < nk) {
 #pragma unroll
                   for (int k = 0; k < kBK / 16; ++k)
-                    umma_f16(d + u * BN, adesc1 + u * kSubStep + 2 * k, bdesc1 + kBStepK * k,
-                             kIdesc, 1u);
-                umma_commit(smem_u32(&bars->empty[stage1]));
+                    umma_f16(d, adesc + q * (C::kABytes >> 4) + 2 * k,
+                             bdesc + q * (8192 >> 4) + kBStepK * k, kIdesc,
+                             (kb > kb0 || q > 0 || k > 0) ? 1u : 0u);
+                }
+              }
+              umma_commit(smem_u32(&bars->empty[stage]));
+            }
+            __syncwarp();
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+        } else {
+          for (int kb = kb0; kb < kb1; kb += 2) {
+            const bool pair = kb + 1 < kb1;
+            const uint32_t stage1 = stage + 1 == kStages ? 0 : stage + 1;
+            const uint32_t phase1 = stage1 == 0 ? phase ^ 1 : phase;
+            if (!mbar_wait2_warp(smem_u32(&bars->full_b[stage]), phase,
+                                 smem_u32(&bars->full_b[stage1]), phase1, pair, abort_flag, tmo)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::kAStage));
+            const uint64_t bdesc = sw128_mnmajor_desc(smem_u32(sB + stage * C::kBBytes));
+            const uint64_t adesc1 = sw128_kmajor_desc(smem_u32(sA + stage1 * C::kAStage));
+            const uint64_t bdesc1 = sw128_mnmajor_desc(smem_u32(sB + stage1 * C::kBBytes));
+            // a sub-tile's A is 16 KB further: + (16384 >> 4) in the descriptor
+            constexpr uint64_t kSubStep = static_cast<uint64_t>(C::kABytes >> 4);
+            if (lane == 0) {
+              if constexpr (kDualMma && MS == 2) {
+                // this issuer's 128-pixel sub-tile
+  #pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                  umma_f16(d + part * BN, adesc + part * kSubStep + 2 * k, bdesc + kBStepK * k,
+                           kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&bars->empty[stage]));
+                if (pair) {
+  #pragma unroll
+                  for (int k = 0; k < kBK / 16; ++k)
+                    umma_f16(d + part * BN, adesc1 + part * kSubStep + 2 * k,
+                             bdesc1 + kBStepK * k, kIdesc, 1u);
+                  umma_commit(smem_u32(&bars->empty[stage1]));
+                }
+              } else {
+  #pragma unroll
+                for (int u = 0; u < MS; ++u)
+  #pragma unroll
+                  for (int k = 0; k < kBK / 16; ++k)
+                    umma_f16(d + u * BN, adesc + u * kSubStep + 2 * k, bdesc + kBStepK * k,
+                             kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&bars->empty[stage]));
+                if (pair) {
+  #pragma unroll
+                  for (int u = 0; u < MS; ++u)
+  #pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k)
+                      umma_f16(d + u * BN, adesc1 + u * kSubStep + 2 * k, bdesc1 + kBStepK * k,
+                               kIdesc, 1u);
+                  umma_commit(smem_u32(&bars->empty[stage1]));
+                }
               }
             }
-          }
-          __syncwarp();
-          if (pair) {
-            stage = stage1 + 1 == kStages ? 0 : stage1 + 1;
-            phase = stage == 0 ? phase1 ^ 1 : phase1;
-          } else {
-            stage = stage1;
-            phase = phase1;
+            __syncwarp();
+            if (pair) {
+              stage = stage1 + 1 == kStages ? 0 : stage1 + 1;
+              phase = stage == 0 ? phase1 ^ 1 : phase1;
+            } else {
+              stage = stage1;
+              phase = phase1;
+            }
           }
         }
         if (!ok) break;
@@ -1643,12 +1697,12 @@ static void note_attributes(Kern kern, int threads, int smem) {
 
 const char *last_launch_note() { return t_kernel_note; }
 
-template <int BN, bool IS_INT8, int MS, bool SPLITK = false, bool WIDEN = false>
+template <int BN, bool IS_INT8, int MS, bool SPLITK = false, bool WIDEN = false, int KPS = 1>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                                 const ConvArgs &args, int grid, bool overlap,
                                 cudaStream_t stream) {
-  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK, WIDEN>;
-  using Cfg = TmaCfg<BN, MS, WIDEN>;
+  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK, WIDEN, KPS>;
+  using Cfg = TmaCfg<BN, MS, WIDEN, KPS>;
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
   if (e == cudaSuccess) {
@@ -1677,6 +1731,9 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
   if (chunked && !is_int8) return cudaErrorInvalidValue;
   if (!gather_supports(gather, block_n, chunked, m_sub)) return cudaErrorInvalidValue;
   if (args.kb_chunk <= 0 || grid <= 0) return cudaErrorInvalidValue;
+  if (args.kps != 1 && (args.kps != 2 || widen || args.splits > 1 || m_sub != 1 ||
+                        gather != Gather::kTmaIm2col))
+    return cudaErrorInvalidValue;
   if (widen) {
     // int8 activations widened in the kernel: TMA gather, unsplit, <= 128 channels
     if (!is_int8 || gather != Gather::kTmaIm2col || args.splits > 1 || block_n > 128 ||
@@ -1712,6 +1769,16 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
       default: return is_int8 ? launch_tma_t<256, true, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream)
                               : launch_tma_t<256, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream);
     }
+  }
+  if (gather == Gather::kTmaIm2col && args.kps == 2) {
+    // two k-blocks a stage: unsplit, unchunked 128-pixel tiles of <= 128 channels
+    if (args.C % kBK != 0 || m_sub != 1 || chunked || block_n > 128)
+      return cudaErrorInvalidValue;
+    if (block_n == 64)
+      return is_int8 ? launch_tma_t<64, true, 1, false, false, 2>(tmap_a, tmap_b, args, grid, overlap, stream)
+                     : launch_tma_t<64, false, 1, false, false, 2>(tmap_a, tmap_b, args, grid, overlap, stream);
+    return is_int8 ? launch_tma_t<128, true, 1, false, false, 2>(tmap_a, tmap_b, args, grid, overlap, stream)
+                   : launch_tma_t<128, false, 1, false, false, 2>(tmap_a, tmap_b, args, grid, overlap, stream);
   }
   if (gather == Gather::kTmaIm2col) {
     if (args.C % kBK != 0) return cudaErrorInvalidValue;

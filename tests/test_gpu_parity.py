@@ -176,6 +176,54 @@ def test_every_tile_gives_the_same_result(dtype):
             assert np.array_equal(v, first)
 
 
+# Plans that fill two k-blocks a pipeline stage (unsplit, unchunked 128-pixel
+# tiles of <= 128 channels and >= 12 k-blocks; int8 sums are unchunked up to
+# 15): (N, H, W, C, K, R, S, stride, pad, side, relu), block_n.  Odd k-block counts end a unit with a stage of one k-block; K not
+# a multiple of 64 takes the 2-D filter boxes (128 k-rows deep).
+KB2_CASES = [
+    ((2, 14, 14, 832, 128, 1, 1, 1, "VALID", False, True), 128),  # 13 k-blocks
+    ((3, 9, 7, 768, 96, 1, 1, 1, "VALID", True, False), 128),     # 12 k-blocks, K = 96, ragged M
+    ((2, 8, 8, 192, 64, 2, 2, 1, "SAME", True, True), 64),        # BN 64, 2x2 filter, 12 k-blocks
+    ((2, 10, 10, 896, 208, 1, 1, 2, "VALID", False, True), 128),  # 14 k-blocks, stride 2, K = 208
+]
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+@pytest.mark.parametrize("i", range(len(KB2_CASES)))
+def test_two_kblock_stages_agree(i, dtype):
+    """Stages of two k-blocks give the oracle's sums and outputs, and (int8)
+    the same sums as stages of one k-block."""
+    params, bn = KB2_CASES[i]
+    c = sweep_case(80 + i, params, dtype)
+    p = c.plan(block_n=bn)
+    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-kb2"
+    fc.fconv_plan_set_debug(p.handle, fc.FCONV_DEBUG_ONE_KBLOCK_STAGES)
+    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col"
+    p.close()
+    acc_ref = c.oracle_acc()
+    two = c.accumulators_gpu(block_n=bn)
+    one = c.accumulators_gpu(block_n=bn, debug=fc.FCONV_DEBUG_ONE_KBLOCK_STAGES)
+    c.check_acc(two, acc_ref)
+    c.check_acc(one, acc_ref)
+    if dtype == "int8":
+        assert np.array_equal(two, one)
+    c.check_output(c.run_gpu(block_n=bn), c.oracle_out(acc_ref))
+    c.check_output(c.run_gpu(block_n=bn, debug=fc.FCONV_DEBUG_ONE_KBLOCK_STAGES),
+                   c.oracle_out(acc_ref))
+
+
+def test_two_kblock_stages_long_bf16():
+    """A 36-k-block bf16 layer (the 32x14x14x256 workload's shape on 2
+    images): two k-blocks a stage against the oracle."""
+    c = sweep_case(90, (2, 14, 14, 256, 256, 3, 3, 1, "SAME", False, True), "bf16")
+    p = c.plan(block_n=128)
+    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-kb2"
+    p.close()
+    acc_ref = c.oracle_acc()
+    c.check_acc(c.accumulators_gpu(block_n=128), acc_ref)
+    c.check_output(c.run_gpu(block_n=128), c.oracle_out(acc_ref))
+
+
 @pytest.mark.parametrize("xv,wv", [(127, 127), (-128, -128), (-128, 127), (None, None)])
 def test_chunked_sums_are_exact_at_extreme_magnitudes(xv, wv):
     """Sums far beyond 2^24 (up to 9*1024*16384), where a single fp32
@@ -288,14 +336,17 @@ def test_run_host_buffers(chunks, splits, dtype):
 
 
 @pytest.mark.parametrize("C,K,kernel", [(16, 16, "cp-async"), (64, 64, "tma-im2col"),
-                                         (64, 256, "tma-im2col"), (64, 128, "tma-im2col-m256")])
+                                         (64, 256, "tma-im2col"), (64, 128, "tma-im2col-m256"),
+                                         (832, 64, "tma-im2col-kb2")])
 def test_timeout_exit_keeps_context_usable(C, K, kernel):
     """A producer that never signals 'stage full' makes the MMA issuer's wait
     run out: the kernel must stop, report FCONV_ERR_TIMEOUT, and the next run
-    must work -- for the cp.async loaders and the TMA producer (64- and
-    256-wide tiles, and 256-pixel tiles)."""
-    c = sweep_case(70, (1, 8, 8, C, K, 3, 3, 1, "SAME", False, True), "int8")
-    p = c.plan(block_n=256 if K == 256 else None)
+    must work -- for the cp.async loaders and the TMA producers (64- and
+    256-wide tiles, 256-pixel tiles, and stages of two k-blocks)."""
+    R = 1 if C > 512 else 3   # 832 channels, 1x1: 13 k-blocks, unchunked
+    c = sweep_case(70, (1, 8, 8, C, K, R, R, 1, "SAME", False, True), "int8")
+    # a fixed tile is unsplit
+    p = c.plan(block_n=256 if K == 256 else (64 if C > 512 else None))
     if kernel.endswith("m256"):
         fc.fconv_plan_set_tile_shape(p.handle, 256, K)
     assert fc.fconv_plan_kernel(p.handle) == kernel
