@@ -1246,6 +1246,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (SPLITK) griddep_wait();
     uint32_t astage = 0, aphase = 0;
     bool ok = true;
+    int wpar_c0 = -1;   // the columns whose bias / scale wpar holds
     for (int unit = blockIdx.x; unit < num_units && ok; unit += gridDim.x) {
       const int tile = unit / splits;
       const int ukb0 = (unit - tile * splits) * kb_per_split;
@@ -1261,17 +1262,32 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const long long mo = out_pixel(args, m);   // the output pixel row m writes
       long long st_mo[SliceGroups<IS_INT8>::kGroups];
       bool st_ok[SliceGroups<IS_INT8>::kGroups];
-      coalesced_rows<IS_INT8>(mo, mvalid, st_mo, st_ok);
+      if (!args.omap) {
+        // output row = GEMM row: a warp's 32 rows are consecutive, so the
+        // rows each lane stores follow without shuffles
+        const long long m_lane0 = m - lane;
+#pragma unroll
+        for (int k = 0; k < SliceGroups<IS_INT8>::kGroups; ++k) {
+          st_mo[k] = m_lane0 + (k * 32 + lane) / SliceGroups<IS_INT8>::kGroups;
+          st_ok[k] = st_mo[k] < args.M;
+        }
+      } else {
+        coalesced_rows<IS_INT8>(mo, mvalid, st_mo, st_ok);
+      }
       const int c0 = n_tile * BN + cbase;
-      __syncwarp();   // every lane is done with the previous tile's copy
-      if (args.mode == kModeFused && args.bias) {  // no bias when only the sums are written
+      // no bias when only the sums are written; a CTA whose units keep their
+      // output-channel tile (the grid a multiple of the channel tiles) loads
+      // it once
+      if (args.mode == kModeFused && args.bias && c0 != wpar_c0) {
+        __syncwarp();   // every lane is done with the previous tile's values
         for (int j = lane; j < C::kHalfCols; j += 32) {
           const bool in = c0 + j < args.K;
           wpar[j] = in ? __ldg(args.bias + c0 + j) : 0.0f;
           if (args.scale_k) wpar[C::kHalfCols + j] = in ? __ldg(args.scale_k + c0 + j) : 0.0f;
         }
+        wpar_c0 = c0;
       }
-      __syncwarp();
+      __syncwarp();   // every lane is done with the previous tile's copy
       const float *wscale = args.scale_k ? wpar + C::kHalfCols : nullptr;
       // the side input this thread reads after the tile's last chunk: into
       // L2 now, so the final epilogue does not wait on DRAM
