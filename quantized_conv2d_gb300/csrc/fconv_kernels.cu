@@ -1538,7 +1538,7 @@ __device__ __forceinline__ long long copy_src_unit(long long g, const WidenMap &
   return ((static_cast<long long>(n) * m.H + h) * m.W + w) * m.units_per_pixel.d + cu;
 }
 
-template <bool IS_INT8, bool MAPPED>
+template <bool IS_INT8, bool MAPPED, int ROUNDS = 8>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_kernel(const void *__restrict__ w, uint16_t *__restrict__ wt, int rows, int K,
                 int pack_blocks, const void *__restrict__ xv, __half *__restrict__ xh,
@@ -1582,28 +1582,31 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
     return;
   }
-  // Input copy, warp-contiguous: in one step a warp handles 8 x 32 units of
-  // 8 elements; for each of the 8 rounds lane l takes unit 32*round + l, so
-  // a warp instruction loads 256 contiguous int8 bytes (or 512 bf16 bytes)
-  // of a dense copy and stores 512 contiguous fp16 bytes.  Subsampled and
-  // upsampled copies read each unit from its own pixel (or write zeros).
+  // Input copy, warp-contiguous: in one step a warp handles ROUNDS x 32
+  // units of 8 elements; for each round lane l takes unit 32*round + l, so a
+  // warp instruction loads 256 contiguous int8 bytes (or 512 bf16 bytes) of
+  // a dense copy and stores 512 contiguous fp16 bytes, with all ROUNDS loads
+  // in flight before the first store.  Subsampled and upsampled copies read
+  // each unit from its own pixel (or write zeros).  Small copies take 2
+  // rounds a step, so that their grid has enough warps to keep DRAM busy.
+  constexpr int kStep = 32 * ROUNDS;
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x - pack_blocks) * (kPrepThreads / 32);
   for (long long base = (static_cast<long long>(blockIdx.x - pack_blocks) * (kPrepThreads / 32) +
-                         (threadIdx.x >> 5)) * 256;
-       base < n8; base += warps * 256) {
+                         (threadIdx.x >> 5)) * kStep;
+       base < n8; base += warps * kStep) {
     if constexpr (IS_INT8) {
       const int8_t *x = static_cast<const int8_t *>(xv);
-      uint2 in[8];
+      uint2 in[ROUNDS];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < ROUNDS; ++u) {
         const long long g = base + u * 32 + lane;
         const long long src = MAPPED ? copy_src_unit(g, map) : g;
         // a zero byte widens to +0.0
         in[u] = (g < n8 && src >= 0) ? ldg_nc_v2(x + 8 * src) : make_uint2(0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < ROUNDS; ++u) {
         const long long g = base + u * 32 + lane;
         if (g < n8) {
           uint4 o;
@@ -1614,15 +1617,15 @@ __global__ void __launch_bounds__(kPrepThreads)
       }
     } else {
       const uint16_t *x = static_cast<const uint16_t *>(xv);
-      uint4 in[8];
+      uint4 in[ROUNDS];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < ROUNDS; ++u) {
         const long long g = base + u * 32 + lane;
         const long long src = MAPPED ? copy_src_unit(g, map) : g;
         in[u] = (g < n8 && src >= 0) ? ldg_nc_v4(x + 8 * src) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < ROUNDS; ++u) {
         const long long g = base + u * 32 + lane;
         if (g < n8) stg_v4(xh + 8 * g, in[u]);
       }
@@ -1848,7 +1851,17 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int rows, int
   // 8-element units the main loop widens: all of a subsampled copy; the
   // whole 64-element groups of a dense one (the tail kernel does the rest)
   const long long n8 = map.mode != kCopyDense ? n / 8 : (n / 64) * 8;
-  long long widen_blocks = (n8 + 8 * kPrepThreads - 1) / (8 * kPrepThreads);
+  // 8 rounds a warp step (256 units), or 2 for copies too small to give each
+  // SM 2 blocks that way: a 3.2 MB subsampled copy ran at ~5 % of the DRAM
+  // peak on 1.3 blocks an SM (64x28x28x256 1x1/2: 16.4 -> 14.3 us a graph
+  // step with 2 rounds; 32x7x7x512 7x7 VALID 40.1 -> 36.8), while copies
+  // already at 2.6-5 blocks an SM ran slower with 4x as many blocks (the
+  // 32x56x56x64 and 64x28x28x256 1x1 layers 18.5 -> 19.6, 32.8 -> 34.0: more
+  // prep blocks hold the SMs the dependent convolution launch starts on)
+  const long long step8_blocks = (n8 + 8 * kPrepThreads - 1) / (8 * kPrepThreads);
+  const bool small = step8_blocks < 2LL * sm_count;
+  const int rounds = small ? 2 : 8;
+  long long widen_blocks = (n8 + rounds * kPrepThreads - 1) / (rounds * kPrepThreads);
   // up to 16 blocks an SM: more resident warps keep more loads in flight
   // (a cap of 4 an SM held the dense copy at ~81 % of the copy bandwidth,
   // 16 at ~96 %)
@@ -1858,19 +1871,18 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int rows, int
   if (grid == 0 && zero_n > 0) grid = 1;
   if (grid == 0) return cudaSuccess;
   const bool mapped = map.mode != kCopyDense;
+  auto go = [&](auto kern) {
+    kern<<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K, pack_blocks, x, xh, n8, map, zero,
+                                            zero_n);
+  };
   if (is_int8 && mapped)
-    prep_kernel<true, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K, pack_blocks,
-                                                                x, xh, n8, map, zero, zero_n);
+    small ? go(prep_kernel<true, true, 2>) : go(prep_kernel<true, true, 8>);
   else if (is_int8)
-    prep_kernel<true, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K, pack_blocks,
-                                                                 x, xh, n8, map, zero, zero_n);
+    small ? go(prep_kernel<true, false, 2>) : go(prep_kernel<true, false, 8>);
   else if (mapped)
-    prep_kernel<false, true><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K, pack_blocks,
-                                                                 x, xh, n8, map, zero, zero_n);
+    small ? go(prep_kernel<false, true, 2>) : go(prep_kernel<false, true, 8>);
   else
-    prep_kernel<false, false><<<grid, kPrepThreads, 0, stream>>>(w, wt, rows, K,
-                                                                  pack_blocks, x, xh, n8, map,
-                                                                  zero, zero_n);
+    small ? go(prep_kernel<false, false, 2>) : go(prep_kernel<false, false, 8>);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !is_int8 || map.mode != kCopyDense) return e;
   const long long n16 = n / 16, first16 = (n / 64) * 4;
