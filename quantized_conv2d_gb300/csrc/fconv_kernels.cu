@@ -1555,30 +1555,49 @@ __global__ void __launch_bounds__(kPrepThreads)
     // units (K is a multiple of 8; rows * K < 2^31)
     const uint32_t per_row = static_cast<uint32_t>(K) / 8;
     const uint32_t units = static_cast<uint32_t>(rows) * per_row;
-    for (uint32_t g = blockIdx.x * kPrepThreads + threadIdx.x; g < units;
-         g += static_cast<uint32_t>(pack_blocks) * kPrepThreads) {
-      const uint32_t row = g / per_row, cu = g - row * per_row;
-      uint32_t src = row;
-      if (map.tap_nR > 0) {
-        // (j, l, c) of the packed filter -> (r, s, c) of the caller's
-        const int C = rows / (map.tap_nR * map.tap_nS);
-        const int c = static_cast<int>(row) % C, jl = static_cast<int>(row) / C;
-        const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
-        const int r = map.tap_r0 + map.tap_rstep * (map.tap_nR - 1 - j);
-        const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
-        src = static_cast<uint32_t>((r * map.tap_S + s2) * C + c);
+    const uint32_t stride = static_cast<uint32_t>(pack_blocks) * kPrepThreads;
+    // four units a pass, their loads in flight together before the stores
+    constexpr int kPackUnroll = 4;
+    for (uint32_t g0 = blockIdx.x * kPrepThreads + threadIdx.x; g0 < units;
+         g0 += kPackUnroll * stride) {
+      uint4 o[kPackUnroll];
+      long long di[kPackUnroll];
+#pragma unroll
+      for (int k = 0; k < kPackUnroll; ++k) {
+        const uint32_t g = g0 + k * stride;
+        di[k] = -1;
+        if (g >= units) continue;
+        const uint32_t row = g / per_row, cu = g - row * per_row;
+        uint32_t src = row;
+        if (map.tap_nR > 0) {
+          // (j, l, c) of the packed filter -> (r, s, c) of the caller's
+          const int C = rows / (map.tap_nR * map.tap_nS);
+          const int c = static_cast<int>(row) % C, jl = static_cast<int>(row) / C;
+          const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
+          const int r = map.tap_r0 + map.tap_rstep * (map.tap_nR - 1 - j);
+          const int s2 = map.tap_s0 + map.tap_sstep * (map.tap_nS - 1 - l);
+          src = static_cast<uint32_t>((r * map.tap_S + s2) * C + c);
+        }
+        const long long si = static_cast<long long>(src) * K + 8 * cu;
+        di[k] = static_cast<long long>(row) * K + 8 * cu;
+        if (IS_INT8) {
+          const uint2 b8 =
+              __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(w) + si));
+          o[k] = make_uint4(b8.x, b8.y, 0u, 0u);   // widened below, after all loads
+        } else {
+          o[k] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(w) + si));
+        }
       }
-      const long long si = static_cast<long long>(src) * K + 8 * cu;
-      const long long di = static_cast<long long>(row) * K + 8 * cu;
-      uint4 o;
-      if (IS_INT8) {
-        const uint2 b8 = __ldg(reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(w) + si));
-        i8x4_to_f16x4(b8.x, o.x, o.y);
-        i8x4_to_f16x4(b8.y, o.z, o.w);
-      } else {
-        o = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(w) + si));
+#pragma unroll
+      for (int k = 0; k < kPackUnroll; ++k) {
+        if (di[k] < 0) continue;
+        uint4 v = o[k];
+        if (IS_INT8) {
+          i8x4_to_f16x4(o[k].x, v.x, v.y);
+          i8x4_to_f16x4(o[k].y, v.z, v.w);
+        }
+        stg_v4(wt + di[k], v);
       }
-      stg_v4(wt + di, o);
     }
     return;
   }
@@ -1843,7 +1862,7 @@ cudaError_t launch_prep(bool is_int8, const void *w, uint16_t *wt, int rows, int
   } else if (!is_int8) {
     n = 0;   // bf16 plans read a dense input as it is
   }
-  // filter rows: 4 8-element units a thread, at most 8 blocks an SM
+  // filter rows: 4 8-element units a thread (one pass), at most 8 blocks an SM
   const long long pack_units = w ? static_cast<long long>(rows) * (K / 8) : 0;
   long long pack_blocks_ll = (pack_units + 4 * kPrepThreads - 1) / (4 * kPrepThreads);
   if (pack_blocks_ll > 8LL * sm_count) pack_blocks_ll = 8LL * sm_count;
