@@ -1416,8 +1416,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           finish_split();
         } else if (uchunks == 1) {
           // the whole sum is in TMEM: epilogue straight from it
-#pragma unroll
-          for (int jj = 0; jj < C::kSlices; ++jj) {
+          auto slice = [&](int jj, const uint4 *side_words) {
             uint32_t v[32];
             tmem_ld32(t_acc + jj * 32, v);
             tmem_wait_ld(v);
@@ -1428,13 +1427,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             for (int i = 0; i < 32; ++i)
               vals[i] = IS_INT8 ? __uint_as_float(v[i]) : __fadd_rn(__uint_as_float(v[i]), 0.0f);
             if (args.mode == kModeFused)
-              epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals,
-                                           preload ? side_pre + jj * SliceGroups<IS_INT8>::kGroups
-                                                   : nullptr,
+              epilogue_slice_warp<IS_INT8>(args, mo, mvalid, c0 + jj * 32, vals, side_words,
                                            wpar + jj * 32, wscale ? wscale + jj * 32 : nullptr,
                                            ostage, st_mo, st_ok);
             else if (mvalid)
               store_raw_slice<IS_INT8>(args, mo, c0 + jj * 32, vals);
+          };
+          // The branch must be the same for the whole warp (the slice code
+          // is warp-collective), so it tests the plan, not this lane's row:
+          // preload also depends on whether the lane's row exists.
+          if (args.use_side && args.mode == kModeFused && splits == 1) {
+            // side words preloaded per slice: static indexes
+#pragma unroll
+            for (int jj = 0; jj < C::kSlices; ++jj)
+              slice(jj, preload ? side_pre + jj * SliceGroups<IS_INT8>::kGroups : nullptr);
+          } else {
+            // one copy of the slice code for all slices: the unrolled form
+            // is kSlices times the instruction footprint of an epilogue
+            // whose warps wait on instruction fetch between tiles
+#pragma unroll 1
+            for (int jj = 0; jj < C::kSlices; ++jj) slice(jj, nullptr);
           }
           tc_fence_before();
           __syncwarp();
