@@ -24,7 +24,7 @@ struct fconv_plan {
   fconv_act act;
   int P, Q, pt, pb, pl, pr;
   long long M;
-  int Ktot, num_kb, Kpad;
+  int Ktot, num_kb;
   int block_n, kb_chunk, num_n_tiles, num_tiles;
   int m_sub;            // 128-pixel sub-tiles per output tile (1 or 2)
   int splits;           // split-K units per tile (1: none; TMA gather only)
@@ -52,11 +52,11 @@ struct fconv_plan {
   // (W-1)*sw+1), and the convolution runs at stride 1 on that copy
   int upsample;
   int tpad[4];   // a transposed plan's pads as given (top, bottom, left, right)
-  // the packed filter's taps (see fconv::WidenMap); tap_nR == 0: as given
+  // the filter copy's taps (see fconv::WidenMap); tap_nR == 0: as given
   int tap_nR, tap_nS, tap_R, tap_S, tap_r0, tap_s0, tap_rstep, tap_sstep;
   // output pixel map (see fconv::ConvArgs); omap == 0: GEMM row = pixel
   int omap, out_H, out_W, o_sh, o_sw, o_h0, o_w0;
-  // where this plan's packed filter and input copy sit in the workspace
+  // where this plan's filter copy and input copy sit in the workspace
   size_t ws_wt_off, ws_xh_off;
   // a strided transposed convolution runs as sh*sw phases, each a forward
   // plan over x with every stride-th filter tap, writing every stride-th
@@ -372,7 +372,7 @@ int device_sm_count(int *dev_out) {
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 
-// Scratch a run needs: the packed filter, and for int8 plans the fp16 copy of
+// Scratch a run needs: the filter copy, and for int8 plans the fp16 copy of
 // the input the gathers read.
 // Split-K scratch after the operand copies: every unit's partial block
 // (128 * m_sub * block_n 32-bit words), then one counter per tile and
@@ -846,7 +846,6 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
   p.M = static_cast<long long>(N) * p.P * p.Q;
   p.Ktot = static_cast<int>(ktot);
   p.num_kb = (p.Ktot + 63) / 64;
-  p.Kpad = p.num_kb * 64;
   if (dtype == FCONV_INT8 && p.num_kb > fconv::kMaxExactKBlocks) {
     const int chunks = (p.num_kb + fconv::kMaxExactKBlocks - 1) / fconv::kMaxExactKBlocks;
     p.kb_chunk = (p.num_kb + chunks - 1) / chunks;
@@ -991,7 +990,7 @@ fconv_status fconv_plan_create_transposed(fconv_plan **plan, int N, int H, int W
     }
   }
   // the whole plan: the geometry above for checks and reports; its
-  // workspace is the phases' packed filters, then one input copy (int8)
+  // workspace is the phases' filter copies, then one input copy (int8)
   fconv_plan *whole = nullptr;
   const fconv_status st = finish_plan(p, &whole);
   if (st != FCONV_OK) {

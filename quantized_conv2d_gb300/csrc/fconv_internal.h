@@ -103,11 +103,11 @@ struct WidenMap {
   int mode;
   int C, H, W, P, Q, sh, sw;
   FastDiv units_per_pixel, pq, q, div_sh, div_sw;   // filled in by launch_prep
-  // filter copy: with tap_nR > 0 the packed filter is [tap_nR][tap_nS][C][K]
+  // filter copy: with tap_nR > 0 the copy is [tap_nR][tap_nS][C][K]
   // whose tap (j, l) is w[tap_r0 + tap_rstep*(tap_nR-1-j)][tap_s0 +
   // tap_sstep*(tap_nS-1-l)] of the caller's [tap_R][tap_S][C][K] filter
   // (flipped, and for a phase of a strided transposed convolution every
-  // stride-th tap); tap_nR == 0 packs the filter as it is
+  // stride-th tap); tap_nR == 0 copies the filter as it is
   int tap_nR, tap_nS, tap_R, tap_S, tap_r0, tap_s0, tap_rstep, tap_sstep;
 };
 // Filter copy (w != nullptr: `rows` rows of K values into the 16-bit

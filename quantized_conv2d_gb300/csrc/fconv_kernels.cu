@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pending = 0;
     bool ok = true;
     const bool drop = (args.debug & 1) != 0;
-    griddep_wait();   // the widened input and packed filter of the prep launch
+    griddep_wait();   // the widened input and filter copy of the prep launch
 
     for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x) {
       const int m_tile = tile / args.num_n_tiles;
@@ -748,10 +748,10 @@ struct TmaRegs {
 };
 
 // MS: M sub-tiles of 128 output pixels per tile.  MS = 2 gives a tile of
-// 256 pixels x BN channels whose two halves share each B stage (one wait,
-// one commit and one B copy per k-block for twice the MMA work), for tiles
-// narrower than 256 channels, where the issuing threads' fixed per-k-block
-// work, not the tensor cores, sets the pace.
+// 256 pixels x BN channels whose two halves share each B stage (one B copy
+// and one A walk per k-block for twice the MMA work, the MMAs from two
+// issuing threads), for tiles narrower than 256 channels, where the issuing
+// threads' fixed per-k-block work, not the tensor cores, sets the pace.
 // WIDEN: int8 activations are loaded as they are (64 bytes a pixel) into a
 // staging ring and widened to fp16 inside the kernel (see the converter
 // role below), instead of being read from a widened copy in global memory.
@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const long long PQ = static_cast<long long>(args.P) * args.Q;
     const int cblocks = args.C / kBK;
     const bool drop = (args.debug & 1) != 0;
-    griddep_wait();   // the widened input and packed filter of the prep launch
+    griddep_wait();   // the widened input and filter copy of the prep launch
     uint32_t stage = 0, phase = 0, issued = 0;
     uint32_t sstage = 0, sphase = 0;   // WIDEN: the staging ring
     bool ok = true;
@@ -1582,7 +1582,7 @@ __global__ void __launch_bounds__(kPrepThreads)
         const uint32_t row = g / per_row, cu = g - row * per_row;
         uint32_t src = row;
         if (map.tap_nR > 0) {
-          // (j, l, c) of the packed filter -> (r, s, c) of the caller's
+          // (j, l, c) of the filter copy -> (r, s, c) of the caller's
           const int C = rows / (map.tap_nR * map.tap_nS);
           const int c = static_cast<int>(row) % C, jl = static_cast<int>(row) / C;
           const int j = jl / map.tap_nS, l = jl - j * map.tap_nS;
