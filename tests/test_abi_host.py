@@ -408,3 +408,41 @@ def test_automatic_split_choice(shape, splits):
         assert got == splits if splits is not None else got > 1
     finally:
         fc.fconv_plan_destroy(h)
+
+
+@pytest.mark.parametrize("name,block_n,form,splits", [
+    ("small_i8_16x16x32", 64, "cp-async", 1),
+    ("resnet_i8_56x56x64", 64, "tma-im2col-m256", 1),
+    ("proj1x1s2_i8_28x28x256", 128, "tma-im2col", 1),
+    ("bf16_14x14x256", 128, "tma-im2col-kb2", 1),
+    ("large_i8_28x28x512", 256, "tma-im2col", 1),
+    ("proj1x1s1_i8_28x28x256", 128, "tma-im2col", 1),
+    ("fullwin_i8_7x7x512", 64, "tma-im2col", 8),
+    ("deep_b1_i8_7x7x512", 64, "tma-im2col", 8),
+    ("deep_b1_i8_14x14x256", 64, "tma-im2col", 6),
+    ("proj_b8_i8_7x7x2048", 64, "tma-im2col", 4),
+    ("deconv_bf16_16x16x256_s2", 128, "tma-im2col-m256", 1),
+    ("deconv_i8_14x14x512_s1", 256, "tma-im2col", 1),
+])
+def test_benchmark_workload_plans(name, block_n, form, splits):
+    # The automatic tile choice for each benchmark workload: tile width,
+    # kernel form (256-pixel tiles, two k-blocks a stage) and split count.
+    # A change to the tile cost model shows here before it shows on a GPU.
+    import fconv_inputs as FI
+    wl = FI.workload(name)
+    dt = fc.FCONV_INT8 if wl.dtype == "int8" else fc.FCONV_BF16
+    st = wl.stride if isinstance(wl.stride, int) else wl.stride[0]
+    if wl.transposed_pads:
+        pt, pb, pl, pr = wl.transposed_pads
+        h = fc.fconv_plan_create_transposed(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S,
+                                            st, st, pt, pb, pl, pr, dt, 1)
+    else:
+        pad = fc.FCONV_SAME if wl.padding == "SAME" else fc.FCONV_VALID
+        h = fc.fconv_plan_create(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S,
+                                 st, st, pad, dt, 1 if wl.relu else 0)
+    try:
+        assert fc.fconv_plan_get_config(h)[0] == block_n
+        assert fc.fconv_plan_kernel(h) == form
+        assert fc.fconv_plan_get_splits(h) == splits
+    finally:
+        fc.fconv_plan_destroy(h)
