@@ -261,10 +261,21 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host,
                             void *device_workspace, size_t workspace_bytes,
                             fconv_stream_t stream);
 
-/* Number of batch chunks fconv_run_host pipelines over (1..16; 0 restores
- * the automatic choice: as many chunks as keep one wave of output tiles
- * (one tile per SM) each, at most 12, so small problems run as one). */
+/* Number of batch chunks fconv_run_host pipelines over, split evenly
+ * (1..16), or 0 for the automatic choice.  Automatic: a batch of at least
+ * ten waves of output tiles (one tile per SM; u images a wave) takes chunks
+ * of about u/6, u/2, 2u images, then middle chunks of about 3u, then 2u, u,
+ * u/3, u/3, so that little of the copy-in, compute and copy-out is left
+ * outside the overlap at either end; a smaller batch takes even chunks of
+ * at least one wave each, at most 12, and one chunk when it has less. */
 fconv_status fconv_plan_set_host_chunks(fconv_plan *plan, int chunks);
+
+/* The image counts of the chunks fconv_run_host would use on a device with
+ * `sm_count` SMs, in batch order (they sum to N): *count gets how many
+ * (at most 16); `sizes`, when not NULL, gets them and must hold *count
+ * entries (max_sizes), else FCONV_ERR_INVALID_VALUE.  Pure host work. */
+fconv_status fconv_plan_host_chunk_sizes(const fconv_plan *plan, int sm_count,
+                                         int *sizes, int max_sizes, int *count);
 
 /* Status of the runs enqueued so far.  MIOpen's fusion API ("use-fusion-api",
  * running a fusion plan) reports an error for a run of a plan that cannot

@@ -78,6 +78,7 @@ def _load():
         "fconv_plan_set_stage_events": [p, ctypes.POINTER(ctypes.c_void_p)],
         "fconv_run_no_alloc": [p, p, p, p, p, f32, f32, p, p],
         "fconv_plan_set_host_chunks": [p, i32],
+        "fconv_plan_host_chunk_sizes": [p, i32, pi, i32, pi],
         "fconv_plan_set_tile_shape": [p, i32, i32],
         "fconv_plan_launch_count": [p, pi],
         "fconv_plan_set_activation_params": [p, f32, f32],
@@ -222,6 +223,16 @@ def fconv_run_host(plan, x_host, w_host, bias_host, side_host, conv_scale, side_
 
 def fconv_plan_set_host_chunks(plan, chunks: int) -> None:
     _check(_load().fconv_plan_set_host_chunks(plan, chunks), "fconv_plan_set_host_chunks")
+
+
+def fconv_plan_host_chunk_sizes(plan, sm_count: int) -> list:
+    n = ctypes.c_int(0)
+    _check(_load().fconv_plan_host_chunk_sizes(plan, sm_count, None, 0, ctypes.byref(n)),
+           "fconv_plan_host_chunk_sizes")
+    buf = (ctypes.c_int * max(n.value, 1))()
+    _check(_load().fconv_plan_host_chunk_sizes(plan, sm_count, buf, n.value, ctypes.byref(n)),
+           "fconv_plan_host_chunk_sizes")
+    return list(buf[:n.value])
 
 
 def fconv_plan_set_tile_shape(plan, pixels: int, channels: int) -> None:

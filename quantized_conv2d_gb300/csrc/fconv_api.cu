@@ -1131,6 +1131,82 @@ fconv_status fconv_host_workspace_size(const fconv_plan *plan, int with_side, si
   return FCONV_OK;
 }
 
+// Image counts of the batch chunks fconv_run_host pipelines over, in order
+// (they sum to N); returns how many.  Copy-in of chunk i+1 and copy-out of
+// chunk i-1 overlap the compute of chunk i, and the host link bounds the
+// whole run, so what is not hidden is the copy-in of the first chunk and
+// the compute and copy-out of the last.  A fixed count (host_chunks > 0)
+// splits the batch evenly.  Automatic, with W(k) the most images whose
+// output tiles fill at most k waves (one tile per SM): a batch of at least
+// ten W(1) ramps up through W(1)/6, W(1)/2 and W(2) images, runs middle
+// chunks of at most W(3), and ramps down through W(2), W(1) and 2 W(1)/3.
+// The first compute then starts after a short copy, each chunk of the
+// ramp-down computes in about the time the next one takes to copy in, and
+// the last chunk's compute and copy-out are short; a chunk one image past
+// a whole number of waves costs a wave more.  (N=256 28x28x512 int8 on 152
+// SMs: 2, 6, 24, 36 x 5, 24, 12, 8 ran 1.26 ms against 1.30-1.31 for
+// twelve even chunks and 1.28 for the same ramp with chunks of 25 and 35.)
+// A smaller batch takes even chunks of at least one wave each, up to 12
+// (4 chunks 1.44 ms, 8 1.34, 12 1.33, 16 1.36 on the same layer), and one
+// chunk when it has less.
+int host_chunk_sizes(const fconv_plan &p, int sms, int sizes[kMaxHostChunks]) {
+  const int N = p.N;
+  auto even = [&](int chunks) {
+    chunks = std::max(1, std::min({chunks, kMaxHostChunks, N}));
+    const int per = (N + chunks - 1) / chunks;
+    int count = 0;
+    for (int left = N; left > 0; left -= per) sizes[count++] = std::min(per, left);
+    return count;
+  };
+  if (p.host_chunks > 0) return even(p.host_chunks);
+  if (sms <= 0 || p.num_tiles <= 0) return even(1);
+  // output tiles of an n-image slice (a plan of sub-pixel phases: in proportion)
+  auto tiles = [&](int n) -> long long {
+    if (p.num_phases > 0)
+      return (static_cast<long long>(p.num_tiles) * n + N - 1) / N;
+    return batch_slice(p, n).num_tiles;
+  };
+  auto most_images = [&](int waves) {   // W(waves), 0 if one image needs more
+    const long long cap = static_cast<long long>(waves) * sms;
+    int lo = 0, hi = N;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (tiles(mid) <= cap) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  const int w1 = most_images(1);
+  if (w1 < 1 || N < 10 * w1) return even(std::min(12, p.num_tiles / sms));
+  const int w2 = most_images(2), w3 = most_images(3);
+  const int head[3] = {std::max(1, w1 / 6), std::max(1, w1 / 2), w2};
+  const int tail[3] = {w2, w1, std::max(1, 2 * w1 / 3)};
+  int fixed = 0;
+  for (int v : head) fixed += v;
+  for (int v : tail) fixed += v;
+  const int rest = N - fixed;   // about 10 W(1) - 6.3 W(1)
+  if (rest < 1) return even(std::min(12, p.num_tiles / sms));
+  const int mids = std::min(kMaxHostChunks - 6, (rest + w3 - 1) / w3);
+  int count = 0;
+  for (int v : head) sizes[count++] = v;
+  for (int i = 0; i < mids; ++i) sizes[count++] = rest / mids + (i < rest % mids ? 1 : 0);
+  for (int v : tail) sizes[count++] = v;
+  return count;
+}
+
+fconv_status fconv_plan_host_chunk_sizes(const fconv_plan *plan, int sm_count, int *sizes,
+                                         int max_sizes, int *count) {
+  if (!plan || !count) return fail(FCONV_ERR_INVALID_VALUE, "plan and count must not be NULL");
+  if (sm_count <= 0) return fail(FCONV_ERR_INVALID_VALUE, "sm_count must be positive");
+  int tmp[kMaxHostChunks];
+  const int n = host_chunk_sizes(*plan, sm_count, tmp);
+  *count = n;
+  if (sizes) {
+    if (max_sizes < n) return fail(FCONV_ERR_INVALID_VALUE, "%d chunks need %d entries", n, n);
+    for (int i = 0; i < n; ++i) sizes[i] = tmp[i];
+  }
+  return FCONV_OK;
+}
+
 fconv_status fconv_run_host(fconv_plan *plan, const void *x_host, const void *w_host,
                             const float *bias_host, const void *side_host, float conv_scale,
                             float side_scale, void *y_host, void *device_workspace,
@@ -1153,23 +1229,8 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host, const void *w_
   const size_t img_y = static_cast<size_t>(plan->P) * plan->Q * plan->K * elt;
   const size_t w_b = static_cast<size_t>(plan->R) * plan->S * plan->C * plan->K * elt;
 
-  // Batch chunks: copy-in of chunk i+1 and copy-out of chunk i-1 overlap the
-  // compute of chunk i.  The host link, not the GPU, bounds the whole run, so
-  // what is not hidden is the compute and copy-out of the last chunk: use as
-  // many chunks as keep at least one wave of output tiles each, up to 12
-  // (measured on the N=256 28x28x512 int8 run: 4 chunks 1.44 ms, 8 1.34,
-  // 12 1.33, 16 1.36).
-  int chunks = plan->host_chunks;
-  if (chunks <= 0) {
-    const int sms = device_sm_count(nullptr);
-    chunks = sms > 0 ? plan->num_tiles / sms : 1;
-    if (chunks > 12) chunks = 12;
-  }
-  if (chunks < 1) chunks = 1;
-  if (chunks > kMaxHostChunks) chunks = kMaxHostChunks;
-  if (chunks > plan->N) chunks = plan->N;
-  const int per = (plan->N + chunks - 1) / chunks;
-  chunks = (plan->N + per - 1) / per;
+  int sizes[kMaxHostChunks];
+  const int chunks = host_chunk_sizes(*plan, device_sm_count(nullptr), sizes);
 
   fconv_status s = ensure_pipeline(plan);
   if (s != FCONV_OK) return s;
@@ -1187,9 +1248,9 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host, const void *w_
       (e = cudaMemcpyAsync(base + off[3], bias_host, static_cast<size_t>(plan->K) * 4,
                            cudaMemcpyHostToDevice, plan->s_in)) != cudaSuccess)
     return cuda_fail(e, "host-to-device copy");
-  for (int i = 0; i < chunks; ++i) {
-    const size_t n0 = static_cast<size_t>(i) * per;
-    const size_t n = std::min(static_cast<size_t>(per), static_cast<size_t>(plan->N) - n0);
+  for (int i = 0, first = 0; i < chunks; first += sizes[i++]) {
+    const size_t n0 = static_cast<size_t>(first);
+    const size_t n = static_cast<size_t>(sizes[i]);
     if ((e = cudaMemcpyAsync(base + off[1] + n0 * img_x, static_cast<const uint8_t *>(x_host) +
                                  n0 * img_x, n * img_x, cudaMemcpyHostToDevice, plan->s_in)) !=
         cudaSuccess)
@@ -1202,9 +1263,9 @@ fconv_status fconv_run_host(fconv_plan *plan, const void *x_host, const void *w_
     if ((e = cudaEventRecord(plan->ev_in[i], plan->s_in)) != cudaSuccess)
       return cuda_fail(e, "event record");
   }
-  for (int i = 0; i < chunks; ++i) {
-    const size_t n0 = static_cast<size_t>(i) * per;
-    const int n = static_cast<int>(std::min(static_cast<size_t>(per), static_cast<size_t>(plan->N) - n0));
+  for (int i = 0, first = 0; i < chunks; first += sizes[i++]) {
+    const size_t n0 = static_cast<size_t>(first);
+    const int n = sizes[i];
     if ((e = cudaStreamWaitEvent(st, plan->ev_in[i], 0)) != cudaSuccess)
       return cuda_fail(e, "stream ordering");
     fconv_plan q = batch_slice(*plan, n);

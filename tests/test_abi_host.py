@@ -446,3 +446,65 @@ def test_benchmark_workload_plans(name, block_n, form, splits):
         assert fc.fconv_plan_get_splits(h) == splits
     finally:
         fc.fconv_plan_destroy(h)
+
+
+@pytest.mark.parametrize("shape,sms", [
+    ((256, 28, 28, 512, 512, 3, 3, 1), 152), ((128, 28, 28, 512, 512, 3, 3, 1), 152),
+    ((124, 28, 28, 512, 512, 3, 3, 1), 152), ((1024, 28, 28, 512, 512, 3, 3, 1), 152),
+    ((32, 56, 56, 64, 64, 3, 3, 1), 152), ((7, 12, 10, 64, 48, 3, 3, 1), 152),
+    ((256, 28, 28, 512, 512, 3, 3, 1), 8), ((2048, 7, 7, 64, 64, 3, 3, 1), 8),
+    ((5000, 4, 4, 16, 16, 1, 1, 1), 8), ((1, 16, 16, 32, 32, 3, 3, 1), 152),
+])
+def test_host_chunk_sizes_cover_the_batch(shape, sms):
+    N, H, W, C, K, R, S, st = shape
+    h = fc.fconv_plan_create(N, H, W, C, K, R, S, st, st, fc.FCONV_SAME, fc.FCONV_INT8, 1)
+    try:
+        sizes = fc.fconv_plan_host_chunk_sizes(h, sms)
+        assert sum(sizes) == N and 1 <= len(sizes) <= 16 and min(sizes) >= 1, sizes
+    finally:
+        fc.fconv_plan_destroy(h)
+
+
+def _tiles(n, P, Q, K, block_n):
+    # 128-pixel output tiles times channel tiles of an n-image slice
+    return -(-n * P * Q // 128) * (K // block_n)
+
+
+def test_host_chunk_ramp_fills_whole_waves():
+    """The automatic host chunks of the N=256 28x28x512 int8 layer on 152 SMs:
+    a ramp whose W(2)- and W(1)-sized chunks are the most images that fill
+    two waves and one wave of 128 x 256 tiles."""
+    h = fc.fconv_plan_create(256, 28, 28, 512, 512, 3, 3, 1, 1, fc.FCONV_SAME, fc.FCONV_INT8, 1)
+    try:
+        assert fc.fconv_plan_get_config(h)[0] == 256
+        sizes = fc.fconv_plan_host_chunk_sizes(h, 152)
+    finally:
+        fc.fconv_plan_destroy(h)
+    w = {k: max(n for n in range(1, 257) if _tiles(n, 28, 28, 512, 256) <= k * 152)
+         for k in (1, 2, 3)}
+    assert (w[1], w[2], w[3]) == (12, 24, 37)
+    assert sizes[:3] == [w[1] // 6, w[1] // 2, w[2]]
+    assert sizes[-3:] == [w[2], w[1], 2 * w[1] // 3]
+    mids = sizes[3:-3]
+    assert max(mids) <= w[3] and max(mids) - min(mids) <= 1 and sum(sizes) == 256
+    assert sizes == [2, 6, 24, 36, 36, 36, 36, 36, 24, 12, 8]
+
+
+def test_host_chunk_sizes_fixed_count_and_errors():
+    h = fc.fconv_plan_create(7, 12, 10, 64, 48, 3, 3, 1, 1, fc.FCONV_SAME, fc.FCONV_INT8, 1)
+    try:
+        fc.fconv_plan_set_host_chunks(h, 3)
+        assert fc.fconv_plan_host_chunk_sizes(h, 152) == [3, 3, 1]
+        fc.fconv_plan_set_host_chunks(h, 0)
+        assert fc.fconv_plan_host_chunk_sizes(h, 152) == [7]   # less than a wave: one chunk
+        n = ctypes.c_int(0)
+        buf = (ctypes.c_int * 1)()
+        lib = fc._load()
+        assert lib.fconv_plan_host_chunk_sizes(h, 0, buf, 1, ctypes.byref(n)) == \
+            fc.FCONV_ERR_INVALID_VALUE
+        fc.fconv_plan_set_host_chunks(h, 3)
+        assert lib.fconv_plan_host_chunk_sizes(h, 152, buf, 1, ctypes.byref(n)) == \
+            fc.FCONV_ERR_INVALID_VALUE
+        assert n.value == 3
+    finally:
+        fc.fconv_plan_destroy(h)

@@ -335,6 +335,30 @@ def test_run_host_buffers(chunks, splits, dtype):
     p.close()
 
 
+def test_run_host_ramped_chunks():
+    """fconv_run_host's automatic chunks on a batch of more than ten waves of
+    output tiles: the ramped schedule (short first and last chunks, whole
+    waves between) on this GPU's SM count, every output against the oracle."""
+    c = sweep_case(91, (64, 28, 28, 32, 256, 3, 3, 1, "SAME", True, True), "int8")
+    p = c.plan()
+    fc.fconv_plan_set_tile(p.handle, 64)           # 4 channel tiles: 24.5 tiles an image
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sizes = fc.fconv_plan_host_chunk_sizes(p.handle, sms)
+    assert sum(sizes) == c.N and len(sizes) > 3 and sizes[0] < sizes[3] > sizes[-1], sizes
+    nbytes = fc.fconv_host_workspace_size(p.handle, True)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    xh, wh = torch.from_numpy(c.x).pin_memory(), torch.from_numpy(c.w).pin_memory()
+    bh, sh = torch.from_numpy(c.bias).pin_memory(), torch.from_numpy(c.side).pin_memory()
+    yh = torch.empty(p.out_shape, dtype=torch.int8).pin_memory()
+    s = torch.cuda.current_stream()
+    fc.fconv_run_host(p.handle, xh.data_ptr(), wh.data_ptr(), bh.data_ptr(), sh.data_ptr(),
+                      c.conv_scale, c.side_scale, yh.data_ptr(), dev.data_ptr(), nbytes,
+                      s.cuda_stream)
+    p.check()
+    c.check_output(yh.numpy(), c.oracle_out())
+    p.close()
+
+
 @pytest.mark.parametrize("C,K,kernel", [(16, 16, "cp-async"), (64, 64, "tma-im2col"),
                                          (64, 256, "tma-im2col"), (64, 128, "tma-im2col-m256"),
                                          (832, 64, "tma-im2col-kb2")])
