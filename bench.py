@@ -350,6 +350,10 @@ def run_fconv(args, rank, world, local_rank):
     plan = fc.Conv2dPlan(n_local, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.padding,
                          wl.dtype, wl.relu if act is None else act, device=dev, alpha=alpha,
                          beta=beta, transposed_pads=wl.transposed_pads)
+    if args.gather:
+        fc.fconv_plan_set_gather(plan.handle, {"auto": fc.FCONV_GATHER_AUTO,
+                                               "im2col": fc.FCONV_GATHER_IM2COL,
+                                               "halo": fc.FCONV_GATHER_HALO}[args.gather])
     if args.tile:
         plan.set_tile(args.tile)
     if args.tile_shape:
@@ -634,6 +638,9 @@ def main():
                     help="run the workload's layer on this many images (profiling only)")
     ap.add_argument("--widen", type=int, default=0, choices=[0, 1, 2],
                     help="int8 input widening: 0 automatic, 1 in the kernel, 2 an fp16 copy")
+    ap.add_argument("--gather", default="", choices=["", "auto", "im2col", "halo"],
+                    help="input gather: the plan's own choice, never the halo gather, or the "
+                         "halo gather (stride-1 layers with 64 input channels)")
     ap.add_argument("--splits", type=int, default=0,
                     help="force a split-K count (1: none; 0: the plan's own choice)")
     ap.add_argument("--no-e2e", action="store_true")

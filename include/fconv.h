@@ -374,6 +374,32 @@ fconv_status fconv_run_no_alloc(fconv_plan *plan, const void *x, const void *w,
 fconv_status fconv_plan_set_input_widening(fconv_plan *plan, int mode);
 fconv_status fconv_plan_get_input_widening(const fconv_plan *plan, int *in_kernel);
 
+/* How the convolution kernel gathers its input operand.  The halo gather
+ * serves forward stride-1 plans with C == 64, at most 9 filter taps, sums in
+ * one exact accumulation and 64-channel tiles, whose input windows fit
+ * shared memory (3x3 int8 layers up to 115 output columns, 86 on 256-pixel
+ * tiles).
+ * A tile is floor(128 * m / (Q + S - 1)) whole output rows of one image (m
+ * = 1 or 2 for 128- or 256-pixel tiles), its GEMM rows those rows padded to
+ * Q + S - 1 columns (the extra rows are computed and dropped).  Once a tile,
+ * one tiled TMA copy brings the window of input rows the tile reads (zero
+ * outside the image); the CTA's filter tile stays in shared memory, and the
+ * MMA reads each filter tap's operand as a row shift of the window.  int8
+ * plans widen the window and the filter inside the kernel: one launch, no
+ * workspace (fconv_plan_set_input_widening with FCONV_WIDEN_COPY moves a
+ * plan off this gather).  FCONV_GATHER_AUTO: the plan's own choice (the
+ * default); FCONV_GATHER_IM2COL: never the halo gather; FCONV_GATHER_HALO:
+ * the halo gather (FCONV_ERR_NOT_SUPPORTED for a plan it does not fit);
+ * after it, fconv_plan_set_tile_shape(plan, 128 or 256, 64) picks the halo
+ * tile of that height, while other tiles, fconv_plan_set_tile and split-K
+ * are tiles of the other gathers.  The workspace size, launch count and tile
+ * count depend on it; results do not (int8 bit for bit).
+ * fconv_plan_kernel reports "tma-halo" / "tma-halo-m256". */
+#define FCONV_GATHER_AUTO 0
+#define FCONV_GATHER_IM2COL 1
+#define FCONV_GATHER_HALO 2
+fconv_status fconv_plan_set_gather(fconv_plan *plan, int mode);
+
 /* Split-K for the plan's current tile: each output tile's k-blocks are
  * divided over `splits` CTAs (1: none; 0: the automatic choice made at
  * plan creation, tile included); every unit writes its partial sums to the

@@ -33,6 +33,7 @@ FCONV_DEBUG_DROP_ARRIVE = 1
 FCONV_DEBUG_GATHER_CPASYNC = 2
 FCONV_DEBUG_ONE_KBLOCK_STAGES = 4
 FCONV_WIDEN_AUTO, FCONV_WIDEN_IN_KERNEL, FCONV_WIDEN_COPY = 0, 1, 2
+FCONV_GATHER_AUTO, FCONV_GATHER_IM2COL, FCONV_GATHER_HALO = 0, 1, 2
 
 
 class FconvError(RuntimeError):
@@ -86,6 +87,7 @@ def _load():
         "fconv_plan_set_splits": [p, i32],
         "fconv_plan_get_splits": [p, pi],
         "fconv_plan_set_input_widening": [p, i32],
+        "fconv_plan_set_gather": [p, i32],
         "fconv_plan_get_input_widening": [p, pi],
     }
     for name, args in sigs.items():
@@ -265,6 +267,10 @@ def fconv_plan_get_splits(plan) -> int:
 
 def fconv_plan_set_input_widening(plan, mode: int) -> None:
     _check(_load().fconv_plan_set_input_widening(plan, mode), "fconv_plan_set_input_widening")
+
+
+def fconv_plan_set_gather(plan, mode: int) -> None:
+    _check(_load().fconv_plan_set_gather(plan, mode), "fconv_plan_set_gather")
 
 
 def fconv_plan_get_input_widening(plan) -> int:

@@ -30,6 +30,10 @@ struct fconv_plan {
   int splits;           // split-K units per tile (1: none; TMA gather only)
   int auto_splits;
   int auto_block_n, auto_m_sub;  // the automatic tile (and auto_splits)
+  // the halo gather (fconv::Gather::kTmaHalo): whether the tile uses it, the
+  // automatic choice, the caller's FCONV_GATHER_* mode, and its window
+  int halo, auto_halo, gather_mode;
+  int halo_q, halo_tr, halo_rows, tiles_per_img, halo_slot, halo_stg;
   uint32_t timeout_ms;
   int debug;
   size_t wt_bytes, xh_bytes;
@@ -182,9 +186,50 @@ fconv::Gather gather_for(const fconv_plan &p, int bn, bool force_cpasync) {
   return fconv::Gather::kCpAsync;
 }
 
+// Whether the next run uses the halo gather (the cp.async test hook wins).
+bool halo_run(const fconv_plan &p) {
+  return p.halo && !(p.debug & FCONV_DEBUG_GATHER_CPASYNC);
+}
+
 // The gather the next run of a plan uses.
 fconv::Gather gather_for_run(const fconv_plan &p) {
+  if (halo_run(p)) return fconv::Gather::kTmaHalo;
   return gather_for(p, p.block_n, (p.debug & FCONV_DEBUG_GATHER_CPASYNC) != 0);
+}
+
+// The halo gather's tiles of 128 * ms GEMM rows x 64 channels, and
+// whether the plan can use them: a forward stride-1 plan with C == 64 (one
+// k-block a filter tap) whose sums fit one fp32 accumulation, whose filter
+// tile (R * S blocks of 64 x 64, 8 KB each) stays resident and whose input
+// window fits its buffer.  A tile is tr = floor(128 * ms / q) whole output
+// rows padded to q = Q + S - 1 columns (an image takes ceil(P / tr) tiles);
+// its window is tr + R - 1 input rows of q pixels.  Shared memory holds two
+// 16-bit windows, for int8 two stagings of the int8 window (each window is
+// copied while the previous one is widened), and the filter tile.  An int8
+// window is widened inside the kernel, so a plan that asks for the fp16
+// input copy (FCONV_WIDEN_COPY) does not use the gather.
+struct HaloGeom {
+  int q, tr, rows, tiles_per_img, slot, stg;
+};
+bool halo_geometry(const fconv_plan &p, int ms, HaloGeom *g) {
+  if (p.transposed || p.upsample || p.subsample || p.tap_nR > 0 || p.num_phases > 0) return false;
+  if (p.sh != 1 || p.sw != 1 || p.C != 64 || p.pt < 0 || p.pl < 0) return false;
+  if (p.kb_chunk < p.num_kb || p.num_kb * 64 * 64 * 2 > fconv::kHaloBMax) return false;
+  if (p.dtype == FCONV_INT8 && p.widen_mode == FCONV_WIDEN_COPY) return false;
+  if (ms != 1 && ms != 2) return false;
+  const int q = p.Q + p.S - 1;
+  if (q > 128 * ms || q > 256) return false;
+  const int tr = 128 * ms / q;
+  const int rows = tr + p.R - 1;
+  if (rows > 256) return false;
+  const long long px = static_cast<long long>(rows) * q;
+  const long long slot = (px * 128 + 1023) / 1024 * 1024;
+  const long long stg = p.dtype == FCONV_INT8 ? (px * 64 + 511) / 512 * 512 : 0;
+  if (2 * slot + 2 * stg + p.num_kb * 64LL * 64 * 2 > fconv::kHaloRegion) return false;
+  const long long tpi = (p.P + tr - 1) / tr;
+  if (tpi * p.N * ((p.K + 63) / 64) > kLimit) return false;
+  if (g) *g = {q, tr, rows, static_cast<int>(tpi), static_cast<int>(slot), static_cast<int>(stg)};
+  return true;
 }
 
 // K-blocks a pipeline stage of the next run: 2 on the TMA gather for
@@ -221,15 +266,34 @@ int kblocks_per_stage(const fconv_plan &p) {
 // back, ~8 cycles per output column per 128 pixels per split at an SM's
 // ~64 bytes per cycle from L2, before the epilogue.
 struct TileChoice {
-  int bn, ms, splits;
+  int bn, ms, splits, halo;
 };
-TileChoice choose_tile(const fconv_plan &p, int sms) {
+TileChoice choose_tile(const fconv_plan &p, int sms, bool allow_halo = true) {
   const bool chunked = p.kb_chunk < p.num_kb;
   // runs with a prep launch whatever the split: an input copy or a filter copy
   const bool needs_prep = p.dtype == FCONV_INT8 || p.upsample || p.transposed;
   const int kp = (p.K + 63) / 64 * 64;   // tiles are whole 64-channel B boxes
-  TileChoice best = {64, 1, 1};
+  TileChoice best = {64, 1, 1, 0};
   long long best_cost = -1;
+  // the halo gather (64-channel tiles, unsplit): per k-block each MMA
+  // issuer's 4 MMAs (~110 cycles each, two issuers on 256-pixel tiles)
+  // against the tensor core's ~48 cycles a 128 x 64 x 16 MMA; the window
+  // copy and widening run on other warps a tile ahead.  (The im2col tiles'
+  // int8 input copy in the prep launch, which this gather avoids, is not
+  // counted.)
+  for (int ms : {1, 2}) {
+    HaloGeom g;
+    if (!allow_halo || !halo_geometry(p, ms, &g)) continue;
+    const long long tiles = static_cast<long long>(p.N) * g.tiles_per_img * ((p.K + 63) / 64);
+    const long long waves = (tiles + sms - 1) / sms;
+    const long long mainloop = p.num_kb * (192LL * ms > 440 ? 192LL * ms : 440);
+    const long long epilogue = 22LL * 64 * ms;
+    const long long cost = waves * (mainloop > epilogue ? mainloop : epilogue) + 8LL * 64 * ms;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = {64, ms, 1, 1};
+    }
+  }
   for (int bn : {256, 128, 64}) {
     for (int ms : {1, 2}) {
       if (bn > kp) continue;
@@ -265,7 +329,7 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
                                split_launch;
         if (best_cost < 0 || cost < best_cost) {
           best_cost = cost;
-          best = {bn, ms, sp};
+          best = {bn, ms, sp, 0};
         }
       }
     }
@@ -274,10 +338,34 @@ TileChoice choose_tile(const fconv_plan &p, int sms) {
 }
 
 void update_widen(fconv_plan &p);
+void set_tiling(fconv_plan &p, int bn, int ms, int splits, int halo);
 
-void set_tiling(fconv_plan &p, int bn, int ms = 1, int splits = 1) {
+// Move a plan off the halo gather, onto the automatic tile without it.
+void retile_without_halo(fconv_plan &p) {
+  const int sms = sm_count_of_current_device(148);
+  const TileChoice t = choose_tile(p, p.sm_share > 1 ? sms / p.sm_share : sms, false);
+  set_tiling(p, t.bn, t.ms, t.splits, 0);
+}
+
+// Output tiles of the plan's tile shape (the halo gather tiles each image's
+// virtual pixels).
+int tile_count(const fconv_plan &p) {
+  if (p.halo) return p.N * p.tiles_per_img * p.num_n_tiles;
+  return static_cast<int>((p.M + 128LL * p.m_sub - 1) / (128LL * p.m_sub)) * p.num_n_tiles;
+}
+
+// halo: use the halo gather (the caller has checked halo_geometry).
+void set_tiling(fconv_plan &p, int bn, int ms, int splits, int halo) {
   p.block_n = bn;
   p.m_sub = ms;
+  HaloGeom g = {0, 0, 0, 0, 0, 0};
+  p.halo = (halo && bn == 64 && splits <= 1 && halo_geometry(p, ms, &g)) ? 1 : 0;
+  p.halo_q = g.q;
+  p.halo_tr = g.tr;
+  p.halo_rows = g.rows;
+  p.tiles_per_img = g.tiles_per_img;
+  p.halo_slot = g.slot;
+  p.halo_stg = g.stg;
   // no empty unit: with ceil(num_kb / splits) k-blocks a unit, that many
   // units cover the tile (9 k-blocks asked in 4 splits run as 3 of 3)
   if (splits > 1) {
@@ -286,7 +374,7 @@ void set_tiling(fconv_plan &p, int bn, int ms = 1, int splits = 1) {
   }
   p.splits = splits < 1 ? 1 : splits;
   p.num_n_tiles = (p.K + bn - 1) / bn;
-  p.num_tiles = static_cast<int>((p.M + 128LL * ms - 1) / (128LL * ms)) * p.num_n_tiles;
+  p.num_tiles = tile_count(p);
   update_widen(p);
 }
 
@@ -295,7 +383,7 @@ void set_tiling(fconv_plan &p, int bn, int ms = 1, int splits = 1) {
 // the input as it is), unsplit, with epilogue threads holding at most 64
 // sums (128-pixel tiles of up to 128 channels, 256-pixel tiles of 64).
 bool widen_eligible(const fconv_plan &p) {
-  if (p.dtype != FCONV_INT8 || p.transposed || p.upsample || p.splits != 1) return false;
+  if (p.dtype != FCONV_INT8 || p.transposed || p.upsample || p.splits != 1 || p.halo) return false;
   if (p.debug & FCONV_DEBUG_GATHER_CPASYNC) return false;
   if (p.m_sub == 1 ? p.block_n > 128 : p.block_n != 64) return false;
   fconv_plan raw = p;
@@ -315,7 +403,7 @@ void update_widen(fconv_plan &p) {
   p.widen = (want && widen_eligible(p)) ? 1 : 0;
   const InputView v = input_view(p);
   const long long xh_elems = static_cast<long long>(p.N) * v.H * v.W * p.C;
-  p.xh_bytes = ((p.dtype == FCONV_INT8 && !p.widen) || p.upsample)
+  p.xh_bytes = ((p.dtype == FCONV_INT8 && !p.widen && !halo_run(p)) || p.upsample)
                    ? align_up(static_cast<size_t>(xh_elems) * 2, 256) : 0;
 }
 
@@ -377,19 +465,28 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Split-K scratch after the operand copies: every unit's partial block
 // (128 * m_sub * block_n 32-bit words), then one counter per tile and
 // epilogue warp.
+// Bytes of the filter copy a run writes (an int8 plan on the halo gather
+// widens its filter inside the convolution kernel instead).
+size_t filter_copy_bytes(const fconv_plan &p) {
+  return (p.pack_filter && !(halo_run(p) && p.dtype == FCONV_INT8)) ? p.wt_bytes : 0;
+}
+// End of the operand copies in the workspace.
+size_t copies_end(const fconv_plan &p) {
+  const size_t wt = filter_copy_bytes(p);
+  const size_t a = wt ? p.ws_wt_off + wt : 0, b = p.xh_bytes ? p.ws_xh_off + p.xh_bytes : 0;
+  return a > b ? a : b;
+}
 size_t split_partial_offset(const fconv_plan &p) {
-  const size_t a = p.ws_wt_off + p.wt_bytes, b = p.ws_xh_off + p.xh_bytes;
-  return align_up(a > b ? a : b, 256);
+  return align_up(copies_end(p), 256);
 }
 size_t split_partial_bytes(const fconv_plan &p) {
   return align_up(static_cast<size_t>(p.num_tiles) * p.splits * 128 * p.m_sub * p.block_n * 4, 256);
 }
 size_t workspace_need(const fconv_plan &p) {
-  const size_t a = p.ws_wt_off + p.wt_bytes, b = p.ws_xh_off + p.xh_bytes;
   if (p.splits > 1)
     return split_partial_offset(p) + split_partial_bytes(p) +
            align_up(static_cast<size_t>(p.num_tiles) * kSplitCountersPerTile * 4, 256);
-  return a > b ? a : b;
+  return copies_end(p);
 }
 
 fconv_plan batch_slice(const fconv_plan &p, int n);
@@ -486,9 +583,9 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   // unsplit 128-pixel tile, from a copy, so the caller's plan keeps its
   // tiling (and its workspace size)
   fconv_plan reduced;
-  if (gather == fconv::Gather::kCpAsync && (p->m_sub != 1 || p->splits != 1)) {
+  if (gather == fconv::Gather::kCpAsync && (p->m_sub != 1 || p->splits != 1 || p->halo)) {
     reduced = *p;
-    set_tiling(reduced, p->block_n, 1, 1);
+    set_tiling(reduced, p->block_n, 1, 1, 0);
     p = &reduced;
   }
   if (!fconv::gather_supports(gather, p->block_n, p->kb_chunk < p->num_kb, p->m_sub))
@@ -503,7 +600,9 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   // convolution reads the copies when there are some
   const InputView view = input_view(*p);
   const int gH = view.H, gW = view.W, gsh = view.sh, gsw = view.sw;
-  const bool copy = (is_int8 && !p->widen) || p->upsample;   // the convolution reads a copy
+  const bool halo = gather == fconv::Gather::kTmaHalo;
+  // the convolution reads a copy (the halo gather widens int8 windows itself)
+  const bool copy = (is_int8 && !p->widen && !halo) || p->upsample;
   const bool do_copy = copy && !skip_copy;            // ... made by this launch
   const void *act = x;
   const long long n = static_cast<long long>(p->N) * gH * gW * p->C;
@@ -518,7 +617,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   }
   // (a run whose filter needs no copy, or has it already, and whose input
   // needs none either still launches it when split-K counters need zeroing)
-  const bool do_pack = !skip_pack && p->pack_filter;
+  const bool do_pack = !skip_pack && filter_copy_bytes(*p) > 0;
   const bool prep = do_pack || do_copy || split_counters;
   if (prep) {
     fconv::WidenMap map;
@@ -548,11 +647,14 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   // block stride 128 bytes), whose {64, 64, block_n / 64} box is a whole B
   // tile in one copy; else the 2-D matrix in 64 x 64 boxes.
   const void *bsrc = p->pack_filter ? static_cast<const void *>(wt) : w;
+  // an int8 plan on the halo gather reads the caller's int8 filter itself
+  const bool b_map = !(halo && is_int8);
   const int b3d = (p->K % 64 == 0 && p->block_n <= p->K) ? 1 : 0;
   const int kps = kblocks_per_stage(*p);   // boxes of 64 * kps k-rows
   const int b_form = b3d | (kps << 1);
   fconv_plan::MapCache &mb = p->map_b;
-  if (!(mb.valid && mb.base == bsrc && mb.form == b_form && (!b3d || mb.n == p->block_n))) {
+  if (b_map &&
+      !(mb.valid && mb.base == bsrc && mb.form == b_form && (!b3d || mb.n == p->block_n))) {
     mb.valid = false;
     memset(&mb.map, 0, sizeof mb.map);
     const CUtensorMapDataType bt =
@@ -585,14 +687,45 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     mb.form = b_form;
     mb.valid = true;
   }
-  const CUtensorMap &tmap = mb.map;
+  static const CUtensorMap kNoMapB = {};
+  const CUtensorMap &tmap = b_map ? mb.map : kNoMapB;
 
   // A: one im2col copy per k-block of a whole tile's pixels (128, or 256
   // for two sub-tiles: the second continues the first's walk); widening in
   // the kernel copies each 128-pixel sub-tile into its own staging slot
   const int a_pixels = p->widen ? 128 : 128 * p->m_sub;
-  const int a_form = (p->widen ? 1 : 0) | (a_pixels << 1);
+  const int a_form = halo ? (3 | (p->halo_q << 2) | (p->halo_rows << 11))
+                          : (p->widen ? 1 : 0) | (a_pixels << 2);
   fconv_plan::MapCache &ma = p->map_a;
+  if (halo && !(ma.valid && ma.base == act && ma.n == p->N && ma.form == a_form)) {
+    // the input itself, NHWC, innermost first: C, W, H, N; a box of the 64
+    // channels of halo_rows x halo_q pixels (parts outside the image read
+    // as zero); int8 unswizzled (the kernel widens it), bf16 with the
+    // 128-byte swizzle the MMA reads
+    ma.valid = false;
+    memset(&ma.map, 0, sizeof ma.map);
+    const int elt = is_int8 ? 1 : 2;
+    const cuuint64_t hdim[4] = {static_cast<cuuint64_t>(p->C), static_cast<cuuint64_t>(p->W),
+                                static_cast<cuuint64_t>(p->H), static_cast<cuuint64_t>(p->N)};
+    const cuuint64_t hstride[3] = {static_cast<cuuint64_t>(p->C) * elt,
+                                   static_cast<cuuint64_t>(p->W) * p->C * elt,
+                                   static_cast<cuuint64_t>(p->H) * p->W * p->C * elt};
+    const cuuint32_t hbox[4] = {64, static_cast<cuuint32_t>(p->halo_q),
+                                static_cast<cuuint32_t>(p->halo_rows), 1};
+    const cuuint32_t hes[4] = {1, 1, 1, 1};
+    CUresult cr = encode(&ma.map,
+                         is_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         4, const_cast<void *>(act), hdim, hstride, hbox, hes,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         is_int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS)
+      return fail(FCONV_ERR_INTERNAL, "window tensor map encode failed (%d)", (int)cr);
+    ma.base = act;
+    ma.n = p->N;
+    ma.form = a_form;
+    ma.valid = true;
+  }
   if (gather == fconv::Gather::kTmaIm2col &&
       !(ma.valid && ma.base == act && ma.n == p->N && ma.form == a_form)) {
     ma.valid = false;
@@ -633,7 +766,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
     ma.valid = true;
   }
   static const CUtensorMap kNoMap = {};
-  const CUtensorMap &tmap_a = gather == fconv::Gather::kTmaIm2col ? ma.map : kNoMap;
+  const CUtensorMap &tmap_a =
+      (gather == fconv::Gather::kTmaIm2col || halo) ? ma.map : kNoMap;
 
   fconv::ConvArgs a;
   memset(&a, 0, sizeof a);
@@ -676,8 +810,17 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.kb_per_split = (p->num_kb + p->splits - 1) / p->splits;
   a.partial = split_partial;
   a.counters = split_counters;
+  a.halo_q = p->halo_q;
+  a.halo_tr = p->halo_tr;
+  a.halo_rows = p->halo_rows;
+  a.tiles_per_img = p->tiles_per_img;
+  a.halo_slot = p->halo_slot;
+  a.halo_stg = p->halo_stg;
+  a.w_i8 = (halo && is_int8) ? static_cast<const int8_t *>(w) : nullptr;
   const long long units = static_cast<long long>(a.num_tiles) * a.splits;
-  const int grid = units < sms ? static_cast<int>(units) : sms;
+  int grid = units < sms ? static_cast<int>(units) : sms;
+  // the halo gather keeps each CTA on one output-channel tile
+  if (halo) grid = grid / p->num_n_tiles * p->num_n_tiles;
   e = fconv::launch_conv(p->block_n, p->m_sub, is_int8, gather, tmap_a, tmap, a, grid,
                         /*overlap=*/prep, stream, p->widen != 0);
   if (e != cudaSuccess)
@@ -697,7 +840,7 @@ fconv_plan batch_slice(const fconv_plan &p, int n) {
   fconv_plan q = p;
   q.N = n;
   q.M = static_cast<long long>(n) * p.P * p.Q;
-  q.num_tiles = static_cast<int>((q.M + 128LL * p.m_sub - 1) / (128LL * p.m_sub)) * p.num_n_tiles;
+  q.num_tiles = tile_count(q);
   q.use_events = false;
   return q;
 }
@@ -860,17 +1003,18 @@ fconv_status finish_plan(fconv_plan &p, fconv_plan **plan) {
           ? 1 : 0;
   // the phases of a strided transposed plan run concurrently (up to four
   // streams), each on its share of the SMs
+  p.pack_filter = (dtype == FCONV_INT8 || p.tap_nR > 0) ? 1 : 0;
   const int sms = sm_count_of_current_device(148);
   const TileChoice tile = choose_tile(p, p.sm_share > 1 ? sms / p.sm_share : sms);
   p.auto_block_n = tile.bn;
   p.auto_m_sub = tile.ms;
   p.auto_splits = tile.splits;
-  set_tiling(p, tile.bn, tile.ms, tile.splits);
+  p.auto_halo = tile.halo;
+  set_tiling(p, tile.bn, tile.ms, tile.splits, tile.halo);
   p.timeout_ms = 2000;
   p.host_chunks = 0;
   p.pipe_dev = -1;
   p.fork_dev = -1;
-  p.pack_filter = (dtype == FCONV_INT8 || p.tap_nR > 0) ? 1 : 0;
   p.wt_bytes = p.pack_filter ? align_up(static_cast<size_t>(K) * p.Ktot * 2, 256) : 0;
   const InputView view = input_view(p);
   const long long xh_elems = static_cast<long long>(N) * view.H * view.W * C;
@@ -1323,7 +1467,8 @@ fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
     return FCONV_OK;
   }
   if (block_n == 0) {
-    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits);
+    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits,
+               plan->gather_mode == FCONV_GATHER_IM2COL ? 0 : plan->auto_halo);
     return FCONV_OK;
   }
   if (block_n != 64 && block_n != 128 && block_n != 256)
@@ -1332,7 +1477,7 @@ fconv_status fconv_plan_set_tile(fconv_plan *plan, int block_n) {
                               plan->kb_chunk < plan->num_kb))
     return fail(FCONV_ERR_NOT_SUPPORTED,
                 "tile %d leaves no tensor memory for the int32 sums this plan needs", block_n);
-  set_tiling(*plan, block_n);
+  set_tiling(*plan, block_n, 1, 1, 0);
   return FCONV_OK;
 }
 
@@ -1351,11 +1496,16 @@ fconv_status fconv_plan_set_tile_shape(fconv_plan *plan, int pixels, int channel
     return FCONV_OK;
   }
   const int ms = pixels / 128;
+  if (plan->gather_mode == FCONV_GATHER_HALO && channels == 64 &&
+      halo_geometry(*plan, ms, nullptr)) {
+    set_tiling(*plan, 64, ms, 1, 1);   // the halo tile of that height
+    return FCONV_OK;
+  }
   if (!fconv::gather_supports(gather_for(*plan, channels, false), channels,
                               plan->kb_chunk < plan->num_kb, ms))
     return fail(FCONV_ERR_NOT_SUPPORTED, "no kernel for %d x %d tiles on this plan", pixels,
                 channels);
-  set_tiling(*plan, channels, ms);
+  set_tiling(*plan, channels, ms, 1, 0);
   return FCONV_OK;
 }
 
@@ -1364,7 +1514,8 @@ fconv_status fconv_plan_set_splits(fconv_plan *plan, int splits) {
   if (splits < 0 || splits > kMaxSplits)
     return fail(FCONV_ERR_INVALID_VALUE, "splits %d: 0 (automatic) or 1 to %d", splits, kMaxSplits);
   if (splits == 0) {
-    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits);
+    set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits,
+               plan->gather_mode == FCONV_GATHER_IM2COL ? 0 : plan->auto_halo);
     return FCONV_OK;
   }
   if (splits > 1) {
@@ -1377,7 +1528,7 @@ fconv_status fconv_plan_set_splits(fconv_plan *plan, int splits) {
     if (splits > plan->num_kb)
       return fail(FCONV_ERR_NOT_SUPPORTED, "%d splits of %d k-blocks", splits, plan->num_kb);
   }
-  set_tiling(*plan, plan->block_n, plan->m_sub, splits);
+  set_tiling(*plan, plan->block_n, plan->m_sub, splits, splits == 1 ? plan->halo : 0);
   return FCONV_OK;
 }
 
@@ -1417,14 +1568,52 @@ fconv_status fconv_plan_set_input_widening(fconv_plan *plan, int mode) {
   if (mode != FCONV_WIDEN_AUTO && mode != FCONV_WIDEN_IN_KERNEL && mode != FCONV_WIDEN_COPY)
     return fail(FCONV_ERR_INVALID_VALUE, "unknown widening mode %d", mode);
   plan->widen_mode = mode;
-  if (plan->num_phases == 0) update_widen(*plan);
+  if (plan->num_phases == 0) {
+    // the halo gather widens int8 windows in the kernel: the fp16 copy
+    // moves the plan off it
+    if (plan->halo && !halo_geometry(*plan, plan->m_sub, nullptr)) retile_without_halo(*plan);
+    update_widen(*plan);
+  }
   return FCONV_OK;
 }
 
 fconv_status fconv_plan_get_input_widening(const fconv_plan *plan, int *in_kernel) {
   if (!plan || !in_kernel)
     return fail(FCONV_ERR_INVALID_VALUE, "plan and in_kernel must not be NULL");
-  *in_kernel = plan->widen;
+  // the halo gather widens int8 windows inside the kernel too
+  *in_kernel = (plan->widen || (plan->dtype == FCONV_INT8 && halo_run(*plan))) ? 1 : 0;
+  return FCONV_OK;
+}
+
+fconv_status fconv_plan_set_gather(fconv_plan *plan, int mode) {
+  if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
+  if (mode != FCONV_GATHER_AUTO && mode != FCONV_GATHER_IM2COL && mode != FCONV_GATHER_HALO)
+    return fail(FCONV_ERR_INVALID_VALUE, "unknown gather mode %d", mode);
+  if (plan->num_phases > 0) {
+    if (mode == FCONV_GATHER_HALO)
+      return fail(FCONV_ERR_NOT_SUPPORTED, "the halo gather is for forward stride-1 plans");
+    return FCONV_OK;
+  }
+  if (mode == FCONV_GATHER_HALO) {
+    // the halo tile the automatic choice would take, else 256 pixels if
+    // they fit, else 128
+    int ms = plan->auto_halo ? plan->auto_m_sub : 2;
+    if (!halo_geometry(*plan, ms, nullptr)) ms = 1;
+    if (!halo_geometry(*plan, ms, nullptr))
+      return fail(FCONV_ERR_NOT_SUPPORTED,
+                  "the halo gather needs a forward stride-1 plan with C == 64, at most 9 "
+                  "filter taps, one exact accumulation and windows that fit %d bytes of "
+                  "shared memory beside the filter tile", fconv::kHaloRegion);
+    plan->gather_mode = mode;
+    set_tiling(*plan, 64, ms, 1, 1);
+    return FCONV_OK;
+  }
+  plan->gather_mode = mode;
+  if (mode == FCONV_GATHER_IM2COL) {
+    if (plan->halo) retile_without_halo(*plan);
+    return FCONV_OK;
+  }
+  set_tiling(*plan, plan->auto_block_n, plan->auto_m_sub, plan->auto_splits, plan->auto_halo);
   return FCONV_OK;
 }
 
@@ -1448,9 +1637,10 @@ fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches) {
   // input is not a multiple of 64 elements, and the convolution
   auto one = [](const fconv_plan &p) {
     const long long n = static_cast<long long>(p.N) * p.H * p.W * p.C;
-    const bool tail =
-        p.dtype == FCONV_INT8 && !p.widen && !p.subsample && !p.upsample && n % 64 != 0;
-    const bool prep = p.pack_filter || p.dtype == FCONV_INT8 || p.upsample || p.splits > 1;
+    const bool tail = p.dtype == FCONV_INT8 && !p.widen && !halo_run(p) && !p.subsample &&
+                      !p.upsample && n % 64 != 0;
+    const bool prep = filter_copy_bytes(p) > 0 || (p.dtype == FCONV_INT8 && !halo_run(p)) ||
+                      p.upsample || p.splits > 1;
     return (prep ? 1 : 0) + (tail ? 1 : 0) + 1;
   };
   int total = 0;
@@ -1469,6 +1659,7 @@ fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches) {
 const char *fconv_plan_kernel(const fconv_plan *plan) {
   if (!plan) return "";
   if (plan->num_phases > 0) plan = plan->phase[0];
+  if (halo_run(*plan)) return plan->m_sub == 2 ? "tma-halo-m256" : "tma-halo";
   if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col && plan->m_sub == 2)
     return "tma-im2col-m256";
   if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col)

@@ -180,6 +180,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+// A 4-D tiled box (coordinates innermost first); parts of the box outside
+// the tensor (negative or past the extent) read as zero.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
 
 // 4-D im2col load (NHWC tensor map): pixelsPerColumn output pixels starting
 // at the filter-window origin (w, h, n) of the first one, walking the
@@ -299,6 +309,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle
   return d;
+}
+
+// The same descriptor for a tile that starts `row` 128-byte rows into a
+// 1024-byte-aligned buffer written with the 128-byte swizzle (a TMA copy
+// XORs each row's 16-byte chunk index with bits 7-9 of the row's address).
+// A start inside an 8-row atom needs nothing more: the MMA takes the XOR
+// pattern from the same address bits of each row it reads, so the
+// base-offset field stays 0.  (Measured on GB300: with that field set to
+// the start's row within its atom, (address >> 7) & 7, every sum came out
+// wrong; with 0 the sums of every tap shift are exact.)
+__device__ __forceinline__ uint64_t sw128_kmajor_desc_at_row(uint32_t buf, uint32_t row) {
+  return sw128_kmajor_desc(buf + row * 128u);
 }
 
 // Shared-memory matrix descriptor for an MN-major operand tile (the N index

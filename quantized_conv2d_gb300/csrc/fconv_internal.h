@@ -57,13 +57,36 @@ struct ConvArgs {
   int splits, kb_per_split;
   uint32_t *partial;
   int *counters;
+  // halo gather (stride 1, C == 64; Gather::kTmaHalo): a tile covers
+  // halo_tr whole output rows of one image (tiles_per_img tiles an image);
+  // its GEMM row i is the pixel (i / halo_q, i % halo_q) of those rows
+  // padded to halo_q = Q + S - 1 columns, an output pixel when the column is
+  // below Q, the row below halo_tr and the image row below P (the other
+  // rows are computed and dropped).  The tile reads a window of halo_rows =
+  // halo_tr + R - 1 input rows x halo_q pixels.  Shared memory: two
+  // 16-bit windows of halo_slot bytes, two int8 stagings of halo_stg bytes
+  // (int8 plans), then the resident filter tile.  w_i8: the caller's int8
+  // filter, which int8 plans widen inside the kernel (no prep launch).
+  int halo_q, halo_tr, halo_rows, tiles_per_img, halo_slot, halo_stg;
+  const int8_t *w_i8;
 };
 
 // How the kernel gathers the A (activation) tile of each k-block.
 enum class Gather {
   kCpAsync = 0,  // 16-byte cp.async per (pixel, 8 channels) with zero fill; any C % 8 == 0
-  kTmaIm2col = 1 // one TMA im2col load of 128 pixels x 64 channels; needs C % 64 == 0
+  kTmaIm2col = 1, // one TMA im2col load of 128 pixels x 64 channels; needs C % 64 == 0
+  // one tiled TMA load a tile of the input window its pixels read (stride
+  // 1, C == 64), the filter tile resident; each tap's A is a row shift of
+  // the window
+  kTmaHalo = 2
 };
+
+// The halo gather's shared memory: two 16-bit input windows (1024-byte
+// multiples), for int8 plans two stagings of the int8 window (512-byte
+// multiples), and the resident filter tile (at most 9 k-blocks of 64 x 64),
+// kHaloRegion bytes in all.
+constexpr int kHaloRegion = 205 * 1024;
+constexpr int kHaloBMax = 72 * 1024;
 
 // m_sub: 128-pixel sub-tiles per output tile (1, or 2 on the TMA gather
 // with block_n <= 128; args.num_tiles counts tiles of 128 * m_sub pixels).
@@ -74,6 +97,11 @@ enum class Gather {
 // convolution may overlap (programmatic dependent launch).
 // widen: int8 plans on the TMA gather, unsplit, block_n <= 128: tmap_a maps
 // the int8 input itself (64-byte pixel rows) and the kernel widens it.
+// Gather::kTmaHalo: tmap_a is the tiled map of the input itself (int8
+// unswizzled, bf16 128-byte swizzled) with a {64, halo_q, halo_rows, 1}
+// box; block_n 64, m_sub 1 or 2, unsplit, one fp32 accumulation, the grid
+// a multiple of num_n_tiles (each CTA keeps one output-channel tile); int8:
+// args.w_i8 is the caller's filter and tmap_b is unused (no prep launch).
 cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
                         const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                         const ConvArgs &args, int grid, bool overlap, cudaStream_t stream,

@@ -127,6 +127,39 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
   hi = *reinterpret_cast<const uint32_t *>(&hb);
 }
 
+// Widen int8 pixel rows [p0, p1) of a staged window (64 bytes a pixel) into
+// the 16-bit window the MMA reads (128 bytes a pixel, 128-byte swizzle:
+// 16-byte chunk j of row r at j ^ (r & 7), as a TMA copy writes it), by one
+// warp: four 16-byte pieces of each lane in flight before their stores.
+__device__ __forceinline__ void widen_rows(const uint8_t *src, uint8_t *dst, int p0, int p1) {
+  const int lane = threadIdx.x & 31;
+  const int n = (p1 - p0) * 4;   // 16-byte pieces
+  const uint8_t *s0 = src + p0 * 64;
+  for (int i0 = 0; i0 < n; i0 += 128) {
+    uint4 in[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int i = i0 + g * 32 + lane;
+      if (i < n) in[g] = *reinterpret_cast<const uint4 *>(s0 + i * 16);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int i = i0 + g * 32 + lane;
+      if (i < n) {
+        const int r = p0 + (i >> 2), pc = i & 3;
+        uint4 lo, hi;
+        i8x4_to_f16x4(in[g].x, lo.x, lo.y);
+        i8x4_to_f16x4(in[g].y, lo.z, lo.w);
+        i8x4_to_f16x4(in[g].z, hi.x, hi.y);
+        i8x4_to_f16x4(in[g].w, hi.z, hi.w);
+        uint8_t *row = dst + r * 128;
+        *reinterpret_cast<uint4 *>(row + (((2 * pc) ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(row + (((2 * pc + 1) ^ (r & 7)) << 4)) = hi;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
   return __uint_as_float(b16 << 16);
 }
@@ -760,20 +793,24 @@ struct TmaRegs {
 // cycles whatever the stage holds, so a stage of two k-blocks halves the
 // producers' cost per k-block; the MMA issuer takes the stage's MMAs after
 // one wait.
-template <int BN, int MS = 1, bool WIDEN = false, int KPS = 1>
+// HALO (the halo gather): instead of the stage ring a region of
+// kHaloRegion bytes holds two input windows, two int8 window stagings and
+// the CTA's whole filter tile, at offsets the plan gives (ConvArgs).
+template <int BN, int MS = 1, bool WIDEN = false, int KPS = 1, bool HALO = false>
 struct TmaCfg {
   static constexpr int kABytes = kBM * kBK * 2;        // one sub-tile's A of one k-block
-  static constexpr int kAStage = KPS * MS * kABytes;
-  static constexpr int kBBytes = KPS * BN * kBK * 2;
+  static constexpr int kAStage = HALO ? 0 : KPS * MS * kABytes;
+  static constexpr int kBBytes = HALO ? 0 : KPS * BN * kBK * 2;
   static constexpr int kStageBytes = kAStage + kBBytes;
   // staging of the int8 A tiles (WIDEN): 128 pixels x 64 bytes a sub-tile
   static constexpr int kStgBytes = WIDEN ? MS * kBM * kBK : 0;
   static constexpr int kStgStages = WIDEN ? (MS == 2 ? 3 : 4) : 0;
-  static constexpr int kStages0 = (200 * 1024 - kStgStages * kStgBytes) / kStageBytes;
-  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  static constexpr int kStages0 =
+      HALO ? 2 : (200 * 1024 - kStgStages * kStgBytes) / kStageBytes;
+  static constexpr int kStages = HALO ? 2 : kStages0 > 8 ? 8 : kStages0;
   static constexpr int kAccCols = MS * BN;             // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols <= 128 ? 128 : 2 * kAccCols <= 256 ? 256 : 512;
-  static constexpr int kStgOffset = kStages * kStageBytes;
+  static constexpr int kStgOffset = HALO ? kHaloRegion : kStages * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + kStgStages * kStgBytes;
   // columns per epilogue thread: MS = 1 splits a row's BN columns between
   // two warps; MS = 2 gives each warp half one sub-tile's whole rows
@@ -792,7 +829,8 @@ struct TmaCfg {
   static_assert(BN == 64 || BN == 128 || BN == 256, "TMA path tile");
   static_assert(MS == 1 || (MS == 2 && BN <= 128), "two sub-tiles need BN <= 128");
   static_assert(2 * kAccCols <= 512, "tensor memory");
-  static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(HALO || kStages >= 3, "pipeline too shallow");
+  static_assert(!HALO || (BN == 64 && !WIDEN && KPS == 1), "halo gather: 64-channel tiles");
   static_assert(!WIDEN || kHalfCols <= 64, "in-kernel widening needs the 96-register control warps");
   static_assert(KPS == 1 || (KPS == 2 && MS == 1 && !WIDEN), "two k-blocks a stage: 128-pixel tiles");
 };
@@ -801,13 +839,17 @@ struct TmaCfg {
 // and the last unit's reduction); the other instance keeps one unit a tile.
 // WIDEN (int8, unsplit, BN <= 128): tmap_a is an im2col map of the int8
 // input itself; warps 2-3 widen each staged A tile into the fp16 stage.
-template <int BN, bool IS_INT8, int MS, bool SPLITK, bool WIDEN = false, int KPS = 1>
+// HALO: the halo gather (see the loader role below): tmap_a is the tiled
+// map of the input itself, the filter tile stays resident, unsplit.
+template <int BN, bool IS_INT8, int MS, bool SPLITK, bool WIDEN = false, int KPS = 1,
+          bool HALO = false>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     conv_fprop_tma_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
   static_assert(!WIDEN || (IS_INT8 && !SPLITK), "widening: int8, unsplit");
   static_assert(KPS == 1 || !SPLITK, "two k-blocks a stage: unsplit");
-  using C = TmaCfg<BN, MS, WIDEN, KPS>;
+  static_assert(!HALO || !SPLITK, "halo gather: unsplit");
+  using C = TmaCfg<BN, MS, WIDEN, KPS, HALO>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8, /*b_mn=*/true);
   constexpr int kTileM = kBM * MS;
@@ -825,8 +867,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  uint8_t *sA = smem;   // per stage: MS sub-tiles of A, 16 KB each
-  uint8_t *sB = smem + kStages * C::kAStage;
+  uint8_t *sA = smem;   // per stage: MS sub-tiles of A, 16 KB each (HALO: two windows)
+  // HALO: the two int8 window stagings, then the resident filter tile
+  uint8_t *sStgH = smem + (HALO ? 2 * args.halo_slot : 0);
+  uint8_t *sB = HALO ? sStgH + 2 * args.halo_stg : smem + kStages * C::kAStage;
   uint8_t *sStg = smem + C::kStgOffset;   // WIDEN: the int8 A staging ring
   Smem *bars = reinterpret_cast<Smem *>(smem + C::kBarOffset);
   // WIDEN: the staging ring's barriers (the TMA kernel has no other use for
@@ -842,12 +886,28 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint64_t tmo = args.timeout_ns;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      // the stage is full once both producers' copies have landed (A from
-      // warp 0, B from warp 2); WIDEN: once the producer's B copy has landed
-      // and both converter warps have written the A tile
-      mbar_init(smem_u32(&bars->full_b[s]), WIDEN ? 3 : 2);
-      mbar_init(smem_u32(&bars->empty[s]), kMmaArrivals);
+    if constexpr (HALO) {
+      // window buffer s: full_b[s] = ready for the MMA (bf16: its copy
+      // landed; int8: both widening warps wrote their halves), empty[s] =
+      // the MMAs that read it are done; int8 staging s: full_a[s] = a
+      // window's copy landed, full_a[2 + s] = both widening warps have read
+      // it; full_b[7] = the resident filter tile is in place (bf16: one
+      // copy; int8: the 8 epilogue warps widened it)
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(smem_u32(&bars->full_b[s]), IS_INT8 ? 2 : 1);
+        mbar_init(smem_u32(&bars->empty[s]), kMmaArrivals);
+        mbar_init(smem_u32(&bars->full_a[s]), 1);
+        mbar_init(smem_u32(&bars->full_a[2 + s]), 2);
+      }
+      mbar_init(smem_u32(&bars->full_b[7]), IS_INT8 ? kTmaEpiWarps : 1);
+    } else {
+      for (int s = 0; s < kStages; ++s) {
+        // the stage is full once both producers' copies have landed (A from
+        // warp 0, B from warp 2); WIDEN: once the producer's B copy has
+        // landed and both converter warps have written the A tile
+        mbar_init(smem_u32(&bars->full_b[s]), WIDEN ? 3 : 2);
+        mbar_init(smem_u32(&bars->empty[s]), kMmaArrivals);
+      }
     }
     for (int i = 0; i < C::kStgStages; ++i) {
       mbar_init(smem_u32(&stg_full[i]), 1);
@@ -879,7 +939,169 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   if (warp < kTmaEpiWarp0) {
    setmaxnreg_dec<TmaRegs<C::kHalfCols>::kCtl>();
-   if (warp == 0) {
+   if constexpr (HALO) {
+    // ------------------------------------------------------------ halo gather
+    // A tile is halo_tr whole output rows p0 .. of one image.  Its GEMM row
+    // i = pr * Qh + q' (Qh = Q + S - 1) is output pixel (p0 + pr, q') when
+    // q' < Q (other rows are computed and dropped), and its tap (r, s) reads
+    // input pixel (p0 + pr + r - pt, q' + s - pl).  With the window of input
+    // rows p0 - pt .. p0 - pt + halo_rows - 1 and columns -pl .. Qh - 1 - pl
+    // stored pixel after pixel, that is window pixel i + r * Qh + s: every
+    // tap's A operand is the window itself, shifted by r * Qh + s rows of
+    // 128 bytes.  One tiled TMA copy a tile brings the window (zero outside
+    // the image) in place of R * S im2col copies, and the CTA's filter tile
+    // (all k-blocks of its output-channel tile: the grid is a multiple of
+    // the channel tiles) is loaded once.
+    const int Qh = args.halo_q;
+    const int tiles_img = args.tiles_per_img;
+    auto window_origin = [&](long long unit, int &n_img, int &p0) {
+      const int m_tile = static_cast<int>(unit / args.num_n_tiles);
+      n_img = m_tile / tiles_img;
+      p0 = (m_tile - n_img * tiles_img) * args.halo_tr;
+    };
+    const int win_px = args.halo_rows * Qh;   // window pixels
+    if (warp == 0 || warp == 2) {
+      // bf16: warp 0 copies the windows of the CTA's even tiles straight
+      // into buffer 0, warp 2 those of its odd tiles into buffer 1, after
+      // warp 2 has copied the filter tile.  int8: warp 0 copies window j
+      // into staging j % 2 (window j + 1's copy is issued before window j is
+      // widened, so it lands meanwhile), and both warps widen half of each
+      // window's pixels into the tile's buffer.
+      const int wi = warp >> 1;
+      const bool drop = (args.debug & 1) != 0;
+      if (!IS_INT8 && warp == 2) {
+        if (lane == 0) {
+          const uint32_t bb = smem_u32(&bars->full_b[7]);
+          mbar_arrive_expect_tx(bb, static_cast<uint32_t>(num_kb) * BN * kBK * 2);
+          const int n_tile = static_cast<int>(blockIdx.x) % args.num_n_tiles;
+          for (int kb = 0; kb < num_kb; ++kb)
+            load_b_tile<BN>(smem_u32(sB + kb * BN * kBK * 2), &tmap_b, kb, n_tile, args.b3d, bb);
+        }
+        __syncwarp();
+      }
+      const uint32_t win_bytes = static_cast<uint32_t>(win_px) * kBK * (IS_INT8 ? 1 : 2);
+      uint32_t issued[2] = {0, 0};   // copies into window buffer / staging s
+      bool ok = true;
+      if constexpr (IS_INT8) {
+        // warp 0: window jj's copy into staging jj % 2, once both warps have
+        // read window jj - 2 from it
+        auto issue = [&](long long jj) -> bool {
+          const long long u = blockIdx.x + jj * gridDim.x;
+          if (u >= args.num_tiles) return true;
+          const int sb = static_cast<int>(jj & 1);
+          const uint32_t sp = static_cast<uint32_t>(jj >> 1) & 1u;
+          if (!mbar_wait_warp(smem_u32(&bars->full_a[2 + sb]), sp ^ 1, abort_flag, tmo))
+            return false;
+          if (!drop) {
+            int n_img, p0;
+            window_origin(u, n_img, p0);
+            if (lane == 0) {
+              const uint32_t sf = smem_u32(&bars->full_a[sb]);
+              mbar_arrive_expect_tx(sf, win_bytes);
+              tma_load_4d(smem_u32(sStgH + sb * args.halo_stg), &tmap_a, 0, -args.pl,
+                          p0 - args.pt, n_img, sf);
+            }
+            __syncwarp();
+            ++issued[sb];
+          }
+          return true;
+        };
+        if (warp == 0) ok = issue(0);
+        for (long long j = 0; ok; ++j) {
+          const long long unit = blockIdx.x + j * gridDim.x;
+          if (unit >= args.num_tiles) break;
+          if (warp == 0 && !issue(j + 1)) break;
+          const int slot = static_cast<int>(j & 1);   // also the staging buffer
+          const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
+          if (!mbar_wait_warp(smem_u32(&bars->full_a[slot]), par, abort_flag, tmo) ||
+              !mbar_wait_warp(smem_u32(&bars->empty[slot]), par ^ 1, abort_flag, tmo))
+            break;
+          const int half_px = (win_px + 1) / 2;
+          widen_rows(sStgH + slot * args.halo_stg, sA + slot * args.halo_slot,
+                     wi ? half_px : 0, wi ? win_px : half_px);
+          fence_proxy_async_smem();   // the window is read by the tensor core
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bars->full_b[slot]));
+            mbar_arrive(smem_u32(&bars->full_a[2 + slot]));
+          }
+        }
+      } else {
+        for (long long j = wi;; j += 2) {
+          const long long unit = blockIdx.x + j * gridDim.x;
+          if (unit >= args.num_tiles) break;
+          const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
+          if (!mbar_wait_warp(smem_u32(&bars->empty[wi]), par ^ 1, abort_flag, tmo)) break;
+          if (!drop) {
+            int n_img, p0;
+            window_origin(unit, n_img, p0);
+            if (lane == 0) {
+              const uint32_t fb = smem_u32(&bars->full_b[wi]);
+              mbar_arrive_expect_tx(fb, win_bytes);
+              tma_load_4d(smem_u32(sA + wi * args.halo_slot), &tmap_a, 0, -args.pl,
+                          p0 - args.pt, n_img, fb);
+            }
+            __syncwarp();
+            ++issued[wi];
+          }
+        }
+      }
+      if (lane == 0) {
+        // copies still in flight after an abort land before the CTA exits
+        // (the last one into each buffer: a buffer's copies wait for each
+        // other)
+        for (int b = 0; b < 2; ++b)
+          if (issued[b] > 0)
+            mbar_wait_drain(smem_u32(IS_INT8 ? &bars->full_a[b] : &bars->full_b[b]),
+                            (issued[b] - 1) & 1u, 100000000ull);
+        if (!IS_INT8 && warp == 2) mbar_wait_drain(smem_u32(&bars->full_b[7]), 0, 100000000ull);
+      }
+      __syncwarp();
+    } else if (warp == 1 || (kDualMma && warp == 3)) {
+      // MMA issuer of sub-tile `part` of every tile (two issuers on
+      // 256-pixel tiles): R * S k-blocks, each the window at its tap's shift
+      // times that tap's resident filter block
+      const int part = warp == 3 ? 1 : 0;
+      bool ok = mbar_wait_warp(smem_u32(&bars->full_b[7]), 0, abort_flag, tmo);
+      uint32_t astage = 0, aphase = 0;
+      const uint32_t bbase = smem_u32(sB);
+      for (long long j = 0; ok; ++j) {
+        const long long unit = blockIdx.x + j * gridDim.x;
+        if (unit >= args.num_tiles) break;
+        const int slot = static_cast<int>(j & 1);
+        const uint32_t par = static_cast<uint32_t>(j >> 1) & 1u;
+        if (!mbar_wait_warp(smem_u32(&bars->acc_empty[astage]), aphase ^ 1, abort_flag, tmo) ||
+            !mbar_wait_warp(smem_u32(&bars->full_b[slot]), par, abort_flag, tmo))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + astage * C::kAccCols + part * BN;
+        const uint32_t wbase = smem_u32(sA + slot * args.halo_slot);
+        if (lane == 0) {
+          int r = 0, s = 0;
+          for (int kb = 0; kb < num_kb; ++kb) {
+            const uint32_t row = static_cast<uint32_t>(part * kBM + r * Qh + s);
+            const uint64_t adesc = sw128_kmajor_desc_at_row(wbase, row);
+            const uint64_t bdesc = sw128_mnmajor_desc(bbase + kb * BN * kBK * 2);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              umma_f16(d, adesc + 2 * k, bdesc + kBStepK * k, kIdesc,
+                       (kb > 0 || k > 0) ? 1u : 0u);
+            if (++s == args.S) { s = 0; ++r; }
+          }
+          umma_commit(smem_u32(&bars->empty[slot]));
+          umma_commit(smem_u32(&bars->acc_full[astage]));
+        }
+        __syncwarp();
+        if (++astage == 2) { astage = 0; aphase ^= 1; }
+      }
+      if (lane == 0) {
+        // every MMA issued above has completed once this arrives
+        umma_commit(smem_u32(&bars->mma_done));
+        mbar_wait_drain(smem_u32(&bars->mma_done), 0, 1000000000ull);
+      }
+      __syncwarp();
+    }
+   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop (warp-uniform state); lane 0 issues.
     const long long PQ = static_cast<long long>(args.P) * args.Q;
@@ -1239,6 +1461,45 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                     (warp - kTmaEpiWarp0) * C::kOutWarpBytes / 16;
     const int ew = warp - kTmaEpiWarp0;
     const int num_units = args.num_tiles * splits;
+    if constexpr (HALO && IS_INT8) {
+      // the CTA's filter tile, widened from the caller's int8 HWIO filter
+      // into the MN-major 128-byte-swizzled blocks the MMA reads (k-row c of
+      // tap kb: 64 output channels, 16-byte chunk j at j ^ (c & 7)); channels
+      // past K read as zero.  All of a thread's loads are issued before its
+      // stores.
+      const int t = (warp - kTmaEpiWarp0) * 32 + lane;   // 0 .. 255
+      const int n0 = (static_cast<int>(blockIdx.x) % args.num_n_tiles) * BN;
+      const int pieces = num_kb * kBK * 4;                 // 16 bytes of int8 each
+      for (int i0 = 0; i0 < pieces; i0 += 256 * 4) {
+        uint4 in[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int i = i0 + g * 256 + t;
+          const int krow = i >> 2, col = n0 + (i & 3) * 16;
+          in[g] = (i < pieces && col < args.K)
+                      ? ldg_nc_v4(args.w_i8 + static_cast<size_t>(krow) * args.K + col)
+                      : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int i = i0 + g * 256 + t;
+          if (i < pieces) {
+            const int krow = i >> 2, pc = i & 3, c = krow & (kBK - 1);
+            uint4 lo, hi;
+            i8x4_to_f16x4(in[g].x, lo.x, lo.y);
+            i8x4_to_f16x4(in[g].y, lo.z, lo.w);
+            i8x4_to_f16x4(in[g].z, hi.x, hi.y);
+            i8x4_to_f16x4(in[g].w, hi.z, hi.w);
+            uint8_t *row = sB + (krow >> 6) * (BN * kBK * 2) + c * 128;
+            *reinterpret_cast<uint4 *>(row + (((2 * pc) ^ (c & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4 *>(row + (((2 * pc + 1) ^ (c & 7)) << 4)) = hi;
+          }
+        }
+      }
+      fence_proxy_async_smem();   // the filter tile is read by the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->full_b[7]));
+    }
     // split-K: the prep launch zeroes the completion counters.  The counter
     // atomics below already follow the producer's wait for that launch
     // (through the stage and accumulator barriers), but they wait for it
@@ -1258,11 +1519,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const int m_tile = tile / args.num_n_tiles;
       const int n_tile = tile - m_tile * args.num_n_tiles;
       const long long m = static_cast<long long>(m_tile) * kTileM + row;
-      const bool mvalid = m < args.M;
-      const long long mo = out_pixel(args, m);   // the output pixel row m writes
+      bool mvalid = m < args.M;
+      long long mo;   // the output pixel row m writes
+      if constexpr (HALO) {
+        // pixel (pr, q') of the tile's output rows padded to halo_q columns
+        const int n_img = m_tile / args.tiles_per_img;
+        const int pr = row / args.halo_q, qv = row - pr * args.halo_q;
+        const int pv = (m_tile - n_img * args.tiles_per_img) * args.halo_tr + pr;
+        mvalid = pr < args.halo_tr && pv < args.P && qv < args.Q;
+        mo = (static_cast<long long>(n_img) * args.P + pv) * args.Q + qv;
+      } else {
+        mo = out_pixel(args, m);
+      }
       long long st_mo[SliceGroups<IS_INT8>::kGroups];
       bool st_ok[SliceGroups<IS_INT8>::kGroups];
-      if (!args.omap) {
+      if (!HALO && !args.omap) {
         // output row = GEMM row: a warp's 32 rows are consecutive, so the
         // rows each lane stores follow without shuffles
         const long long m_lane0 = m - lane;
@@ -1747,12 +2018,13 @@ static void note_attributes(Kern kern, int threads, int smem) {
 
 const char *last_launch_note() { return t_kernel_note; }
 
-template <int BN, bool IS_INT8, int MS, bool SPLITK = false, bool WIDEN = false, int KPS = 1>
+template <int BN, bool IS_INT8, int MS, bool SPLITK = false, bool WIDEN = false, int KPS = 1,
+          bool HALO = false>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                                 const ConvArgs &args, int grid, bool overlap,
                                 cudaStream_t stream) {
-  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK, WIDEN, KPS>;
-  using Cfg = TmaCfg<BN, MS, WIDEN, KPS>;
+  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK, WIDEN, KPS, HALO>;
+  using Cfg = TmaCfg<BN, MS, WIDEN, KPS, HALO>;
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
   if (e == cudaSuccess) {
@@ -1765,6 +2037,7 @@ static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tm
 
 bool gather_supports(Gather gather, int block_n, bool chunked, int m_sub) {
   if (m_sub != 1 && m_sub != 2) return false;
+  if (gather == Gather::kTmaHalo) return block_n == 64 && !chunked;
   if (gather == Gather::kTmaIm2col)
     return m_sub == 1 ? (block_n == 64 || block_n == 128 || block_n == 256)
                       : (block_n == 64 || block_n == 128);
@@ -1784,6 +2057,28 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
   if (args.kps != 1 && (args.kps != 2 || widen || args.splits > 1 || m_sub != 1 ||
                         gather != Gather::kTmaIm2col))
     return cudaErrorInvalidValue;
+  if (gather == Gather::kTmaHalo) {
+    // the window and filter tile fit their buffers, a tile's output rows fit
+    // its GEMM rows, and every CTA keeps one output-channel tile
+    if (widen || args.splits != 1 || args.kps != 1 || args.C != kBK || args.sh != 1 ||
+        args.sw != 1 || args.num_kb * block_n * kBK * 2 > kHaloBMax ||
+        args.halo_q != args.Q + args.S - 1 || args.halo_q > 256 || args.halo_tr <= 0 ||
+        args.halo_tr * args.halo_q > kBM * m_sub || args.halo_rows != args.halo_tr + args.R - 1 ||
+        args.halo_rows > 256 || args.halo_slot % 1024 != 0 || args.halo_stg % 512 != 0 ||
+        args.halo_rows * args.halo_q * 128 > args.halo_slot ||
+        (is_int8 && args.halo_rows * args.halo_q * 64 > args.halo_stg) ||
+        2 * args.halo_slot + 2 * args.halo_stg + args.num_kb * block_n * kBK * 2 > kHaloRegion ||
+        args.tiles_per_img != (args.P + args.halo_tr - 1) / args.halo_tr ||
+        grid % args.num_n_tiles != 0 ||
+        args.num_tiles != args.N * args.tiles_per_img * args.num_n_tiles ||
+        (is_int8 && args.w_i8 == nullptr))
+      return cudaErrorInvalidValue;
+    if (m_sub == 2)
+      return is_int8 ? launch_tma_t<64, true, 2, false, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                     : launch_tma_t<64, false, 2, false, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+    return is_int8 ? launch_tma_t<64, true, 1, false, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                   : launch_tma_t<64, false, 1, false, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+  }
   if (widen) {
     // int8 activations widened in the kernel: TMA gather, unsplit, <= 128 channels
     if (!is_int8 || gather != Gather::kTmaIm2col || args.splits > 1 || block_n > 128 ||

@@ -359,24 +359,35 @@ def test_run_host_ramped_chunks():
     p.close()
 
 
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
 @pytest.mark.parametrize("C,K,kernel", [(16, 16, "cp-async"), (64, 64, "tma-im2col"),
                                          (64, 256, "tma-im2col"), (64, 128, "tma-im2col-m256"),
-                                         (832, 64, "tma-im2col-kb2")])
-def test_timeout_exit_keeps_context_usable(C, K, kernel):
+                                         (832, 64, "tma-im2col-kb2"), (64, 64, "tma-halo"),
+                                         (64, 128, "tma-halo-m256")])
+def test_timeout_exit_keeps_context_usable(C, K, kernel, dtype):
     """A producer that never signals 'stage full' makes the MMA issuer's wait
     run out: the kernel must stop, report FCONV_ERR_TIMEOUT, and the next run
     must work -- for the cp.async loaders and the TMA producers (64- and
-    256-wide tiles, 256-pixel tiles, and stages of two k-blocks)."""
+    256-wide tiles, 256-pixel tiles, stages of two k-blocks, and the halo
+    gather's window loaders, whose int8 form waits for its own copy)."""
+    if dtype == "bf16" and not kernel.startswith("tma-halo"):
+        pytest.skip("the other loaders wait the same way for both dtypes")
     R = 1 if C > 512 else 3   # 832 channels, 1x1: 13 k-blocks, unchunked
-    c = sweep_case(70, (1, 8, 8, C, K, R, R, 1, "SAME", False, True), "int8")
+    c = sweep_case(70, (1, 8, 8, C, K, R, R, 1, "SAME", False, True), dtype)
     # a fixed tile is unsplit
     p = c.plan(block_n=256 if K == 256 else (64 if C > 512 else None))
+    if kernel.startswith("tma-im2col"):
+        fc.fconv_plan_set_gather(p.handle, fc.FCONV_GATHER_IM2COL)
+    if kernel.startswith("tma-halo"):
+        fc.fconv_plan_set_gather(p.handle, fc.FCONV_GATHER_HALO)
     if kernel.endswith("m256"):
-        fc.fconv_plan_set_tile_shape(p.handle, 256, K)
+        fc.fconv_plan_set_tile_shape(p.handle, 256, 64 if kernel.startswith("tma-halo") else K)
+    elif kernel == "tma-halo":
+        fc.fconv_plan_set_tile_shape(p.handle, 128, 64)
     assert fc.fconv_plan_kernel(p.handle) == kernel
     fc.fconv_plan_set_timeout_ms(p.handle, 50)
     fc.fconv_plan_set_debug(p.handle, fc.FCONV_DEBUG_DROP_ARRIVE)
-    x, w = to_dev(c.x, "int8"), to_dev(c.w, "int8")
+    x, w = to_dev(c.x, dtype), to_dev(c.w, dtype)
     bias = torch.from_numpy(c.bias).cuda()
     p.run(x, w, bias, None, c.conv_scale, 0.0)
     with pytest.raises(fc.FconvError) as ei:
@@ -765,6 +776,7 @@ def test_in_kernel_widening(i, item):
     got = {}
     for mode in (fc.FCONV_WIDEN_IN_KERNEL, fc.FCONV_WIDEN_COPY):
         p = c.plan()
+        fc.fconv_plan_set_gather(p.handle, fc.FCONV_GATHER_IM2COL)   # the im2col form widens
         if shape:
             fc.fconv_plan_set_tile_shape(p.handle, *shape)
         fc.fconv_plan_set_splits(p.handle, 1)   # widening runs unsplit
@@ -782,3 +794,63 @@ def test_in_kernel_widening(i, item):
         got[mode] = to_host(y)
         p.close()
     assert np.array_equal(got[fc.FCONV_WIDEN_IN_KERNEL], got[fc.FCONV_WIDEN_COPY])
+
+
+# ---------------------------------------------------------------- halo gather
+# stride-1 layers with 64 input channels: one window copy a tile, the filter
+# tile resident, each tap a row shift of the window (virtual pixel rows of
+# Q + S - 1 columns).  Against the oracle and against the im2col gather.
+HALO_CASES = [
+    # params, tile pixels (None: the plan's own height)
+    ((2, 9, 11, 64, 80, 3, 3, 1, "SAME", True, True), None),      # K tail, two channel tiles
+    ((3, 10, 10, 64, 64, 3, 3, 1, "SAME", True, True), 256),
+    ((2, 13, 17, 64, 64, 3, 3, 1, "VALID", False, True), 128),    # no padding
+    ((1, 5, 7, 64, 48, 3, 3, 1, "SAME", True, False), None),      # K below the tile
+    ((2, 12, 10, 64, 32, 1, 3, 1, "SAME", False, True), None),    # R != S
+    ((2, 7, 9, 64, 64, 2, 2, 1, "SAME", True, True), 256),        # even filter: pads 0 / 1
+    ((64, 24, 24, 64, 64, 3, 3, 1, "SAME", True, True), None),    # several tiles a CTA
+    ((2, 6, 90, 64, 64, 3, 3, 1, "SAME", False, True), 128),      # a 92-pixel-wide window
+    ((3, 1, 1, 64, 64, 1, 1, 1, "SAME", True, True), None),       # 1x1 images
+    ((2, 4, 40, 64, 128, 3, 3, 1, "SAME", True, True), 256),      # window rows past the image
+]
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+@pytest.mark.parametrize("i,item", list(enumerate(HALO_CASES)))
+def test_halo_gather(i, item, dtype):
+    params, pixels = item
+    c = sweep_case(1200 + i, params, dtype)
+    acc_ref = c.oracle_acc()
+    ref = c.oracle_out(acc_ref)
+    p = c.plan()
+    fc.fconv_plan_set_gather(p.handle, fc.FCONV_GATHER_HALO)
+    if pixels:
+        fc.fconv_plan_set_tile_shape(p.handle, pixels, 64)
+    kern = fc.fconv_plan_kernel(p.handle)
+    assert kern.startswith("tma-halo") and (pixels is None or kern.endswith("m256") == (pixels == 256))
+    # one launch, no workspace: an int8 filter is widened inside the kernel too
+    assert fc.fconv_plan_launch_count(p.handle) == 1
+    assert fc.fconv_workspace_size(p.handle) == 0
+    assert fc.fconv_plan_get_input_widening(p.handle) == (dtype == "int8")
+    x, w = to_dev(c.x, dtype), to_dev(c.w, dtype)
+    bias, side = torch.from_numpy(c.bias).cuda(), to_dev(c.side, dtype)
+    acc = p.accumulators(x, w)
+    y = p.run(x, w, bias, side, c.conv_scale, c.side_scale)
+    y2 = p.run(x, w, bias, side, c.conv_scale, c.side_scale)   # both window buffers reused
+    p.check()
+    c.check_acc(acc.cpu().numpy(), acc_ref)
+    c.check_output(to_host(y), ref)
+    assert torch.equal(y, y2)
+    halo = to_host(y)
+    p.close()
+    # the same plan on the im2col gather
+    q = c.plan()
+    fc.fconv_plan_set_gather(q.handle, fc.FCONV_GATHER_IM2COL)
+    assert not fc.fconv_plan_kernel(q.handle).startswith("tma-halo")
+    y3 = q.run(x, w, bias, side, c.conv_scale, c.side_scale)
+    q.check()
+    q.close()
+    if dtype == "int8":
+        assert np.array_equal(halo, to_host(y3))
+    else:
+        c.check_output(to_host(y3), ref)
