@@ -888,7 +888,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   if (threadIdx.x == 0) {
     if constexpr (HALO) {
       // window buffer s: full_b[s] = ready for the MMA (bf16: its copy
-      // landed; int8: both widening warps wrote their halves), empty[s] =
+      // landed; int8: both loader warps arrived, having widened their halves
+      // or, for the first window, seen the epilogue warps widen it), empty[s] =
       // the MMAs that read it are done; int8 staging s: full_a[s] = a
       // window's copy landed, full_a[2 + s] = both widening warps have read
       // it; full_b[7] = the resident filter tile is in place (bf16: one
@@ -899,6 +900,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         mbar_init(smem_u32(&bars->full_a[s]), 1);
         mbar_init(smem_u32(&bars->full_a[2 + s]), 2);
       }
+      // int8: the epilogue warps widened the CTA's first window
+      mbar_init(smem_u32(&bars->full_a[4]), kTmaEpiWarps);
       mbar_init(smem_u32(&bars->full_b[7]), IS_INT8 ? kTmaEpiWarps : 1);
     } else {
       for (int s = 0; s < kStages; ++s) {
@@ -980,7 +983,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         __syncwarp();
       }
       const uint32_t win_bytes = static_cast<uint32_t>(win_px) * kBK * (IS_INT8 ? 1 : 2);
-      uint32_t issued[2] = {0, 0};   // copies into window buffer / staging s
+      // copies into window buffer / staging 0 and 1 (scalars: a runtime
+      // index into a register array would put it in local memory)
+      uint32_t issued0 = 0, issued1 = 0;
       bool ok = true;
       if constexpr (IS_INT8) {
         // warp 0: window jj's copy into staging jj % 2, once both warps have
@@ -1002,7 +1007,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                           p0 - args.pt, n_img, sf);
             }
             __syncwarp();
-            ++issued[sb];
+            if (sb) ++issued1; else ++issued0;
           }
           return true;
         };
@@ -1016,11 +1021,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           if (!mbar_wait_warp(smem_u32(&bars->full_a[slot]), par, abort_flag, tmo) ||
               !mbar_wait_warp(smem_u32(&bars->empty[slot]), par ^ 1, abort_flag, tmo))
             break;
-          const int half_px = (win_px + 1) / 2;
-          widen_rows(sStgH + slot * args.halo_stg, sA + slot * args.halo_slot,
-                     wi ? half_px : 0, wi ? win_px : half_px);
-          fence_proxy_async_smem();   // the window is read by the tensor core
-          __syncwarp();
+          if (j == 0) {
+            // the epilogue warps widen the first window (see there)
+            if (!mbar_wait_warp(smem_u32(&bars->full_a[4]), 0, abort_flag, tmo)) break;
+          } else {
+            const int half_px = (win_px + 1) / 2;
+            widen_rows(sStgH + slot * args.halo_stg, sA + slot * args.halo_slot,
+                       wi ? half_px : 0, wi ? win_px : half_px);
+            fence_proxy_async_smem();   // the window is read by the tensor core
+            __syncwarp();
+          }
           if (lane == 0) {
             mbar_arrive(smem_u32(&bars->full_b[slot]));
             mbar_arrive(smem_u32(&bars->full_a[2 + slot]));
@@ -1042,7 +1052,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                           p0 - args.pt, n_img, fb);
             }
             __syncwarp();
-            ++issued[wi];
+            if (wi) ++issued1; else ++issued0;
           }
         }
       }
@@ -1050,10 +1060,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         // copies still in flight after an abort land before the CTA exits
         // (the last one into each buffer: a buffer's copies wait for each
         // other)
-        for (int b = 0; b < 2; ++b)
-          if (issued[b] > 0)
-            mbar_wait_drain(smem_u32(IS_INT8 ? &bars->full_a[b] : &bars->full_b[b]),
-                            (issued[b] - 1) & 1u, 100000000ull);
+        if (issued0 > 0)
+          mbar_wait_drain(smem_u32(IS_INT8 ? &bars->full_a[0] : &bars->full_b[0]),
+                          (issued0 - 1) & 1u, 100000000ull);
+        if (issued1 > 0)
+          mbar_wait_drain(smem_u32(IS_INT8 ? &bars->full_a[1] : &bars->full_b[1]),
+                          (issued1 - 1) & 1u, 100000000ull);
         if (!IS_INT8 && warp == 2) mbar_wait_drain(smem_u32(&bars->full_b[7]), 0, 100000000ull);
       }
       __syncwarp();
@@ -1462,6 +1474,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int ew = warp - kTmaEpiWarp0;
     const int num_units = args.num_tiles * splits;
     if constexpr (HALO && IS_INT8) {
+      // (at kernel start the epilogue warps have no accumulator to read yet)
       // the CTA's filter tile, widened from the caller's int8 HWIO filter
       // into the MN-major 128-byte-swizzled blocks the MMA reads (k-row c of
       // tap kb: 64 output channels, 16-byte chunk j at j ^ (c & 7)); channels
@@ -1499,6 +1512,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       fence_proxy_async_smem();   // the filter tile is read by the tensor core
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->full_b[7]));
+      // then the CTA's first window (eight warps instead of the loader
+      // warps' two: the tensor core waits for it), once its copy has landed;
+      // full_a[4] counts the warps done with it.  A wait that runs out skips
+      // the widening: the loader warps' wait for full_a[4] runs out too.
+      if (mbar_wait_warp(smem_u32(&bars->full_a[0]), 0, abort_flag, tmo)) {
+        const int win_px = args.halo_rows * args.halo_q;
+        const int per = (win_px + kTmaEpiWarps - 1) / kTmaEpiWarps;
+        const int p0 = min(win_px, ew * per), p1 = min(win_px, p0 + per);
+        widen_rows(sStgH, sA, p0, p1);
+        fence_proxy_async_smem();   // the window is read by the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->full_a[4]));
+      }
     }
     // split-K: the prep launch zeroes the completion counters.  The counter
     // atomics below already follow the producer's wait for that launch
