@@ -317,10 +317,13 @@ fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms);
  * channel count allows the TMA im2col input gather (C % 64 == 0) use the
  * general cp.async gather instead.  FCONV_DEBUG_ONE_KBLOCK_STAGES keeps
  * every pipeline stage at one k-block (plans that would fill two a stage,
- * "tma-im2col-kb2", run "tma-im2col").  0 restores normal runs. */
+ * "tma-im2col-kb2", run "tma-im2col").  FCONV_DEBUG_ONE_MMA_ISSUER keeps
+ * one MMA-issuing thread and one accumulator on tiles that would split each
+ * k-block's MMAs between two ("...-dual" kernels).  0 restores normal runs. */
 #define FCONV_DEBUG_DROP_ARRIVE 1
 #define FCONV_DEBUG_GATHER_CPASYNC 2
 #define FCONV_DEBUG_ONE_KBLOCK_STAGES 4
+#define FCONV_DEBUG_ONE_MMA_ISSUER 8
 fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags);
 
 /* Record caller-created CUDA events (cudaEvent_t) at the stage boundaries
@@ -423,7 +426,11 @@ fconv_status fconv_plan_launch_count(const fconv_plan *plan, int *launches);
 /* Which convolution kernel the plan's next run uses: "tma-im2col" (A
  * gathered by TMA im2col loads, 128-pixel tiles), "tma-im2col-kb2" (the
  * same with two k-blocks a pipeline stage: unsplit, unchunked tiles of up to
- * 128 channels and 12 or more k-blocks of 64), "tma-im2col-m256" (256-pixel tiles) or "cp-async" (the
+ * 128 channels and 12 or more k-blocks of 64), either with "-dual" (unsplit
+ * tiles of up to 128 channels and 12 or more k-blocks: two threads issue
+ * each k-block's MMAs into two accumulators the epilogue adds),
+ * "tma-im2col-m256" (256-pixel tiles), "tma-halo" / "tma-halo-m256" (the
+ * halo gather, fconv_plan_set_gather) or "cp-async" (the
  * general gather); for a strided transposed plan, its first phase's.
  * Static text; "" for a NULL plan. */
 const char *fconv_plan_kernel(const fconv_plan *plan);

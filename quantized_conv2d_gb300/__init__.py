@@ -32,6 +32,7 @@ FCONV_ACT_NONE, FCONV_ACT_RELU, FCONV_ACT_LEAKY_RELU, FCONV_ACT_CLIPPED_RELU, FC
 FCONV_DEBUG_DROP_ARRIVE = 1
 FCONV_DEBUG_GATHER_CPASYNC = 2
 FCONV_DEBUG_ONE_KBLOCK_STAGES = 4
+FCONV_DEBUG_ONE_MMA_ISSUER = 8
 FCONV_WIDEN_AUTO, FCONV_WIDEN_IN_KERNEL, FCONV_WIDEN_COPY = 0, 1, 2
 FCONV_GATHER_AUTO, FCONV_GATHER_IM2COL, FCONV_GATHER_HALO = 0, 1, 2
 

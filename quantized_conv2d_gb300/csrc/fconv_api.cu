@@ -248,6 +248,18 @@ int kblocks_per_stage(const fconv_plan &p) {
   return ok ? 2 : 1;
 }
 
+// Whether the next run splits each k-block's MMAs between two issuing
+// threads (two accumulators, added in the epilogue): the TMA gather's
+// unsplit 128-pixel tiles of up to 128 channels with at least
+// kKps2MinKBlocks k-blocks, where one thread's MMA issue (~110 cycles an
+// MMA, 4 a k-block) bounds the mainloop; short tiles keep one accumulator,
+// whose epilogue reads half as much tensor memory.
+bool split_mma_issue(const fconv_plan &p) {
+  if (p.debug & FCONV_DEBUG_ONE_MMA_ISSUER) return false;
+  return gather_for_run(p) == fconv::Gather::kTmaIm2col && p.m_sub == 1 && p.block_n <= 128 &&
+         p.splits == 1 && !p.widen && p.num_kb >= kKps2MinKBlocks;
+}
+
 
 // Tile: the candidate (BN output channels x 128*MS output pixels) with the
 // least estimated time.  A unit (a tile, or its split) costs the longer of
@@ -300,7 +312,11 @@ TileChoice choose_tile(const fconv_plan &p, int sms, bool allow_halo = true) {
       fconv::Gather g = gather_for(p, bn, false);
       if (!fconv::gather_supports(g, bn, chunked, ms)) continue;
       // 128-pixel tiles of <= 128 channels, unsplit and unchunked, run two
-      // k-blocks a stage: bound by one MMA issuer (4 MMAs of ~105 cycles)
+      // k-blocks a stage (costed as one MMA issuer: 4 MMAs of ~105 cycles a
+      // k-block; they run with two, split_mma_issue, which measured faster
+      // on the 32x14x14x256 bf16 layer, 14.3 -> 12.4 us a graph step, but
+      // costing them so moved the bf16 4x4/2 transposed layer's phases to
+      // 128 x 128 tiles, 30.5 -> 36.7 us)
       const bool kb2 = g == fconv::Gather::kTmaIm2col && ms == 1 && bn <= 128 && !chunked &&
                        p.num_kb >= 12;   // kblocks_per_stage's rule
       const long long fixed =
@@ -787,6 +803,7 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   a.num_tiles = p->num_tiles;
   a.b3d = b3d;
   a.kps = kps;
+  a.kdual = split_mma_issue(*p) ? 1 : 0;
   a.conv_scale = conv_scale;
   a.side_scale = side_scale;
   a.act = static_cast<int>(p->act);
@@ -1556,7 +1573,7 @@ fconv_status fconv_plan_set_timeout_ms(fconv_plan *plan, uint32_t ms) {
 fconv_status fconv_plan_set_debug(fconv_plan *plan, int flags) {
   if (!plan) return fail(FCONV_ERR_INVALID_VALUE, "plan is NULL");
   if (flags & ~(FCONV_DEBUG_DROP_ARRIVE | FCONV_DEBUG_GATHER_CPASYNC |
-                FCONV_DEBUG_ONE_KBLOCK_STAGES))
+                FCONV_DEBUG_ONE_KBLOCK_STAGES | FCONV_DEBUG_ONE_MMA_ISSUER))
     return fail(FCONV_ERR_INVALID_VALUE, "unknown flags");
   plan->debug = flags;
   if (plan->num_phases == 0) update_widen(*plan);
@@ -1662,8 +1679,11 @@ const char *fconv_plan_kernel(const fconv_plan *plan) {
   if (halo_run(*plan)) return plan->m_sub == 2 ? "tma-halo-m256" : "tma-halo";
   if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col && plan->m_sub == 2)
     return "tma-im2col-m256";
-  if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col)
+  if (gather_for_run(*plan) == fconv::Gather::kTmaIm2col) {
+    if (split_mma_issue(*plan))
+      return kblocks_per_stage(*plan) == 2 ? "tma-im2col-kb2-dual" : "tma-im2col-dual";
     return kblocks_per_stage(*plan) == 2 ? "tma-im2col-kb2" : "tma-im2col";
+  }
   return "cp-async";
 }
 

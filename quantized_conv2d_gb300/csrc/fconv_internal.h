@@ -69,6 +69,9 @@ struct ConvArgs {
   // filter, which int8 plans widen inside the kernel (no prep launch).
   int halo_q, halo_tr, halo_rows, tiles_per_img, halo_slot, halo_stg;
   const int8_t *w_i8;
+  // two MMA issuers splitting each k-block's k16 steps into two
+  // accumulators (TMA im2col, unsplit, 128-pixel tiles of <= 128 channels)
+  int kdual;
 };
 
 // How the kernel gathers the A (activation) tile of each k-block.

@@ -796,7 +796,10 @@ struct TmaRegs {
 // HALO (the halo gather): instead of the stage ring a region of
 // kHaloRegion bytes holds two input windows, two int8 window stagings and
 // the CTA's whole filter tile, at offsets the plan gives (ConvArgs).
-template <int BN, int MS = 1, bool WIDEN = false, int KPS = 1, bool HALO = false>
+// KDUAL: two accumulators per tile, each k-block's k16 steps split between
+// two MMA issuers (see the kernel); they are summed in the epilogue.
+template <int BN, int MS = 1, bool WIDEN = false, int KPS = 1, bool HALO = false,
+          bool KDUAL = false>
 struct TmaCfg {
   static constexpr int kABytes = kBM * kBK * 2;        // one sub-tile's A of one k-block
   static constexpr int kAStage = HALO ? 0 : KPS * MS * kABytes;
@@ -808,7 +811,7 @@ struct TmaCfg {
   static constexpr int kStages0 =
       HALO ? 2 : (200 * 1024 - kStgStages * kStgBytes) / kStageBytes;
   static constexpr int kStages = HALO ? 2 : kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kAccCols = MS * BN;             // one accumulator buffer
+  static constexpr int kAccCols = MS * BN * (KDUAL ? 2 : 1);   // one accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols <= 128 ? 128 : 2 * kAccCols <= 256 ? 256 : 512;
   static constexpr int kStgOffset = HALO ? kHaloRegion : kStages * kStageBytes;
   static constexpr int kBarOffset = kStgOffset + kStgStages * kStgBytes;
@@ -831,6 +834,8 @@ struct TmaCfg {
   static_assert(2 * kAccCols <= 512, "tensor memory");
   static_assert(HALO || kStages >= 3, "pipeline too shallow");
   static_assert(!HALO || (BN == 64 && !WIDEN && KPS == 1), "halo gather: 64-channel tiles");
+  static_assert(!KDUAL || (MS == 1 && BN <= 128 && !WIDEN && !HALO),
+                "split k16 steps: 128-pixel tiles of up to 128 channels");
   static_assert(!WIDEN || kHalfCols <= 64, "in-kernel widening needs the 96-register control warps");
   static_assert(KPS == 1 || (KPS == 2 && MS == 1 && !WIDEN), "two k-blocks a stage: 128-pixel tiles");
 };
@@ -841,15 +846,22 @@ struct TmaCfg {
 // input itself; warps 2-3 widen each staged A tile into the fp16 stage.
 // HALO: the halo gather (see the loader role below): tmap_a is the tiled
 // map of the input itself, the filter tile stays resident, unsplit.
+// KDUAL: warps 1 and 3 both issue the MMAs of every k-block of a
+// 128-pixel tile, warp 1 its first two k16 steps into accumulator 0, warp 3
+// the last two into accumulator 1 (BN columns further); the epilogue adds
+// the two.  One thread issues a tcgen05.mma about every 110 cycles, so a
+// 128 x 128 tile's 4 MMAs a k-block take ~440 cycles from one thread
+// against 256 cycles of tensor time; two threads issue 2 each.
 template <int BN, bool IS_INT8, int MS, bool SPLITK, bool WIDEN = false, int KPS = 1,
-          bool HALO = false>
+          bool HALO = false, bool KDUAL = false>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     conv_fprop_tma_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b, const ConvArgs args) {
   static_assert(!WIDEN || (IS_INT8 && !SPLITK), "widening: int8, unsplit");
   static_assert(KPS == 1 || !SPLITK, "two k-blocks a stage: unsplit");
   static_assert(!HALO || !SPLITK, "halo gather: unsplit");
-  using C = TmaCfg<BN, MS, WIDEN, KPS, HALO>;
+  static_assert(!KDUAL || !SPLITK, "split k16 steps: unsplit");
+  using C = TmaCfg<BN, MS, WIDEN, KPS, HALO, KDUAL>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_f16(kBM, BN, !IS_INT8, /*b_mn=*/true);
   constexpr int kTileM = kBM * MS;
@@ -861,7 +873,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   // commits to the stage and accumulator barriers, which then take two
   // arrivals.  (Splitting a 128-pixel tile's channels between two issuers,
   // N = BN / 2 each, measured slower on every 128 x 128 workload.)
-  constexpr bool kDualMma = !WIDEN && MS == 2;
+  constexpr bool kDualMma = (!WIDEN && MS == 2) || KDUAL;
   constexpr int kMmaArrivals = kDualMma ? 2 : 1;
 
   extern __shared__ uint8_t smem_raw[];
@@ -1366,11 +1378,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll
               for (int q = 0; q < KPS; ++q) {
                 if (q < nk) {
+                  // KDUAL: this issuer's half of the k16 steps, its own accumulator
+                  constexpr int k_n = KDUAL ? kBK / 32 : kBK / 16;
+                  const int k_0 = KDUAL ? part * k_n : 0;
+                  const uint32_t dd = KDUAL ? d + part * BN : d;
 #pragma unroll
-                  for (int k = 0; k < kBK / 16; ++k)
-                    umma_f16(d, adesc + q * (C::kABytes >> 4) + 2 * k,
+                  for (int kk = 0; kk < k_n; ++kk) {
+                    const int k = k_0 + kk;
+                    umma_f16(dd, adesc + q * (C::kABytes >> 4) + 2 * k,
                              bdesc + q * (8192 >> 4) + kBStepK * k, kIdesc,
-                             (kb > kb0 || q > 0 || k > 0) ? 1u : 0u);
+                             (kb > kb0 || q > 0 || kk > 0) ? 1u : 0u);
+                  }
                 }
               }
               umma_commit(smem_u32(&bars->empty[stage]));
@@ -1396,7 +1414,24 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             // a sub-tile's A is 16 KB further: + (16384 >> 4) in the descriptor
             constexpr uint64_t kSubStep = static_cast<uint64_t>(C::kABytes >> 4);
             if (lane == 0) {
-              if constexpr (kDualMma && MS == 2) {
+              if constexpr (KDUAL) {
+                // this issuer's half of the k16 steps, its own accumulator
+  #pragma unroll
+                for (int kk = 0; kk < kBK / 32; ++kk) {
+                  const int k = part * (kBK / 32) + kk;
+                  umma_f16(d + part * BN, adesc + 2 * k, bdesc + kBStepK * k, kIdesc,
+                           (kb > kb0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(smem_u32(&bars->empty[stage]));
+                if (pair) {
+  #pragma unroll
+                  for (int kk = 0; kk < kBK / 32; ++kk) {
+                    const int k = part * (kBK / 32) + kk;
+                    umma_f16(d + part * BN, adesc1 + 2 * k, bdesc1 + kBStepK * k, kIdesc, 1u);
+                  }
+                  umma_commit(smem_u32(&bars->empty[stage1]));
+                }
+              } else if constexpr (kDualMma && MS == 2) {
                 // this issuer's 128-pixel sub-tile
   #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k)
@@ -1689,6 +1724,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         tc_fence_after();
         const uint32_t t_acc = tmem_base + lane_off + astage * C::kAccCols + tcol;
+        // 32 columns of this thread's row: KDUAL adds the second accumulator
+        // (BN columns further) in fp32, exactly for int8 sums (integers whose
+        // total stays below 2^24 within a chunk)
+        auto acc_ld = [&](uint32_t taddr, uint32_t (&v)[32]) {
+          tmem_ld32(taddr, v);
+          if constexpr (KDUAL) {
+            uint32_t v2[32];
+            tmem_ld32(taddr + BN, v2);
+            tmem_wait_ld(v);
+            tmem_wait_ld(v2);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[i] = __float_as_uint(__fadd_rn(__uint_as_float(v[i]), __uint_as_float(v2[i])));
+          } else {
+            tmem_wait_ld(v);
+          }
+        };
         if (SPLITK && uchunks == 1) {
           // split-K, one chunk: the unit's sums (int32 for int8 plans, exact
           // here) from TMEM to its partial block, then the count
@@ -1715,8 +1767,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           // the whole sum is in TMEM: epilogue straight from it
           auto slice = [&](int jj, const uint4 *side_words) {
             uint32_t v[32];
-            tmem_ld32(t_acc + jj * 32, v);
-            tmem_wait_ld(v);
+            acc_ld(t_acc + jj * 32, v);
             float vals[32];
             // bf16: + 0.0f turns a -0 sum into +0; int8: a zero of either
             // sign gives code 0 (and the raw int32 0), so it is skipped
@@ -1754,8 +1805,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < C::kSlices; ++jj) {
             uint32_t v[32];
-            tmem_ld32(t_acc + jj * 32, v);
-            tmem_wait_ld(v);
+            acc_ld(t_acc + jj * 32, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int add = __float2int_rn(__uint_as_float(v[i]));
@@ -2045,12 +2095,12 @@ static void note_attributes(Kern kern, int threads, int smem) {
 const char *last_launch_note() { return t_kernel_note; }
 
 template <int BN, bool IS_INT8, int MS, bool SPLITK = false, bool WIDEN = false, int KPS = 1,
-          bool HALO = false>
+          bool HALO = false, bool KDUAL = false>
 static cudaError_t launch_tma_t(const CUtensorMap &tmap_a, const CUtensorMap &tmap_b,
                                 const ConvArgs &args, int grid, bool overlap,
                                 cudaStream_t stream) {
-  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK, WIDEN, KPS, HALO>;
-  using Cfg = TmaCfg<BN, MS, WIDEN, KPS, HALO>;
+  auto kern = conv_fprop_tma_kernel<BN, IS_INT8, MS, SPLITK, WIDEN, KPS, HALO, KDUAL>;
+  using Cfg = TmaCfg<BN, MS, WIDEN, KPS, HALO, KDUAL>;
   static std::atomic<unsigned long long> configured{0};
   cudaError_t e = ensure_smem_limit(kern, Cfg::kSmemBytes, configured);
   if (e == cudaSuccess) {
@@ -2140,6 +2190,25 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
       default: return is_int8 ? launch_tma_t<256, true, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream)
                               : launch_tma_t<256, false, 1, true>(tmap_a, tmap_b, args, grid, overlap, stream);
     }
+  }
+  if (gather == Gather::kTmaIm2col && args.kdual) {
+    // two MMA issuers splitting each k-block: unsplit 128-pixel tiles of <= 128 channels
+    if (args.C % kBK != 0 || m_sub != 1 || args.splits != 1 || block_n > 128 ||
+        (args.kps != 1 && args.kps != 2))
+      return cudaErrorInvalidValue;
+    if (args.kps == 2) {
+      if (chunked) return cudaErrorInvalidValue;
+      if (block_n == 64)
+        return is_int8 ? launch_tma_t<64, true, 1, false, false, 2, false, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                       : launch_tma_t<64, false, 1, false, false, 2, false, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+      return is_int8 ? launch_tma_t<128, true, 1, false, false, 2, false, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                     : launch_tma_t<128, false, 1, false, false, 2, false, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+    }
+    if (block_n == 64)
+      return is_int8 ? launch_tma_t<64, true, 1, false, false, 1, false, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                     : launch_tma_t<64, false, 1, false, false, 1, false, true>(tmap_a, tmap_b, args, grid, overlap, stream);
+    return is_int8 ? launch_tma_t<128, true, 1, false, false, 1, false, true>(tmap_a, tmap_b, args, grid, overlap, stream)
+                   : launch_tma_t<128, false, 1, false, false, 1, false, true>(tmap_a, tmap_b, args, grid, overlap, stream);
   }
   if (gather == Gather::kTmaIm2col && args.kps == 2) {
     // two k-blocks a stage: unsplit, unchunked 128-pixel tiles of <= 128 channels

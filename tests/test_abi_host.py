@@ -166,7 +166,7 @@ def test_run_argument_errors_before_any_launch():
         assert _err(fc.fconv_run_channel_scale, h, A, A, A, None, A + 4, 0.0, A, A, ws,
                     None) == fc.FCONV_ERR_MISALIGNED
         assert _err(fc.fconv_plan_set_timeout_ms, h, 0) == fc.FCONV_ERR_INVALID_VALUE
-        assert _err(fc.fconv_plan_set_debug, h, 8) == fc.FCONV_ERR_INVALID_VALUE
+        assert _err(fc.fconv_plan_set_debug, h, 16) == fc.FCONV_ERR_INVALID_VALUE
     finally:
         fc.fconv_plan_destroy(h)
 
@@ -414,7 +414,7 @@ def test_automatic_split_choice(shape, splits):
     ("small_i8_16x16x32", 64, "cp-async", 1),
     ("resnet_i8_56x56x64", 64, "tma-halo-m256", 1),
     ("proj1x1s2_i8_28x28x256", 128, "tma-im2col", 1),
-    ("bf16_14x14x256", 128, "tma-im2col-kb2", 1),
+    ("bf16_14x14x256", 128, "tma-im2col-kb2-dual", 1),
     ("large_i8_28x28x512", 256, "tma-im2col", 1),
     ("proj1x1s1_i8_28x28x256", 128, "tma-im2col", 1),
     ("fullwin_i8_7x7x512", 64, "tma-im2col", 8),

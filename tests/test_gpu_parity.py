@@ -196,9 +196,9 @@ def test_two_kblock_stages_agree(i, dtype):
     params, bn = KB2_CASES[i]
     c = sweep_case(80 + i, params, dtype)
     p = c.plan(block_n=bn)
-    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-kb2"
+    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-kb2-dual"
     fc.fconv_plan_set_debug(p.handle, fc.FCONV_DEBUG_ONE_KBLOCK_STAGES)
-    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col"
+    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-dual"
     p.close()
     acc_ref = c.oracle_acc()
     two = c.accumulators_gpu(block_n=bn)
@@ -212,12 +212,40 @@ def test_two_kblock_stages_agree(i, dtype):
                    c.oracle_out(acc_ref))
 
 
+# two threads issuing each k-block's MMAs (half the k16 steps each) into two
+# accumulators the epilogue adds, against one issuing thread and the oracle
+DUAL_CASES = KB2_CASES + [
+    ((1, 30, 30, 1024, 32, 3, 3, 1, "SAME", True, True), 128),   # 144 k-blocks (int8: chunked)
+    ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True), 128),   # 72 k-blocks, K tail
+]
+
+
+@pytest.mark.parametrize("dtype", ["int8", "bf16"])
+@pytest.mark.parametrize("i", range(len(DUAL_CASES)))
+def test_split_mma_issue_agrees(i, dtype):
+    params, bn = DUAL_CASES[i]
+    c = sweep_case(1300 + i, params, dtype)
+    p = c.plan(block_n=bn)
+    assert fc.fconv_plan_kernel(p.handle).endswith("-dual")
+    fc.fconv_plan_set_debug(p.handle, fc.FCONV_DEBUG_ONE_MMA_ISSUER)
+    assert not fc.fconv_plan_kernel(p.handle).endswith("-dual")
+    p.close()
+    acc_ref = c.oracle_acc()
+    two = c.accumulators_gpu(block_n=bn)
+    one = c.accumulators_gpu(block_n=bn, debug=fc.FCONV_DEBUG_ONE_MMA_ISSUER)
+    c.check_acc(two, acc_ref)
+    c.check_acc(one, acc_ref)
+    if dtype == "int8":
+        assert np.array_equal(two, one)
+    c.check_output(c.run_gpu(block_n=bn), c.oracle_out(acc_ref))
+
+
 def test_two_kblock_stages_long_bf16():
     """A 36-k-block bf16 layer (the 32x14x14x256 workload's shape on 2
     images): two k-blocks a stage against the oracle."""
     c = sweep_case(90, (2, 14, 14, 256, 256, 3, 3, 1, "SAME", False, True), "bf16")
     p = c.plan(block_n=128)
-    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-kb2"
+    assert fc.fconv_plan_kernel(p.handle) == "tma-im2col-kb2-dual"
     p.close()
     acc_ref = c.oracle_acc()
     c.check_acc(c.accumulators_gpu(block_n=128), acc_ref)
@@ -362,7 +390,7 @@ def test_run_host_ramped_chunks():
 @pytest.mark.parametrize("dtype", ["int8", "bf16"])
 @pytest.mark.parametrize("C,K,kernel", [(16, 16, "cp-async"), (64, 64, "tma-im2col"),
                                          (64, 256, "tma-im2col"), (64, 128, "tma-im2col-m256"),
-                                         (832, 64, "tma-im2col-kb2"), (64, 64, "tma-halo"),
+                                         (832, 64, "tma-im2col-kb2-dual"), (64, 64, "tma-halo"),
                                          (64, 128, "tma-halo-m256")])
 def test_timeout_exit_keeps_context_usable(C, K, kernel, dtype):
     """A producer that never signals 'stage full' makes the MMA issuer's wait
