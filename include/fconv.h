@@ -378,8 +378,9 @@ fconv_status fconv_plan_set_input_widening(fconv_plan *plan, int mode);
 fconv_status fconv_plan_get_input_widening(const fconv_plan *plan, int *in_kernel);
 
 /* How the convolution kernel gathers its input operand.  The halo gather
- * serves forward stride-1 plans with C == 64, at most 9 filter taps, sums in
- * one exact accumulation and 64-channel tiles, whose input windows fit
+ * serves forward stride-1 plans with C == 64 (or C == 32, int8), at most 9
+ * filter taps, sums in one exact accumulation and 64-channel tiles, whose
+ * input windows fit
  * shared memory (3x3 int8 layers up to 115 output columns, 86 on 256-pixel
  * tiles).
  * A tile is floor(128 * m / (Q + S - 1)) whole output rows of one image (m

@@ -213,8 +213,12 @@ struct HaloGeom {
 };
 bool halo_geometry(const fconv_plan &p, int ms, HaloGeom *g) {
   if (p.transposed || p.upsample || p.subsample || p.tap_nR > 0 || p.num_phases > 0) return false;
-  if (p.sh != 1 || p.sw != 1 || p.C != 64 || p.pt < 0 || p.pl < 0) return false;
-  if (p.kb_chunk < p.num_kb || p.num_kb * 64 * 64 * 2 > fconv::kHaloBMax) return false;
+  // C == 32 (int8): a window pixel's upper 32 channels are the copy's zero
+  // fill and the filter tile's rows for them zero
+  const bool c_ok = p.C == 64 || (p.C == 32 && p.dtype == FCONV_INT8);
+  if (p.sh != 1 || p.sw != 1 || !c_ok || p.pt < 0 || p.pl < 0) return false;
+  const int taps = p.R * p.S;
+  if (p.kb_chunk < p.num_kb || taps * 64 * 64 * 2 > fconv::kHaloBMax) return false;
   if (p.dtype == FCONV_INT8 && p.widen_mode == FCONV_WIDEN_COPY) return false;
   if (ms != 1 && ms != 2) return false;
   const int q = p.Q + p.S - 1;
@@ -225,7 +229,7 @@ bool halo_geometry(const fconv_plan &p, int ms, HaloGeom *g) {
   const long long px = static_cast<long long>(rows) * q;
   const long long slot = (px * 128 + 1023) / 1024 * 1024;
   const long long stg = p.dtype == FCONV_INT8 ? (px * 64 + 511) / 512 * 512 : 0;
-  if (2 * slot + 2 * stg + p.num_kb * 64LL * 64 * 2 > fconv::kHaloRegion) return false;
+  if (2 * slot + 2 * stg + taps * 64LL * 64 * 2 > fconv::kHaloRegion) return false;
   const long long tpi = (p.P + tr - 1) / tr;
   if (tpi * p.N * ((p.K + 63) / 64) > kLimit) return false;
   if (g) *g = {q, tr, rows, static_cast<int>(tpi), static_cast<int>(slot), static_cast<int>(stg)};
@@ -298,7 +302,7 @@ TileChoice choose_tile(const fconv_plan &p, int sms, bool allow_halo = true) {
     if (!allow_halo || !halo_geometry(p, ms, &g)) continue;
     const long long tiles = static_cast<long long>(p.N) * g.tiles_per_img * ((p.K + 63) / 64);
     const long long waves = (tiles + sms - 1) / sms;
-    const long long mainloop = p.num_kb * (192LL * ms > 440 ? 192LL * ms : 440);
+    const long long mainloop = static_cast<long long>(p.R) * p.S * (192LL * ms > 440 ? 192LL * ms : 440);
     const long long epilogue = 22LL * 64 * ms;
     const long long cost = waves * (mainloop > epilogue ? mainloop : epilogue) + 8LL * 64 * ms;
     if (best_cost < 0 || cost < best_cost) {
@@ -340,9 +344,13 @@ TileChoice choose_tile(const fconv_plan &p, int sms, bool allow_halo = true) {
         // split-K needs its counters zeroed by a prep launch; a plan with no
         // other prep work (bf16 forward) pays a whole launch for it (~4 us)
         const long long split_launch = (sp > 1 && !needs_prep) ? 8000 : 0;
+        // an int8 run's prep launch (the fp16 input copy), which the halo
+        // gather's candidates above do not have
+        const long long prep_launch = (p.dtype == FCONV_INT8 && halo_geometry(p, 1, nullptr))
+                                          ? 6000 : 0;
         const long long cost = waves * (mainloop > epilogue ? mainloop : epilogue) +
                                8LL * bn * ms + (sp > 1 ? 8LL * bn * ms * (sp + 1) : 0) +
-                               split_launch;
+                               split_launch + prep_launch;
         if (best_cost < 0 || cost < best_cost) {
           best_cost = cost;
           best = {bn, ms, sp, 0};
@@ -1618,9 +1626,9 @@ fconv_status fconv_plan_set_gather(fconv_plan *plan, int mode) {
     if (!halo_geometry(*plan, ms, nullptr)) ms = 1;
     if (!halo_geometry(*plan, ms, nullptr))
       return fail(FCONV_ERR_NOT_SUPPORTED,
-                  "the halo gather needs a forward stride-1 plan with C == 64, at most 9 "
-                  "filter taps, one exact accumulation and windows that fit %d bytes of "
-                  "shared memory beside the filter tile", fconv::kHaloRegion);
+                  "the halo gather needs a forward stride-1 plan with C == 64 (or 32, int8), "
+                  "at most 9 filter taps, one exact accumulation and windows that fit %d "
+                  "bytes of shared memory beside the filter tile", fconv::kHaloRegion);
     plan->gather_mode = mode;
     set_tiling(*plan, 64, ms, 1, 1);
     return FCONV_OK;

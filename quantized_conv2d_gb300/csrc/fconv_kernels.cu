@@ -969,6 +969,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // the channel tiles) is loaded once.
     const int Qh = args.halo_q;
     const int tiles_img = args.tiles_per_img;
+    // one k-block a filter tap: 64 channels (C == 32: the upper 32 are the
+    // window's zero fill and the filter tile's zero rows, and only the
+    // first two k16 steps are issued)
+    const int taps = args.R * args.S;
+    const int ksteps = args.C / 16;
     auto window_origin = [&](long long unit, int &n_img, int &p0) {
       const int m_tile = static_cast<int>(unit / args.num_n_tiles);
       n_img = m_tile / tiles_img;
@@ -987,9 +992,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       if (!IS_INT8 && warp == 2) {
         if (lane == 0) {
           const uint32_t bb = smem_u32(&bars->full_b[7]);
-          mbar_arrive_expect_tx(bb, static_cast<uint32_t>(num_kb) * BN * kBK * 2);
+          mbar_arrive_expect_tx(bb, static_cast<uint32_t>(taps) * BN * kBK * 2);
           const int n_tile = static_cast<int>(blockIdx.x) % args.num_n_tiles;
-          for (int kb = 0; kb < num_kb; ++kb)
+          for (int kb = 0; kb < taps; ++kb)
             load_b_tile<BN>(smem_u32(sB + kb * BN * kBK * 2), &tmap_b, kb, n_tile, args.b3d, bb);
         }
         __syncwarp();
@@ -1102,14 +1107,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const uint32_t wbase = smem_u32(sA + slot * args.halo_slot);
         if (lane == 0) {
           int r = 0, s = 0;
-          for (int kb = 0; kb < num_kb; ++kb) {
+          for (int kb = 0; kb < taps; ++kb) {
             const uint32_t row = static_cast<uint32_t>(part * kBM + r * Qh + s);
             const uint64_t adesc = sw128_kmajor_desc_at_row(wbase, row);
             const uint64_t bdesc = sw128_mnmajor_desc(bbase + kb * BN * kBK * 2);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              umma_f16(d, adesc + 2 * k, bdesc + kBStepK * k, kIdesc,
-                       (kb > 0 || k > 0) ? 1u : 0u);
+              if (k < ksteps)
+                umma_f16(d, adesc + 2 * k, bdesc + kBStepK * k, kIdesc,
+                         (kb > 0 || k > 0) ? 1u : 0u);
             if (++s == args.S) { s = 0; ++r; }
           }
           umma_commit(smem_u32(&bars->empty[slot]));
@@ -1512,20 +1518,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       // (at kernel start the epilogue warps have no accumulator to read yet)
       // the CTA's filter tile, widened from the caller's int8 HWIO filter
       // into the MN-major 128-byte-swizzled blocks the MMA reads (k-row c of
-      // tap kb: 64 output channels, 16-byte chunk j at j ^ (c & 7)); channels
-      // past K read as zero.  All of a thread's loads are issued before its
-      // stores.
+      // tap kb: 64 output channels, 16-byte chunk j at j ^ (c & 7)); output
+      // channels past K and input channels past C (C == 32) read as zero.
+      // All of a thread's loads are issued before its stores.
       const int t = (warp - kTmaEpiWarp0) * 32 + lane;   // 0 .. 255
       const int n0 = (static_cast<int>(blockIdx.x) % args.num_n_tiles) * BN;
-      const int pieces = num_kb * kBK * 4;                 // 16 bytes of int8 each
+      const int pieces = args.R * args.S * kBK * 4;        // 16 bytes of int8 each
       for (int i0 = 0; i0 < pieces; i0 += 256 * 4) {
         uint4 in[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int i = i0 + g * 256 + t;
           const int krow = i >> 2, col = n0 + (i & 3) * 16;
-          in[g] = (i < pieces && col < args.K)
-                      ? ldg_nc_v4(args.w_i8 + static_cast<size_t>(krow) * args.K + col)
+          const int tap = krow >> 6, c = krow & (kBK - 1);
+          in[g] = (i < pieces && col < args.K && c < args.C)
+                      ? ldg_nc_v4(args.w_i8 + (static_cast<size_t>(tap) * args.C + c) * args.K + col)
                       : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -2136,14 +2143,15 @@ cudaError_t launch_conv(int block_n, int m_sub, bool is_int8, Gather gather,
   if (gather == Gather::kTmaHalo) {
     // the window and filter tile fit their buffers, a tile's output rows fit
     // its GEMM rows, and every CTA keeps one output-channel tile
-    if (widen || args.splits != 1 || args.kps != 1 || args.C != kBK || args.sh != 1 ||
-        args.sw != 1 || args.num_kb * block_n * kBK * 2 > kHaloBMax ||
+    if (widen || args.splits != 1 || args.kps != 1 ||
+        (args.C != kBK && !(is_int8 && args.C == 32)) || args.sh != 1 || args.sw != 1 ||
+        args.R * args.S * block_n * kBK * 2 > kHaloBMax ||
         args.halo_q != args.Q + args.S - 1 || args.halo_q > 256 || args.halo_tr <= 0 ||
         args.halo_tr * args.halo_q > kBM * m_sub || args.halo_rows != args.halo_tr + args.R - 1 ||
         args.halo_rows > 256 || args.halo_slot % 1024 != 0 || args.halo_stg % 512 != 0 ||
         args.halo_rows * args.halo_q * 128 > args.halo_slot ||
         (is_int8 && args.halo_rows * args.halo_q * 64 > args.halo_stg) ||
-        2 * args.halo_slot + 2 * args.halo_stg + args.num_kb * block_n * kBK * 2 > kHaloRegion ||
+        2 * args.halo_slot + 2 * args.halo_stg + args.R * args.S * block_n * kBK * 2 > kHaloRegion ||
         args.tiles_per_img != (args.P + args.halo_tr - 1) / args.halo_tr ||
         grid % args.num_n_tiles != 0 ||
         args.num_tiles != args.N * args.tiles_per_img * args.num_n_tiles ||

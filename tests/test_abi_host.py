@@ -411,7 +411,7 @@ def test_automatic_split_choice(shape, splits):
 
 
 @pytest.mark.parametrize("name,block_n,form,splits", [
-    ("small_i8_16x16x32", 64, "cp-async", 1),
+    ("small_i8_16x16x32", 64, "tma-halo", 1),
     ("resnet_i8_56x56x64", 64, "tma-halo-m256", 1),
     ("proj1x1s2_i8_28x28x256", 128, "tma-im2col", 1),
     ("bf16_14x14x256", 128, "tma-im2col-kb2-dual", 1),

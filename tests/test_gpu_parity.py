@@ -840,6 +840,8 @@ HALO_CASES = [
     ((2, 6, 90, 64, 64, 3, 3, 1, "SAME", False, True), 128),      # a 92-pixel-wide window
     ((3, 1, 1, 64, 64, 1, 1, 1, "SAME", True, True), None),       # 1x1 images
     ((2, 4, 40, 64, 128, 3, 3, 1, "SAME", True, True), 256),      # window rows past the image
+    ((2, 16, 16, 32, 32, 3, 3, 1, "SAME", True, True), None),     # C = 32 (int8): zero-filled half
+    ((3, 9, 11, 32, 80, 3, 3, 1, "VALID", False, True), 256),     # C = 32, two channel tiles
 ]
 
 
@@ -847,6 +849,8 @@ HALO_CASES = [
 @pytest.mark.parametrize("i,item", list(enumerate(HALO_CASES)))
 def test_halo_gather(i, item, dtype):
     params, pixels = item
+    if dtype == "bf16" and params[3] != 64:
+        pytest.skip("the halo gather takes 32 input channels for int8 only")
     c = sweep_case(1200 + i, params, dtype)
     acc_ref = c.oracle_acc()
     ref = c.oracle_out(acc_ref)
