@@ -508,3 +508,96 @@ def test_host_chunk_sizes_fixed_count_and_errors():
         assert n.value == 3
     finally:
         fc.fconv_plan_destroy(h)
+
+
+def _plan(shape, dtype=None, stride=1, pad=None):
+    N, H, W, C, K, R, S = shape
+    return fc.fconv_plan_create(N, H, W, C, K, R, S, stride, stride,
+                                fc.FCONV_SAME if pad is None else pad,
+                                fc.FCONV_INT8 if dtype is None else dtype, 1)
+
+
+@pytest.mark.parametrize("shape,dtype,stride,ok", [
+    ((2, 20, 20, 64, 64, 3, 3), fc.FCONV_INT8, 1, True),
+    ((2, 20, 20, 64, 64, 3, 3), fc.FCONV_BF16, 1, True),
+    ((2, 20, 20, 32, 64, 3, 3), fc.FCONV_INT8, 1, True),     # C = 32: int8 only
+    ((2, 20, 20, 32, 64, 3, 3), fc.FCONV_BF16, 1, False),
+    ((2, 20, 20, 128, 64, 3, 3), fc.FCONV_INT8, 1, False),   # one k-block a tap: C <= 64
+    ((2, 20, 20, 64, 64, 3, 3), fc.FCONV_INT8, 2, False),    # stride 1 only
+    ((2, 20, 20, 64, 64, 5, 5), fc.FCONV_INT8, 1, False),    # 25 taps: the filter tile is too big
+    ((1, 8, 300, 64, 64, 3, 3), fc.FCONV_INT8, 1, False),    # a window wider than the buffers
+    ((1, 8, 115, 64, 64, 3, 3), fc.FCONV_INT8, 1, True),     # the widest int8 3x3 window
+])
+def test_halo_gather_rules(shape, dtype, stride, ok):
+    """Which plans the halo gather takes (forward, stride 1, C == 64 or int8
+    C == 32, at most 9 taps, windows that fit shared memory), and what it
+    changes: one launch, and no workspace for int8 plans."""
+    h = _plan(shape, dtype, stride)
+    try:
+        if not ok:
+            assert _err(fc.fconv_plan_set_gather, h, fc.FCONV_GATHER_HALO) == \
+                fc.FCONV_ERR_NOT_SUPPORTED
+            assert not fc.fconv_plan_kernel(h).startswith("tma-halo")
+            return
+        fc.fconv_plan_set_gather(h, fc.FCONV_GATHER_HALO)
+        assert fc.fconv_plan_kernel(h).startswith("tma-halo")
+        assert fc.fconv_plan_launch_count(h) == 1
+        assert fc.fconv_workspace_size(h) == 0
+        # the im2col gather (or cp.async for C = 32) brings the prep launch back for int8
+        fc.fconv_plan_set_gather(h, fc.FCONV_GATHER_IM2COL)
+        assert not fc.fconv_plan_kernel(h).startswith("tma-halo")
+        if dtype == fc.FCONV_INT8:
+            assert fc.fconv_plan_launch_count(h) == 2
+            assert fc.fconv_workspace_size(h) > 0
+        fc.fconv_plan_set_gather(h, fc.FCONV_GATHER_AUTO)
+    finally:
+        fc.fconv_plan_destroy(h)
+
+
+def test_halo_gather_controls():
+    h = _plan((4, 28, 28, 64, 64, 3, 3))
+    try:
+        assert _err(fc.fconv_plan_set_gather, h, 3) == fc.FCONV_ERR_INVALID_VALUE
+        fc.fconv_plan_set_gather(h, fc.FCONV_GATHER_HALO)
+        # a halo tile of either height; tile widths and split-K leave the gather
+        fc.fconv_plan_set_tile_shape(h, 128, 64)
+        assert fc.fconv_plan_kernel(h) == "tma-halo"
+        fc.fconv_plan_set_tile_shape(h, 256, 64)
+        assert fc.fconv_plan_kernel(h) == "tma-halo-m256"
+        fc.fconv_plan_set_splits(h, 1)
+        assert fc.fconv_plan_kernel(h) == "tma-halo-m256"
+        fc.fconv_plan_set_tile(h, 128)
+        assert not fc.fconv_plan_kernel(h).startswith("tma-halo")
+        fc.fconv_plan_set_gather(h, fc.FCONV_GATHER_HALO)
+        assert fc.fconv_plan_kernel(h).startswith("tma-halo")
+        # the fp16 input copy moves an int8 plan off the gather
+        fc.fconv_plan_set_input_widening(h, fc.FCONV_WIDEN_COPY)
+        assert not fc.fconv_plan_kernel(h).startswith("tma-halo")
+        assert _err(fc.fconv_plan_set_gather, h, fc.FCONV_GATHER_HALO) == \
+            fc.FCONV_ERR_NOT_SUPPORTED
+        fc.fconv_plan_set_input_widening(h, fc.FCONV_WIDEN_AUTO)
+        fc.fconv_plan_set_gather(h, fc.FCONV_GATHER_HALO)
+        assert fc.fconv_plan_kernel(h).startswith("tma-halo")
+        # the cp.async test hook runs the general gather, with its copies
+        fc.fconv_plan_set_debug(h, fc.FCONV_DEBUG_GATHER_CPASYNC)
+        assert fc.fconv_plan_kernel(h) == "cp-async"
+        assert fc.fconv_workspace_size(h) > 0
+        fc.fconv_plan_set_debug(h, 0)
+        assert fc.fconv_workspace_size(h) == 0
+    finally:
+        fc.fconv_plan_destroy(h)
+
+
+def test_halo_tiles_cover_whole_output_rows():
+    """Halo tiles are floor(128 * m / (Q + S - 1)) whole output rows of one
+    image: the tile count is N * ceil(P / rows) (x the channel tiles)."""
+    for (N, H, W, K), px in [((3, 56, 56, 64), 256), ((2, 14, 14, 128), 128), ((5, 9, 30, 64), 256)]:
+        h = _plan((N, H, W, 64, K, 3, 3))
+        try:
+            fc.fconv_plan_set_gather(h, fc.FCONV_GATHER_HALO)
+            fc.fconv_plan_set_tile_shape(h, px, 64)
+            rows = px // (W + 2)
+            tiles = N * -(-H // rows) * -(-K // 64)
+            assert fc.fconv_plan_get_config(h)[2] == tiles
+        finally:
+            fc.fconv_plan_destroy(h)
