@@ -232,6 +232,8 @@ bool halo_geometry(const fconv_plan &p, int ms, HaloGeom *g) {
   if (2 * slot + 2 * stg + taps * 64LL * 64 * 2 > fconv::kHaloRegion) return false;
   const long long tpi = (p.P + tr - 1) / tr;
   if (tpi * p.N * ((p.K + 63) / 64) > kLimit) return false;
+  // every CTA keeps one channel tile: at least one CTA for each of them
+  if ((p.K + 63) / 64 > sm_count_of_current_device(148)) return false;
   if (g) *g = {q, tr, rows, static_cast<int>(tpi), static_cast<int>(slot), static_cast<int>(stg)};
   return true;
 }
@@ -846,6 +848,8 @@ fconv_status enqueue(fconv_plan *p, const void *x, const void *w, const float *b
   int grid = units < sms ? static_cast<int>(units) : sms;
   // the halo gather keeps each CTA on one output-channel tile
   if (halo) grid = grid / p->num_n_tiles * p->num_n_tiles;
+  if (grid <= 0)
+    return fail(FCONV_ERR_NOT_SUPPORTED, "%d output-channel tiles on %d SMs", p->num_n_tiles, sms);
   e = fconv::launch_conv(p->block_n, p->m_sub, is_int8, gather, tmap_a, tmap, a, grid,
                         /*overlap=*/prep, stream, p->widen != 0);
   if (e != cudaSuccess)

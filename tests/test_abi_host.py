@@ -601,3 +601,15 @@ def test_halo_tiles_cover_whole_output_rows():
             assert fc.fconv_plan_get_config(h)[2] == tiles
         finally:
             fc.fconv_plan_destroy(h)
+
+
+def test_halo_gather_needs_a_cta_per_channel_tile():
+    # each CTA keeps one 64-channel tile: more channel tiles than SMs rules
+    # the gather out (152 SMs on GB300; 148 where no GPU reports a count)
+    h = _plan((1, 8, 8, 64, 64 * 400, 3, 3))
+    try:
+        assert not fc.fconv_plan_kernel(h).startswith("tma-halo")
+        assert _err(fc.fconv_plan_set_gather, h, fc.FCONV_GATHER_HALO) == \
+            fc.FCONV_ERR_NOT_SUPPORTED
+    finally:
+        fc.fconv_plan_destroy(h)
