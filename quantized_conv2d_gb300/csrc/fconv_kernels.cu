@@ -1003,8 +1003,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       // copies into window buffer / staging 0 and 1 (scalars: a runtime
       // index into a register array would put it in local memory)
       uint32_t issued0 = 0, issued1 = 0;
-      bool ok = true;
       if constexpr (IS_INT8) {
+        bool ok = true;
         // warp 0: window jj's copy into staging jj % 2, once both warps have
         // read window jj - 2 from it
         auto issue = [&](long long jj) -> bool {
