@@ -164,9 +164,9 @@ fconv_status fconv_plan_padding(const fconv_plan *plan, int *pad_top,
  * and for transposed plans with a stride above the filter (zeros
  * inserted), and for a split-K plan (fconv_plan_set_splits) every unit's
  * 32-bit partial sums and one counter per tile and epilogue warp.  It
- * depends on the tile and split in force: query it after changing them.
- * It may be 0 (an unsplit bf16 forward plan); the run then accepts a NULL
- * workspace. */
+ * depends on the tile, split and gather in force: query it after changing
+ * them.  It may be 0 (an unsplit bf16 forward plan, or a plan on the halo
+ * gather, fconv_plan_set_gather); the run then accepts a NULL workspace. */
 fconv_status fconv_workspace_size(const fconv_plan *plan, size_t *bytes);
 
 /* Run the fused convolution on `stream`.
