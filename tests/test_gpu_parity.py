@@ -217,6 +217,7 @@ def test_two_kblock_stages_agree(i, dtype):
 DUAL_CASES = KB2_CASES + [
     ((1, 30, 30, 1024, 32, 3, 3, 1, "SAME", True, True), 128),   # 144 k-blocks (int8: chunked)
     ((2, 12, 12, 512, 272, 3, 3, 1, "SAME", True, True), 128),   # 72 k-blocks, K tail
+    ((128, 14, 14, 256, 128, 3, 3, 1, "SAME", True, True), 128), # 196 tiles: CTAs with two
 ]
 
 
@@ -842,6 +843,8 @@ HALO_CASES = [
     ((2, 4, 40, 64, 128, 3, 3, 1, "SAME", True, True), 256),      # window rows past the image
     ((2, 16, 16, 32, 32, 3, 3, 1, "SAME", True, True), None),     # C = 32 (int8): zero-filled half
     ((3, 9, 11, 32, 80, 3, 3, 1, "VALID", False, True), 256),     # C = 32, two channel tiles
+    ((256, 16, 16, 64, 64, 3, 3, 1, "SAME", True, True), 256),    # 512 tiles: 3-4 a CTA
+    ((400, 12, 12, 32, 64, 3, 3, 1, "SAME", True, True), 128),    # C = 32, ~5 tiles a CTA
 ]
 
 
