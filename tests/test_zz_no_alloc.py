@@ -52,13 +52,20 @@ def _run_both(plan, c):
     return to_host(y_ref), to_host(y_na)
 
 
+@pytest.mark.parametrize("gather", ["im2col", "halo"])
 @pytest.mark.parametrize("dtype", ["int8", "bf16"])
-def test_no_alloc_matches_fconv_run_twice(dtype):
+def test_no_alloc_matches_fconv_run_twice(dtype, gather):
     # two calls in a row on the same plan, different inputs each time: the
-    # second call must not see anything the first left in the scratch
+    # second call must not see anything the first left in the scratch (the
+    # im2col gather's int8 plan keeps its fp16 input and filter copies there;
+    # the halo gather needs no scratch at all)
     first = _case(501, 4, 19, 21, 64, 96, dtype)
     second = _case(502, 4, 19, 21, 64, 96, dtype)
     plan = first.plan()
+    fc.fconv_plan_set_gather(plan.handle, fc.FCONV_GATHER_IM2COL if gather == "im2col"
+                             else fc.FCONV_GATHER_HALO)
+    ws = fc.fconv_workspace_size(plan.handle)
+    assert (ws > 0) == (gather == "im2col" and dtype == "int8")
     for c in (first, second):
         y_ref, y_na = _run_both(plan, c)
         c.check_output(y_na, c.oracle_out())
