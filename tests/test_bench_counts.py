@@ -1,12 +1,14 @@
-"""The benchmark's roofline numerator, bench.ops_counts, against a count made
-another way: the oracle's convolution of an all-ones int8 input with an
+"""The benchmark's roofline numerators against counts made another way.
+bench.ops_counts: the oracle's convolution of an all-ones int8 input with an
 all-ones filter gives every output C times the number of its in-bounds
 filter taps (for a transposed convolution, C times the number of input
 pixel / tap pairs that land on it), so twice the sum of all outputs is the
 in-bounds operation count, and the result's shape gives P and Q.  The
 nominal count of a transposed convolution is the same sum with no output
 cropping (pads 0: every pair lands).  Reduced N, C and K keep each
-workload's geometry; both counts are linear in them."""
+workload's geometry; both counts are linear in them.  bench.algorithmic_bytes:
+the generated tensors' sizes, the output's, and the input pixels that a
+brute-force walk over output positions and taps finds read."""
 import dataclasses
 import os
 import sys
@@ -57,3 +59,30 @@ def test_padding_lowers_the_in_bounds_count():
     assert (P, Q) == (4, 4)
     assert nominal == 2 * 16 * 9
     assert inbounds == 2 * 10 * 10
+
+
+def _read_extent(size, out, filt, stride, pad):
+    # input positions along one axis that some output position reads
+    return len({o * stride + t - pad for o in range(out) for t in range(filt)} & set(range(size)))
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_algorithmic_bytes_match_the_tensors(name):
+    """The roofline's byte count against the generated tensors' own sizes,
+    the output's, and the input pixels a brute-force walk finds read."""
+    wl = dataclasses.replace(FI.workload(name), N=2, C=16, K=8)
+    _, _, P, Q = bench.ops_counts(wl)
+    t = FI.generate(wl, (P, Q))
+    elt = t["x"].itemsize
+    if wl.transposed_pads is None:
+        pad = oracle.SAME if wl.padding == "SAME" else oracle.VALID
+        g = oracle.Geometry(wl.N, wl.H, wl.W, wl.C, wl.K, wl.R, wl.S, wl.stride, wl.stride, pad)
+        assert (g.P, g.Q) == (P, Q)
+        rows = _read_extent(wl.H, P, wl.R, wl.stride, g.pt)
+        cols = _read_extent(wl.W, Q, wl.S, wl.stride, g.pl)
+    else:
+        rows, cols = wl.H, wl.W   # every input pixel is scattered somewhere
+    x_read = wl.N * rows * cols * wl.C * elt
+    y = wl.N * P * Q * wl.K * elt
+    side = t["side"].nbytes if t["side"] is not None else 0
+    assert bench.algorithmic_bytes(wl) == x_read + t["w"].nbytes + side + y + t["bias"].nbytes
