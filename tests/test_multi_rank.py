@@ -37,7 +37,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_take_the_slowest_rank():
     world, port = 2, _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
@@ -62,7 +62,7 @@ def _ref_worker(rank, world, port, out):
 
 def test_reference_arm_reports_on_rank_zero_only():
     world, port = 2, _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_ref_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
@@ -125,7 +125,7 @@ def _shard_worker(rank, world, port, out):
 def test_batch_shards_reassemble_the_unsharded_result():
     import numpy as np
     world, port = 2, _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_shard_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
